@@ -1,0 +1,310 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each ``check_*`` takes the oracle package (or a copy with a planted mistake) and
+raises AssertionError when the oracle disagrees with the pin.  The normal tests
+run them on the real oracle; ``test_oracle_mutations.py`` runs them on oracles
+with planted mistakes and expects them to fail.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import workloads as wl
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+with open(os.path.join(_HERE, "golden", "page_facts.json")) as _f:
+    FACTS = json.load(_f)
+
+FMT_KEY = {wl.MLX_AFFINE4_G64: "mlx_affine4_g64", wl.MXFP4: "mxfp4", wl.NVFP4: "nvfp4", wl.Q6K: "q6k"}
+
+
+# ----------------------------------------------------------------- exact helpers
+def frac_round_bf16(fr: Fraction) -> Fraction:
+    """Exact round-to-nearest-even of a rational to bf16 (8 significant bits,
+    subnormal quantum 2**-133); returns +-inf as float('inf') for overflow."""
+    if fr == 0:
+        return Fraction(0)
+    sign = -1 if fr < 0 else 1
+    a = abs(fr)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** (e - 1) > a:
+        e -= 1
+    while Fraction(2) ** e <= a:
+        e += 1
+    q = max(e - 8, -133)
+    s = a / (Fraction(2) ** q)
+    fl = math.floor(s)
+    rem = s - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    r = fl * Fraction(2) ** q
+    if r >= Fraction(2) ** 128:
+        return sign * float("inf")
+    return sign * r
+
+
+def e2m1_from_page(code: int) -> Fraction:
+    """E2M1 value from the page's magnitude set: codes 0..7 take the magnitudes in
+    increasing order, bit 3 is the sign."""
+    mags = [Fraction(str(v)) for v in FACTS["e2m1_magnitudes"]["value"]]
+    v = mags[code & 7]
+    return -v if code & 8 else v
+
+
+def torch_e4m3(byte: int) -> Fraction:
+    t = torch.tensor([byte], dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    return Fraction(float(t.item()))
+
+
+def torch_e8m0(byte: int) -> Fraction:
+    t = torch.tensor([byte], dtype=torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64)
+    return Fraction(float(t.item()))
+
+
+def exact_weight(w, n: int, k: int) -> Fraction:
+    """Exact real value of weight (n, k) written from the format definitions with
+    library decoders (numpy fp16, torch fp8) and the page's E2M1 table."""
+    c = int(w.codes[n, k])
+    if w.fmt == wl.MLX_AFFINE4_G64:
+        return Fraction(float(w.scales[n, k // 64])) * c + Fraction(float(w.aux[n, k // 64]))
+    if w.fmt == wl.MXFP4:
+        return e2m1_from_page(c) * torch_e8m0(int(w.scales[n, k // 32]))
+    if w.fmt == wl.NVFP4:
+        return Fraction(float(np.float32(w.tensor_scale))) * torch_e4m3(int(w.scales[n, k // 16])) * e2m1_from_page(c)
+    if w.fmt == wl.Q6K:
+        return Fraction(float(w.aux[n, k // 256])) * int(w.scales[n, k // 16]) * (c - 32)
+    raise ValueError(w.fmt)
+
+
+def bf16_frac(bits: int) -> Fraction:
+    return Fraction(float(np.array([int(bits) << 16], dtype=np.uint32).view(np.float32)[0]))
+
+
+# ----------------------------------------------------------------- pins
+def check_e2m1(o):
+    vals = o.e2m1_value(np.arange(16))
+    mags = sorted(set(np.abs(vals).tolist()))
+    assert mags == [float(v) for v in FACTS["e2m1_magnitudes"]["value"]], mags
+    assert np.all(np.diff(vals[:8]) > 0), "codes 0..7 must increase"
+    assert np.array_equal(vals[8:], -vals[:8]), "bit 3 is the sign"
+    assert np.all(np.signbit(vals[8:])), "codes 8..15 carry the sign bit"
+
+
+def check_e8m0(o):
+    b = np.arange(256)
+    got = o.e8m0_value(b)
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert got[127] == 1.0 and np.isnan(got[255])
+
+
+def check_e4m3(o):
+    got = o.e4m3fn_value(np.arange(256))
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.nanmax(got) == 448.0
+
+
+def check_bf16_rounding(o, seed=1):
+    rng = np.random.default_rng(seed)
+    # fp32 inputs: torch's fp32 -> bf16 cast rounds once, so both must agree exactly
+    a = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32),
+        (rng.standard_normal(2000) * 1e-39).astype(np.float32),  # subnormals
+        np.clip(rng.standard_normal(2000) * 3e38, -3.4e38, 3.4e38).astype(np.float32),  # near overflow
+        np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 2 ** -133, 3 * 2 ** -134], np.float32),
+    ])
+    ref = torch.from_numpy(a).to(torch.bfloat16).to(torch.float64).numpy()
+    got = o.round_to_bf16(a.astype(np.float64))
+    assert np.array_equal(got, ref), np.nonzero(got != ref)[0][:5]
+    # one rounding from fp64: 1 + 2^-8 + 2^-30 rounds up, while fp32 first would make a tie -> 1.0
+    v = 1.0 + 2.0 ** -8 + 2.0 ** -30
+    assert o.round_to_bf16(np.array([v]))[0] == 1.0 + 2.0 ** -7
+
+
+def check_bpw(o):
+    page = FACTS["bits_per_weight"]["value"]
+    for fmt, key in [(wl.MLX_AFFINE4_G64, "mlx_affine4_g64"), (wl.MXFP4, "mxfp4"), (wl.NVFP4, "nvfp4")]:
+        assert o.bits_per_weight(fmt) == page[key], key
+        c, s, a = o.packed_sizes(fmt, 1024, 2048)
+        assert (c + s + a) * 8 / (1024 * 2048) == page[key], key
+    q = FACTS["q6k_output_layer"]
+    c, s, a = o.packed_sizes(wl.Q6K, q["n"], q["k"])
+    total = c + s + a
+    assert total == q["n"] * q["k"] * o.bits_per_weight(wl.Q6K) / 8
+    assert round(total / 1e9, 2) == q["gigabytes"], total
+
+
+def check_q6k_operand(o):
+    f = FACTS["q6k_operand"]
+    codes = np.arange(64)
+    half = o.q6k_half_operand_bits(codes).view(np.float16)
+    assert np.array_equal(half.astype(np.float64), 1.0 + codes / 64.0)
+    diff = (half - np.float16(f["subtract"])).astype(np.float64)  # fp16 arithmetic
+    assert np.array_equal(diff, (codes - f["zero_point"]) / 64.0)
+    # the oracle's Q6_K dequantisation must use the same zero point
+    w = wl.QWeight(wl.Q6K, 1, 256, codes=np.tile(np.arange(64, dtype=np.uint8), 4)[None, :],
+                   scales=np.ones((1, 16), np.int8), aux=np.ones((1, 1), np.float16))
+    got = o.dequant(w)[0].astype(np.float64)
+    assert np.array_equal(got, 64.0 * np.tile(diff, 4))
+
+
+def check_q6k_old_seed(seed=3):
+    """(128 + c) operands seeded with -160 * sum(x) give the same exact dot as (c - 32)."""
+    f = FACTS["q6k_old_seed"]
+    rng = np.random.default_rng(seed)
+    for _ in range(20):
+        c = rng.integers(0, 64, f["chain"])
+        x = [Fraction(int(v), 1024) for v in rng.integers(-4096, 4096, f["chain"])]
+        old = sum((f["operand_offset"] + int(ci)) * xi for ci, xi in zip(c, x)) + f["seed_per_input"] * sum(x)
+        new = sum((int(ci) - FACTS["q6k_operand"]["zero_point"]) * xi for ci, xi in zip(c, x))
+        assert old == new
+
+
+def check_dequant_exact(o, fmt, seed=5):
+    n, k = (8, 256) if fmt == wl.Q6K else (8, 128)
+    w = wl.weight(fmt, n, k, seed)
+    got = o.dequant(w)
+    for i in range(n):
+        for j in range(k):
+            ex = exact_weight(w, i, j)
+            assert Fraction(float(ex)) == ex  # exactly representable in fp64
+            assert got[i, j] == np.float32(float(ex)), (fmt, i, j)
+
+
+def check_gemv_brute_force(o, fmt, m, residual, seed=7):
+    n, k = (16, 256) if fmt == wl.Q6K else (16, 64)
+    w, x, res = wl.gemv_case(fmt, n, k, m, seed=seed, residual=residual)
+    y, v = o.gemv(w, x, res)
+    w32 = o.dequant(w)
+    for mi in range(m):
+        for ni in range(n):
+            terms = [Fraction(float(w32[ni, kk])) * bf16_frac(x[mi, kk]) for kk in range(k)]
+            ex = sum(terms, Fraction(0))
+            if res is not None:
+                ex += bf16_frac(res[mi, ni])
+            mag = float(sum(abs(t) for t in terms)) + (abs(float(bf16_frac(res[mi, ni]))) if res is not None else 0)
+            bound = (k + 2) * 2.0 ** -52 * mag
+            assert abs(Fraction(float(v[mi, ni])) - ex) <= Fraction(bound), (fmt, mi, ni)
+            lo, hi = frac_round_bf16(ex - Fraction(bound)), frac_round_bf16(ex + Fraction(bound))
+            if lo == hi:
+                assert Fraction(float(y[mi, ni])) == lo, (fmt, mi, ni, float(y[mi, ni]), float(lo))
+            else:
+                assert Fraction(float(y[mi, ni])) in (lo, hi)
+
+
+def check_dense_special_case(o, fmt, seed=11):
+    """Unit scales reduce every format to a dense matmul of its integer / E2M1 values."""
+    n, k, m = (32, 256, 3) if fmt == wl.Q6K else (32, 128, 3)
+    w, x, _ = wl.gemv_case(fmt, n, k, m, seed=seed)
+    if fmt == wl.MLX_AFFINE4_G64:
+        w.scales = np.ones_like(w.scales)
+        w.aux = np.zeros_like(w.aux)
+        dense = w.codes.astype(np.float64)
+    elif fmt == wl.MXFP4:
+        w.scales = np.full_like(w.scales, 127)
+        dense = np.vectorize(lambda c: float(e2m1_from_page(int(c))))(w.codes)
+    elif fmt == wl.NVFP4:
+        w.scales = np.full_like(w.scales, 0x38)  # E4M3 1.0
+        w.tensor_scale = 1.0
+        dense = np.vectorize(lambda c: float(e2m1_from_page(int(c))))(w.codes)
+    else:
+        w.scales = np.ones_like(w.scales)
+        w.aux = np.ones_like(w.aux)
+        dense = w.codes.astype(np.float64) - 32.0
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    ref = torch.matmul(xt, torch.from_numpy(dense).T).numpy()
+    _, v = o.gemv(w, x)
+    assert np.allclose(v, ref, rtol=1e-12, atol=1e-12)
+
+
+def check_route_brute_force(o, seed=13):
+    rng = np.random.default_rng(seed)
+    for _ in range(30):
+        t, e, kk = 3, 8, 3
+        lg = rng.integers(-3, 3, size=(t, e)).astype(np.float32)  # many ties
+        ids, p = o.route(lg, kk)
+        for ti in range(t):
+            # rank-based definition: e is kept iff fewer than k experts beat it
+            beats = [sum(1 for f in range(e) if lg[ti, f] > lg[ti, g] or (lg[ti, f] == lg[ti, g] and f < g))
+                     for g in range(e)]
+            chosen = [g for g in range(e) if beats[g] < kk]
+            assert sorted(ids[ti].tolist()) == chosen
+            assert [beats[g] for g in ids[ti]] == list(range(kk)), "descending order, ties to lower index"
+            z = np.exp(lg[ti, ids[ti]].astype(np.float64) - lg[ti, ids[ti]].max())
+            assert np.allclose(p[ti], z / z.sum(), rtol=1e-15)
+    # permutation invariance of the weights
+    lg = rng.standard_normal((5, 64)).astype(np.float32)
+    perm = rng.permutation(64)
+    ids, p = o.route(lg, 10)
+    ids2, p2 = o.route(lg[:, perm], 10)
+    assert np.array_equal(perm[ids2], ids) and np.array_equal(p, p2)
+    assert np.allclose(p.sum(axis=1), 1.0, rtol=0, atol=1e-15)
+
+
+def check_route_statistics(o):
+    r = FACTS["routing"]
+    e, kk, t = r["experts"], r["topk"], r["decode_rows"]
+    closed = e * (1 - (1 - kk / e) ** t)
+    lg = wl.router_logits(t, e, seed=17, sets=3000)
+    distinct = [len(np.unique(o.route(lg[s], kk)[0])) for s in range(lg.shape[0])]
+    mean = float(np.mean(distinct))
+    assert abs(mean - closed) < 0.15, (mean, closed)
+    assert round(mean) == r["distinct_experts_synthetic"]
+    big = wl.router_logits(r["prefill_tokens"], e, seed=19)
+    ids, _ = o.route(big, kk)
+    counts = np.bincount(ids.ravel(), minlength=e)
+    assert counts.sum() / e == r["tokens_per_expert"]
+    assert counts.min() > 80 and counts.max() < 260  # binomial(8192, 10/512) spread
+
+
+def check_silu(o, seed=23):
+    assert o.silu(np.array([0.0]))[0] == 0.0
+    assert o.silu(np.array([60.0]))[0] == 60.0
+    assert abs(o.silu(np.array([-60.0]))[0]) < 1e-24
+    g = np.random.default_rng(seed).standard_normal(1000) * 6
+    ref = torch.nn.functional.silu(torch.from_numpy(g)).numpy()
+    assert np.allclose(o.silu(g), ref, rtol=1e-14, atol=0)
+
+
+def check_moe_composition(o, seed=29):
+    """The MoE chain against the dense GEMV oracle: top-1 routing (p = 1) through one
+    expert equals gate/up GEMV -> SwiGLU -> down GEMV, and relabelling the experts
+    (with the logits) leaves the output unchanged."""
+    layer = wl.moe_layer(wl.MXFP4, 6, 64, 32, seed=seed, shared=True)
+    x = wl.moe_tokens(3, 64, seed=seed)
+    lg = wl.router_logits(3, 6, seed=seed)
+    out = o.moe_forward(layer, x, lg, topk=1)
+    ids, p = o.route(lg, 1)
+    assert np.all(p == 1.0)
+    x64 = o.bf16_value(x)
+    for t in range(3):
+        acc = np.zeros(64)
+        for gu, dn in [(layer.gate_up[ids[t, 0]], layer.down[ids[t, 0]]), (layer.shared_gate_up, layer.shared_down)]:
+            _, v = o.gemv(gu, x[t:t + 1])
+            g, u = v[0, :32].astype(np.float32), v[0, 32:].astype(np.float32)
+            h = o.round_to_bf16(o.silu(g) * u.astype(np.float64))
+            acc += o.gemv(dn, o.bf16_bits_of(h)[None, :])[1][0]
+        assert np.array_equal(out[t], o.round_to_bf16(acc)), t
+    perm = np.random.default_rng(seed).permutation(6)  # new index i holds old expert perm[i]
+    layer2 = wl.MoELayer(layer.fmt, 6, 64, 32, [layer.gate_up[j] for j in perm], [layer.down[j] for j in perm],
+                         layer.shared_gate_up, layer.shared_down)
+    lg2 = wl.router_logits(3, 6, seed=seed + 1)
+    a1 = o.moe_forward(layer, x, lg2, topk=3, with_intermediates=True)[1]
+    a2 = o.moe_forward(layer2, x, lg2[:, perm], topk=3, with_intermediates=True)[1]
+    assert np.allclose(a1, a2, rtol=1e-12, atol=0)
+    # all experts, equal logits: p = 1/E for every slot
+    eq = np.zeros((3, 6), np.float32)
+    _, p = o.route(eq, 6)
+    assert np.allclose(p, 1 / 6, rtol=1e-15)

@@ -1,0 +1,163 @@
+"""Planted mistakes in the oracle (on the CPU) must be caught by the pins.
+
+Each case patches one oracle function with a plausible bug (dropped term, wrong
+sign, wrong constant, transposed operand, double rounding, wrong tie-break) and
+checks that at least one pin fails.
+"""
+import sys
+
+import numpy as np
+import torch
+
+import oracle
+import workloads as wl
+from tests import pins
+
+F = sys.modules["oracle.formats"]
+G = sys.modules["oracle.gemv"]  # the package re-exports a function under the same name
+MO = sys.modules["oracle.moe"]
+
+
+def _fails(fn, *a, **kw):
+    try:
+        fn(*a, **kw)
+    except (AssertionError, ValueError):
+        return True
+    return False
+
+
+def test_e2m1_sign_dropped(monkeypatch):
+    orig = F.e2m1_value
+    monkeypatch.setattr(oracle, "e2m1_value", lambda c: np.abs(orig(c)))
+    assert _fails(pins.check_e2m1, oracle)
+
+
+def test_e2m1_magnitudes_swapped(monkeypatch):
+    orig = F.e2m1_value
+
+    def bad(c):
+        c = np.asarray(c)
+        swapped = np.where((c & 7) == 3, (c & 8) | 4, np.where((c & 7) == 4, (c & 8) | 3, c))
+        return orig(swapped)
+    monkeypatch.setattr(oracle, "e2m1_value", bad)
+    assert _fails(pins.check_e2m1, oracle)
+
+
+def test_e4m3_wrong_bias(monkeypatch):
+    monkeypatch.setattr(oracle, "e4m3fn_value", lambda b: F.e4m3fn_value(b) / 2)
+    assert _fails(pins.check_e4m3, oracle)
+
+
+def test_e8m0_off_by_one(monkeypatch):
+    monkeypatch.setattr(oracle, "e8m0_value", lambda b: F.e8m0_value(np.asarray(b) + 1))
+    assert _fails(pins.check_e8m0, oracle)
+
+
+def test_bf16_double_rounding(monkeypatch):
+    def via_fp32(v):
+        t = torch.from_numpy(np.asarray(v, np.float64).astype(np.float32)).to(torch.bfloat16)
+        return t.to(torch.float64).numpy()
+    monkeypatch.setattr(oracle, "round_to_bf16", via_fp32)
+    assert _fails(pins.check_bf16_rounding, oracle)
+
+
+def _patch_exact(monkeypatch, fmt_target, transform):
+    orig = F._exact_values
+
+    def bad(fmt, codes, scales, aux, ts):
+        v = orig(fmt, codes, scales, aux, ts)
+        return transform(v, fmt, codes, scales, aux, ts) if fmt == fmt_target else v
+    monkeypatch.setattr(F, "_exact_values", bad)
+
+
+def test_q6k_zero_point_31(monkeypatch):
+    def t(v, fmt, codes, scales, aux, ts):
+        sc = np.repeat(np.asarray(scales, np.int8).astype(np.float64), 16, axis=1)
+        d = np.repeat(np.asarray(aux, np.float16).astype(np.float64), 256, axis=1)
+        return d * sc * (np.asarray(codes, np.float64) - 31.0)
+    _patch_exact(monkeypatch, wl.Q6K, t)
+    assert _fails(pins.check_q6k_operand, oracle)
+    assert _fails(pins.check_dequant_exact, oracle, wl.Q6K)
+
+
+def test_nvfp4_tensor_scale_dropped(monkeypatch):
+    _patch_exact(monkeypatch, wl.NVFP4, lambda v, fmt, c, s, a, ts: v / float(np.float32(ts)))
+    assert _fails(pins.check_dequant_exact, oracle, wl.NVFP4)
+
+
+def test_mlx_bias_sign_flipped(monkeypatch):
+    def t(v, fmt, codes, scales, aux, ts):
+        b = np.repeat(np.asarray(aux, np.float16).astype(np.float64), 64, axis=1)
+        return v - 2 * b
+    _patch_exact(monkeypatch, wl.MLX_AFFINE4_G64, t)
+    assert _fails(pins.check_dequant_exact, oracle, wl.MLX_AFFINE4_G64)
+
+
+def test_mxfp4_scale_block_16_instead_of_32(monkeypatch):
+    def t(v, fmt, codes, scales, aux, ts):
+        s = np.repeat(F.e8m0_value(scales), 16, axis=1)
+        s = np.concatenate([s, s], axis=1)[:, :np.asarray(codes).shape[1]]
+        return F.e2m1_value(codes) * s
+    _patch_exact(monkeypatch, wl.MXFP4, t)
+    assert _fails(pins.check_dequant_exact, oracle, wl.MXFP4)
+
+
+def test_gemv_residual_dropped(monkeypatch):
+    orig = G.gemv_rows
+    monkeypatch.setattr(oracle, "gemv", lambda w, x, res=None: orig(w, x, np.arange(w.n), None))
+    assert _fails(pins.check_gemv_brute_force, oracle, wl.NVFP4, 4, True)
+
+
+def test_gemv_transposed_operand(monkeypatch):
+    def bad(w, x, res=None):
+        w32 = F.dequant(w).astype(np.float64)
+        v = F.bf16_value(x) @ w32  # W instead of W^T
+        return F.round_to_bf16(v), v
+    monkeypatch.setattr(oracle, "gemv", bad)
+    assert _fails(pins.check_gemv_brute_force, oracle, wl.MXFP4, 1, False)
+
+
+def test_gemv_wrong_sign(monkeypatch):
+    orig = G.gemv_rows
+
+    def bad(w, x, res=None):
+        y, v = orig(w, x, np.arange(w.n), res)
+        return -y, -v
+    monkeypatch.setattr(oracle, "gemv", bad)
+    assert _fails(pins.check_dense_special_case, oracle, wl.MLX_AFFINE4_G64)
+
+
+def test_route_ties_to_higher_index(monkeypatch):
+    def bad(logits, topk):
+        lg = np.asarray(logits, np.float32)[:, ::-1]
+        ids, p = MO.route(lg, topk)
+        return lg.shape[1] - 1 - ids, p
+    monkeypatch.setattr(oracle, "route", bad)
+    assert _fails(pins.check_route_brute_force, oracle)
+
+
+def test_route_softmax_over_all_experts(monkeypatch):
+    def bad(logits, topk):
+        ids, _ = MO.route(logits, topk)
+        lg = np.asarray(logits, np.float64)
+        z = np.exp(lg - lg.max(axis=1, keepdims=True))
+        z = z / z.sum(axis=1, keepdims=True)
+        return ids, np.take_along_axis(z, ids, axis=1)
+    monkeypatch.setattr(oracle, "route", bad)
+    assert _fails(pins.check_route_brute_force, oracle)
+
+
+def test_moe_shared_expert_dropped(monkeypatch):
+    orig = MO.moe_forward
+
+    def bad(layer, x, lg, topk, tokens=None, with_intermediates=False):
+        l2 = wl.MoELayer(layer.fmt, layer.n_experts, layer.hidden, layer.ffn, layer.gate_up, layer.down, None, None)
+        return orig(l2, x, lg, topk, tokens, with_intermediates)
+    monkeypatch.setattr(oracle, "moe_forward", bad)
+    assert _fails(pins.check_moe_composition, oracle)
+
+
+def test_moe_swiglu_swapped(monkeypatch):
+    orig = MO.swiglu_bf16
+    monkeypatch.setattr(MO, "swiglu_bf16", lambda g, u: orig(u, g))
+    assert _fails(pins.check_moe_composition, oracle)
