@@ -1,0 +1,156 @@
+/*
+ * qgemv.h -- C ABI of the GB300 (sm_103a) weight-only quantized GEMV / GEMM library.
+ *
+ * The operation (TurboEXL3 article §2.2, "NVFP4 with 4-bit and with 16-bit
+ * activations", W4A16 case): every weight is expanded from its block-scaled
+ * code inside the multiply, activations stay 16-bit (bf16), products are
+ * accumulated in fp32 and each output is rounded to bf16 once:
+ *
+ *     y[m, n] = bf16( sum_k w[n, k] * x[m, k]  (+ residual[m, n]) )
+ *
+ * Weight formats (TurboEXL3 article §2.1, "Block-scaled 4-bit formats";
+ * Q6_K operand PR #19, "What changed"):
+ *   QG_FMT_MLX_AFFINE4_G64  w = s * code + b; code 0..15; fp16 s, b per 64 weights (4.5 bpw)
+ *   QG_FMT_MXFP4            w = e2m1(code) * 2^(E-127); E8M0 byte E per 32 weights (4.25 bpw)
+ *   QG_FMT_NVFP4            w = ts * e4m3(S) * e2m1(code); E4M3 byte S per 16 weights,
+ *                           one fp32 tensor scale ts (4.5 bpw)
+ *   QG_FMT_Q6K              w = d * sc * (code - 32); code 0..63; int8 sc per 16 weights,
+ *                           fp16 d per 256 weights (6.5625 bpw)
+ *
+ * Conventions shared by every entry point:
+ *   - Matrices are N x K (outputs x inputs).  Activations x are bf16 [m][ldx],
+ *     outputs y and residuals are bf16 [m][ldy] / [m][ldr] (row m = token).
+ *   - Every device pointer must be 16-byte aligned and every leading dimension a
+ *     multiple of 8 elements, else QG_ERR_MISALIGNED.
+ *   - Memory is owned by the caller; the library allocates nothing and keeps no
+ *     mutable global state except a per-device attribute cache filled once.
+ *   - Calls are asynchronous on the given stream (a cudaStream_t passed as
+ *     void*; NULL = legacy default stream).  Argument errors are found on the
+ *     host and returned before anything is launched.  A failed launch returns
+ *     QG_ERR_CUDA.  Outputs are undefined after an error.  No C++ exception
+ *     crosses this boundary.
+ *   - Results are deterministic: every sum runs in a fixed order and no output
+ *     is accumulated with floating-point atomics (TurboEXL3 article §4.4).
+ *
+ * Packed weight layout "T128x64" (written by qg_pack_host, read by every kernel):
+ *   Rows are padded to NP = 128*ceil(N/128) and the inputs to KP = KB*ceil(K/KB),
+ *   KB = 64 (4-bit formats) or 256 (Q6_K).  Tile (q, g) -- rows 128q..128q+127,
+ *   inputs 64g..64g+63 -- has index t = q*KG + g, KG = KP/64.  Padding holds
+ *   zero codes and zero scales.
+ *   codes : TB bytes per tile at t*TB, TB = 4096 (4-bit) or 6144 (Q6_K).  Row r of
+ *           the tile (rt = r/32, lane = r%32) owns the 16-byte chunks at byte
+ *           ((rt*CH + c)*32 + lane)*16, CH = 2 (4-bit) or 3 (Q6_K).
+ *           4-bit, chunk c = 0,1: byte b holds code (64g + 32c + 2b) in its low
+ *           nibble and code (64g + 32c + 2b + 1) in its high nibble.
+ *           Q6_K: chunks 0,1 hold the low nibbles (code & 15) as above; chunk 2 is
+ *           four little-endian 32-bit words, word w holding in nibble j (bits
+ *           4j..4j+3) hi(64g+16w+j) | hi(64g+16w+8+j) << 2, hi(code) = code >> 4.
+ *   scales: 128*SB bytes per tile at t*128*SB, SB bytes for row r at r*SB:
+ *           NVFP4 (SB=4) byte i = E4M3 scale of inputs 64g+16i..+15;
+ *           MXFP4 (SB=2) byte i = E8M0 scale of inputs 64g+32i..+31;
+ *           MLX   (SB=4) fp16 s then fp16 b (little-endian) of the 64-input group;
+ *           Q6_K  (SB=4) byte i = int8 scale of inputs 64g+16i..+15.
+ *   aux   : Q6_K only: fp16 d of inputs 256u..256u+255 for row r of row tile q at
+ *           byte (q*(KG/4) + u)*256 + 2r.  NULL for the other formats.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QG_FMT_MLX_AFFINE4_G64 = 1,
+  QG_FMT_MXFP4 = 2,
+  QG_FMT_NVFP4 = 3,
+  QG_FMT_Q6K = 4
+} qg_format;
+
+typedef enum {
+  QG_OK = 0,
+  QG_ERR_INVALID_ARG = 1,        /* null pointer, bad size or enum, n/k not a multiple of the block */
+  QG_ERR_UNSUPPORTED = 2,        /* valid request this build does not handle (e.g. m out of range) */
+  QG_ERR_MISALIGNED = 3,         /* pointer not 16-byte aligned or leading dimension not a multiple of 8 */
+  QG_ERR_WORKSPACE_TOO_SMALL = 4,
+  QG_ERR_CUDA = 5,               /* a CUDA runtime call or a launch failed */
+  QG_ERR_TIMEOUT = 6             /* a bounded device-side wait gave up (reported via qg_read_device_status) */
+} qg_status;
+
+typedef enum { QG_OUT_F32 = 0, QG_OUT_BF16 = 1 } qg_out_dtype;
+
+/* A packed weight matrix in device memory (layout "T128x64" above).
+ * n, k are the logical sizes; k must be a multiple of the format's block (64 MLX,
+ * 32 MXFP4, 16 NVFP4, 256 Q6_K).  tensor_scale is used by NVFP4 only and must be
+ * 1.0f for the other formats. */
+typedef struct {
+  int32_t fmt;            /* qg_format */
+  int32_t reserved;       /* must be 0 */
+  int64_t n;
+  int64_t k;
+  const void* codes;      /* device, 16-byte aligned */
+  const void* scales;     /* device, 16-byte aligned */
+  const void* aux;        /* device, 16-byte aligned; Q6_K d, NULL otherwise */
+  float tensor_scale;
+  float reserved2;        /* must be 0 */
+} qg_weight;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* qg_status_str(int status);
+
+/* Byte sizes of the packed codes / scales / aux buffers of an n x k matrix
+ * (TurboEXL3 article §2.1 bits per weight; Q6_K operand PR #19: 1.04 GB for the
+ * 248320 x 5120 output layer).  Host only; no GPU needed. */
+qg_status qg_packed_sizes(int fmt, int64_t n, int64_t k,
+                          size_t* codes_bytes, size_t* scales_bytes, size_t* aux_bytes);
+
+/* Host-side packer: logical row-major arrays -> packed layout (host memory).
+ *   logical_codes  : uint8 [n][k], one code per byte (0..15, or 0..63 for Q6_K)
+ *   logical_scales : MLX fp16 s [n][k/64]; MXFP4 uint8 E8M0 [n][k/32];
+ *                    NVFP4 uint8 E4M3 [n][k/16]; Q6_K int8 sc [n][k/16]
+ *   logical_aux    : MLX fp16 b [n][k/64]; Q6_K fp16 d [n][k/256]; NULL otherwise
+ *   codes/scales/aux: outputs sized by qg_packed_sizes (aux NULL unless Q6_K).
+ * Codes out of range return QG_ERR_INVALID_ARG.  No GPU needed. */
+qg_status qg_pack_host(int fmt, int64_t n, int64_t k,
+                       const uint8_t* logical_codes, const void* logical_scales, const void* logical_aux,
+                       void* codes, void* scales, void* aux);
+
+/* Debug / test: dequantise the whole matrix into out [n][ldo] (device).
+ *   QG_OUT_F32 : the exact weight rounded once to fp32 (NVFP4 includes the tensor scale).
+ *   QG_OUT_BF16: the operand the prefill GEMM feeds the tensor cores: for MXFP4 /
+ *                NVFP4 the block-scaled E2M1 value without the tensor scale (exact in
+ *                bf16); for MLX / Q6_K the fp32 weight rounded to bf16. */
+qg_status qg_dequant(const qg_weight* w, int out_dtype, void* out, int64_t ldo, void* stream);
+
+/* Workspace bytes qgemv needs for this shape on the current device (split-K
+ * partial sums and per-row-tile tickets).  The workspace must be zero-filled
+ * before its first use (qg_workspace_init); every successful call leaves it
+ * ready for the next.  One workspace per stream: calls that overlap on the
+ * GPU must not share it. */
+size_t qg_gemv_workspace_size(int fmt, int64_t n, int64_t k, int m);
+
+/* Zero a workspace of `bytes` bytes on `stream` (cudaMemsetAsync). */
+qg_status qg_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/* Read (and clear) the device status word at the start of a workspace: QG_OK, or
+ * QG_ERR_TIMEOUT if a bounded wait inside a kernel gave up.  Synchronises `stream`. */
+qg_status qg_workspace_status(void* workspace, int* status, void* stream);
+
+/* Quantized GEMV for 1..4 activation rows (speculative-verify widths):
+ *   y[m][n] = bf16( sum_k w[n,k] * x[m][k] (+ residual[m][n]) ),  m = 0..m_rows-1.
+ * Each weight is read from memory once for all rows (TurboEXL3 article §4.2: tokens
+ * share one decode; §4.3: 1-4 rows in one launch, the last-arriving block of
+ * an output tile finishes it).  residual may be NULL (ldr ignored).  x, residual
+ * and y must not overlap.  m_rows outside 1..4 returns QG_ERR_UNSUPPORTED. */
+qg_status qgemv(const qg_weight* w, const void* x, int m_rows, int64_t ldx,
+                const void* residual, int64_t ldr, void* y, int64_t ldy,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

@@ -20,7 +20,7 @@ Parity pins for every function live in ``tests/test_oracle_pins.py``.
 """
 from .formats import (  # noqa: F401
     e2m1_value, e8m0_value, e4m3fn_value, bf16_value, bf16_bits_of, round_to_bf16, dequant, dequant_rows,
-    bits_per_weight, q6k_half_operand_bits,
+    bits_per_weight, q6k_half_operand_bits, dequant_operand_bf16,
 )
 from .gemv import gemv, gemv_rows, row_norms, tolerance  # noqa: F401
 from .moe import route, silu, swiglu_bf16, moe_forward, expert_ffn  # noqa: F401

@@ -128,6 +128,21 @@ def dequant_rows(w, rows) -> np.ndarray:
                          w.tensor_scale).astype(np.float32)
 
 
+def dequant_operand_bf16(w) -> np.ndarray:
+    """bf16-exact fp64 values [N, K] of the 16-bit operand a prefill GEMM multiplies
+    (TurboEXL3 article §2.2: W4A16 expands each weight to 16 bits).  MXFP4 and NVFP4:
+    the E2M1 value times its block scale, without the NVFP4 tensor scale (exact in
+    bf16: at most 6 significant bits); MLX affine and Q6_K: the fp32 weight rounded
+    to bf16 (a second rounding, since these weights carry up to 24 bits)."""
+    if w.fmt == MXFP4:
+        v = e2m1_value(w.codes) * np.repeat(e8m0_value(w.scales), BLOCK[MXFP4], axis=1)
+    elif w.fmt == NVFP4:
+        v = e2m1_value(w.codes) * np.repeat(e4m3fn_value(w.scales), BLOCK[NVFP4], axis=1)
+    else:
+        v = dequant(w).astype(np.float64)
+    return round_to_bf16(v)
+
+
 def bits_per_weight(fmt: int) -> float:
     """Storage bits per weight of the logical format: code bits plus the per-block
     scale data spread over the block (TurboEXL3 article §2.1)."""

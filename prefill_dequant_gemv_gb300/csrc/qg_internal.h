@@ -1,0 +1,51 @@
+// Host-side internals shared by the C ABI entry points and the kernel launchers.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/qgemv.h"
+
+namespace qg {
+
+// Geometry of the packed "T128x64" layout.
+struct Geometry {
+  int fmt;
+  int64_t n, k;      // logical
+  int64_t np, kp;    // padded
+  int64_t nt, kg;    // row tiles of 128, input groups of 64
+  int tile_bytes;    // codes per tile
+  int sb;            // scale bytes per row per tile
+};
+bool geometry(int fmt, int64_t n, int64_t k, Geometry* g);
+int format_block(int fmt);  // k must be a multiple of this (64, 32, 16, 256); 0 if unknown
+
+// Per-device attributes, cached once per device.
+struct DeviceInfo {
+  int sms;
+  int max_smem_optin;
+};
+bool device_info(int device, DeviceInfo* out);
+bool current_device_info(DeviceInfo* out);
+
+// GEMV launch plan (persistent stream-K over 128 x 64 tiles).
+struct GemvPlan {
+  int grid;          // CTAs
+  int nslots;        // staged 64-wide activation groups per CTA
+  int stages;        // weight pipeline depth
+  size_t smem;       // dynamic shared memory bytes
+  size_t ws_bytes;   // workspace bytes
+  size_t off_cnt, off_part;  // workspace offsets
+  int64_t units;
+};
+bool plan_gemv(const Geometry& g, int m, const DeviceInfo& dev, GemvPlan* p);
+
+// Launchers (return a qg_status).
+int launch_gemv(const Geometry& g, const qg_weight* w, const void* x, int m, int64_t ldx,
+                const void* res, int64_t ldr, void* y, int64_t ldy, void* ws, const GemvPlan& p,
+                void* stream);
+int launch_dequant(const Geometry& g, const qg_weight* w, int out_dtype, void* out, int64_t ldo, void* stream);
+
+constexpr size_t kWsHeader = 256;  // status word + reserved
+
+}  // namespace qg

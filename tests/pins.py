@@ -308,3 +308,23 @@ def check_moe_composition(o, seed=29):
     eq = np.zeros((3, 6), np.float32)
     _, p = o.route(eq, 6)
     assert np.allclose(p, 1 / 6, rtol=1e-15)
+
+
+def check_operand_bf16(o, fmt, seed=31):
+    """The bf16 prefill operand: exact for the E2M1 formats (rounding changes nothing and
+    the NVFP4 tensor scale times the operand rounds to the fp32 weight); one extra
+    rounding of the fp32 weight for MLX affine and Q6_K."""
+    n, k = (8, 256) if fmt == wl.Q6K else (8, 128)
+    w = wl.weight(fmt, n, k, seed)
+    op = o.dequant_operand_bf16(w)
+    w32 = o.dequant(w).astype(np.float64)
+    if fmt in (wl.MXFP4, wl.NVFP4):
+        exact = np.array([[float(exact_weight(w, i, j) / (Fraction(float(np.float32(w.tensor_scale)))
+                                                            if fmt == wl.NVFP4 else 1)) for j in range(k)]
+                          for i in range(n)])
+        assert np.array_equal(op, exact)
+        ts = float(np.float32(w.tensor_scale)) if fmt == wl.NVFP4 else 1.0
+        assert np.array_equal((op * ts).astype(np.float32).astype(np.float64), w32)
+    else:
+        ref = torch.from_numpy(w32.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+        assert np.array_equal(op, ref)

@@ -1,0 +1,124 @@
+"""The C-ABI library loads, exports every declared symbol, and validates arguments
+on the host (no GPU needed: nothing here launches a kernel)."""
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def q():
+    from prefill_dequant_gemv_gb300 import build as b
+    b.build()
+    import prefill_dequant_gemv_gb300 as q
+    q.lib()
+    return q
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(q\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(q):
+    names = declared_functions()
+    assert "qgemv" in names and "qg_pack_host" in names
+    lib = ctypes.CDLL(q.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(q):
+    assert q.qg_status_str(0) == "QG_OK"
+    assert q.qg_status_str(6) == "QG_ERR_TIMEOUT"
+    assert q.qg_status_str(99) == "QG_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("fmt,bpw", [(wl.MLX_AFFINE4_G64, 4.5), (wl.MXFP4, 4.25), (wl.NVFP4, 4.5), (wl.Q6K, 6.5625)])
+def test_packed_sizes_match_spec_and_bpw(q, fmt, bpw):
+    for n, k in [(1024, 2048), (300, 768), (17408, 5120)]:
+        assert q.qg_packed_sizes(fmt, n, k) == oracle.packed_sizes(fmt, n, k)
+    c, s, a = q.qg_packed_sizes(fmt, 1024, 2048)
+    assert (c + s + a) * 8 / (1024 * 2048) == bpw
+
+
+def test_q6k_output_layer_is_1_04_gb(q):
+    assert round(sum(q.qg_packed_sizes(wl.Q6K, 248320, 5120)) / 1e9, 2) == 1.04
+
+
+@pytest.mark.parametrize("fmt", [wl.MLX_AFFINE4_G64, wl.MXFP4, wl.NVFP4, wl.Q6K])
+@pytest.mark.parametrize("shape", [(128, 256), (300, 768), (1, 256), (129, 512)])
+def test_pack_round_trip_through_oracle_reader(q, fmt, shape):
+    n, k = shape
+    w = wl.weight(fmt, n, k, seed=n + k)
+    c, s, a = q.qg_pack_host(fmt, n, k, w.codes, w.scales, w.aux)
+    lc, ls, la = oracle.unpack(fmt, n, k, c, s, a if a.size else None)
+    assert np.array_equal(lc, w.codes)
+    assert np.array_equal(np.asarray(ls).view(np.uint8), np.asarray(w.scales).view(np.uint8))
+    if w.aux is not None:
+        assert np.array_equal(la.view(np.uint16), w.aux.view(np.uint16))
+    # padding holds zero codes and zero scales
+    fc, fs, fa = oracle.unpack(fmt, n, k, c, s, a if a.size else None, full=True)
+    assert not fc[n:].any() and not fc[:, k:].any()
+
+
+def test_pack_ragged_k_for_small_blocks(q):
+    # NVFP4 K = 208 (13 blocks of 16) and MXFP4 K = 96 pad to whole 64-input groups
+    for fmt, k in [(wl.NVFP4, 208), (wl.MXFP4, 96)]:
+        w = wl.weight(fmt, 130, k, seed=3)
+        c, s, a = q.qg_pack_host(fmt, 130, k, w.codes, w.scales, None)
+        lc, ls, _ = oracle.unpack(fmt, 130, k, c, s)
+        assert np.array_equal(lc, w.codes) and np.array_equal(ls, w.scales)
+
+
+def test_pack_rejects_bad_input(q):
+    w = wl.weight(wl.MLX_AFFINE4_G64, 128, 128, seed=1)
+    bad = w.codes.copy()
+    bad[3, 5] = 16
+    with pytest.raises(q.QGError) as e:
+        q.qg_pack_host(wl.MLX_AFFINE4_G64, 128, 128, bad, w.scales, w.aux)
+    assert e.value.status == 1
+    with pytest.raises(q.QGError):
+        q.qg_packed_sizes(wl.NVFP4, 128, 100)  # K not a multiple of 16
+    with pytest.raises(q.QGError):
+        q.qg_packed_sizes(9, 128, 128)  # unknown format
+
+
+def _desc(q, **kw):
+    d = dict(fmt=wl.NVFP4, reserved=0, n=256, k=256, codes=0x1000, scales=0x2000, aux=None, tensor_scale=1.0,
+             reserved2=0.0)
+    d.update(kw)
+    return q.qg_weight(**d)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt=7), 1), (dict(k=100), 1), (dict(codes=None), 1), (dict(reserved=1), 1),
+    (dict(fmt=wl.MXFP4, tensor_scale=0.5), 1), (dict(fmt=wl.Q6K, k=512, aux=None), 1),
+    (dict(codes=0x1008), 3),
+])
+def test_qgemv_host_validation(q, kw, status):
+    w = _desc(q, **kw)
+    st = q.lib().qgemv(ctypes.byref(w), 0x3000, 1, 256, None, 0, 0x4000, 256, 0x5000, 1 << 20, None)
+    assert st == status
+
+
+def test_qgemv_rejects_bad_rows_and_strides(q):
+    w = _desc(q)
+    L = q.lib()
+    assert L.qgemv(ctypes.byref(w), 0x3000, 0, 256, None, 0, 0x4000, 256, 0x5000, 1 << 20, None) == 2
+    assert L.qgemv(ctypes.byref(w), 0x3000, 5, 256, None, 0, 0x4000, 256, 0x5000, 1 << 20, None) == 2
+    assert L.qgemv(ctypes.byref(w), 0x3000, 1, 260, None, 0, 0x4000, 256, 0x5000, 1 << 20, None) == 3
+    assert L.qgemv(ctypes.byref(w), 0x3008, 1, 256, None, 0, 0x4000, 256, 0x5000, 1 << 20, None) == 3
+    assert L.qgemv(ctypes.byref(w), None, 1, 256, None, 0, 0x4000, 256, 0x5000, 1 << 20, None) == 1
+    assert L.qgemv(ctypes.byref(w), 0x3000, 1, 128, None, 0, 0x4000, 256, 0x5000, 1 << 20, None) == 1

@@ -66,3 +66,8 @@ def test_silu():
 
 def test_moe_chain_composition():
     pins.check_moe_composition(oracle)
+
+
+@pytest.mark.parametrize("fmt", ALL_FMTS)
+def test_bf16_operand(fmt):
+    pins.check_operand_bf16(oracle, fmt)
