@@ -54,10 +54,11 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantArgs a) {
       } else {
         S = e8m0_f32(sp[kq >> 1]);
       }
-      const float2 p[4] = {e2m1x2_f32<0>(wd), e2m1x2_f32<1>(wd), e2m1x2_f32<2>(wd), e2m1x2_f32<3>(wd)};
+      const uint32_t h[4] = {e2m1x2_h2<0>(wd), e2m1x2_h2<1>(wd), e2m1x2_h2<2>(wd), e2m1x2_h2<3>(wd)};
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        float lo = S * p[b].x, hi = S * p[b].y;  // exact: <= 6 significant bits
+        const float2 e = __half22float2(*reinterpret_cast<const __half2*>(&h[b]));
+        float lo = S * e.x, hi = S * e.y;  // exact: <= 6 significant bits
         if (!a.bf16 && FMT == FMT_NVFP4) {
           lo = a.ts * lo;
           hi = a.ts * hi;
@@ -66,41 +67,43 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantArgs a) {
         o[2 * b + 1] = hi;
       }
     } else {
-      float2 p[4];
+      // the GEMV's f16 operands: op0 = (n0, n4) and op2 = (n2, n6) are 1 + code/1024,
+      // op1 = (n1, n5) and op3 = (n3, n7) are 1 + code/64
+      uint32_t op[4];
+      const uint32_t r = rot8(wd);
       if (FMT == FMT_MLX) {
-        p[0] = int4_pair(wd);
-        p[1] = int4_pair(rot8(wd));
-        p[2] = int4_pair(rot16(wd));
-        p[3] = int4_pair(rot24(wd));
+        op[0] = i4_op_lo(wd);
+        op[1] = i4_op_hi(wd);
+        op[2] = i4_op_lo(r);
+        op[3] = i4_op_hi(r);
       } else {
         const uint32_t hw = *reinterpret_cast<const uint32_t*>(tc + ((rt * 3 + 2) * 32 + lane) * 16 + kq * 4);
-        const uint32_t h = q6k_hi_for(hw, wi);
-        p[0] = int6_pair(wd, h);
-        p[1] = int6_pair(rot8(wd), rot8(h));
-        p[2] = int6_pair(rot16(wd), rot16(h));
-        p[3] = int6_pair(rot24(wd), rot24(h));
+        const uint32_t hh = q6k_hi_for(hw, wi), hr = rot8(hh);
+        op[0] = i6_op_lo(wd, hh);
+        op[1] = i6_op_hi(wd, hh);
+        op[2] = i6_op_lo(r, hr);
+        op[3] = i6_op_hi(r, hr);
       }
-      // operand pair r holds nibbles (3+2r)%8 (class 12) and (4+2r)%8 (class 16)
+      float code[8];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float codeo = (p[r].x - 1.0f) * kClass12;  // exact
-        const float codee = (p[r].y - 1.0f) * kClass16;
-        float wo, we;
+      for (int j = 0; j < 4; ++j) {
+        const float2 e = __half22float2(*reinterpret_cast<const __half2*>(&op[j]));
+        const float mul = (j & 1) ? 64.0f : 1024.0f;
+        code[j] = (e.x - 1.0f) * mul;  // exact
+        code[j + 4] = (e.y - 1.0f) * mul;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
         if (FMT == FMT_MLX) {
           const uint32_t sw = *reinterpret_cast<const uint32_t*>(sp);
           const float s = __half2float(__ushort_as_half((unsigned short)(sw & 0xFFFFu)));
           const float bias = __half2float(__ushort_as_half((unsigned short)(sw >> 16)));
-          wo = fmaf(s, codeo, bias);
-          we = fmaf(s, codee, bias);
+          o[j] = fmaf(s, code[j], bias);
         } else {
           const float sc = (float)(int8_t)sp[kq];
           const float d = __half2float(*reinterpret_cast<const __half*>(a.aux + (q * (a.kg / 4) + g / 4) * 256 + row * 2));
-          const float ds = d * sc;
-          wo = ds * (codeo - 32.0f);
-          we = ds * (codee - 32.0f);
+          o[j] = (d * sc) * (code[j] - 32.0f);
         }
-        o[(3 + 2 * r) % 8] = wo;
-        o[(4 + 2 * r) % 8] = we;
       }
     }
   }

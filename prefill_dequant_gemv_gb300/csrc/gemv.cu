@@ -30,10 +30,9 @@
 
 namespace qg {
 
-constexpr int kCW = 12;                 // consumer warps (13 warps in all -> 128 registers)
-constexpr int kCT = kCW * 32;           // consumer threads
-constexpr int kGemvThreads = kCT + 32;  // + one producer warp
-constexpr int kGroups = kCW / 4;        // unit groups (4 warps: one per 16-input quarter)
+// Consumer warps: 16 for 1-2 rows; 12 for 3-4 rows, whose accumulators need the
+// 128 registers a 13-warp CTA allows (warps are allocated in groups of four).
+__host__ __device__ constexpr int consumer_warps(int m) { return m >= 3 ? 12 : 16; }
 constexpr int kMaxStages = 48;
 
 struct GemvArgs {
@@ -55,18 +54,24 @@ struct GemvArgs {
   int* status;
 };
 
+// One pipeline stage holds a chunk of C consecutive units (tile index = unit index,
+// so a chunk is one contiguous range of codes and one of scales): a single bulk
+// copy per array per chunk keeps the copy engine at HBM speed, which 4-6 KB
+// copies do not reach.
 template <int FMT> struct Stage {
-  static constexpr int CODE = Fmt<FMT>::TB;
-  static constexpr int SCALE = 128 * Fmt<FMT>::SB;
-  static constexpr int AUX = (FMT == FMT_Q6K) ? 256 : 0;
-  static constexpr int BYTES = CODE + SCALE + AUX;
+  static constexpr int CODE = Fmt<FMT>::TB;            // per unit
+  static constexpr int SCALE = 128 * Fmt<FMT>::SB;     // per unit
+  static constexpr int AUX = (FMT == FMT_Q6K) ? 256 : 0;  // per 4 units (Q6_K d)
+  __host__ __device__ static constexpr int bytes(int C) { return C * (CODE + SCALE) + 2 * AUX; }
 };
 
 struct SmemLayout {
-  size_t bars, stages, xs, sums, red, flag, total;
+  size_t bars, stages, xs, sums, red, lut, misc, total;
 };
 
 __host__ __device__ inline SmemLayout gemv_smem_layout(int stage_bytes, int S, int M, int nslots) {
+  // stage_bytes: bytes of one chunk stage
+  const int kCW = consumer_warps(M);
   SmemLayout L;
   size_t o = 0;
   L.bars = o;
@@ -76,13 +81,15 @@ __host__ __device__ inline SmemLayout gemv_smem_layout(int stage_bytes, int S, i
   o += (size_t)S * stage_bytes;
   o = (o + 127) & ~(size_t)127;
   L.xs = o;
-  o += (size_t)M * nslots * 64 * 4;
+  o += (size_t)M * nslots * 64 * 2;  // f16 activations
   L.sums = o;
   o += (size_t)M * nslots * 8 * 4;  // (Z, X) per 16-input quarter
   L.red = o;
   o += (size_t)kCW * M * 128 * 4;
-  L.flag = o;
-  o += 16;
+  L.lut = o;
+  o += 256 * 4;  // E4M3 -> fp32
+  L.misc = o;
+  o += 64;  // inv_scale[4], maxbits[4], flag
   L.total = o;
   return L;
 }
@@ -97,62 +104,110 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t v, float& lo, float& hi) 
   hi = __uint_as_float(v & 0xFFFF0000u);
 }
 
-// Stage x rows (bf16) into shared memory as fp32, 16 inputs per item.  Integer
-// formats store each group of eight in the operand-pair order [3,4,5,6,7,0,1,2]
-// and record, per 16-input quarter, Z = c12 * X_odd + c16 * X_even and X = X_odd +
-// X_even (sums over odd / even input positions), which remove the operands'
-// constant 1 and the zero point in the fold.
-template <int FMT, int M>
-__device__ void stage_x(const GemvArgs& a, float* xs, float* sums, int sbase, int nslots, int tid) {
+// Stage the activation rows into shared memory as f16, exactly: each CTA scales
+// row m by a power of two 2^P_m chosen from the largest |x| it stages, so every
+// bf16 value (8 significant bits) lands inside f16's range; values more than
+// 2^27 below that maximum would round, which the stated tolerance dwarfs.  The
+// partial sums are scaled back by 2^-P_m before they leave the CTA.
+// Layout per 8 inputs (one code word) and row m: four f16x2 words in the order the
+// decoder produces operand pairs -- E2M1: (x0,x1) (x2,x3) (x4,x5) (x6,x7); integer
+// formats: (16x0,16x4) (x1,x5) (16x2,16x6) (x3,x7).  Integer formats also record,
+// per 16-input quarter, Z and X that remove the operand constant and zero point.
+template <int FMT, int M, int kCT>
+__device__ void stage_x(const GemvArgs& a, uint32_t* xs, float* sums, float* inv_scale, int* maxbits, int sbase,
+                        int nslots, int tid) {
   constexpr bool kInt = (FMT == FMT_MLX || FMT == FMT_Q6K);
-  constexpr float c12 = (FMT == FMT_Q6K) ? 2080.0f : 2048.0f;  // 2^11 (+32 for the Q6_K zero point)
-  constexpr float c16 = (FMT == FMT_Q6K) ? 160.0f : 128.0f;    // 2^7  (+32)
   const int items = M * nslots * 4;
+  if (tid < M) maxbits[tid] = 0;
+  named_sync(1, kCT);
+  uint32_t lm[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) lm[m] = 0;
   for (int it = tid; it < items; it += kCT) {
-    const int kq = it & 3;
-    const int s = (it >> 2) % nslots;
-    const int m = (it >> 2) / nslots;
-    const int g = (sbase + s) % a.KG;
-    const int64_t k0 = (int64_t)g * 64 + kq * 16;
+    const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
+    const int64_t k0 = (int64_t)((sbase + s) % a.KG) * 64 + kq * 16;
+    if (k0 >= a.k) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + m * a.ldx + k0);
+    const uint4 r0 = src[0], r1 = src[1];
+    const uint32_t u[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx = max(mx, max(u[i] & 0x7FFFu, (u[i] >> 16) & 0x7FFFu));
+#pragma unroll
+    for (int mm = 0; mm < M; ++mm)
+      if (mm == m) lm[mm] = max(lm[mm], mx);
+  }
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const uint32_t v = __reduce_max_sync(0xFFFFFFFFu, lm[m]);
+    if ((tid & 31) == 0 && v) atomicMax(&maxbits[m], (int)v);
+  }
+  named_sync(1, kCT);
+  float scale[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const int mb = maxbits[m];
+    const int e = mb >= 0x80 ? (mb >> 7) - 127 : -127;
+    int P = (kInt ? 10 : 14) - e;
+    if (mb >= 0x7F80) P = 0;  // inf / nan: leave as is
+    P = max(-126, min(126, P));
+    scale[m] = __uint_as_float((uint32_t)(P + 127) << 23);
+    if (tid == 0) inv_scale[m] = __uint_as_float((uint32_t)(127 - P) << 23);
+  }
+  for (int it = tid; it < items; it += kCT) {
+    const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
+    const int64_t k0 = (int64_t)((sbase + s) % a.KG) * 64 + kq * 16;
     float v[16];
     if (k0 < a.k) {
       const uint4* src = reinterpret_cast<const uint4*>(a.x + m * a.ldx + k0);
       const uint4 r0 = src[0], r1 = src[1];
       const uint32_t u[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) bf16x2_to_f32(u[i], v[2 * i], v[2 * i + 1]);
+      for (int i = 0; i < 8; ++i) {
+        float lo, hi;
+        bf16x2_to_f32(u[i], lo, hi);
+        v[2 * i] = __half2float(__float2half_rn(lo * scale[m]));
+        v[2 * i + 1] = __half2float(__float2half_rn(hi * scale[m]));
+      }
     } else {
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] = 0.0f;
     }
-    float* dst = xs + (size_t)(m * nslots + s) * 64 + kq * 16;
+    uint32_t* dst = xs + (size_t)(m * nslots + s) * 32 + kq * 8;
+    auto h2 = [](float lo, float hi) {
+      __half2 h = __floats2half2_rn(lo, hi);
+      return *reinterpret_cast<uint32_t*>(&h);
+    };
     if (kInt) {
-      float xo = 0.0f, xe = 0.0f;
+      float x16 = 0.0f, x1 = 0.0f;
 #pragma unroll
       for (int w = 0; w < 2; ++w) {
-        const float* s8 = v + 8 * w;
-        reinterpret_cast<float4*>(dst)[2 * w] = make_float4(s8[3], s8[4], s8[5], s8[6]);
-        reinterpret_cast<float4*>(dst)[2 * w + 1] = make_float4(s8[7], s8[0], s8[1], s8[2]);
-        xo += (s8[1] + s8[3]) + (s8[5] + s8[7]);
-        xe += (s8[0] + s8[2]) + (s8[4] + s8[6]);
+        const float* q = v + 8 * w;
+        reinterpret_cast<uint4*>(dst)[w] = make_uint4(h2(16.0f * q[0], 16.0f * q[4]), h2(q[1], q[5]),
+                                                      h2(16.0f * q[2], 16.0f * q[6]), h2(q[3], q[7]));
+        x16 += (q[0] + q[4]) + (q[2] + q[6]);
+        x1 += (q[1] + q[5]) + (q[3] + q[7]);
       }
       float* z = sums + ((size_t)(m * nslots + s) * 4 + kq) * 2;
-      z[0] = c12 * xo + c16 * xe;
-      z[1] = xo + xe;
+      const float xsum = x16 + x1;                // X'
+      const float xop = fmaf(16.0f, x16, x1);     // X'' = sum of the staged operands' partners
+      z[0] = (FMT == FMT_Q6K) ? fmaf(64.0f, xop, 32.0f * xsum) : 64.0f * xop;
+      z[1] = xsum;
     } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      for (int i = 0; i < 2; ++i)
+        reinterpret_cast<uint4*>(dst)[i] = make_uint4(h2(v[8 * i], v[8 * i + 1]), h2(v[8 * i + 2], v[8 * i + 3]),
+                                                      h2(v[8 * i + 4], v[8 * i + 5]), h2(v[8 * i + 6], v[8 * i + 7]));
     }
   }
 }
 
 // One consumer warp, one unit, one 16-input quarter: accumulate 4 rows x M.
 template <int FMT, int M>
-__device__ __forceinline__ void consume(const uint8_t* st, const float* xq, int mstride, const float* sq,
-                                        int sstride, int kq, int lane, float (&acc)[4][M]) {
+__device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, const uint8_t* aux, const uint32_t* xq,
+                                        int mstride, const float* sq, int sstride, const float* e4m3_lut, int kq,
+                                        int lane, float (&acc)[4][M]) {
   using F = Fmt<FMT>;
-  using SG = Stage<FMT>;
   uint32_t wd[4][2];
   uint32_t hw[4];
 #pragma unroll
@@ -162,47 +217,53 @@ __device__ __forceinline__ void consume(const uint8_t* st, const float* xq, int 
     wd[rt][1] = v.y;
     if (FMT == FMT_Q6K) hw[rt] = *reinterpret_cast<const uint32_t*>(st + ((rt * 3 + 2) * 32 + lane) * 16 + kq * 4);
   }
-  float2 P[4][M];
+  float P[4][M][2];
 #pragma unroll
   for (int rt = 0; rt < 4; ++rt)
 #pragma unroll
-    for (int m = 0; m < M; ++m) P[rt][m] = make_float2(0.0f, 0.0f);
+    for (int m = 0; m < M; ++m) P[rt][m][0] = P[rt][m][1] = 0.0f;
 
 #pragma unroll
   for (int wi = 0; wi < 2; ++wi) {
-    float4 xa[M], xb[M];
+    uint4 X[M];
 #pragma unroll
-    for (int m = 0; m < M; ++m) {
-      xa[m] = *reinterpret_cast<const float4*>(xq + m * mstride + wi * 8);
-      xb[m] = *reinterpret_cast<const float4*>(xq + m * mstride + wi * 8 + 4);
-    }
+    for (int m = 0; m < M; ++m) X[m] = *reinterpret_cast<const uint4*>(xq + m * mstride + wi * 4);
 #pragma unroll
     for (int rt = 0; rt < 4; ++rt) {
       const uint32_t w = wd[rt][wi];
-      float2 p0, p1, p2, p3;
+      uint32_t o0, o1, o2, o3;
       if (FMT == FMT_MXFP4 || FMT == FMT_NVFP4) {
-        p0 = e2m1x2_f32<0>(w);
-        p1 = e2m1x2_f32<1>(w);
-        p2 = e2m1x2_f32<2>(w);
-        p3 = e2m1x2_f32<3>(w);
+        o0 = e2m1x2_h2<0>(w);
+        o1 = e2m1x2_h2<1>(w);
+        o2 = e2m1x2_h2<2>(w);
+        o3 = e2m1x2_h2<3>(w);
       } else if (FMT == FMT_MLX) {
-        p0 = int4_pair(w);
-        p1 = int4_pair(rot8(w));
-        p2 = int4_pair(rot16(w));
-        p3 = int4_pair(rot24(w));
+        const uint32_t r = rot8(w);
+        o0 = i4_op_lo(w);
+        o1 = i4_op_hi(w);
+        o2 = i4_op_lo(r);
+        o3 = i4_op_hi(r);
       } else {
         const uint32_t h = q6k_hi_for(hw[rt], wi);
-        p0 = int6_pair(w, h);
-        p1 = int6_pair(rot8(w), rot8(h));
-        p2 = int6_pair(rot16(w), rot16(h));
-        p3 = int6_pair(rot24(w), rot24(h));
+        const uint32_t r = rot8(w), hr = rot8(h);
+        o0 = i6_op_lo(w, h);
+        o1 = i6_op_hi(w, h);
+        o2 = i6_op_lo(r, hr);
+        o3 = i6_op_hi(r, hr);
       }
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        P[rt][m] = ffma2(p0, make_float2(xa[m].x, xa[m].y), P[rt][m]);
-        P[rt][m] = ffma2(p1, make_float2(xa[m].z, xa[m].w), P[rt][m]);
-        P[rt][m] = ffma2(p2, make_float2(xb[m].x, xb[m].y), P[rt][m]);
-        P[rt][m] = ffma2(p3, make_float2(xb[m].z, xb[m].w), P[rt][m]);
+        float p0 = P[rt][m][0], p1 = P[rt][m][1];
+        p0 = hfma_lo(o0, X[m].x, p0);
+        p1 = hfma_hi(o0, X[m].x, p1);
+        p0 = hfma_lo(o1, X[m].y, p0);
+        p1 = hfma_hi(o1, X[m].y, p1);
+        p0 = hfma_lo(o2, X[m].z, p0);
+        p1 = hfma_hi(o2, X[m].z, p1);
+        p0 = hfma_lo(o3, X[m].w, p0);
+        p1 = hfma_hi(o3, X[m].w, p1);
+        P[rt][m][0] = p0;
+        P[rt][m][1] = p1;
       }
     }
   }
@@ -210,33 +271,31 @@ __device__ __forceinline__ void consume(const uint8_t* st, const float* xq, int 
 #pragma unroll
   for (int rt = 0; rt < 4; ++rt) {
     const int row = rt * 32 + lane;
-    const uint8_t* sp = st + SG::CODE + row * F::SB;
+    const uint8_t* sp = scl + row * F::SB;
     if (FMT == FMT_NVFP4) {
-      const uint32_t sw = *reinterpret_cast<const uint32_t*>(sp);
-      const float2 s01 = (kq >> 1) ? e4m3x2_f32<1>(sw) : e4m3x2_f32<0>(sw);
-      const float S = (kq & 1) ? s01.y : s01.x;
+      const float S = e4m3_lut[sp[kq]];
 #pragma unroll
-      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S, P[rt][m].x + P[rt][m].y, acc[rt][m]);
+      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S, P[rt][m][0] + P[rt][m][1], acc[rt][m]);
     } else if (FMT == FMT_MXFP4) {
       const float S = e8m0_f32(sp[kq >> 1]);
 #pragma unroll
-      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S, P[rt][m].x + P[rt][m].y, acc[rt][m]);
+      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S, P[rt][m][0] + P[rt][m][1], acc[rt][m]);
     } else if (FMT == FMT_MLX) {
       const uint32_t sw = *reinterpret_cast<const uint32_t*>(sp);
       const float s = __half2float(__ushort_as_half((unsigned short)(sw & 0xFFFFu)));
       const float bias = __half2float(__ushort_as_half((unsigned short)(sw >> 16)));
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        const float dot = fmaf(kClass12, P[rt][m].x, fmaf(kClass16, P[rt][m].y, -sq[m * sstride]));
+        const float dot = fmaf(64.0f, P[rt][m][0] + P[rt][m][1], -sq[m * sstride]);
         acc[rt][m] = fmaf(s, dot, fmaf(bias, sq[m * sstride + 1], acc[rt][m]));
       }
     } else {
       const float sc = (float)(int8_t)sp[kq];
-      const float d = __half2float(*reinterpret_cast<const __half*>(st + SG::CODE + SG::SCALE + row * 2));
+      const float d = __half2float(*reinterpret_cast<const __half*>(aux + row * 2));
       const float ds = d * sc;
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        const float dot = fmaf(kClass12, P[rt][m].x, fmaf(kClass16, P[rt][m].y, -sq[m * sstride]));
+        const float dot = fmaf(64.0f, P[rt][m][0] + P[rt][m][1], -sq[m * sstride]);
         acc[rt][m] = fmaf(ds, dot, acc[rt][m]);
       }
     }
@@ -244,9 +303,9 @@ __device__ __forceinline__ void consume(const uint8_t* st, const float* xq, int 
 }
 
 template <int M>
-__device__ __forceinline__ void finish_out(const GemvArgs& a, int64_t q, int e, float v) {
+__device__ __forceinline__ void finish_out(const GemvArgs& a, uint32_t q, int e, float v) {
   const int m = e / 128, row = e % 128;
-  const int64_t n = q * 128 + row;
+  const int64_t n = (int64_t)q * 128 + row;
   if (n >= a.n) return;
   float r = a.ts * v;
   if (a.res) r += __bfloat162float(a.res[m * a.ldr + n]);
@@ -254,18 +313,24 @@ __device__ __forceinline__ void finish_out(const GemvArgs& a, int64_t q, int e, 
 }
 
 template <int FMT, int M>
-__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(const GemvArgs a) {
+  constexpr int kCW = consumer_warps(M);  // consumer warps
+  constexpr int kCT = kCW * 32;           // consumer threads (one producer warp follows)
+  constexpr int kGroups = kCW / 4;        // unit groups (4 warps: one per 16-input quarter)
   extern __shared__ __align__(128) uint8_t smem[];
   using SG = Stage<FMT>;
   const int S = a.stages, nslots = a.nslots;
-  const SmemLayout L = gemv_smem_layout(SG::BYTES, S, M, nslots);
+  const SmemLayout L = gemv_smem_layout(Stage<FMT>::bytes(consumer_warps(M) / 4), S, M, nslots);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + S;
   uint8_t* stages = smem + L.stages;
-  float* xs = reinterpret_cast<float*>(smem + L.xs);
+  uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.xs);
   float* sums = reinterpret_cast<float*>(smem + L.sums);
   float* red = reinterpret_cast<float*>(smem + L.red);
-  int* flag = reinterpret_cast<int*>(smem + L.flag);
+  float* lut = reinterpret_cast<float*>(smem + L.lut);
+  float* inv_scale = reinterpret_cast<float*>(smem + L.misc);
+  int* maxbits = reinterpret_cast<int*>(smem + L.misc + 16);
+  int* flag = reinterpret_cast<int*>(smem + L.misc + 32);
 
   const int64_t U = a.U;
   const int64_t G = gridDim.x;
@@ -277,63 +342,101 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a)
   const int sbase = len >= KG ? 0 : (int)(u0 % KG);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  constexpr int C = kGroups;  // units per chunk: one per unit group
+  const int SB = Stage<FMT>::bytes(C);
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4);
+      mbar_init(&empty[s], kCW);  // every consumer warp releases each chunk once
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kCW) {  // producer: stream whole tiles into the ring
+  // All loop indices below are 32-bit and advanced incrementally (the host
+  // guarantees fewer than 2^31 units): 64-bit division in the per-unit path costs
+  // more than the decode itself.
+  const uint32_t uu0 = (uint32_t)u0, uu1 = (uint32_t)u1;
+  const int nch = (int)((len + C - 1) / C);
+  if (warp == kCW) {  // producer: stream chunks of whole tiles into the ring
     if (lane == 0) {
-      for (int64_t i = 0; i < len; ++i) {
-        const int s = (int)(i % S);
-        const uint32_t use = (uint32_t)(i / S);
-        if (use > 0 && !mbar_wait_bounded(&empty[s], (use - 1) & 1, a.status)) break;
-        const int64_t uu = u0 + i, q = uu / KG;
-        const int g = (int)(uu % KG);
-        const int64_t t = q * KG + g;
-        uint8_t* dst = stages + (size_t)s * SG::BYTES;
-        mbar_arrive_expect_tx(&full[s], SG::BYTES);
-        bulk_g2s(dst, a.codes + t * SG::CODE, SG::CODE, &full[s]);
-        bulk_g2s(dst + SG::CODE, a.scales + t * SG::SCALE, SG::SCALE, &full[s]);
-        if (SG::AUX) bulk_g2s(dst + SG::CODE + SG::SCALE, a.aux + (q * (KG / 4) + g / 4) * 256, 256, &full[s]);
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t ua = uu0;
+      for (int j = 0; j < nch; ++j) {
+        if (j >= S && !mbar_wait_bounded(&empty[s], ph ^ 1u, a.status)) break;
+        const uint32_t ub = min(uu1, ua + C);
+        const uint32_t nu = ub - ua;
+        uint8_t* dst = stages + (size_t)s * SB;
+        uint32_t bytes = nu * (SG::CODE + SG::SCALE);
+        uint32_t aux_a = 0, aux_n = 0;
+        if (SG::AUX) {
+          aux_a = ua >> 2;
+          aux_n = ((ub - 1) >> 2) - aux_a + 1;
+          bytes += aux_n * SG::AUX;
+        }
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_g2s(dst, a.codes + (size_t)ua * SG::CODE, nu * SG::CODE, &full[s]);
+        bulk_g2s(dst + C * SG::CODE, a.scales + (size_t)ua * SG::SCALE, nu * SG::SCALE, &full[s]);
+        if (SG::AUX)
+          bulk_g2s(dst + C * (SG::CODE + SG::SCALE), a.aux + (size_t)aux_a * SG::AUX, aux_n * SG::AUX, &full[s]);
+        ua = ub;
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
     }
     return;
   }
 
-  stage_x<FMT, M>(a, xs, sums, sbase, nslots, tid);
+  if (FMT == FMT_NVFP4 && tid < 128) {  // E4M3 -> fp32 table (exact), two entries per thread
+    const float2 v = e4m3x2_f32<0>((uint32_t)(2 * tid) | ((uint32_t)(2 * tid + 1) << 8));
+    lut[2 * tid] = v.x;
+    lut[2 * tid + 1] = v.y;
+  }
+  stage_x<FMT, M, kCT>(a, xs, sums, inv_scale, maxbits, sbase, nslots, tid);
   named_sync(1, kCT);
 
+  // This warp's units: relative index i = C * chunk + ug, one per chunk, processed
+  // in order; (stage, parity, activation slot) advance incrementally.
   const int ug = warp >> 2, kq = warp & 3;
   bool ok = true;
-  int64_t u = u0;
-  while (u < u1) {
-    const int64_t q = u / KG;
-    const int64_t seg_end = min(u1, (q + 1) * KG);
+  uint32_t i = (uint32_t)ug;
+  int s = 0;
+  uint32_t ph = 0;
+  int slot = (int)((uu0 + i) % (uint32_t)KG) - sbase;
+  if (slot < 0) slot += KG;
+  const uint8_t* xq_base = reinterpret_cast<const uint8_t*>(xs) + kq * 32;
+  const float* sq_base = sums + kq * 2;
+  uint32_t u = uu0;
+  while (u < uu1) {
+    const uint32_t q = u / (uint32_t)KG;
+    const uint32_t seg_end = min(uu1, (q + 1) * (uint32_t)KG);
     float acc[4][M];
 #pragma unroll
     for (int rt = 0; rt < 4; ++rt)
 #pragma unroll
       for (int m = 0; m < M; ++m) acc[rt][m] = 0.0f;
-    int64_t i = u - u0;
-    i += (ug - (int)(i % kGroups) + kGroups) % kGroups;
-    for (; ok && i < seg_end - u0; i += kGroups) {
-      const int s = (int)(i % S);
-      const uint32_t use = (uint32_t)(i / S);
-      if (!mbar_wait_bounded(&full[s], use & 1, a.status)) {
+    for (; ok && uu0 + i < seg_end; i += C) {
+      if (!mbar_wait_bounded(&full[s], ph, a.status)) {
         ok = false;
         break;
       }
-      const int g = (int)((u0 + i) % KG);
-      const int slot = (g - sbase + KG) % KG;
-      consume<FMT, M>(stages + (size_t)s * SG::BYTES, xs + (size_t)slot * 64 + kq * 16, nslots * 64,
-                      sums + ((size_t)slot * 4 + kq) * 2, nslots * 8, kq, lane, acc);
+      const uint8_t* st = stages + (size_t)s * SB;
+      const uint32_t uu = uu0 + i;
+      const uint8_t* aux = st + C * (SG::CODE + SG::SCALE) + ((uu >> 2) - ((uu - ug) >> 2)) * SG::AUX;
+      consume<FMT, M>(st + ug * SG::CODE, st + C * SG::CODE + ug * SG::SCALE, aux,
+                      reinterpret_cast<const uint32_t*>(xq_base + (size_t)slot * 128), nslots * 32,
+                      sq_base + (size_t)slot * 8, nslots * 8, lut, kq, lane, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
+      slot += C;
+      while (slot >= KG) slot -= KG;
     }
 #pragma unroll
     for (int rt = 0; rt < 4; ++rt)
@@ -341,34 +444,51 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a)
       for (int m = 0; m < M; ++m) red[(warp * M + m) * 128 + rt * 32 + lane] = acc[rt][m];
     named_sync(1, kCT);
 
-    const bool whole = (u == q * KG) && (seg_end == (q + 1) * KG);
-    const int slot_ws = (u == u0) ? 0 : 1;
+    const bool whole = (u == q * (uint32_t)KG) && (seg_end == (q + 1) * (uint32_t)KG);
+    const int slot_ws = (u == uu0) ? 0 : 1;
     for (int e = tid; e < M * 128; e += kCT) {
       float v = 0.0f;
 #pragma unroll 4
       for (int w2 = 0; w2 < kCW; ++w2) v += red[w2 * M * 128 + e];
+      v *= inv_scale[e / 128];  // exact: undo this CTA's activation scaling
       if (whole)
         finish_out<M>(a, q, e, v);
       else
         a.ws_part[(size_t)((b * 2 + slot_ws) * M) * 128 + e] = v;
     }
     if (!whole) {
-      __threadfence();
+      // Publish the partial (CTA barrier, then one gpu-scope fence before the ticket);
+      // the CTA that takes the last ticket sums all partials of the row tile in CTA
+      // order.  Its first contributor may hold the tile as its last segment (slot 1);
+      // every later contributor starts inside the tile (slot 0).
       named_sync(1, kCT);
-      const int64_t bf = owner_cta(q * KG, U, G), bl = owner_cta((q + 1) * KG - 1, U, G);
+      const int64_t qk = (int64_t)q * KG;
+      const int64_t bf = owner_cta(qk, U, G), bl = owner_cta(qk + KG - 1, U, G);
       if (tid == 0) {
+        __threadfence();
         const int old = atomicAdd(&a.ws_cnt[q], 1);
+        __threadfence();
         *flag = (old == (int)(bl - bf)) ? 1 : 0;
       }
       named_sync(1, kCT);
       if (*flag) {
-        __threadfence();
+        const int first_sl = (bf * U / G < qk) ? 1 : 0;
+        const int nc = (int)(bl - bf + 1);
+        const float* part = a.ws_part + (size_t)(bf * 2) * M * 128;
         for (int e = tid; e < M * 128; e += kCT) {
-          float v = 0.0f;
-          for (int64_t bb = bf; bb <= bl; ++bb) {
-            const int sl = ((bb * U / G) / KG == q) ? 0 : 1;
-            v += __ldcg(&a.ws_part[(size_t)((bb * 2 + sl) * M) * 128 + e]);
+          float v = __ldcg(part + (size_t)first_sl * M * 128 + e);
+          int c = 1;
+          for (; c + 4 <= nc; c += 4) {  // independent loads, summed in order
+            const float v0 = __ldcg(part + (size_t)(2 * c) * M * 128 + e);
+            const float v1 = __ldcg(part + (size_t)(2 * c + 2) * M * 128 + e);
+            const float v2 = __ldcg(part + (size_t)(2 * c + 4) * M * 128 + e);
+            const float v3 = __ldcg(part + (size_t)(2 * c + 6) * M * 128 + e);
+            v += v0;
+            v += v1;
+            v += v2;
+            v += v3;
           }
+          for (; c < nc; ++c) v += __ldcg(part + (size_t)(2 * c) * M * 128 + e);
           finish_out<M>(a, q, e, v);
         }
         if (tid == 0) a.ws_cnt[q] = 0;
@@ -380,18 +500,21 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a)
 }
 
 // ---------------------------------------------------------------- host side
-static int stage_bytes_of(int fmt) {
+static int stage_bytes_of(int fmt, int m) {
+  const int C = consumer_warps(m) / 4;
   switch (fmt) {
-    case FMT_MLX: return Stage<FMT_MLX>::BYTES;
-    case FMT_MXFP4: return Stage<FMT_MXFP4>::BYTES;
-    case FMT_NVFP4: return Stage<FMT_NVFP4>::BYTES;
-    default: return Stage<FMT_Q6K>::BYTES;
+    case FMT_MLX: return Stage<FMT_MLX>::bytes(C);
+    case FMT_MXFP4: return Stage<FMT_MXFP4>::bytes(C);
+    case FMT_NVFP4: return Stage<FMT_NVFP4>::bytes(C);
+    default: return Stage<FMT_Q6K>::bytes(C);
   }
 }
 
 bool plan_gemv(const Geometry& g, int m, const DeviceInfo& dev, GemvPlan* p) {
-  const int sbytes = stage_bytes_of(g.fmt);
+  const int sbytes = stage_bytes_of(g.fmt, m);
+  const int C = consumer_warps(m) / 4;
   const int64_t U = g.nt * g.kg;
+  if (U >= (int64_t(1) << 31)) return false;
   const size_t budget = (size_t)dev.max_smem_optin;
   int64_t G = std::min<int64_t>(dev.sms, U);
   for (;;) {
@@ -400,7 +523,7 @@ bool plan_gemv(const Geometry& g, int m, const DeviceInfo& dev, GemvPlan* p) {
     const SmemLayout L0 = gemv_smem_layout(sbytes, 2, m, nslots);
     if (L0.total <= budget || G >= U) {
       if (L0.total > budget) return false;
-      int S = (int)std::min<int64_t>(len, (int64_t)kMaxStages);
+      int S = (int)std::min<int64_t>((len + C - 1) / C, (int64_t)kMaxStages);
       S = std::max(S, 2);
       while (S > 2 && gemv_smem_layout(sbytes, S, m, nslots).total > budget) --S;
       p->grid = (int)G;
@@ -430,7 +553,7 @@ static int launch_t(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
       return QG_ERR_CUDA;
     configured.fetch_or(bit);
   }
-  gemv_kernel<FMT, M><<<p.grid, kGemvThreads, p.smem, s>>>(a);
+  gemv_kernel<FMT, M><<<p.grid, consumer_warps(M) * 32 + 32, p.smem, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 

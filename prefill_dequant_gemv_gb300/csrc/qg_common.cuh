@@ -1,16 +1,18 @@
 // Device-side building blocks shared by the kernels of the quantized GEMV / GEMM
 // library: format traits of the packed "T128x64" layout, streaming loads, and the
-// in-register decoders that turn packed codes into fp32 operands.
+// in-register decoders that turn packed codes into exact f16 operands.
 //
 // Decoders (TurboEXL3 article §2.1 formats; Q6_K operand PR #19, "What changed"):
-//  * E2M1 (MXFP4, NVFP4): the hardware e2m1x2 -> f16x2 conversion, then f16 -> f32;
-//    every E2M1 value is exact in f16 and f32.
+//  * E2M1 (MXFP4, NVFP4): the hardware e2m1x2 -> f16x2 conversion; every E2M1 value
+//    is exact in f16.
 //  * Integer codes (MLX affine, Q6_K): the zero point and the integer-to-float
 //    conversion live in the operand's bit pattern.  The code is placed in the
-//    mantissa of 1.0f, giving the exact operand 1 + code * 2^-11 (code in bits
-//    12..) or 1 + code * 2^-7 (code in bits 16..); the constant 1 is removed once
-//    per block with the block's input sums.  This is the fp32 form of the PR's
-//    half operand 1 + code/64, whose offset is removed by subtracting 1.5.
+//    mantissa of 1.0 (f16), giving the exact operand 1 + code/1024 or 1 + code/64;
+//    the constant 1 (and Q6_K's zero point 32) is removed once per block with the
+//    block's input sums instead of once per weight.  This is the PR's half operand
+//    1 + code/64, whose offset the PR removes by subtracting 1.5.
+// Products are formed with the mixed-precision FMA f32 += f16 * f16 (exact
+// products, fp32 accumulation).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -47,16 +49,6 @@ __device__ __forceinline__ uint32_t ld_stream2(const void* p) {
 }
 
 // ------------------------------------------------------------------ decoders
-// Two E2M1 codes (low nibble, high nibble of byte `b` of `wd`) -> fp32 pair (lo, hi).
-template <int b>
-__device__ __forceinline__ float2 e2m1x2_f32(uint32_t wd) {
-  uint32_t h2;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(h2) : "r"(wd >> (8 * b)));
-  __half2 h = *reinterpret_cast<__half2*>(&h2);
-  return __half22float2(h);
-}
-
 // Two E4M3FN bytes (bytes 2i, 2i+1 of `wd`) -> fp32 pair; exact (E4M3 fits f16).
 template <int i>
 __device__ __forceinline__ float2 e4m3x2_f32(uint32_t wd) {
@@ -77,29 +69,6 @@ __device__ __forceinline__ float e8m0_f32(uint32_t e) {
 
 // Byte rotations of a 32-bit word (one PRMT each).
 __device__ __forceinline__ uint32_t rot8(uint32_t w)  { return __byte_perm(w, w, 0x0321); }
-__device__ __forceinline__ uint32_t rot16(uint32_t w) { return __byte_perm(w, w, 0x1032); }
-__device__ __forceinline__ uint32_t rot24(uint32_t w) { return __byte_perm(w, w, 0x2103); }
-
-// Integer-code operands.  For a word holding eight 4-bit codes n0..n7 (nibble i at
-// bits 4i..4i+3), rotation by 8r bits brings nibbles (3+2r)%8 to bits 12..15 and
-// (4+2r)%8 to bits 16..19.  The operand pair is
-//   x: 1 + n_odd  * 2^-11   (odd nibble, "class 12")
-//   y: 1 + n_even * 2^-7    (even nibble, "class 16")
-// Pair order over r = 0..3: (n3,n4) (n5,n6) (n7,n0) (n1,n2); the activations are
-// staged in the matching order [3,4,5,6,7,0,1,2] within each group of eight.
-// For Q6_K the two high bits of each code sit just above the nibble (bits 16..17
-// for class 12, 20..21 for class 16) and `hi` supplies them after the same rotation.
-__device__ __forceinline__ float2 int4_pair(uint32_t rotated) {
-  return make_float2(__uint_as_float((rotated & 0x0000F000u) | 0x3F800000u),
-                     __uint_as_float((rotated & 0x000F0000u) | 0x3F800000u));
-}
-__device__ __forceinline__ float2 int6_pair(uint32_t rot_lo, uint32_t rot_hi) {
-  return make_float2(__uint_as_float((rot_lo & 0x0000F000u) | (rot_hi & 0x00030000u) | 0x3F800000u),
-                     __uint_as_float((rot_lo & 0x000F0000u) | (rot_hi & 0x00300000u) | 0x3F800000u));
-}
-// Scale factors that turn (operand - 1) back into the integer code.
-constexpr float kClass12 = 2048.0f;  // 2^11
-constexpr float kClass16 = 128.0f;   // 2^7
 
 // Q6_K high-bit word for the low-nibble word `half` (0: codes 16w..16w+7, 1: codes
 // 16w+8..16w+15) of the layout's chunk-2 word: after this shift, the high bits of
@@ -109,6 +78,50 @@ __device__ __forceinline__ uint32_t q6k_hi_for(uint32_t hw, int half) {
   return half ? __funnelshift_l(hw, hw, 2) : __funnelshift_l(hw, hw, 4);
 }
 
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+// ---------------------------------------------------------------- f16 operands
+// Mixed-precision FMA: c + a.half * b.half in fp32 (the f16 x f16 product is exact
+// in fp32, so this equals an fp32 FMA of the two exact operands).
+__device__ __forceinline__ float hfma_lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float hfma_hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, ah, bh, %3;\n\t}" : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
+// Two E2M1 codes (byte b of wd) -> f16x2 (low nibble in the low half); exact.
+template <int b>
+__device__ __forceinline__ uint32_t e2m1x2_h2(uint32_t wd) {
+  uint32_t h2;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(h2) : "r"(wd >> (8 * b)));
+  return h2;
+}
+
+// Integer codes as exact f16 operands (the Q6_K operand PR's zero-point-in-the-
+// operand idea: the code sits in the mantissa of 1.0).  For a word of eight 4-bit
+// codes n0..n7 (nibble i at bits 4i..4i+3) and r = the word rotated right by 8:
+//   op0 = halves (n0, n4) = 1 + n/1024   (mantissa bits 0..3,  "class 1024")
+//   op1 = halves (n1, n5) = 1 + n/64     (mantissa bits 4..7,  "class 64")
+//   op2 = halves (n2, n6) from r, class 1024;  op3 = halves (n3, n7) from r, class 64.
+// Activations of class-1024 positions are staged multiplied by 16, so every
+// product is 16*x + code*x/64 (class 1024) or x + code*x/64 (class 64): one
+// accumulator, and the constants are removed per block with precomputed sums.
+__device__ __forceinline__ uint32_t i4_op_lo(uint32_t w) { return (w & 0x000F000Fu) | 0x3C003C00u; }
+__device__ __forceinline__ uint32_t i4_op_hi(uint32_t w) { return (w & 0x00F000F0u) | 0x3C003C00u; }
+// Q6_K: the two high bits of each code sit just above its nibble (bits 4..5 for
+// class 1024, 8..9 for class 64); `h` is the high-bit word aligned by q6k_hi_for and
+// rotated like the low word.
+__device__ __forceinline__ uint32_t i6_op_lo(uint32_t w, uint32_t h) {
+  return (w & 0x000F000Fu) | (h & 0x00300030u) | 0x3C003C00u;
+}
+__device__ __forceinline__ uint32_t i6_op_hi(uint32_t w, uint32_t h) {
+  return (w & 0x00F000F0u) | (h & 0x03000300u) | 0x3C003C00u;
+}
 
 }  // namespace qg

@@ -4,7 +4,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/qgemv.h"
+#include "qgemv.h"
 
 namespace qg {
 
