@@ -83,13 +83,13 @@ __host__ __device__ inline SmemLayout gemv_smem_layout(int stage_bytes, int S, i
   L.xs = o;
   o += (size_t)M * nslots * 64 * 2;  // f16 activations
   L.sums = o;
-  o += (size_t)M * nslots * 8 * 4;  // (Z, X) per 16-input quarter
+  o += (size_t)M * nslots * 16 * 4;  // {scale, Z, X, 0} per 16-input quarter
   L.red = o;
   o += (size_t)kCW * M * 128 * 4;
   L.lut = o;
   o += 256 * 4;  // E4M3 -> fp32
   L.misc = o;
-  o += 64;  // inv_scale[4], maxbits[4], flag
+  o += 64;  // ticket flag
   L.total = o;
   return L;
 }
@@ -104,80 +104,56 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t v, float& lo, float& hi) 
   hi = __uint_as_float(v & 0xFFFF0000u);
 }
 
-// Stage the activation rows into shared memory as f16, exactly: each CTA scales
-// row m by a power of two 2^P_m chosen from the largest |x| it stages, so every
-// bf16 value (8 significant bits) lands inside f16's range; values more than
-// 2^27 below that maximum would round, which the stated tolerance dwarfs.  The
-// partial sums are scaled back by 2^-P_m before they leave the CTA.
+// Stage the activation rows into shared memory as f16, exactly: every 16-input
+// quarter of row m is scaled by its own power of two 2^p chosen from its largest
+// |x|, so each bf16 value (8 significant bits) lands inside f16's range; a value
+// more than 2^27 below its quarter's maximum would round, far below the stated
+// tolerance.  Per quarter the staging records four floats: {2^-p (E2M1) or
+// 64 * 2^-p (integer formats), Z, X, 0}; Z and X, in unscaled units, remove the
+// integer operands' constant and the Q6_K zero point in the fold.
 // Layout per 8 inputs (one code word) and row m: four f16x2 words in the order the
 // decoder produces operand pairs -- E2M1: (x0,x1) (x2,x3) (x4,x5) (x6,x7); integer
-// formats: (16x0,16x4) (x1,x5) (16x2,16x6) (x3,x7).  Integer formats also record,
-// per 16-input quarter, Z and X that remove the operand constant and zero point.
+// formats: (16x0,16x4) (x1,x5) (16x2,16x6) (x3,x7).
 template <int FMT, int M, int kCT>
-__device__ void stage_x(const GemvArgs& a, uint32_t* xs, float* sums, float* inv_scale, int* maxbits, int sbase,
-                        int nslots, int tid) {
+__device__ void stage_x(const GemvArgs& a, uint32_t* xs, float* sums, int sbase, int nslots, int tid) {
   constexpr bool kInt = (FMT == FMT_MLX || FMT == FMT_Q6K);
   const int items = M * nslots * 4;
-  if (tid < M) maxbits[tid] = 0;
-  named_sync(1, kCT);
-  uint32_t lm[M];
-#pragma unroll
-  for (int m = 0; m < M; ++m) lm[m] = 0;
   for (int it = tid; it < items; it += kCT) {
     const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
     const int64_t k0 = (int64_t)((sbase + s) % a.KG) * 64 + kq * 16;
-    if (k0 >= a.k) continue;
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + m * a.ldx + k0);
-    const uint4 r0 = src[0], r1 = src[1];
-    const uint32_t u[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-    uint32_t mx = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mx = max(mx, max(u[i] & 0x7FFFu, (u[i] >> 16) & 0x7FFFu));
-#pragma unroll
-    for (int mm = 0; mm < M; ++mm)
-      if (mm == m) lm[mm] = max(lm[mm], mx);
-  }
-#pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const uint32_t v = __reduce_max_sync(0xFFFFFFFFu, lm[m]);
-    if ((tid & 31) == 0 && v) atomicMax(&maxbits[m], (int)v);
-  }
-  named_sync(1, kCT);
-  float scale[M];
-#pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const int mb = maxbits[m];
-    const int e = mb >= 0x80 ? (mb >> 7) - 127 : -127;
-    int P = (kInt ? 10 : 14) - e;
-    if (mb >= 0x7F80) P = 0;  // inf / nan: leave as is
-    P = max(-126, min(126, P));
-    scale[m] = __uint_as_float((uint32_t)(P + 127) << 23);
-    if (tid == 0) inv_scale[m] = __uint_as_float((uint32_t)(127 - P) << 23);
-  }
-  for (int it = tid; it < items; it += kCT) {
-    const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
-    const int64_t k0 = (int64_t)((sbase + s) % a.KG) * 64 + kq * 16;
-    float v[16];
+    uint32_t u[8];
     if (k0 < a.k) {
       const uint4* src = reinterpret_cast<const uint4*>(a.x + m * a.ldx + k0);
       const uint4 r0 = src[0], r1 = src[1];
-      const uint32_t u[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float lo, hi;
-        bf16x2_to_f32(u[i], lo, hi);
-        v[2 * i] = __half2float(__float2half_rn(lo * scale[m]));
-        v[2 * i + 1] = __half2float(__float2half_rn(hi * scale[m]));
-      }
+      u[0] = r0.x; u[1] = r0.y; u[2] = r0.z; u[3] = r0.w;
+      u[4] = r1.x; u[5] = r1.y; u[6] = r1.z; u[7] = r1.w;
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+      for (int i = 0; i < 8; ++i) u[i] = 0;
+    }
+    uint32_t mb = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mb = max(mb, max(u[i] & 0x7FFFu, (u[i] >> 16) & 0x7FFFu));
+    const int e = mb >= 0x80 ? (int)(mb >> 7) - 127 : -127;
+    int p = (kInt ? 10 : 14) - e;
+    if (mb >= 0x7F80u || mb == 0) p = 0;  // inf / nan / all zero: leave as is
+    p = max(-126, min(126, p));
+    const float scale = __uint_as_float((uint32_t)(p + 127) << 23);
+    const float inv = __uint_as_float((uint32_t)(127 - p) << 23);
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float lo, hi;
+      bf16x2_to_f32(u[i], lo, hi);
+      v[2 * i] = __half2float(__float2half_rn(lo * scale));
+      v[2 * i + 1] = __half2float(__float2half_rn(hi * scale));
     }
     uint32_t* dst = xs + (size_t)(m * nslots + s) * 32 + kq * 8;
     auto h2 = [](float lo, float hi) {
       __half2 h = __floats2half2_rn(lo, hi);
       return *reinterpret_cast<uint32_t*>(&h);
     };
+    float4 z = make_float4(inv, 0.0f, 0.0f, 0.0f);
     if (kInt) {
       float x16 = 0.0f, x1 = 0.0f;
 #pragma unroll
@@ -188,17 +164,18 @@ __device__ void stage_x(const GemvArgs& a, uint32_t* xs, float* sums, float* inv
         x16 += (q[0] + q[4]) + (q[2] + q[6]);
         x1 += (q[1] + q[5]) + (q[3] + q[7]);
       }
-      float* z = sums + ((size_t)(m * nslots + s) * 4 + kq) * 2;
-      const float xsum = x16 + x1;                // X'
-      const float xop = fmaf(16.0f, x16, x1);     // X'' = sum of the staged operands' partners
-      z[0] = (FMT == FMT_Q6K) ? fmaf(64.0f, xop, 32.0f * xsum) : 64.0f * xop;
-      z[1] = xsum;
+      const float xsum = (x16 + x1) * inv;           // X, unscaled
+      const float xop = fmaf(16.0f, x16, x1) * inv;  // the operands' constant part, unscaled
+      z.x = 64.0f * inv;
+      z.y = (FMT == FMT_Q6K) ? fmaf(64.0f, xop, 32.0f * xsum) : 64.0f * xop;
+      z.z = xsum;
     } else {
 #pragma unroll
       for (int i = 0; i < 2; ++i)
         reinterpret_cast<uint4*>(dst)[i] = make_uint4(h2(v[8 * i], v[8 * i + 1]), h2(v[8 * i + 2], v[8 * i + 3]),
                                                       h2(v[8 * i + 4], v[8 * i + 5]), h2(v[8 * i + 6], v[8 * i + 7]));
     }
+    reinterpret_cast<float4*>(sums)[(size_t)(m * nslots + s) * 4 + kq] = z;
   }
 }
 
@@ -268,6 +245,9 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
     }
   }
   // Fold the quarter's partial with the block scale (once per block and row).
+  float4 zq[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) zq[m] = *reinterpret_cast<const float4*>(sq + m * sstride);
 #pragma unroll
   for (int rt = 0; rt < 4; ++rt) {
     const int row = rt * 32 + lane;
@@ -275,19 +255,19 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
     if (FMT == FMT_NVFP4) {
       const float S = e4m3_lut[sp[kq]];
 #pragma unroll
-      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S, P[rt][m][0] + P[rt][m][1], acc[rt][m]);
+      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * zq[m].x, P[rt][m][0] + P[rt][m][1], acc[rt][m]);
     } else if (FMT == FMT_MXFP4) {
       const float S = e8m0_f32(sp[kq >> 1]);
 #pragma unroll
-      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S, P[rt][m][0] + P[rt][m][1], acc[rt][m]);
+      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * zq[m].x, P[rt][m][0] + P[rt][m][1], acc[rt][m]);
     } else if (FMT == FMT_MLX) {
       const uint32_t sw = *reinterpret_cast<const uint32_t*>(sp);
       const float s = __half2float(__ushort_as_half((unsigned short)(sw & 0xFFFFu)));
       const float bias = __half2float(__ushort_as_half((unsigned short)(sw >> 16)));
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        const float dot = fmaf(64.0f, P[rt][m][0] + P[rt][m][1], -sq[m * sstride]);
-        acc[rt][m] = fmaf(s, dot, fmaf(bias, sq[m * sstride + 1], acc[rt][m]));
+        const float dot = fmaf(zq[m].x, P[rt][m][0] + P[rt][m][1], -zq[m].y);
+        acc[rt][m] = fmaf(s, dot, fmaf(bias, zq[m].z, acc[rt][m]));
       }
     } else {
       const float sc = (float)(int8_t)sp[kq];
@@ -295,7 +275,7 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
       const float ds = d * sc;
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        const float dot = fmaf(64.0f, P[rt][m][0] + P[rt][m][1], -sq[m * sstride]);
+        const float dot = fmaf(zq[m].x, P[rt][m][0] + P[rt][m][1], -zq[m].y);
         acc[rt][m] = fmaf(ds, dot, acc[rt][m]);
       }
     }
@@ -328,9 +308,7 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
   float* sums = reinterpret_cast<float*>(smem + L.sums);
   float* red = reinterpret_cast<float*>(smem + L.red);
   float* lut = reinterpret_cast<float*>(smem + L.lut);
-  float* inv_scale = reinterpret_cast<float*>(smem + L.misc);
-  int* maxbits = reinterpret_cast<int*>(smem + L.misc + 16);
-  int* flag = reinterpret_cast<int*>(smem + L.misc + 32);
+  int* flag = reinterpret_cast<int*>(smem + L.misc);
 
   const int64_t U = a.U;
   const int64_t G = gridDim.x;
@@ -395,7 +373,7 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
     lut[2 * tid] = v.x;
     lut[2 * tid + 1] = v.y;
   }
-  stage_x<FMT, M, kCT>(a, xs, sums, inv_scale, maxbits, sbase, nslots, tid);
+  stage_x<FMT, M, kCT>(a, xs, sums, sbase, nslots, tid);
   named_sync(1, kCT);
 
   // This warp's units: relative index i = C * chunk + ug, one per chunk, processed
@@ -408,7 +386,7 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
   int slot = (int)((uu0 + i) % (uint32_t)KG) - sbase;
   if (slot < 0) slot += KG;
   const uint8_t* xq_base = reinterpret_cast<const uint8_t*>(xs) + kq * 32;
-  const float* sq_base = sums + kq * 2;
+  const float* sq_base = sums + kq * 4;
   uint32_t u = uu0;
   while (u < uu1) {
     const uint32_t q = u / (uint32_t)KG;
@@ -428,7 +406,7 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
       const uint8_t* aux = st + C * (SG::CODE + SG::SCALE) + ((uu >> 2) - ((uu - ug) >> 2)) * SG::AUX;
       consume<FMT, M>(st + ug * SG::CODE, st + C * SG::CODE + ug * SG::SCALE, aux,
                       reinterpret_cast<const uint32_t*>(xq_base + (size_t)slot * 128), nslots * 32,
-                      sq_base + (size_t)slot * 8, nslots * 8, lut, kq, lane, acc);
+                      sq_base + (size_t)slot * 16, nslots * 16, lut, kq, lane, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       if (++s == S) {
@@ -450,7 +428,6 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
       float v = 0.0f;
 #pragma unroll 4
       for (int w2 = 0; w2 < kCW; ++w2) v += red[w2 * M * 128 + e];
-      v *= inv_scale[e / 128];  // exact: undo this CTA's activation scaling
       if (whole)
         finish_out<M>(a, q, e, v);
       else
