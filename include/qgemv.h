@@ -149,6 +149,21 @@ qg_status qgemv(const qg_weight* w, const void* x, int m_rows, int64_t ldx,
                 const void* residual, int64_t ldr, void* y, int64_t ldy,
                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Workspace-free variant of qgemv, for callers that cannot allocate device memory:
+ * plugins hosted by a runtime that owns all of the GPU's memory and gives them no
+ * allocator, and code on paths where cudaMalloc's implicit device synchronisation is not
+ * acceptable.  The source pages have no counterpart; it exists for such callers only.
+ * Same arguments and results as qgemv, minus the workspace.  The split-K scratch lives in
+ * a fixed device array of QG_STATIC_WORKSPACE_BYTES inside the library, present on every
+ * GPU that loads the library until the process exits.  The first call on a device looks
+ * up that array's address (make it before any stream capture).  Every call clears the
+ * array's status word and tickets; all calls share the array, so calls that overlap on
+ * the GPU race -- serialise them (one stream).  Shapes needing more scratch than the
+ * array holds return QG_ERR_WORKSPACE_TOO_SMALL; nothing is allocated. */
+#define QG_STATIC_WORKSPACE_BYTES (4u << 20)
+qg_status qgemv_static_ws(const qg_weight* w, const void* x, int m_rows, int64_t ldx,
+                          const void* residual, int64_t ldr, void* y, int64_t ldy, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -48,6 +48,7 @@ _SIGNATURES = {
     "qg_workspace_init": (_I, [_P, _SZ, _P]),
     "qg_workspace_status": (_I, [_P, ctypes.POINTER(_I), _P]),
     "qgemv": (_I, [ctypes.POINTER(qg_weight), _P, _I, _I64, _P, _I64, _P, _I64, _P, _SZ, _P]),
+    "qgemv_static_ws": (_I, [ctypes.POINTER(qg_weight), _P, _I, _I64, _P, _I64, _P, _I64, _P]),
 }
 
 
@@ -117,6 +118,13 @@ def qgemv(w: qg_weight, x_ptr: int, m: int, ldx: int, res_ptr: Optional[int], ld
           ws_ptr: int, ws_bytes: int, stream: int = 0):
     _check(lib().qgemv(ctypes.byref(w), x_ptr, m, ldx, res_ptr, ldr, y_ptr, ldy, ws_ptr, ws_bytes, stream),
            "qgemv")
+
+
+def qgemv_static_ws(w: qg_weight, x_ptr: int, m: int, ldx: int, res_ptr: Optional[int], ldr: int, y_ptr: int,
+                    ldy: int, stream: int = 0):
+    """qgemv without a workspace argument, for callers that cannot allocate device memory
+    (its scratch is a fixed array inside the library, shared by all calls)."""
+    _check(lib().qgemv_static_ws(ctypes.byref(w), x_ptr, m, ldx, res_ptr, ldr, y_ptr, ldy, stream), "qgemv_static_ws")
 
 
 # ------------------------------------------------------------------ torch helpers

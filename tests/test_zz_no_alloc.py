@@ -1,0 +1,53 @@
+"""The workspace-free GEMV entry point, for callers that cannot allocate device memory
+(plugins whose host runtime owns all GPU memory, or paths that cannot afford cudaMalloc's
+implicit synchronisation).  Its scratch is a fixed array inside the library shared by all
+calls, so two calls in a row must both match the workspace entry point, and the second
+must not see state left by the first.  Collected last on purpose."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tests.gpu_util import dev_bf16, qlib, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("fmt,n,k,m,residual", [
+    (wl.NVFP4, 1000, 1280, 3, True),
+    (wl.Q6K, 640, 1536, 1, False),
+    (wl.MXFP4, 17408 // 8, 5120, 4, True),
+])
+def test_static_workspace_matches_workspace_entry_on_two_calls(fmt, n, k, m, residual):
+    q = qlib()
+    w = wl.weight(fmt, n, k, seed=41)
+    pw = q.PackedWeight.from_logical(w)
+    stream = torch.cuda.current_stream().cuda_stream
+    for call in range(2):
+        x = wl.activations(m, k, seed=50 + call)
+        res = wl.activations(m, n, seed=60 + call, stream="residual") if residual else None
+        xt = dev_bf16(x)
+        rt = dev_bf16(res) if residual else None
+        ref = q.gemv(pw, xt, rt)  # the existing entry point, own workspace
+        out = torch.empty_like(torch.empty((m, (n + 7) // 8 * 8), dtype=torch.bfloat16, device="cuda"))[:, :n]
+        out.fill_(float("nan"))
+        q.qgemv_static_ws(pw.desc, xt.data_ptr(), m, xt.stride(0), None if rt is None else rt.data_ptr(),
+                          0 if rt is None else rt.stride(0), out.data_ptr(), out.stride(0), stream)
+        torch.cuda.synchronize()
+        got, want = to_f64(out), to_f64(ref)
+        tol = oracle.tolerance(w, x, res)
+        assert np.all(np.isfinite(got))
+        assert np.all(np.abs(got - want) <= tol), f"call {call}: max diff {np.max(np.abs(got - want))}"
+        ref_o, _ = oracle.gemv(w, x, res)
+        assert np.all(np.abs(got - ref_o) <= tol)
+
+
+def test_static_workspace_validates_on_host():
+    q = qlib()
+    w = q.qg_weight(wl.NVFP4, 0, 256, 100, 0x1000, 0x2000, None, 1.0, 0.0)  # K not a multiple of 16
+    assert q.lib().qgemv_static_ws(ctypes.byref(w), 0x3000, 1, 256, None, 0, 0x4000, 256, None) == 1
+    w = q.qg_weight(wl.NVFP4, 0, 256, 256, 0x1000, 0x2000, None, 1.0, 0.0)
+    assert q.lib().qgemv_static_ws(ctypes.byref(w), 0x3000, 5, 256, None, 0, 0x4000, 256, None) == 2
