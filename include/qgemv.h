@@ -149,6 +149,22 @@ qg_status qgemv(const qg_weight* w, const void* x, int m_rows, int64_t ldx,
                 const void* residual, int64_t ldr, void* y, int64_t ldy,
                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Workspace bytes qgemm needs: the qgemv size for 1..4 rows, else 256 (status word). */
+size_t qg_gemm_workspace_size(int fmt, int64_t n, int64_t k, int m);
+
+/* Quantized GEMM for any number of activation rows (tokens), dispatching by rows
+ * (TurboEXL3 article §4.3, a path per row count): 1..4 rows run qgemv; more rows run the
+ * prefill kernel, which decodes each 128 x 64 weight slice once into shared memory as
+ * bf16 and multiplies it against up to 256 tokens on the tensor cores (tcgen05, fp32
+ * accumulation in tensor memory) -- TurboEXL3 article §4.1, "decode once, multiply many
+ * times"; no dequantised copy of the weights is written to device memory.
+ *   y[t][n] = bf16( sum_k w[n,k] * x[t][k] (+ residual[t][n]) ),  t = 0..m_rows-1.
+ * Same argument rules as qgemv; the workspace holds the device status word
+ * (qg_workspace_status) and must be zero-filled before first use. */
+qg_status qgemm(const qg_weight* w, const void* x, int64_t m_rows, int64_t ldx,
+                const void* residual, int64_t ldr, void* y, int64_t ldy,
+                void* workspace, size_t workspace_bytes, void* stream);
+
 /* Workspace-free variant of qgemv, for callers that cannot allocate device memory:
  * plugins hosted by a runtime that owns all of the GPU's memory and gives them no
  * allocator, and code on paths where cudaMalloc's implicit device synchronisation is not

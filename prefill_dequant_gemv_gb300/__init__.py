@@ -49,6 +49,8 @@ _SIGNATURES = {
     "qg_workspace_status": (_I, [_P, ctypes.POINTER(_I), _P]),
     "qgemv": (_I, [ctypes.POINTER(qg_weight), _P, _I, _I64, _P, _I64, _P, _I64, _P, _SZ, _P]),
     "qgemv_static_ws": (_I, [ctypes.POINTER(qg_weight), _P, _I, _I64, _P, _I64, _P, _I64, _P]),
+    "qg_gemm_workspace_size": (_SZ, [_I, _I64, _I64, _I]),
+    "qgemm": (_I, [ctypes.POINTER(qg_weight), _P, _I64, _I64, _P, _I64, _P, _I64, _P, _SZ, _P]),
 }
 
 
@@ -118,6 +120,15 @@ def qgemv(w: qg_weight, x_ptr: int, m: int, ldx: int, res_ptr: Optional[int], ld
           ws_ptr: int, ws_bytes: int, stream: int = 0):
     _check(lib().qgemv(ctypes.byref(w), x_ptr, m, ldx, res_ptr, ldr, y_ptr, ldy, ws_ptr, ws_bytes, stream),
            "qgemv")
+
+
+def qg_gemm_workspace_size(fmt: int, n: int, k: int, m: int) -> int:
+    return lib().qg_gemm_workspace_size(fmt, n, k, m)
+
+
+def qgemm(w: qg_weight, x_ptr: int, m: int, ldx: int, res_ptr: Optional[int], ldr: int, y_ptr: int, ldy: int,
+          ws_ptr: int, ws_bytes: int, stream: int = 0):
+    _check(lib().qgemm(ctypes.byref(w), x_ptr, m, ldx, res_ptr, ldr, y_ptr, ldy, ws_ptr, ws_bytes, stream), "qgemm")
 
 
 def qgemv_static_ws(w: qg_weight, x_ptr: int, m: int, ldx: int, res_ptr: Optional[int], ldr: int, y_ptr: int,
@@ -193,6 +204,20 @@ def gemv(pw: PackedWeight, x, residual=None, out=None, workspace: Optional[Works
     if workspace is None:
         workspace = Workspace(qg_gemv_workspace_size(pw.fmt, pw.n, pw.k, m), x.device)
     qgemv(pw.desc, x.data_ptr(), m, x.stride(0), None if residual is None else residual.data_ptr(),
+          0 if residual is None else residual.stride(0), out.data_ptr(), out.stride(0), workspace.ptr,
+          workspace.nbytes, _stream_ptr())
+    return out
+
+
+def gemm(pw: PackedWeight, x, residual=None, out=None, workspace: Optional[Workspace] = None):
+    """y = bf16(W x (+ residual)) for x bf16 [m, k] on the device, any m (tokens)."""
+    import torch
+    m = x.shape[0]
+    if out is None:
+        out = torch.empty((m, (pw.n + 7) // 8 * 8), dtype=torch.bfloat16, device=x.device)[:, :pw.n]
+    if workspace is None:
+        workspace = Workspace(qg_gemm_workspace_size(pw.fmt, pw.n, pw.k, min(m, 2 ** 31 - 1)), x.device)
+    qgemm(pw.desc, x.data_ptr(), m, x.stride(0), None if residual is None else residual.data_ptr(),
           0 if residual is None else residual.stride(0), out.data_ptr(), out.stride(0), workspace.ptr,
           workspace.nbytes, _stream_ptr())
     return out

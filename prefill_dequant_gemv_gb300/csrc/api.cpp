@@ -120,3 +120,28 @@ extern "C" qg_status qg_workspace_status(void* workspace, int* status, void* str
   *status = v;
   return QG_OK;
 }
+
+extern "C" size_t qg_gemm_workspace_size(int fmt, int64_t n, int64_t k, int m) {
+  if (m >= 1 && m <= 4) return qg_gemv_workspace_size(fmt, n, k, m);
+  Geometry g;
+  if (!geometry(fmt, n, k, &g) || m < 1) return 0;
+  return kWsHeader;
+}
+
+extern "C" qg_status qgemm(const qg_weight* w, const void* x, int64_t m, int64_t ldx, const void* residual,
+                           int64_t ldr, void* y, int64_t ldy, void* workspace, size_t workspace_bytes, void* stream) {
+  if (m >= 1 && m <= 4)  // 1..4 rows: the GEMV reads each weight once for all rows
+    return qgemv(w, x, (int)m, ldx, residual, ldr, y, ldy, workspace, workspace_bytes, stream);
+  Geometry g;
+  int st = check_weight(w, &g);
+  if (st != QG_OK) return (qg_status)st;
+  if (m < 1) return QG_ERR_UNSUPPORTED;
+  if (!x || !y || !workspace) return QG_ERR_INVALID_ARG;
+  if (ldx < w->k || ldy < w->n || (residual && ldr < w->n)) return QG_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)) || !aligned16(workspace))
+    return QG_ERR_MISALIGNED;
+  if (ldx % 8 || ldy % 8 || (residual && ldr % 8)) return QG_ERR_MISALIGNED;
+  if (workspace_bytes < kWsHeader) return QG_ERR_WORKSPACE_TOO_SMALL;
+  if ((m + 255) / 256 > 65535 || g.nt > 0x7FFFFFFF) return QG_ERR_UNSUPPORTED;
+  return (qg_status)launch_prefill(g, w, x, m, ldx, residual, ldr, y, ldy, workspace, stream);
+}

@@ -1,0 +1,357 @@
+// Prefill GEMM on GB300 tensor cores: Y[t, n] = bf16( sum_k W[n, k] X[t, k] (+ R[t, n]) )
+// for quantized W and bf16 X with many tokens (TurboEXL3 article §4.1, "decode once,
+// multiply many times": each 64-deep slice of the weights is decoded once into on-chip
+// memory and multiplied against up to 256 tokens; the decoded weights never reach device
+// memory and no 16-bit copy is written).
+//
+// One CTA computes a 128-row x 256-token output tile over the whole K:
+//   warp 0      producer: per 64-deep stage, bulk-copies the packed weight tile (codes,
+//               scales, Q6_K d) and TMA-loads the 256 x 64 activation tile (128-byte swizzle)
+//   warps 2..9  decode the stage's 128 x 64 weights to bf16 in the tensor cores' 128-byte
+//               swizzled K-major layout (E2M1 x block scale is exact in bf16), then run the
+//               epilogue (TMEM -> registers -> bf16 output, tensor scale and residual)
+//   warp 1      allocates 256 TMEM columns and issues tcgen05.mma (M=128, N=256, K=16,
+//               bf16 x bf16 -> fp32) from one lane; completion is committed to mbarriers.
+// Every wait is bounded (QG_ERR_TIMEOUT in the workspace status word) and TMEM is freed
+// on every path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "qg_common.cuh"
+#include "qg_internal.h"
+#include "qg_sync.cuh"
+#include "qg_tc.cuh"
+
+namespace qg {
+
+constexpr int kPfBN = 256;                                   // tokens per tile (MMA N)
+constexpr int kPfStages = 4;
+constexpr int kPfDeqWarps = 8;
+constexpr int kPfThreads = (2 + kPfDeqWarps) * 32;           // 320
+constexpr int kATile = 128 * 128;                            // 128 rows x 64 bf16
+constexpr int kBTile = kPfBN * 128;                          // 256 tokens x 64 bf16
+constexpr int kRawMax = 7168;                                // >= Q6_K tile 6144 + 512 + 256
+constexpr int kPfStageBytes = kATile + kBTile + kRawMax;     // 56320, a multiple of 1024
+constexpr int kPfSmem = 1024 + kPfStages * kPfStageBytes + 256;
+constexpr uint32_t kPfTmemCols = 256;
+
+struct PrefillArgs {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const uint8_t* aux;
+  const __nv_bfloat16* res;
+  __nv_bfloat16* y;
+  int64_t ldr, ldy;
+  int64_t n, t;
+  int KG;
+  float ts;
+  int* status;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Decode one thread's share of a stage: row r, inputs 32h..32h+31 -> four 16-byte
+// chunks of the swizzled A tile (chunk j of row r lives at (r/8)*1024 + (r%8)*128 +
+// ((j ^ (r%8)) * 16)).
+template <int FMT>
+__device__ __forceinline__ void decode_stage(const uint8_t* raw, uint8_t* A, int r, int h) {
+  using F = Fmt<FMT>;
+  const int rt = r >> 5, lane = r & 31;
+  const uint4 cw = *reinterpret_cast<const uint4*>(raw + ((rt * F::CH + h) * 32 + lane) * 16);
+  const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+  const uint8_t* sp = raw + F::TB + r * F::SB;
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi) {
+    const uint32_t w = words[wi];
+    float v[8];
+    if (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
+      float S;
+      if (FMT == FMT_NVFP4) {
+        const int blk = 2 * h + (wi >> 1);
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(sp);
+        const float2 s01 = (blk >> 1) ? e4m3x2_f32<1>(sw) : e4m3x2_f32<0>(sw);
+        S = (blk & 1) ? s01.y : s01.x;
+      } else {
+        S = e8m0_f32(sp[h]);
+      }
+      const uint32_t hb[4] = {e2m1x2_h2<0>(w), e2m1x2_h2<1>(w), e2m1x2_h2<2>(w), e2m1x2_h2<3>(w)};
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float2 e = __half22float2(*reinterpret_cast<const __half2*>(&hb[b]));
+        v[2 * b] = S * e.x;  // exact
+        v[2 * b + 1] = S * e.y;
+      }
+    } else {
+      uint32_t op[4];
+      const uint32_t rw = rot8(w);
+      if (FMT == FMT_MLX) {
+        op[0] = i4_op_lo(w);
+        op[1] = i4_op_hi(w);
+        op[2] = i4_op_lo(rw);
+        op[3] = i4_op_hi(rw);
+      } else {
+        const int quarter = 2 * h + (wi >> 1);
+        const uint32_t hw = *reinterpret_cast<const uint32_t*>(raw + ((rt * 3 + 2) * 32 + lane) * 16 + quarter * 4);
+        const uint32_t hh = q6k_hi_for(hw, wi & 1), hr = rot8(hh);
+        op[0] = i6_op_lo(w, hh);
+        op[1] = i6_op_hi(w, hh);
+        op[2] = i6_op_lo(rw, hr);
+        op[3] = i6_op_hi(rw, hr);
+      }
+      float code[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 e = __half22float2(*reinterpret_cast<const __half2*>(&op[j]));
+        const float mul = (j & 1) ? 64.0f : 1024.0f;
+        code[j] = (e.x - 1.0f) * mul;  // exact integer code
+        code[j + 4] = (e.y - 1.0f) * mul;
+      }
+      if (FMT == FMT_MLX) {
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(sp);
+        const float s = __half2float(__ushort_as_half((unsigned short)(sw & 0xFFFFu)));
+        const float bias = __half2float(__ushort_as_half((unsigned short)(sw >> 16)));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = fmaf(s, code[j], bias);
+      } else {
+        const float sc = (float)(int8_t)sp[2 * h + (wi >> 1)];
+        const float d = __half2float(*reinterpret_cast<const __half*>(raw + F::TB + 128 * F::SB + r * 2));
+        const float ds = d * sc;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = ds * (code[j] - 32.0f);
+      }
+    }
+    const int j = 4 * h + wi;
+    const uint4 out = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                 pack_bf16x2(v[6], v[7]));
+    *reinterpret_cast<uint4*>(A + (r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4)) = out;
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmx, const PrefillArgs a) {
+  using F = Fmt<FMT>;
+  constexpr int kRaw = F::TB + 128 * F::SB + (FMT == FMT_Q6K ? 256 : 0);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPfStages * kPfStageBytes);
+  uint64_t* full = bars;
+  uint64_t* afull = bars + kPfStages;
+  uint64_t* empty = bars + 2 * kPfStages;
+  uint64_t* done = bars + 3 * kPfStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kPfStages + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tile_n = blockIdx.x;
+  const int t0 = blockIdx.y * kPfBN;
+  const int KG = a.KG;
+
+  if (tid == 0) {
+    for (int s = 0; s < kPfStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&afull[s], kPfDeqWarps);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kPfTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {  // producer
+      int s = 0;
+      uint32_t ph = 0;
+      int issued = 0;
+      for (int kt = 0; kt < KG; ++kt) {
+        if (kt >= kPfStages && !mbar_wait_bounded(&empty[s], ph ^ 1u, a.status)) break;
+        uint8_t* st = smem + s * kPfStageBytes;
+        const int64_t tile = (int64_t)tile_n * KG + kt;
+        mbar_arrive_expect_tx(&full[s], kRaw + kBTile);
+        bulk_g2s(st + kATile + kBTile, a.codes + tile * F::TB, F::TB, &full[s]);
+        bulk_g2s(st + kATile + kBTile + F::TB, a.scales + tile * (128 * F::SB), 128 * F::SB, &full[s]);
+        if (FMT == FMT_Q6K)
+          bulk_g2s(st + kATile + kBTile + F::TB + 128 * F::SB, a.aux + ((int64_t)tile_n * (KG / 4) + kt / 4) * 256,
+                   256, &full[s]);
+        tma_load_2d(st + kATile, &tmx, kt * 64, t0, &full[s]);
+        ++issued;
+        if (++s == kPfStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      // do not leave copies in flight into this CTA's shared memory
+      for (int i = (issued > kPfStages ? issued - kPfStages : 0); i < issued; ++i)
+        mbar_wait_bounded(&full[i % kPfStages], (uint32_t)(i / kPfStages) & 1u, a.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kPfBN);
+      int s = 0;
+      uint32_t ph = 0;
+      for (int kt = 0; kt < KG; ++kt) {
+        if (!mbar_wait_bounded(&afull[s], ph, a.status) || !mbar_wait_bounded(&full[s], ph, a.status)) break;
+        tc_fence_after();
+        const uint32_t abase = smem_u32(smem + s * kPfStageBytes);
+        const uint32_t bbase = abase + kATile;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16_ss(tmem, sw128_desc(abase + kk * 32), sw128_desc(bbase + kk * 32), idesc, (kt | kk) ? 1u : 0u);
+        mma_commit(&empty[s]);
+        if (++s == kPfStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      mma_commit(done);  // also drains whatever was issued if the loop stopped early
+    }
+    __syncwarp();
+  } else {
+    // decode warps
+    const int dt = tid - 64;
+    const int r = dt & 127, h = dt >> 7;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int kt = 0; kt < KG; ++kt) {
+      if (!mbar_wait_bounded(&full[s], ph, a.status)) {
+        ok = false;
+        break;
+      }
+      uint8_t* st = smem + s * kPfStageBytes;
+      decode_stage<FMT>(st + kATile + kBTile, st, r, h);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull[s]);
+      if (++s == kPfStages) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    // epilogue: TMEM lanes 32*(warp%4).. hold output rows; warps 2-5 take tokens 0..127,
+    // warps 6-9 tokens 128..255
+    if (mbar_wait_bounded(done, 0, a.status) && ok) {
+      tc_fence_after();
+      const int quarter = warp & 3;
+      const int col0 = ((warp - 2) >> 2) * (kPfBN / 2);
+      const int64_t n = (int64_t)tile_n * 128 + quarter * 32 + lane;
+      for (int c = 0; c < kPfBN / 2; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(col0 + c), v);
+        tmem_ld_wait();
+        if (n < a.n) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int64_t t = t0 + col0 + c + j;
+            if (t < a.t) {
+              float o = a.ts * __uint_as_float(v[j]);
+              if (a.res) o += __bfloat162float(a.res[t * a.ldr + n]);
+              a.y[t * a.ldy + n] = __float2bfloat16_rn(o);
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kPfTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeFn g_encode = nullptr;
+
+EncodeFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeFn>(fn);
+  });
+  return g_encode;
+}
+}  // namespace
+
+int launch_prefill(const Geometry& g, const qg_weight* w, const void* x, int64_t t, int64_t ldx, const void* res,
+                   int64_t ldr, void* y, int64_t ldy, void* ws, void* stream) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return QG_ERR_CUDA;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)g.k, (cuuint64_t)t};
+  const cuuint64_t strides[1] = {(cuuint64_t)ldx * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kPfBN};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return QG_ERR_CUDA;
+  PrefillArgs a;
+  a.codes = static_cast<const uint8_t*>(w->codes);
+  a.scales = static_cast<const uint8_t*>(w->scales);
+  a.aux = static_cast<const uint8_t*>(w->aux);
+  a.res = static_cast<const __nv_bfloat16*>(res);
+  a.y = static_cast<__nv_bfloat16*>(y);
+  a.ldr = ldr;
+  a.ldy = ldy;
+  a.n = g.n;
+  a.t = t;
+  a.KG = (int)g.kg;
+  a.ts = (g.fmt == FMT_NVFP4) ? w->tensor_scale : 1.0f;
+  a.status = static_cast<int*>(ws);
+  const dim3 grid((unsigned)g.nt, (unsigned)((t + kPfBN - 1) / kPfBN));
+  if (grid.y > 65535u) return QG_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  static std::atomic<unsigned long long> configured[5];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QG_ERR_CUDA;
+  const unsigned long long bit = 1ull << (dev & 63);
+  auto config = [&](const void* fn) -> bool {
+    if (configured[g.fmt].load() & bit) return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem) != cudaSuccess) return false;
+    configured[g.fmt].fetch_or(bit);
+    return true;
+  };
+  switch (g.fmt) {
+    case FMT_MLX:
+      if (!config((const void*)prefill_kernel<FMT_MLX>)) return QG_ERR_CUDA;
+      prefill_kernel<FMT_MLX><<<grid, kPfThreads, kPfSmem, s>>>(map, a);
+      break;
+    case FMT_MXFP4:
+      if (!config((const void*)prefill_kernel<FMT_MXFP4>)) return QG_ERR_CUDA;
+      prefill_kernel<FMT_MXFP4><<<grid, kPfThreads, kPfSmem, s>>>(map, a);
+      break;
+    case FMT_NVFP4:
+      if (!config((const void*)prefill_kernel<FMT_NVFP4>)) return QG_ERR_CUDA;
+      prefill_kernel<FMT_NVFP4><<<grid, kPfThreads, kPfSmem, s>>>(map, a);
+      break;
+    default:
+      if (!config((const void*)prefill_kernel<FMT_Q6K>)) return QG_ERR_CUDA;
+      prefill_kernel<FMT_Q6K><<<grid, kPfThreads, kPfSmem, s>>>(map, a);
+      break;
+  }
+  return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+}
+
+}  // namespace qg

@@ -45,6 +45,8 @@ int launch_gemv(const Geometry& g, const qg_weight* w, const void* x, int m, int
                 const void* res, int64_t ldr, void* y, int64_t ldy, void* ws, const GemvPlan& p,
                 void* stream);
 int launch_dequant(const Geometry& g, const qg_weight* w, int out_dtype, void* out, int64_t ldo, void* stream);
+int launch_prefill(const Geometry& g, const qg_weight* w, const void* x, int64_t t, int64_t ldx, const void* res,
+                   int64_t ldr, void* y, int64_t ldy, void* ws, void* stream);
 
 constexpr size_t kWsHeader = 256;  // status word + reserved
 
