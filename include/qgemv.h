@@ -165,6 +165,56 @@ qg_status qgemm(const qg_weight* w, const void* x, int64_t m_rows, int64_t ldx,
                 const void* residual, int64_t ldr, void* y, int64_t ldy,
                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------ mixture of experts
+ * A layer of n_experts routed experts plus an optional shared expert, each an FFN with
+ * gate/up (2F x H: rows 0..F-1 gate, F..2F-1 up) and down (H x F) quantized matrices.
+ * The routed experts' packed matrices lie back to back: expert e's gate/up codes start
+ * at gu_codes + e * (codes bytes of one 2F x H matrix), and likewise for every array
+ * (sizes from qg_packed_sizes).  Limits: n_experts <= 512, topk <= 16. */
+typedef struct {
+  int32_t fmt;              /* qg_format of every matrix */
+  int32_t n_experts;
+  int64_t hidden;           /* H */
+  int64_t ffn;              /* F */
+  const void* gu_codes;     /* device, n_experts packed 2F x H matrices */
+  const void* gu_scales;
+  const void* gu_aux;       /* Q6_K d, else NULL */
+  const void* dn_codes;     /* device, n_experts packed H x F matrices */
+  const void* dn_scales;
+  const void* dn_aux;
+  float tensor_scale;       /* NVFP4 tensor scale of the routed experts, else 1.0f */
+  int32_t has_shared;       /* 1: the shared expert below joins every token with weight 1 */
+  qg_weight shared_gate_up; /* 2F x H */
+  qg_weight shared_down;    /* H x F */
+} qg_moe_layer;
+
+/* Router workspace bytes for t tokens. */
+size_t qmoe_route_workspace_size(int64_t t, int n_experts, int topk);
+
+/* Router (TurboEXL3 article §4.1 "Route", §4.2 top-k and softmax): for each token the
+ * topk experts by fp32 logit (ties to the lower index) and the softmax of the kept logits,
+ *   topk_ids [t][topk] int32, topk_w [t][topk] fp32 (device),
+ * and, in route_ws, the (token, slot) pairs grouped by expert -- experts ascending, tokens
+ * ascending within an expert -- with counts, offsets, the active experts and a tile
+ * table; deterministic, one launch for up to 32 tokens.  logits: fp32 [t][n_experts]. */
+qg_status qmoe_route(const float* logits, int64_t t, int n_experts, int topk,
+                     int32_t* topk_ids, float* topk_w, void* route_ws, size_t route_ws_bytes, void* stream);
+
+/* Workspace bytes qmoe_ffn needs for t tokens on the current device. */
+size_t qmoe_workspace_size(const qg_moe_layer* layer, int64_t t, int topk);
+
+/* One MoE FFN layer for 1..4 tokens (decode / speculative verify), after qmoe_route on the
+ * same logits:  out[t] = bf16( sum_j topk_w[t][j] * down_e(h) + shared(h) ),
+ * h = bf16(silu(gate) * up) per (token, expert), in five launches (TurboEXL3 article
+ * §4.2): gate/up as one grouped GEMV over the active experts that reads each expert's
+ * weights once for all its tokens, with the shared expert as extra groups; mid; down;
+ * finish.  x: bf16 [t][ldx] (H inputs); out: bf16 [t][ldo].  The workspace must be
+ * zero-filled before first use and not be shared by overlapping calls.
+ * t outside 1..4 returns QG_ERR_UNSUPPORTED. */
+qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t t, int64_t ldx, int topk,
+                   const float* topk_w, const void* route_ws, void* out, int64_t ldo,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Workspace-free variant of qgemv, for callers that cannot allocate device memory:
  * plugins hosted by a runtime that owns all of the GPU's memory and gives them no
  * allocator, and code on paths where cudaMalloc's implicit device synchronisation is not

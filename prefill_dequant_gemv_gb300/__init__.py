@@ -37,6 +37,14 @@ class qg_weight(ctypes.Structure):
                 ("aux", ctypes.c_void_p), ("tensor_scale", ctypes.c_float), ("reserved2", ctypes.c_float)]
 
 
+class qg_moe_layer(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("n_experts", ctypes.c_int32), ("hidden", ctypes.c_int64),
+                ("ffn", ctypes.c_int64), ("gu_codes", ctypes.c_void_p), ("gu_scales", ctypes.c_void_p),
+                ("gu_aux", ctypes.c_void_p), ("dn_codes", ctypes.c_void_p), ("dn_scales", ctypes.c_void_p),
+                ("dn_aux", ctypes.c_void_p), ("tensor_scale", ctypes.c_float), ("has_shared", ctypes.c_int32),
+                ("shared_gate_up", qg_weight), ("shared_down", qg_weight)]
+
+
 _lib = None
 _P, _I64, _I, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
 _SIGNATURES = {
@@ -51,6 +59,10 @@ _SIGNATURES = {
     "qgemv_static_ws": (_I, [ctypes.POINTER(qg_weight), _P, _I, _I64, _P, _I64, _P, _I64, _P]),
     "qg_gemm_workspace_size": (_SZ, [_I, _I64, _I64, _I]),
     "qgemm": (_I, [ctypes.POINTER(qg_weight), _P, _I64, _I64, _P, _I64, _P, _I64, _P, _SZ, _P]),
+    "qmoe_route_workspace_size": (_SZ, [_I64, _I, _I]),
+    "qmoe_route": (_I, [_P, _I64, _I, _I, _P, _P, _P, _SZ, _P]),
+    "qmoe_workspace_size": (_SZ, [ctypes.POINTER(qg_moe_layer), _I64, _I]),
+    "qmoe_ffn": (_I, [ctypes.POINTER(qg_moe_layer), _P, _I64, _I64, _I, _P, _P, _P, _I64, _P, _SZ, _P]),
 }
 
 
@@ -129,6 +141,25 @@ def qg_gemm_workspace_size(fmt: int, n: int, k: int, m: int) -> int:
 def qgemm(w: qg_weight, x_ptr: int, m: int, ldx: int, res_ptr: Optional[int], ldr: int, y_ptr: int, ldy: int,
           ws_ptr: int, ws_bytes: int, stream: int = 0):
     _check(lib().qgemm(ctypes.byref(w), x_ptr, m, ldx, res_ptr, ldr, y_ptr, ldy, ws_ptr, ws_bytes, stream), "qgemm")
+
+
+def qmoe_route_workspace_size(t: int, n_experts: int, topk: int) -> int:
+    return lib().qmoe_route_workspace_size(t, n_experts, topk)
+
+
+def qmoe_route(logits_ptr: int, t: int, n_experts: int, topk: int, ids_ptr: int, w_ptr: int, ws_ptr: int,
+               ws_bytes: int, stream: int = 0):
+    _check(lib().qmoe_route(logits_ptr, t, n_experts, topk, ids_ptr, w_ptr, ws_ptr, ws_bytes, stream), "qmoe_route")
+
+
+def qmoe_workspace_size(layer: qg_moe_layer, t: int, topk: int) -> int:
+    return lib().qmoe_workspace_size(ctypes.byref(layer), t, topk)
+
+
+def qmoe_ffn(layer: qg_moe_layer, x_ptr: int, t: int, ldx: int, topk: int, w_ptr: int, route_ws_ptr: int,
+             out_ptr: int, ldo: int, ws_ptr: int, ws_bytes: int, stream: int = 0):
+    _check(lib().qmoe_ffn(ctypes.byref(layer), x_ptr, t, ldx, topk, w_ptr, route_ws_ptr, out_ptr, ldo, ws_ptr,
+                          ws_bytes, stream), "qmoe_ffn")
 
 
 def qgemv_static_ws(w: qg_weight, x_ptr: int, m: int, ldx: int, res_ptr: Optional[int], ldr: int, y_ptr: int,
@@ -220,4 +251,68 @@ def gemm(pw: PackedWeight, x, residual=None, out=None, workspace: Optional[Works
     qgemm(pw.desc, x.data_ptr(), m, x.stride(0), None if residual is None else residual.data_ptr(),
           0 if residual is None else residual.stride(0), out.data_ptr(), out.stride(0), workspace.ptr,
           workspace.nbytes, _stream_ptr())
+    return out
+
+
+class PackedMoE:
+    """A mixture-of-experts layer packed on the host and resident in device memory: the
+    routed experts' packed matrices back to back, the shared expert separate."""
+
+    def __init__(self, layer, device="cuda"):
+        import torch
+        self.fmt, self.n_experts, self.hidden, self.ffn = layer.fmt, layer.n_experts, layer.hidden, layer.ffn
+
+        def pack_all(ws):
+            parts = [qg_pack_host(w.fmt, w.n, w.k, w.codes, w.scales, w.aux) for w in ws]
+            out = []
+            for i in range(3):
+                cat = np.concatenate([p[i] for p in parts]) if parts[0][i].size else np.zeros(0, np.uint8)
+                out.append(torch.from_numpy(cat).to(device) if cat.size else None)
+            return out
+
+        self.gu = pack_all(layer.gate_up)
+        self.dn = pack_all(layer.down)
+        self.shared = None
+        if layer.shared_gate_up is not None:
+            self.shared = (PackedWeight.from_logical(layer.shared_gate_up, device),
+                           PackedWeight.from_logical(layer.shared_down, device))
+        ts = layer.gate_up[0].tensor_scale if layer.fmt == FMT_NVFP4 else 1.0
+        empty = qg_weight(layer.fmt, 0, 0, 0, None, None, None, 1.0, 0.0)
+        self.desc = qg_moe_layer(
+            layer.fmt, layer.n_experts, layer.hidden, layer.ffn,
+            self.gu[0].data_ptr(), self.gu[1].data_ptr(), self.gu[2].data_ptr() if self.gu[2] is not None else None,
+            self.dn[0].data_ptr(), self.dn[1].data_ptr(), self.dn[2].data_ptr() if self.dn[2] is not None else None,
+            ts, 1 if self.shared else 0,
+            self.shared[0].desc if self.shared else empty, self.shared[1].desc if self.shared else empty)
+
+    @property
+    def nbytes_per_expert(self) -> int:
+        tot = sum(t.numel() for t in self.gu if t is not None) + sum(t.numel() for t in self.dn if t is not None)
+        return tot // self.n_experts
+
+
+def route(logits, topk: int, workspace: Optional[Workspace] = None):
+    """(topk_ids int32 [t, topk], topk_w fp32 [t, topk], route workspace) for fp32 logits [t, E] on the device."""
+    import torch
+    t, e = logits.shape
+    ids = torch.empty((t, topk), dtype=torch.int32, device=logits.device)
+    w = torch.empty((t, topk), dtype=torch.float32, device=logits.device)
+    if workspace is None:
+        workspace = Workspace(qmoe_route_workspace_size(t, e, topk), logits.device)
+    qmoe_route(logits.data_ptr(), t, e, topk, ids.data_ptr(), w.data_ptr(), workspace.ptr, workspace.nbytes,
+               _stream_ptr())
+    return ids, w, workspace
+
+
+def moe_ffn(pm: PackedMoE, x, topk_w, route_ws: Workspace, out=None, workspace: Optional[Workspace] = None):
+    """One MoE FFN layer for the routed tokens x bf16 [t, H] (t = 1..4)."""
+    import torch
+    t = x.shape[0]
+    topk = topk_w.shape[1]
+    if out is None:
+        out = torch.empty((t, (pm.hidden + 7) // 8 * 8), dtype=torch.bfloat16, device=x.device)[:, :pm.hidden]
+    if workspace is None:
+        workspace = Workspace(qmoe_workspace_size(pm.desc, t, topk), x.device)
+    qmoe_ffn(pm.desc, x.data_ptr(), t, x.stride(0), topk, topk_w.data_ptr(), route_ws.ptr, out.data_ptr(),
+             out.stride(0), workspace.ptr, workspace.nbytes, _stream_ptr())
     return out

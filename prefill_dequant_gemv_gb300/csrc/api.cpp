@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "qg_internal.h"
+#include "qg_route.h"
 
 namespace qg {
 
@@ -144,4 +145,73 @@ extern "C" qg_status qgemm(const qg_weight* w, const void* x, int64_t m, int64_t
   if (workspace_bytes < kWsHeader) return QG_ERR_WORKSPACE_TOO_SMALL;
   if ((m + 255) / 256 > 65535 || g.nt > 0x7FFFFFFF) return QG_ERR_UNSUPPORTED;
   return (qg_status)launch_prefill(g, w, x, m, ldx, residual, ldr, y, ldy, workspace, stream);
+}
+
+extern "C" size_t qmoe_route_workspace_size(int64_t t, int n_experts, int topk) {
+  if (t < 1 || n_experts < 1 || n_experts > kMaxExperts || topk < 1 || topk > kMaxTopk || topk > n_experts) return 0;
+  return route_layout(t, n_experts, topk).total;
+}
+
+extern "C" qg_status qmoe_route(const float* logits, int64_t t, int n_experts, int topk, int32_t* topk_ids,
+                                float* topk_w, void* route_ws, size_t route_ws_bytes, void* stream) {
+  if (t < 1 || n_experts < 1 || topk < 1 || topk > n_experts) return QG_ERR_INVALID_ARG;
+  if (n_experts > kMaxExperts || topk > kMaxTopk || t * topk > 0x7FFFFFFF) return QG_ERR_UNSUPPORTED;
+  if (!logits || !topk_ids || !topk_w || !route_ws) return QG_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w) || !aligned16(route_ws))
+    return QG_ERR_MISALIGNED;
+  if (route_ws_bytes < route_layout(t, n_experts, topk).total) return QG_ERR_WORKSPACE_TOO_SMALL;
+  return (qg_status)launch_route(logits, t, n_experts, topk, topk_ids, topk_w, route_ws, stream);
+}
+
+static int check_moe(const qg_moe_layer* m, int64_t t, int topk, Geometry* gu, Geometry* dn) {
+  if (!m || t < 1 || topk < 1) return QG_ERR_INVALID_ARG;
+  if (m->n_experts < 1 || topk > m->n_experts) return QG_ERR_INVALID_ARG;
+  if (m->n_experts > kMaxExperts || topk > kMaxTopk) return QG_ERR_UNSUPPORTED;
+  if (!geometry(m->fmt, 2 * m->ffn, m->hidden, gu) || !geometry(m->fmt, m->hidden, m->ffn, dn))
+    return QG_ERR_INVALID_ARG;
+  if (!m->gu_codes || !m->gu_scales || !m->dn_codes || !m->dn_scales) return QG_ERR_INVALID_ARG;
+  if (m->fmt == QG_FMT_Q6K && (!m->gu_aux || !m->dn_aux)) return QG_ERR_INVALID_ARG;
+  if (m->fmt != QG_FMT_NVFP4 && m->tensor_scale != 1.0f) return QG_ERR_INVALID_ARG;
+  if (!aligned16(m->gu_codes) || !aligned16(m->gu_scales) || !aligned16(m->dn_codes) || !aligned16(m->dn_scales) ||
+      (m->gu_aux && !aligned16(m->gu_aux)) || (m->dn_aux && !aligned16(m->dn_aux)))
+    return QG_ERR_MISALIGNED;
+  if (m->has_shared) {
+    Geometry g1, g2;
+    int st = check_weight(&m->shared_gate_up, &g1);
+    if (st != QG_OK) return st;
+    st = check_weight(&m->shared_down, &g2);
+    if (st != QG_OK) return st;
+    if (m->shared_gate_up.fmt != m->fmt || m->shared_down.fmt != m->fmt || g1.n != gu->n || g1.k != gu->k ||
+        g2.n != dn->n || g2.k != dn->k)
+      return QG_ERR_INVALID_ARG;
+  }
+  return QG_OK;
+}
+
+extern "C" size_t qmoe_workspace_size(const qg_moe_layer* layer, int64_t t, int topk) {
+  Geometry gu, dn;
+  if (check_moe(layer, t, topk, &gu, &dn) != QG_OK) return 0;
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return 0;
+  return moe_layout(gu, dn, t, layer->n_experts, topk, dev.sms).total;
+}
+
+extern "C" qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t t, int64_t ldx, int topk,
+                              const float* topk_w, const void* route_ws, void* out, int64_t ldo, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  Geometry gu, dn;
+  int st = check_moe(layer, t, topk, &gu, &dn);
+  if (st != QG_OK) return (qg_status)st;
+  if (t > 4) return QG_ERR_UNSUPPORTED;
+  if (!x || !topk_w || !route_ws || !out || !workspace) return QG_ERR_INVALID_ARG;
+  if (ldx < layer->hidden || ldo < layer->hidden) return QG_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(workspace) || !aligned16(route_ws) || !aligned16(topk_w))
+    return QG_ERR_MISALIGNED;
+  if (ldx % 8 || ldo % 8) return QG_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return QG_ERR_CUDA;
+  if (workspace_bytes < moe_layout(gu, dn, t, layer->n_experts, topk, dev.sms).total)
+    return QG_ERR_WORKSPACE_TOO_SMALL;
+  return (qg_status)launch_moe_decode(layer, gu, dn, x, t, ldx, topk, topk_w, route_ws, out, ldo, workspace, dev,
+                                      stream);
 }

@@ -25,15 +25,11 @@
 #include <atomic>
 
 #include "qg_common.cuh"
+#include "qg_gemv_core.cuh"
 #include "qg_internal.h"
 #include "qg_sync.cuh"
 
 namespace qg {
-
-// Consumer warps: 16 for 1-2 rows; 12 for 3-4 rows, whose accumulators need the
-// 128 registers a 13-warp CTA allows (warps are allocated in groups of four).
-__host__ __device__ constexpr int consumer_warps(int m) { return m >= 3 ? 12 : 16; }
-constexpr int kMaxStages = 48;
 
 struct GemvArgs {
   const uint8_t* codes;
@@ -52,17 +48,6 @@ struct GemvArgs {
   float* ws_part;  // [grid][2][M][128]
   int* ws_cnt;     // [NT]
   int* status;
-};
-
-// One pipeline stage holds a chunk of C consecutive units (tile index = unit index,
-// so a chunk is one contiguous range of codes and one of scales): a single bulk
-// copy per array per chunk keeps the copy engine at HBM speed, which 4-6 KB
-// copies do not reach.
-template <int FMT> struct Stage {
-  static constexpr int CODE = Fmt<FMT>::TB;            // per unit
-  static constexpr int SCALE = 128 * Fmt<FMT>::SB;     // per unit
-  static constexpr int AUX = (FMT == FMT_Q6K) ? 256 : 0;  // per 4 units (Q6_K d)
-  __host__ __device__ static constexpr int bytes(int C) { return C * (CODE + SCALE) + 2 * AUX; }
 };
 
 struct SmemLayout {
@@ -94,29 +79,10 @@ __host__ __device__ inline SmemLayout gemv_smem_layout(int stage_bytes, int S, i
   return L;
 }
 
-__host__ __device__ inline int64_t owner_cta(int64_t u, int64_t U, int64_t G) {
-  // CTA b owns units [b*U/G, (b+1)*U/G); the owner of u is the largest b with b*U/G <= u.
-  return ((u + 1) * G - 1) / U;
-}
-
-__device__ __forceinline__ void bf16x2_to_f32(uint32_t v, float& lo, float& hi) {
-  lo = __uint_as_float(v << 16);
-  hi = __uint_as_float(v & 0xFFFF0000u);
-}
-
-// Stage the activation rows into shared memory as f16, exactly: every 16-input
-// quarter of row m is scaled by its own power of two 2^p chosen from its largest
-// |x|, so each bf16 value (8 significant bits) lands inside f16's range; a value
-// more than 2^27 below its quarter's maximum would round, far below the stated
-// tolerance.  Per quarter the staging records four floats: {2^-p (E2M1) or
-// 64 * 2^-p (integer formats), Z, X, 0}; Z and X, in unscaled units, remove the
-// integer operands' constant and the Q6_K zero point in the fold.
-// Layout per 8 inputs (one code word) and row m: four f16x2 words in the order the
-// decoder produces operand pairs -- E2M1: (x0,x1) (x2,x3) (x4,x5) (x6,x7); integer
-// formats: (16x0,16x4) (x1,x5) (16x2,16x6) (x3,x7).
+// Stage the activation rows of a CTA's input groups into shared memory (see
+// stage_quarter): row m, slot s, quarter kq -> 8 staging words and one record.
 template <int FMT, int M, int kCT>
 __device__ void stage_x(const GemvArgs& a, uint32_t* xs, float* sums, int sbase, int nslots, int tid) {
-  constexpr bool kInt = (FMT == FMT_MLX || FMT == FMT_Q6K);
   const int items = M * nslots * 4;
   for (int it = tid; it < items; it += kCT) {
     const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
@@ -131,154 +97,8 @@ __device__ void stage_x(const GemvArgs& a, uint32_t* xs, float* sums, int sbase,
 #pragma unroll
       for (int i = 0; i < 8; ++i) u[i] = 0;
     }
-    uint32_t mb = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mb = max(mb, max(u[i] & 0x7FFFu, (u[i] >> 16) & 0x7FFFu));
-    const int e = mb >= 0x80 ? (int)(mb >> 7) - 127 : -127;
-    int p = (kInt ? 10 : 14) - e;
-    if (mb >= 0x7F80u || mb == 0) p = 0;  // inf / nan / all zero: leave as is
-    p = max(-126, min(126, p));
-    const float scale = __uint_as_float((uint32_t)(p + 127) << 23);
-    const float inv = __uint_as_float((uint32_t)(127 - p) << 23);
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float lo, hi;
-      bf16x2_to_f32(u[i], lo, hi);
-      v[2 * i] = __half2float(__float2half_rn(lo * scale));
-      v[2 * i + 1] = __half2float(__float2half_rn(hi * scale));
-    }
-    uint32_t* dst = xs + (size_t)(m * nslots + s) * 32 + kq * 8;
-    auto h2 = [](float lo, float hi) {
-      __half2 h = __floats2half2_rn(lo, hi);
-      return *reinterpret_cast<uint32_t*>(&h);
-    };
-    float4 z = make_float4(inv, 0.0f, 0.0f, 0.0f);
-    if (kInt) {
-      float x16 = 0.0f, x1 = 0.0f;
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        const float* q = v + 8 * w;
-        reinterpret_cast<uint4*>(dst)[w] = make_uint4(h2(16.0f * q[0], 16.0f * q[4]), h2(q[1], q[5]),
-                                                      h2(16.0f * q[2], 16.0f * q[6]), h2(q[3], q[7]));
-        x16 += (q[0] + q[4]) + (q[2] + q[6]);
-        x1 += (q[1] + q[5]) + (q[3] + q[7]);
-      }
-      const float xsum = (x16 + x1) * inv;           // X, unscaled
-      const float xop = fmaf(16.0f, x16, x1) * inv;  // the operands' constant part, unscaled
-      z.x = 64.0f * inv;
-      z.y = (FMT == FMT_Q6K) ? fmaf(64.0f, xop, 32.0f * xsum) : 64.0f * xop;
-      z.z = xsum;
-    } else {
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-        reinterpret_cast<uint4*>(dst)[i] = make_uint4(h2(v[8 * i], v[8 * i + 1]), h2(v[8 * i + 2], v[8 * i + 3]),
-                                                      h2(v[8 * i + 4], v[8 * i + 5]), h2(v[8 * i + 6], v[8 * i + 7]));
-    }
+    const float4 z = stage_quarter<FMT>(u, xs + (size_t)(m * nslots + s) * 32 + kq * 8);
     reinterpret_cast<float4*>(sums)[(size_t)(m * nslots + s) * 4 + kq] = z;
-  }
-}
-
-// One consumer warp, one unit, one 16-input quarter: accumulate 4 rows x M.
-template <int FMT, int M>
-__device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, const uint8_t* aux, const uint32_t* xq,
-                                        int mstride, const float* sq, int sstride, const float* e4m3_lut, int kq,
-                                        int lane, float (&acc)[4][M]) {
-  using F = Fmt<FMT>;
-  uint32_t wd[4][2];
-  uint32_t hw[4];
-#pragma unroll
-  for (int rt = 0; rt < 4; ++rt) {
-    const uint2 v = *reinterpret_cast<const uint2*>(st + ((rt * F::CH + (kq >> 1)) * 32 + lane) * 16 + (kq & 1) * 8);
-    wd[rt][0] = v.x;
-    wd[rt][1] = v.y;
-    if (FMT == FMT_Q6K) hw[rt] = *reinterpret_cast<const uint32_t*>(st + ((rt * 3 + 2) * 32 + lane) * 16 + kq * 4);
-  }
-  float P[4][M][2];
-#pragma unroll
-  for (int rt = 0; rt < 4; ++rt)
-#pragma unroll
-    for (int m = 0; m < M; ++m) P[rt][m][0] = P[rt][m][1] = 0.0f;
-
-#pragma unroll
-  for (int wi = 0; wi < 2; ++wi) {
-    uint4 X[M];
-#pragma unroll
-    for (int m = 0; m < M; ++m) X[m] = *reinterpret_cast<const uint4*>(xq + m * mstride + wi * 4);
-#pragma unroll
-    for (int rt = 0; rt < 4; ++rt) {
-      const uint32_t w = wd[rt][wi];
-      uint32_t o0, o1, o2, o3;
-      if (FMT == FMT_MXFP4 || FMT == FMT_NVFP4) {
-        o0 = e2m1x2_h2<0>(w);
-        o1 = e2m1x2_h2<1>(w);
-        o2 = e2m1x2_h2<2>(w);
-        o3 = e2m1x2_h2<3>(w);
-      } else if (FMT == FMT_MLX) {
-        const uint32_t r = rot8(w);
-        o0 = i4_op_lo(w);
-        o1 = i4_op_hi(w);
-        o2 = i4_op_lo(r);
-        o3 = i4_op_hi(r);
-      } else {
-        const uint32_t h = q6k_hi_for(hw[rt], wi);
-        const uint32_t r = rot8(w), hr = rot8(h);
-        o0 = i6_op_lo(w, h);
-        o1 = i6_op_hi(w, h);
-        o2 = i6_op_lo(r, hr);
-        o3 = i6_op_hi(r, hr);
-      }
-#pragma unroll
-      for (int m = 0; m < M; ++m) {
-        float p0 = P[rt][m][0], p1 = P[rt][m][1];
-        p0 = hfma_lo(o0, X[m].x, p0);
-        p1 = hfma_hi(o0, X[m].x, p1);
-        p0 = hfma_lo(o1, X[m].y, p0);
-        p1 = hfma_hi(o1, X[m].y, p1);
-        p0 = hfma_lo(o2, X[m].z, p0);
-        p1 = hfma_hi(o2, X[m].z, p1);
-        p0 = hfma_lo(o3, X[m].w, p0);
-        p1 = hfma_hi(o3, X[m].w, p1);
-        P[rt][m][0] = p0;
-        P[rt][m][1] = p1;
-      }
-    }
-  }
-  // Fold the quarter's partial with the block scale (once per block and row).
-  float4 zq[M];
-#pragma unroll
-  for (int m = 0; m < M; ++m) zq[m] = *reinterpret_cast<const float4*>(sq + m * sstride);
-#pragma unroll
-  for (int rt = 0; rt < 4; ++rt) {
-    const int row = rt * 32 + lane;
-    const uint8_t* sp = scl + row * F::SB;
-    if (FMT == FMT_NVFP4) {
-      const float S = e4m3_lut[sp[kq]];
-#pragma unroll
-      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * zq[m].x, P[rt][m][0] + P[rt][m][1], acc[rt][m]);
-    } else if (FMT == FMT_MXFP4) {
-      const float S = e8m0_f32(sp[kq >> 1]);
-#pragma unroll
-      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * zq[m].x, P[rt][m][0] + P[rt][m][1], acc[rt][m]);
-    } else if (FMT == FMT_MLX) {
-      const uint32_t sw = *reinterpret_cast<const uint32_t*>(sp);
-      const float s = __half2float(__ushort_as_half((unsigned short)(sw & 0xFFFFu)));
-      const float bias = __half2float(__ushort_as_half((unsigned short)(sw >> 16)));
-#pragma unroll
-      for (int m = 0; m < M; ++m) {
-        const float dot = fmaf(zq[m].x, P[rt][m][0] + P[rt][m][1], -zq[m].y);
-        acc[rt][m] = fmaf(s, dot, fmaf(bias, zq[m].z, acc[rt][m]));
-      }
-    } else {
-      const float sc = (float)(int8_t)sp[kq];
-      const float d = __half2float(*reinterpret_cast<const __half*>(aux + row * 2));
-      const float ds = d * sc;
-#pragma unroll
-      for (int m = 0; m < M; ++m) {
-        const float dot = fmaf(zq[m].x, P[rt][m][0] + P[rt][m][1], -zq[m].y);
-        acc[rt][m] = fmaf(ds, dot, acc[rt][m]);
-      }
-    }
   }
 }
 
@@ -404,9 +224,14 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
       const uint8_t* st = stages + (size_t)s * SB;
       const uint32_t uu = uu0 + i;
       const uint8_t* aux = st + C * (SG::CODE + SG::SCALE) + ((uu >> 2) - ((uu - ug) >> 2)) * SG::AUX;
-      consume<FMT, M>(st + ug * SG::CODE, st + C * SG::CODE + ug * SG::SCALE, aux,
-                      reinterpret_cast<const uint32_t*>(xq_base + (size_t)slot * 128), nslots * 32,
-                      sq_base + (size_t)slot * 16, nslots * 16, lut, kq, lane, acc);
+      const uint32_t* xr[M];
+      const float* zr[M];
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        xr[m] = reinterpret_cast<const uint32_t*>(xq_base + (size_t)slot * 128) + (size_t)m * nslots * 32;
+        zr[m] = sq_base + (size_t)slot * 16 + (size_t)m * nslots * 16;
+      }
+      consume<FMT, M>(st + ug * SG::CODE, st + C * SG::CODE + ug * SG::SCALE, aux, xr, zr, lut, kq, lane, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       if (++s == S) {

@@ -1,0 +1,204 @@
+// GEMV building blocks shared by the dense and the grouped (mixture-of-experts)
+// quantized GEMV kernels: pipeline-stage geometry, activation staging as exact f16,
+// and the per-quarter decode + mixed-precision FMA + block-scale fold.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "qg_common.cuh"
+
+namespace qg {
+
+// Consumer warps: 16 for 1-2 rows; 12 for 3-4 rows, whose accumulators need the
+// 128 registers a 13-warp CTA allows (warps are allocated in groups of four).
+__host__ __device__ constexpr int consumer_warps(int m) { return m >= 3 ? 12 : 16; }
+constexpr int kMaxStages = 48;
+
+// One pipeline stage holds a chunk of C consecutive units (tile index = unit index,
+// so a chunk is one contiguous range of codes and one of scales): a single bulk
+// copy per array per chunk keeps the copy engine at HBM speed, which 4-6 KB
+// copies do not reach.
+template <int FMT> struct Stage {
+  static constexpr int CODE = Fmt<FMT>::TB;            // per unit
+  static constexpr int SCALE = 128 * Fmt<FMT>::SB;     // per unit
+  static constexpr int AUX = (FMT == FMT_Q6K) ? 256 : 0;  // per 4 units (Q6_K d)
+  __host__ __device__ static constexpr int bytes(int C) { return C * (CODE + SCALE) + 2 * AUX; }
+};
+
+__host__ __device__ inline int64_t owner_cta(int64_t u, int64_t U, int64_t G) {
+  // CTA b owns units [b*U/G, (b+1)*U/G); the owner of u is the largest b with b*U/G <= u.
+  return ((u + 1) * G - 1) / U;
+}
+
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t v, float& lo, float& hi) {
+  lo = __uint_as_float(v << 16);
+  hi = __uint_as_float(v & 0xFFFF0000u);
+}
+
+// Stage 16 activations (eight bf16 pairs `u`) of one row as f16, exactly: the quarter is
+// scaled by its own power of two 2^p chosen from its largest |x|, so each bf16 value
+// (8 significant bits) lands inside f16's range; a value more than 2^27 below the
+// quarter's maximum would round, far below the stated tolerance.  Writes the two 16-byte
+// staging words to `dst` and returns the quarter's record {2^-p (E2M1) or 64 * 2^-p
+// (integer formats), Z, X, 0}; Z and X, in unscaled units, remove the integer operands'
+// constant and the Q6_K zero point in the fold.
+// Layout per 8 inputs (one code word): four f16x2 words in the order the decoder
+// produces operand pairs -- E2M1: (x0,x1) (x2,x3) (x4,x5) (x6,x7); integer formats:
+// (16x0,16x4) (x1,x5) (16x2,16x6) (x3,x7).
+template <int FMT>
+__device__ __forceinline__ float4 stage_quarter(const uint32_t (&u)[8], uint32_t* dst) {
+  constexpr bool kInt = (FMT == FMT_MLX || FMT == FMT_Q6K);
+  uint32_t mb = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mb = max(mb, max(u[i] & 0x7FFFu, (u[i] >> 16) & 0x7FFFu));
+  const int e = mb >= 0x80 ? (int)(mb >> 7) - 127 : -127;
+  int p = (kInt ? 10 : 14) - e;
+  if (mb >= 0x7F80u || mb == 0) p = 0;  // inf / nan / all zero: leave as is
+  p = max(-126, min(126, p));
+  const float scale = __uint_as_float((uint32_t)(p + 127) << 23);
+  const float inv = __uint_as_float((uint32_t)(127 - p) << 23);
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float lo, hi;
+    bf16x2_to_f32(u[i], lo, hi);
+    v[2 * i] = __half2float(__float2half_rn(lo * scale));
+    v[2 * i + 1] = __half2float(__float2half_rn(hi * scale));
+  }
+  auto h2 = [](float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  };
+  float4 z = make_float4(inv, 0.0f, 0.0f, 0.0f);
+  if (kInt) {
+    float x16 = 0.0f, x1 = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const float* q = v + 8 * w;
+      reinterpret_cast<uint4*>(dst)[w] = make_uint4(h2(16.0f * q[0], 16.0f * q[4]), h2(q[1], q[5]),
+                                                    h2(16.0f * q[2], 16.0f * q[6]), h2(q[3], q[7]));
+      x16 += (q[0] + q[4]) + (q[2] + q[6]);
+      x1 += (q[1] + q[5]) + (q[3] + q[7]);
+    }
+    const float xsum = (x16 + x1) * inv;           // X, unscaled
+    const float xop = fmaf(16.0f, x16, x1) * inv;  // the operands' constant part, unscaled
+    z.x = 64.0f * inv;
+    z.y = (FMT == FMT_Q6K) ? fmaf(64.0f, xop, 32.0f * xsum) : 64.0f * xop;
+    z.z = xsum;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      reinterpret_cast<uint4*>(dst)[i] = make_uint4(h2(v[8 * i], v[8 * i + 1]), h2(v[8 * i + 2], v[8 * i + 3]),
+                                                    h2(v[8 * i + 4], v[8 * i + 5]), h2(v[8 * i + 6], v[8 * i + 7]));
+  }
+  return z;
+}
+
+// One consumer warp, one unit, one 16-input quarter: accumulate 4 rows x M (of arrays
+// sized MA >= M).  xr[m] points at row m's 8 staging words of this quarter, zr[m] at its
+// record.
+template <int FMT, int M, int MA = M>
+__device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, const uint8_t* aux,
+                                        const uint32_t* const (&xr)[MA], const float* const (&zr)[MA],
+                                        const float* e4m3_lut, int kq, int lane, float (&acc)[4][MA]) {
+  using F = Fmt<FMT>;
+  uint32_t wd[4][2];
+  uint32_t hw[4];
+#pragma unroll
+  for (int rt = 0; rt < 4; ++rt) {
+    const uint2 v = *reinterpret_cast<const uint2*>(st + ((rt * F::CH + (kq >> 1)) * 32 + lane) * 16 + (kq & 1) * 8);
+    wd[rt][0] = v.x;
+    wd[rt][1] = v.y;
+    if (FMT == FMT_Q6K) hw[rt] = *reinterpret_cast<const uint32_t*>(st + ((rt * 3 + 2) * 32 + lane) * 16 + kq * 4);
+  }
+  float P[4][M][2];
+#pragma unroll
+  for (int rt = 0; rt < 4; ++rt)
+#pragma unroll
+    for (int m = 0; m < M; ++m) P[rt][m][0] = P[rt][m][1] = 0.0f;
+
+#pragma unroll
+  for (int wi = 0; wi < 2; ++wi) {
+    uint4 X[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) X[m] = *reinterpret_cast<const uint4*>(xr[m] + wi * 4);
+#pragma unroll
+    for (int rt = 0; rt < 4; ++rt) {
+      const uint32_t w = wd[rt][wi];
+      uint32_t o0, o1, o2, o3;
+      if (FMT == FMT_MXFP4 || FMT == FMT_NVFP4) {
+        o0 = e2m1x2_h2<0>(w);
+        o1 = e2m1x2_h2<1>(w);
+        o2 = e2m1x2_h2<2>(w);
+        o3 = e2m1x2_h2<3>(w);
+      } else if (FMT == FMT_MLX) {
+        const uint32_t r = rot8(w);
+        o0 = i4_op_lo(w);
+        o1 = i4_op_hi(w);
+        o2 = i4_op_lo(r);
+        o3 = i4_op_hi(r);
+      } else {
+        const uint32_t h = q6k_hi_for(hw[rt], wi);
+        const uint32_t r = rot8(w), hr = rot8(h);
+        o0 = i6_op_lo(w, h);
+        o1 = i6_op_hi(w, h);
+        o2 = i6_op_lo(r, hr);
+        o3 = i6_op_hi(r, hr);
+      }
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        float p0 = P[rt][m][0], p1 = P[rt][m][1];
+        p0 = hfma_lo(o0, X[m].x, p0);
+        p1 = hfma_hi(o0, X[m].x, p1);
+        p0 = hfma_lo(o1, X[m].y, p0);
+        p1 = hfma_hi(o1, X[m].y, p1);
+        p0 = hfma_lo(o2, X[m].z, p0);
+        p1 = hfma_hi(o2, X[m].z, p1);
+        p0 = hfma_lo(o3, X[m].w, p0);
+        p1 = hfma_hi(o3, X[m].w, p1);
+        P[rt][m][0] = p0;
+        P[rt][m][1] = p1;
+      }
+    }
+  }
+  // Fold the quarter's partial with the block scale (once per block and row).
+  float4 zq[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) zq[m] = *reinterpret_cast<const float4*>(zr[m]);
+#pragma unroll
+  for (int rt = 0; rt < 4; ++rt) {
+    const int row = rt * 32 + lane;
+    const uint8_t* sp = scl + row * F::SB;
+    if (FMT == FMT_NVFP4) {
+      const float S = e4m3_lut[sp[kq]];
+#pragma unroll
+      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * zq[m].x, P[rt][m][0] + P[rt][m][1], acc[rt][m]);
+    } else if (FMT == FMT_MXFP4) {
+      const float S = e8m0_f32(sp[kq >> 1]);
+#pragma unroll
+      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * zq[m].x, P[rt][m][0] + P[rt][m][1], acc[rt][m]);
+    } else if (FMT == FMT_MLX) {
+      const uint32_t sw = *reinterpret_cast<const uint32_t*>(sp);
+      const float s = __half2float(__ushort_as_half((unsigned short)(sw & 0xFFFFu)));
+      const float bias = __half2float(__ushort_as_half((unsigned short)(sw >> 16)));
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const float dot = fmaf(zq[m].x, P[rt][m][0] + P[rt][m][1], -zq[m].y);
+        acc[rt][m] = fmaf(s, dot, fmaf(bias, zq[m].z, acc[rt][m]));
+      }
+    } else {
+      const float sc = (float)(int8_t)sp[kq];
+      const float d = __half2float(*reinterpret_cast<const __half*>(aux + row * 2));
+      const float ds = d * sc;
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const float dot = fmaf(zq[m].x, P[rt][m][0] + P[rt][m][1], -zq[m].y);
+        acc[rt][m] = fmaf(ds, dot, acc[rt][m]);
+      }
+    }
+  }
+}
+
+}  // namespace qg

@@ -50,4 +50,14 @@ int launch_prefill(const Geometry& g, const qg_weight* w, const void* x, int64_t
 
 constexpr size_t kWsHeader = 256;  // status word + reserved
 
+// Mixture-of-experts decode workspace (after the status header).
+struct MoeLayout {
+  size_t cnt, part, gu, h, d, total;
+  int64_t ld_gu, ld_h, ld_d;
+};
+MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, int topk, int grid);
+int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
+                      int64_t ldx, int topk, const float* topk_w, const void* route_ws, void* out, int64_t ldo,
+                      void* ws, const DeviceInfo& dev, void* stream);
+
 }  // namespace qg

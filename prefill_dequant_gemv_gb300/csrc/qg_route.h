@@ -1,0 +1,57 @@
+// Router workspace layout (host and device).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace qg {
+
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopk = 16;
+constexpr int kRouteTile = 256;  // pairs per grouped-prefill tile (the tensor-core N)
+
+struct RouteLayout {
+  size_t meta, counts, offsets, active, pair_list, pair_pos, tiles, block_counts, block_start, total;
+  int64_t max_tiles, nblocks;
+};
+
+__host__ __device__ inline RouteLayout route_layout(int64_t T, int E, int k) {
+  RouteLayout L;
+  const int64_t P = T * k;
+  L.nblocks = (P + 1023) / 1024;
+  L.max_tiles = (P + kRouteTile - 1) / kRouteTile + E;
+  size_t o = 0;
+  auto take = [&o](size_t bytes) {
+    const size_t at = o;
+    o += (bytes + 255) & ~(size_t)255;
+    return at;
+  };
+  L.meta = take(64);                      // [0] active experts, [1] tiles
+  L.counts = take((size_t)E * 4);
+  L.offsets = take((size_t)(E + 1) * 4);
+  L.active = take((size_t)E * 4);
+  L.pair_list = take((size_t)P * 4);      // grouped position -> pair t*k + j
+  L.pair_pos = take((size_t)P * 4);       // pair -> grouped position
+  L.tiles = take((size_t)L.max_tiles * 12);  // (expert, first position, count)
+  L.block_counts = take((size_t)L.nblocks * E * 4);
+  L.block_start = take((size_t)L.nblocks * E * 4);
+  L.total = o;
+  return L;
+}
+
+struct RouteView {
+  int* meta;
+  int* counts;
+  int* offsets;
+  int* active;
+  int* pair_list;
+  int* pair_pos;
+  int* tiles;
+  int* block_counts;
+  int* block_start;
+};
+
+RouteView route_view(void* ws, int64_t T, int E, int k);
+int launch_route(const float* logits, int64_t T, int E, int k, int32_t* ids, float* wts, void* ws, void* stream);
+
+}  // namespace qg

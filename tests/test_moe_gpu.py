@@ -1,0 +1,128 @@
+"""GPU parity of the mixture-of-experts decode chain (route, grouped gate/up GEMV, SwiGLU,
+grouped down GEMV, weighted finish) against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from tests.gpu_util import dev_bf16, qlib, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q():
+    return qlib()
+
+
+def _route(q, lg):
+    lt = torch.from_numpy(np.ascontiguousarray(lg, dtype=np.float32)).cuda()
+    ids, w, ws = q.route(lt, TOPK[0])
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy(), ws
+
+
+TOPK = [10]
+
+
+@pytest.mark.parametrize("t,e,k", [(1, 512, 10), (4, 512, 10), (3, 64, 4), (32, 512, 10), (300, 128, 6), (8192, 512, 10)])
+def test_route_matches_oracle(q, t, e, k):
+    lg = wl.router_logits(t, e, seed=t + e + k)
+    lt = torch.from_numpy(np.ascontiguousarray(lg)).cuda()
+    ids, w, ws = q.route(lt, k)
+    torch.cuda.synchronize()
+    rid, rp = oracle.route(lg, k)
+    assert np.array_equal(ids.cpu().numpy(), rid)  # integer decisions from the same fp32 logits
+    assert np.allclose(w.cpu().numpy(), rp, rtol=2e-6, atol=1e-7)
+    ids2, w2, _ = q.route(lt, k)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids2) and torch.equal(w, w2)
+
+
+def test_route_ties_go_to_lower_index(q):
+    lg = np.zeros((4, 64), np.float32)
+    lg[:, 10] = 1.0
+    lg[:, 20] = 1.0
+    lg[2, :] = 0.5
+    lt = torch.from_numpy(lg).cuda()
+    ids, w, _ = q.route(lt, 3)
+    torch.cuda.synchronize()
+    rid, rp = oracle.route(lg, 3)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+
+
+def moe_tolerance(o, layer, x, lg, topk, out_ref):
+    """Per-element bound: each expert's down output within the GEMV bound of its (bf16) input
+    h plus one bf16 ulp of h (rounding flips between the two sides), weighted by p; plus one
+    output ulp."""
+    _, _, ids, p, inter = o.moe_forward(layer, x, lg, topk, with_intermediates=True)
+    T = x.shape[0]
+    tol = np.zeros((T, layer.hidden))
+    rn = {}
+    for t in range(T):
+        for j in range(topk):
+            e = int(ids[t, j])
+            if e not in rn:
+                rn[e] = float(np.max(o.row_norms(layer.down[e])))
+            h = inter[(t, e)][2]
+            tol[t] += p[t, j] * (2e-3 + 2.0 ** -8) * np.linalg.norm(h) * rn[e]
+        if layer.shared_down is not None:
+            h = inter[(t, -1)][2]
+            tol[t] += (2e-3 + 2.0 ** -8) * np.linalg.norm(h) * float(np.max(o.row_norms(layer.shared_down)))
+    return tol + 2.0 ** -7 * np.abs(out_ref)
+
+
+@pytest.mark.parametrize("fmt", [wl.MXFP4, wl.NVFP4, wl.MLX_AFFINE4_G64, wl.Q6K])
+@pytest.mark.parametrize("t", [1, 2, 4])
+def test_moe_decode_small(q, fmt, t):
+    E, H, F, k = 16, 512 if fmt == wl.Q6K else 256, 256 if fmt == wl.Q6K else 128, 4
+    layer = wl.moe_layer(fmt, E, H, F, seed=300 + fmt, shared=True)
+    x = wl.moe_tokens(t, H, seed=301)
+    lg = wl.router_logits(t, E, seed=302)
+    pm = q.PackedMoE(layer)
+    lt = torch.from_numpy(lg).cuda()
+    ids, w, rws = q.route(lt, k)
+    out = q.moe_ffn(pm, dev_bf16(x), w, rws)
+    torch.cuda.synchronize()
+    got = to_f64(out)
+    ref = oracle.moe_forward(layer, x, lg, k)
+    tol = moe_tolerance(oracle, layer, x, lg, k, ref)
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got))
+    assert np.all(err <= tol), f"{np.sum(err > tol)} out of tolerance, worst {np.max(err - tol)}"
+
+
+def test_moe_decode_without_shared(q):
+    E, H, F, k, t = 8, 256, 128, 3, 4
+    layer = wl.moe_layer(wl.MXFP4, E, H, F, seed=310, shared=False)
+    x = wl.moe_tokens(t, H, seed=311)
+    lg = wl.router_logits(t, E, seed=312)
+    pm = q.PackedMoE(layer)
+    ids, w, rws = q.route(torch.from_numpy(lg).cuda(), k)
+    out = q.moe_ffn(pm, dev_bf16(x), w, rws)
+    torch.cuda.synchronize()
+    ref = oracle.moe_forward(layer, x, lg, k)
+    assert np.all(np.abs(to_f64(out) - ref) <= moe_tolerance(oracle, layer, x, lg, k, ref))
+
+
+def test_moe_decode_full_config(q):
+    """The MoE decode benchmark layer: 512 MXFP4 experts, hidden 2048, FFN 512, top-10,
+    shared expert, 4 tokens; two routings in a row on one workspace (deterministic)."""
+    c = wl.MOE_DECODE
+    layer = wl.moe_layer(c["fmt"], c["n_experts"], c["hidden"], c["ffn"], seed=0, shared=True)
+    pm = q.PackedMoE(layer)
+    ws = q.Workspace(q.qmoe_workspace_size(pm.desc, c["tokens"], c["topk"]))
+    for rep in range(2):
+        x = wl.moe_tokens(c["tokens"], c["hidden"], seed=10 + rep)
+        lg = wl.router_logits(c["tokens"], c["n_experts"], seed=20 + rep)
+        ids, w, rws = q.route(torch.from_numpy(lg).cuda(), c["topk"])
+        out = q.moe_ffn(pm, dev_bf16(x), w, rws, workspace=ws)
+        out2 = q.moe_ffn(pm, dev_bf16(x), w, rws, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+        ref = oracle.moe_forward(layer, x, lg, c["topk"])
+        tol = moe_tolerance(oracle, layer, x, lg, c["topk"], ref)
+        err = np.abs(to_f64(out) - ref)
+        assert np.all(err <= tol), f"rep {rep}: {np.sum(err > tol)} out of tolerance"
+        assert ws.status() == 0
