@@ -203,14 +203,20 @@ qg_status qmoe_route(const float* logits, int64_t t, int n_experts, int topk,
 /* Workspace bytes qmoe_ffn needs for t tokens on the current device. */
 size_t qmoe_workspace_size(const qg_moe_layer* layer, int64_t t, int topk);
 
-/* One MoE FFN layer for 1..4 tokens (decode / speculative verify), after qmoe_route on the
- * same logits:  out[t] = bf16( sum_j topk_w[t][j] * down_e(h) + shared(h) ),
- * h = bf16(silu(gate) * up) per (token, expert), in five launches (TurboEXL3 article
- * §4.2): gate/up as one grouped GEMV over the active experts that reads each expert's
- * weights once for all its tokens, with the shared expert as extra groups; mid; down;
- * finish.  x: bf16 [t][ldx] (H inputs); out: bf16 [t][ldo].  The workspace must be
- * zero-filled before first use and not be shared by overlapping calls.
- * t outside 1..4 returns QG_ERR_UNSUPPORTED. */
+/* One MoE FFN layer after qmoe_route on the same logits:
+ *   out[t] = bf16( sum_j topk_w[t][j] * down_e(h) + shared(h) ),
+ *   h = bf16(silu(gate) * up) per (token, expert), gate = rows 0..F-1 and up = rows
+ *   F..2F-1 of the expert's 2F x H gate/up weight.
+ * 1..4 tokens (decode / speculative verify; TurboEXL3 article §4.2): five launches --
+ *   gate/up as one grouped GEMV over the active experts that reads each expert's weights
+ *   once for all its tokens, with the shared expert as extra groups; mid; down; finish.
+ * More tokens (prefill; §4.1): three launches -- one grouped tensor-core GEMM over the
+ *   router's tile table for gate/up whose epilogue runs the mid, the same GEMM for down,
+ *   and the finish; the shared expert runs as extra tiles of both GEMMs.  Needs
+ *   ffn % 128 == 0 and hidden % 8 == 0, else QG_ERR_UNSUPPORTED.
+ * x: bf16 [t][ldx] (H inputs); out: bf16 [t][ldo].  The workspace (qmoe_workspace_size
+ * bytes for this t) must be zero-filled before first use and not be shared by
+ * overlapping calls.  Deterministic: no atomics in any sum. */
 qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t t, int64_t ldx, int topk,
                    const float* topk_w, const void* route_ws, void* out, int64_t ldo,
                    void* workspace, size_t workspace_bytes, void* stream);

@@ -305,7 +305,8 @@ def route(logits, topk: int, workspace: Optional[Workspace] = None):
 
 
 def moe_ffn(pm: PackedMoE, x, topk_w, route_ws: Workspace, out=None, workspace: Optional[Workspace] = None):
-    """One MoE FFN layer for the routed tokens x bf16 [t, H] (t = 1..4)."""
+    """One MoE FFN layer for the routed tokens x bf16 [t, H]: 1..4 tokens take the grouped-GEMV
+    decode chain, more tokens the grouped tensor-core prefill chain."""
     import torch
     t = x.shape[0]
     topk = topk_w.shape[1]

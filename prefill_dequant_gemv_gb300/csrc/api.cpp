@@ -202,8 +202,11 @@ extern "C" qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t 
   Geometry gu, dn;
   int st = check_moe(layer, t, topk, &gu, &dn);
   if (st != QG_OK) return (qg_status)st;
-  if (t > 4) return QG_ERR_UNSUPPORTED;
   if (!x || !topk_w || !route_ws || !out || !workspace) return QG_ERR_INVALID_ARG;
+  // the prefill chain pairs gate rows f.. with up rows F+f.. inside one 128-row tile and
+  // finishes four features at a time
+  if (t > 4 && (layer->ffn % 128 != 0 || layer->hidden % 8 != 0)) return QG_ERR_UNSUPPORTED;
+  if (t * (int64_t)(topk + 1) >= ((int64_t)1 << 31)) return QG_ERR_UNSUPPORTED;
   if (ldx < layer->hidden || ldo < layer->hidden) return QG_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(out) || !aligned16(workspace) || !aligned16(route_ws) || !aligned16(topk_w))
     return QG_ERR_MISALIGNED;
@@ -212,6 +215,9 @@ extern "C" qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t 
   if (!current_device_info(&dev)) return QG_ERR_CUDA;
   if (workspace_bytes < moe_layout(gu, dn, t, layer->n_experts, topk, dev.sms).total)
     return QG_ERR_WORKSPACE_TOO_SMALL;
+  if (t > 4)
+    return (qg_status)launch_moe_prefill(layer, gu, dn, x, t, ldx, topk, topk_w, route_ws, out, ldo, workspace, dev,
+                                         stream);
   return (qg_status)launch_moe_decode(layer, gu, dn, x, t, ldx, topk, topk_w, route_ws, out, ldo, workspace, dev,
                                       stream);
 }

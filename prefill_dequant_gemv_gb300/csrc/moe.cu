@@ -393,11 +393,14 @@ MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, i
     o += (bytes + 255) & ~(size_t)255;
     return at;
   };
+  // the prefill chain (more than kGMaxRows tokens) fuses the mid into the gate/up GEMM and
+  // needs neither the split-K tickets and partials nor the fp32 gate/up rows
+  const bool decode = T <= kGMaxRows;
   const int64_t nt_max = std::max(gu.nt, dn.nt);
-  L.cnt = take((size_t)(E + 1) * nt_max * 4);
-  L.part = take((size_t)grid * 2 * kGMaxRows * 128 * 4);
+  L.cnt = take(decode ? (size_t)(E + 1) * nt_max * 4 : 0);
+  L.part = take(decode ? (size_t)grid * 2 * kGMaxRows * 128 * 4 : 0);
   L.ld_gu = (gu.n + 7) / 8 * 8;
-  L.gu = take((size_t)R * L.ld_gu * 4);
+  L.gu = take(decode ? (size_t)R * L.ld_gu * 4 : 0);
   L.ld_h = (dn.k + 7) / 8 * 8;
   L.h = take((size_t)R * L.ld_h * 2);
   L.ld_d = (dn.n + 7) / 8 * 8;

@@ -59,5 +59,8 @@ MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, i
 int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
                       int64_t ldx, int topk, const float* topk_w, const void* route_ws, void* out, int64_t ldo,
                       void* ws, const DeviceInfo& dev, void* stream);
+int launch_moe_prefill(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
+                       int64_t ldx, int topk, const float* topk_w, const void* route_ws, void* out, int64_t ldo,
+                       void* ws, const DeviceInfo& dev, void* stream);
 
 }  // namespace qg

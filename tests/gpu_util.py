@@ -31,3 +31,24 @@ def dev_bf16(bits: np.ndarray, device="cuda"):
 
 def to_f64(t) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
+
+
+def moe_tolerance(o, layer, x, lg, topk, out_ref, tokens=None):
+    """Per-element bound for a mixture-of-experts output (rows = `tokens`, all by default):
+    each expert's down output within the GEMV bound of its (bf16) input h plus one bf16 ulp
+    of h (rounding flips between the two sides), weighted by p; plus one output ulp."""
+    _, _, ids, p, inter = o.moe_forward(layer, x, lg, topk, tokens=tokens, with_intermediates=True)
+    toks = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens)
+    tol = np.zeros((toks.size, layer.hidden))
+    rn = {}
+    for i, t in enumerate(toks):
+        for j in range(topk):
+            e = int(ids[t, j])
+            if e not in rn:
+                rn[e] = float(np.max(o.row_norms(layer.down[e])))
+            h = inter[(int(t), e)][2]
+            tol[i] += p[t, j] * (2e-3 + 2.0 ** -8) * np.linalg.norm(h) * rn[e]
+        if layer.shared_down is not None:
+            h = inter[(int(t), -1)][2]
+            tol[i] += (2e-3 + 2.0 ** -8) * np.linalg.norm(h) * float(np.max(o.row_norms(layer.shared_down)))
+    return tol + 2.0 ** -7 * np.abs(out_ref)

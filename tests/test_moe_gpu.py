@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import workloads as wl
-from tests.gpu_util import dev_bf16, qlib, to_f64
+from tests.gpu_util import dev_bf16, moe_tolerance, qlib, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -50,27 +50,6 @@ def test_route_ties_go_to_lower_index(q):
     torch.cuda.synchronize()
     rid, rp = oracle.route(lg, 3)
     assert np.array_equal(ids.cpu().numpy(), rid)
-
-
-def moe_tolerance(o, layer, x, lg, topk, out_ref):
-    """Per-element bound: each expert's down output within the GEMV bound of its (bf16) input
-    h plus one bf16 ulp of h (rounding flips between the two sides), weighted by p; plus one
-    output ulp."""
-    _, _, ids, p, inter = o.moe_forward(layer, x, lg, topk, with_intermediates=True)
-    T = x.shape[0]
-    tol = np.zeros((T, layer.hidden))
-    rn = {}
-    for t in range(T):
-        for j in range(topk):
-            e = int(ids[t, j])
-            if e not in rn:
-                rn[e] = float(np.max(o.row_norms(layer.down[e])))
-            h = inter[(t, e)][2]
-            tol[t] += p[t, j] * (2e-3 + 2.0 ** -8) * np.linalg.norm(h) * rn[e]
-        if layer.shared_down is not None:
-            h = inter[(t, -1)][2]
-            tol[t] += (2e-3 + 2.0 ** -8) * np.linalg.norm(h) * float(np.max(o.row_norms(layer.shared_down)))
-    return tol + 2.0 ** -7 * np.abs(out_ref)
 
 
 @pytest.mark.parametrize("fmt", [wl.MXFP4, wl.NVFP4, wl.MLX_AFFINE4_G64, wl.Q6K])
