@@ -1,27 +1,30 @@
 // Mixture-of-experts layer for many tokens (TurboEXL3 article §4.1, "Prefill: decode once,
 // multiply many times"): after the route (route.cu) groups every (token, expert) pair by
-// expert and cuts each expert's run into tiles of at most 256 pairs,
+// expert and cuts each expert's run into tiles of at most 192 pairs,
 //
 //   gate/up  one grouped tensor-core GEMM over the tile table: each work item is (tile,
 //            128 features); it decodes the expert's gate rows f.. and up rows F+f.. of every
-//            64-deep stage once into shared memory, multiplies both by the tile's tokens
+//            64-deep stage once into tensor memory, multiplies both by the tile's tokens
 //            gathered straight from x (no grouped copy of x is written), and its epilogue
 //            runs the mid step -- h = bf16(silu(gate) * up) in fp32 (§4.1 "Mid") -- so the
 //            gate/up outputs never reach device memory
 //   down     the same GEMM body on h (rows already in grouped order), fp32 outputs per pair
 //   finish   out[t] = bf16( sum_j p[t, j] * down[pos(t, j)] + shared[t] ) (§4.1 "Finish")
 //
-// The shared expert runs as extra tiles of both GEMMs (every token, in 256-token tiles).
+// The shared expert runs as extra tiles of both GEMMs (every token, in 192-token tiles).
 // Tile widths are ragged: the MMA's N is the tile's pair count rounded up to 16, so an
-// expert with 160 tokens costs 160 columns, not 256.
+// expert with 160 tokens costs 160 columns, not 192.
 //
 // The GEMM is persistent (one CTA per SM walks the work items) and warp-specialised:
 //   warp 0       raw-weight producer: bulk copies of the packed tiles into a deep ring
 //   warp 1       TMEM allocation and the tcgen05.mma issuer (one lane)
-//   warps 2-9    decode a stage's tiles into the bf16 operand ring
-//   warps 10-13  epilogue: TMEM -> registers -> h (bf16) or per-pair outputs (fp32)
-//   warps 14-17  gather: cp.async of the tile's activation rows, by row index, into the
-//                128-byte swizzled operand ring
+//   warps 2-9    decode a stage's tiles into the bf16 A operand ring in tensor memory
+//                (tcgen05.st), so the decoded weights cost no shared-memory bandwidth
+//   warps 10-17  epilogue: TMEM -> registers -> h (bf16) or per-pair outputs (fp32)
+//   warps 18-21  gather: cp.async of the tile's activation rows, by row index, into the
+//                128-byte swizzled operand ring; each thread's copies arrive on the
+//                stage's mbarrier when they land, and the MMA thread fences the generic
+//                proxy writes before the tensor cores read them
 // The three rings (raw, decoded A, gathered B) have their own full/empty mbarriers, so HBM
 // latency on the weights, L2 latency on the gathers and the decode overlap one another and
 // the tensor cores.  The down GEMM double-buffers its accumulator in TMEM so an item's
@@ -42,37 +45,44 @@
 
 namespace qg {
 
-constexpr int kMpDecWarps = 8;
-constexpr int kMpEpiWarps = 4;
+constexpr int kMpDecWarps = 8;  // two per TMEM lane quarter, one per half of a stage's 64 inputs
+constexpr int kMpEpiWarps = 8;  // two per TMEM lane quarter, alternate 16-column chunks
 constexpr int kMpGatWarps = 4;
-constexpr int kMpWarps = 2 + kMpDecWarps + kMpEpiWarps + kMpGatWarps;  // 18
-constexpr int kMpThreads = kMpWarps * 32;                               // 576
+constexpr int kMpGatThreads = kMpGatWarps * 32;
+constexpr int kMpWarps = 2 + kMpDecWarps + kMpEpiWarps + kMpGatWarps;  // 22
+constexpr int kMpThreads = kMpWarps * 32;                               // 704
 constexpr int kMpEpiWarp0 = 2 + kMpDecWarps;                            // 10
-constexpr int kMpGatWarp0 = kMpEpiWarp0 + kMpEpiWarps;                  // 14
+constexpr int kMpGatWarp0 = kMpEpiWarp0 + kMpEpiWarps;                  // 18
 constexpr int kMpTile = kRouteTile;  // pairs per tile = largest MMA N
-constexpr int kMpLag = 2;            // gather groups kept in flight per thread
 constexpr int kMpSmemCap = 232448;   // opt-in shared memory per block on sm_100-family GPUs
 
+// Tensor memory (512 columns x 128 lanes of 32 bits) holds the accumulators and the decoded
+// weight operand A:
+//   gate/up: gate accumulator [0, 192), up accumulator [192, 384), A ring of 2 stages x 64
+//            columns (gate rows' 64 inputs in 32 columns, then the up rows')
+//   down:    two accumulators [0, 192) and [192, 384), A ring of 4 stages x 32 columns
+// so shared memory holds only the raw packed tiles and the gathered activation rows.
 template <int FMT, bool DUAL>
 struct MpCfg {
   using F = Fmt<FMT>;
   static constexpr int RAW1 = F::TB + 128 * F::SB + (FMT == FMT_Q6K ? 256 : 0);  // one packed tile
   static constexpr int RAWB = (DUAL ? 2 : 1) * RAW1;
-  static constexpr int A = (DUAL ? 2 : 1) * kATileBytes;
-  static constexpr int B = kMpTile * 128;
-  static constexpr int AS = DUAL ? 2 : 3;
-  static constexpr int BS = 3;
-  static constexpr int ACC = DUAL ? 1 : 2;  // accumulators of 256 columns (DUAL: gate + up)
-  static constexpr int FIT = (kMpSmemCap - 1024 - 512 - AS * A - BS * B) / RAWB;
+  static constexpr int B = kMpTile * 128;      // gathered rows, 128-byte swizzled
+  static constexpr int BS = 6;
+  static constexpr int ACC = DUAL ? 1 : 2;      // accumulator buffers
+  static constexpr uint32_t ACC_COLS = DUAL ? 2 * kMpTile : kMpTile;
+  static constexpr int AS = DUAL ? 2 : 4;       // A stages in TMEM
+  static constexpr uint32_t A_COLS = DUAL ? 64 : 32;
+  static constexpr uint32_t A0 = 2 * kMpTile;  // first A column
+  static_assert(A0 + AS * A_COLS <= 512, "tensor memory");
+  static constexpr int FIT = (kMpSmemCap - 1024 - 512 - BS * B) / RAWB;
   static constexpr int RS = FIT > 16 ? 16 : FIT;
-  static constexpr int OFF_B = AS * A;
-  static constexpr int OFF_RAW = OFF_B + BS * B;
+  static constexpr int OFF_RAW = BS * B;
   static constexpr int OFF_BAR = OFF_RAW + RS * RAWB;
   static constexpr int NBAR = 2 * RS + 2 * AS + 2 * BS + 2 * 2 + 1;
   static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
-  static_assert(RS >= 3, "raw ring too shallow");
+  static_assert(RS >= 4, "raw ring too shallow");
   static_assert(SMEM <= kMpSmemCap, "shared memory");
-  static_assert(kMpLag < BS, "gather lag must leave a stage free");
 };
 
 struct MpArgs {
@@ -153,8 +163,7 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
   using C = MpCfg<FMT, DUAL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + C::OFF_B;
+  uint8_t* sB = smem;
   uint8_t* sR = smem + C::OFF_RAW;
   uint64_t* r_full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* r_empty = r_full + C::RS;
@@ -183,7 +192,7 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < C::BS; ++s) {
-      mbar_init(&b_full[s], kMpGatWarps);
+      mbar_init(&b_full[s], kMpGatThreads);  // one cp.async completion arrival per gather thread
       mbar_init(&b_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -241,7 +250,7 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
           break;
         }
         tc_fence_after();
-        const uint32_t d0 = tmem + acc * 256u;
+        const uint32_t d0 = tmem + acc * C::ACC_COLS;
         for (int kt = 0; kt < KG; ++kt, ++gs) {
           const uint32_t sa = gs % C::AS, sb = gs % C::BS;
           if (!mbar_wait_bounded(&a_full[sa], (gs / C::AS) & 1u, a.status) ||
@@ -250,14 +259,17 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
             break;
           }
           tc_fence_after();
-          const uint32_t abase = smem_u32(sA + sa * C::A);
+          // the gathered rows were written by cp.async (generic proxy); order them before
+          // the tensor cores' (async proxy) reads of this stage
+          fence_proxy_async_smem();
+          const uint32_t ta = tmem + C::A0 + sa * C::A_COLS;
           const uint32_t bbase = smem_u32(sB + sb * C::B);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t accum = (kt | kk) ? 1u : 0u;
             const uint64_t bd = sw128_desc(bbase + kk * 32);
-            mma_bf16_ss(d0, sw128_desc(abase + kk * 32), bd, idesc, accum);
-            if (DUAL) mma_bf16_ss(tmem + 256u, sw128_desc(abase + kATileBytes + kk * 32), bd, idesc, accum);
+            mma_bf16_ts(d0, ta + kk * 8, bd, idesc, accum);
+            if (DUAL) mma_bf16_ts(tmem + kMpTile, ta + 32 + kk * 8, bd, idesc, accum);
           }
           mma_commit(&a_empty[sa]);
           mma_commit(&b_empty[sb]);
@@ -271,8 +283,10 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
     __syncwarp();
   } else if (warp < kMpEpiWarp0) {
     // ------------------------------------------------------------ decode
-    const int dt = tid - 64;
-    const int r = dt & 127, h = dt >> 7;
+    // Warp w may only touch TMEM lanes 32*(w%4)..: it decodes rows 32*(w%4)+lane, inputs
+    // 32h..32h+31 of each 64-deep stage (h = 0 for warps 2-5, 1 for warps 6-9).
+    const int r = (warp & 3) * 32 + lane, h = (warp - 2) >> 2;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     uint32_t gs = 0;
     bool ok = true;
     for (int i = b; ok && i < n_items; i += G) {
@@ -283,11 +297,18 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
           ok = false;
           break;
         }
+        tc_fence_after();
         const uint8_t* raw = sR + sr * C::RAWB;
-        uint8_t* A = sA + sa * C::A;
-        decode_stage<FMT>(raw, A, r, h);
-        if (DUAL) decode_stage<FMT>(raw + C::RAW1, A + kATileBytes, r, h);
-        fence_proxy_async_smem();
+        const uint32_t ta = tmem + lane_base + C::A0 + sa * C::A_COLS + 16 * h;
+        uint32_t o[16];
+        decode_regs<FMT>(raw, r, h, o);
+        tmem_st16(ta, o);
+        if (DUAL) {
+          decode_regs<FMT>(raw + C::RAW1, r, h, o);
+          tmem_st16(ta + 32, o);
+        }
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&a_full[sa]);
@@ -297,7 +318,7 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
     }
   } else if (warp < kMpGatWarp0) {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;
+    const int quarter = warp & 3, half = (warp - kMpEpiWarp0) >> 2;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     uint32_t itc = 0;
     for (int i = b; i < n_items; i += G, ++itc) {
@@ -307,30 +328,31 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
       if (!mbar_wait_bounded(&t_full[acc], (itc / C::ACC) & 1u, a.status)) break;
       tc_fence_after();
       const int64_t n = (int64_t)it.q * 128 + quarter * 32 + lane;
-      for (int c = 0; c < N; c += 16) {
+      for (int c = 16 * half; c < N; c += 32) {
         uint32_t v[16];
-        tmem_ld16(tmem + lane_base + acc * 256u + (uint32_t)c, v);
+        tmem_ld16(tmem + lane_base + acc * C::ACC_COLS + (uint32_t)c, v);
         if (DUAL) {
           uint32_t u[16];
-          tmem_ld16(tmem + lane_base + 256u + (uint32_t)c, u);
+          tmem_ld16(tmem + lane_base + kMpTile + (uint32_t)c, u);
           tmem_ld_wait();
-          __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(a.out);
+          __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(a.out) + (int64_t)(it.out_base + c) * a.ldo + n;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             if (c + j < it.count) {
               const float g = it.ts * __uint_as_float(v[j]);
               const float up = it.ts * __uint_as_float(u[j]);
-              const float silu = g / (1.0f + expf(-g));
-              hout[(int64_t)(it.out_base + c + j) * a.ldo + n] = __float2bfloat16_rn(silu * up);
+              // silu(g) = g / (1 + e^-g); e^-g capped at e^80 keeps the quotient finite
+              const float silu = __fdividef(g, 1.0f + __expf(-fmaxf(g, -80.0f)));
+              hout[(int64_t)j * a.ldo] = __float2bfloat16_rn(silu * up);
             }
           }
         } else {
           tmem_ld_wait();
-          float* dout = static_cast<float*>(a.out);
           if (n < a.n_out) {
+            float* dout = static_cast<float*>(a.out) + (int64_t)(it.out_base + c) * a.ldo + n;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (c + j < it.count) dout[(int64_t)(it.out_base + c + j) * a.ldo + n] = it.ts * __uint_as_float(v[j]);
+              if (c + j < it.count) dout[(int64_t)j * a.ldo] = it.ts * __uint_as_float(v[j]);
           }
         }
       }
@@ -340,6 +362,9 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
     }
   } else {
     // ------------------------------------------------------------ activation gather
+    // Each thread copies 16-byte chunks of the stage's rows and arrives on the stage's
+    // barrier when its copies land (cp.async.mbarrier.arrive.noinc), so the gather runs up
+    // to BS stages ahead without waiting on its own loads.
     const int gt = tid - kMpGatWarp0 * 32;
     const int c8 = gt & 7, rs = gt >> 3;  // 16-byte chunk of a 128-byte row; row within 16
     uint32_t gs = 0;
@@ -371,20 +396,10 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
             cp_async16(dst + (j >> 3) * 1024 + (j & 7) * 128 + ((c8 ^ (j & 7)) << 4), src, live ? kb : 0u);
           }
         }
-        cp_async_commit();
-        if (gs >= (uint32_t)kMpLag) {
-          cp_async_wait<kMpLag>();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&b_full[(gs - kMpLag) % C::BS]);
-        }
+        cp_async_arrive_noinc(&b_full[s]);
       }
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0)
-      for (uint32_t g2 = gs > (uint32_t)kMpLag ? gs - kMpLag : 0; g2 < gs; ++g2) mbar_arrive(&b_full[g2 % C::BS]);
+    cp_async_wait_all();  // no copy in flight into shared memory past this point
   }
 
   tc_fence_before();

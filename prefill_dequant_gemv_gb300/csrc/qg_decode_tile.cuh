@@ -19,11 +19,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Decode one thread's share of a stage: row r, inputs 32h..32h+31 -> four 16-byte
-// chunks of the swizzled A tile (chunk j of row r lives at (r/8)*1024 + (r%8)*128 +
-// ((j ^ (r%8)) * 16)).
+// Decode one thread's share of a stage: row r, inputs 32h..32h+31, as 16 bf16x2 words in
+// input order (word i holds inputs 32h+2i (low half) and 32h+2i+1).
 template <int FMT>
-__device__ __forceinline__ void decode_stage(const uint8_t* raw, uint8_t* A, int r, int h) {
+__device__ __forceinline__ void decode_regs(const uint8_t* raw, int r, int h, uint32_t (&o)[16]) {
   using F = Fmt<FMT>;
   const int rt = r >> 5, lane = r & 31;
   const uint4 cw = *reinterpret_cast<const uint4*>(raw + ((rt * F::CH + h) * 32 + lane) * 16);
@@ -89,10 +88,24 @@ __device__ __forceinline__ void decode_stage(const uint8_t* raw, uint8_t* A, int
         for (int j = 0; j < 8; ++j) v[j] = ds * (code[j] - 32.0f);
       }
     }
+    o[4 * wi] = pack_bf16x2(v[0], v[1]);
+    o[4 * wi + 1] = pack_bf16x2(v[2], v[3]);
+    o[4 * wi + 2] = pack_bf16x2(v[4], v[5]);
+    o[4 * wi + 3] = pack_bf16x2(v[6], v[7]);
+  }
+}
+
+// The same share written as four 16-byte chunks of the 128-byte swizzled K-major shared
+// memory tile (chunk j of row r lives at (r/8)*1024 + (r%8)*128 + ((j ^ (r%8)) * 16)).
+template <int FMT>
+__device__ __forceinline__ void decode_stage(const uint8_t* raw, uint8_t* A, int r, int h) {
+  uint32_t o[16];
+  decode_regs<FMT>(raw, r, h, o);
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi) {
     const int j = 4 * h + wi;
-    const uint4 out = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                                 pack_bf16x2(v[6], v[7]));
-    *reinterpret_cast<uint4*>(A + (r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4)) = out;
+    *reinterpret_cast<uint4*>(A + (r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4)) =
+        make_uint4(o[4 * wi], o[4 * wi + 1], o[4 * wi + 2], o[4 * wi + 3]);
   }
 }
 

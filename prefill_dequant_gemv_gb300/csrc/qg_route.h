@@ -8,7 +8,7 @@ namespace qg {
 
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopk = 16;
-constexpr int kRouteTile = 256;  // pairs per grouped-prefill tile (the tensor-core N)
+constexpr int kRouteTile = 192;  // pairs per grouped-prefill tile (the tensor-core N)
 
 struct RouteLayout {
   size_t meta, counts, offsets, active, pair_list, pair_pos, tiles, block_counts, block_start, total;

@@ -40,15 +40,32 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
+// try_wait that may suspend the thread for up to `ns` nanoseconds; the hardware resumes it
+// as soon as the phase completes, so a waiting warp takes no issue slots from the warps
+// doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `bar` with the given parity to complete, at most kWaitLimitNs.
+// The clock is read only after a batch of sleeping tries has failed, so a wait that ends
+// within the first batch costs no timer read.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
+  unsigned long long t0 = 0;
   while (true) {
     #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+    const unsigned long long t = global_ns();
+    if (t0 == 0) {
+      t0 = t;
+    } else if (t - t0 > kWaitLimitNs) {
       if (status) atomicExch(status, kStatusTimeout);
       return false;
     }
