@@ -176,22 +176,26 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0;
+      int gcur = -1;  // the group whose weight bases are loaded (reloaded only on a change)
+      const uint8_t *bc = nullptr, *bs = nullptr, *ba = nullptr;
       for (int j = 0; j < nch; ++j) {
         if (j >= S && !mbar_wait_bounded(&empty[s], ph ^ 1u, a.status)) break;
         const int64_t c = c0 + j;
         const int g = (int)(c / cpg);
         const int l0 = (int)(c % cpg) * kGC;
         const int nu = min(kGC, upg_real - l0);
-        const uint8_t *bc, *bs, *ba;
-        if (g < n_active) {
-          const int e = a.active[g];
-          bc = a.codes + (int64_t)e * a.cstride;
-          bs = a.scales + (int64_t)e * a.sstride;
-          ba = a.aux ? a.aux + (int64_t)e * a.astride : nullptr;
-        } else {
-          bc = a.sh_codes;
-          bs = a.sh_scales;
-          ba = a.sh_aux;
+        if (g != gcur) {
+          gcur = g;
+          if (g < n_active) {
+            const int e = a.active[g];
+            bc = a.codes + (int64_t)e * a.cstride;
+            bs = a.scales + (int64_t)e * a.sstride;
+            ba = a.aux ? a.aux + (int64_t)e * a.astride : nullptr;
+          } else {
+            bc = a.sh_codes;
+            bs = a.sh_scales;
+            ba = a.sh_aux;
+          }
         }
         uint8_t* dst = stages + (size_t)s * SBY;
         uint32_t bytes = (uint32_t)nu * (SG::CODE + SG::SCALE);

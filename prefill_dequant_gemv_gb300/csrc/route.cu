@@ -18,51 +18,81 @@ namespace qg {
 
 constexpr int kRouteBlock = 1024;  // pairs per grouping block (one thread per pair)
 
-// Warp-level top-k of one token's logits; lane l holds logits l, l+32, ... (<= 32 each).
+// Compare-exchange for a descending order by value, ties to the lower expert index.
+__device__ __forceinline__ void cx(float& va, int& ia, float& vb, int& ib) {
+  const bool swap = vb > va || (vb == va && ib < ia);
+  const float tv = swap ? vb : va, tw = swap ? va : vb;
+  const int ti = swap ? ib : ia, tj = swap ? ia : ib;
+  va = tv;
+  vb = tw;
+  ia = ti;
+  ib = tj;
+}
+
+// Warp-level top-k of one token's logits (E <= 512): lane l holds logits l, l+32, ...,
+// sorts its 16 once (bitonic network, fixed register indices), then k rounds of a warp
+// tournament on the lanes' heads pick the winners in descending order; lane j keeps the
+// j-th winner and the k lanes compute the softmax over the kept logits in parallel.
 __device__ void warp_topk(const float* lg, int E, int k, int32_t* ids, float* wts) {
   const int lane = threadIdx.x & 31;
-  float v[32];
-  uint32_t taken = 0;
+  float v[16];
+  int id[16];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = (lane + 32 * i < E) ? lg[lane + 32 * i] : 0.0f;
-  float sel[16];
-  int sid[16];
-  for (int j = 0; j < k; ++j) {
-    // lane-local best: largest value, lowest index on ties
-    float bv = 0.0f;
-    int bi = 0x7FFFFFFF;
+  for (int i = 0; i < 16; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? lg[e] : -INFINITY;
+    id[i] = e < E ? e : 0x7FFFFFFF;
+  }
+  // bitonic sort of 16 (descending)
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (bi == 0x7FFFFFFF || v[i] > bv || (v[i] == bv && e < bi))) {
-        bv = v[i];
-        bi = e;
+  for (int size = 2; size <= 16; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          if ((i & size) == 0) cx(v[i], id[i], v[j], id[j]);
+          else cx(v[j], id[j], v[i], id[i]);
+        }
       }
-    }
+  float mine = 0.0f, top = 0.0f;
+  int mine_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = v[0];
+    int bi = id[0];
 #pragma unroll
     for (int off = 16; off; off >>= 1) {
       const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
       const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-      if (oi != 0x7FFFFFFF && (bi == 0x7FFFFFFF || ov > bv || (ov == bv && oi < bi))) {
+      if (ov > bv || (ov == bv && oi < bi)) {
         bv = ov;
         bi = oi;
       }
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    sel[j] = bv;
-    sid[j] = bi;
+    if (j == 0) top = bv;
+    if (lane == j) {
+      mine = bv;
+      mine_id = bi;
+    }
+    if ((bi & 31) == lane && bi == id[0]) {  // the winner's lane advances its head
+#pragma unroll
+      for (int i = 0; i < 15; ++i) {
+        v[i] = v[i + 1];
+        id[i] = id[i + 1];
+      }
+      v[15] = -INFINITY;
+      id[15] = 0x7FFFFFFF;
+    }
   }
-  if (lane == 0) {
-    // softmax over the k kept logits, in selection (descending) order
-    float z[16], sum = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      z[j] = expf(sel[j] - sel[0]);
-      sum += z[j];
-    }
-    for (int j = 0; j < k; ++j) {
-      ids[j] = sid[j];
-      wts[j] = z[j] / sum;
-    }
+  // softmax over the k kept logits (descending order), shifted by the largest
+  const float z = lane < k ? expf(mine - top) : 0.0f;
+  float sum = z;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
+  if (lane < k) {
+    ids[lane] = mine_id;
+    wts[lane] = z / sum;
   }
 }
 
@@ -85,43 +115,99 @@ __device__ void block_count(const int32_t* ids, int64_t P, int E, int b, int* ou
   __syncthreads();
 }
 
-// Totals, exclusive offsets, per-block starting positions, active list, tile table.
-__device__ void scan_groups(const RouteView& r, int E, int nblocks, int tile) {
-  __shared__ int tot[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int s = 0;
-    for (int b = 0; b < nblocks; ++b) s += r.block_counts[(size_t)b * E + e];
-    tot[e] = s;
-    r.counts[e] = s;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int off = 0, na = 0, nt = 0;
-    for (int e = 0; e < E; ++e) {
-      r.offsets[e] = off;
-      if (tot[e] > 0) {
-        r.active[na++] = e;
-        for (int s = 0; s < tot[e]; s += tile) {
-          r.tiles[3 * nt] = e;
-          r.tiles[3 * nt + 1] = off + s;
-          r.tiles[3 * nt + 2] = min(tile, tot[e] - s);
-          ++nt;
-        }
-      }
-      off += tot[e];
+// Block-wide exclusive scan of three counters (every thread of the block calls it;
+// blockDim.x a multiple of 32, <= 1024); the totals go to *tot (shared memory).
+__device__ __forceinline__ int3 block_scan3(int3 x, int3* tot) {
+  __shared__ int3 wsum[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int3 inc = x;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int a = __shfl_up_sync(0xFFFFFFFFu, inc.x, off), b = __shfl_up_sync(0xFFFFFFFFu, inc.y, off),
+              c = __shfl_up_sync(0xFFFFFFFFu, inc.z, off);
+    if (lane >= off) {
+      inc.x += a;
+      inc.y += b;
+      inc.z += c;
     }
-    r.offsets[E] = off;
-    r.meta[0] = na;
-    r.meta[1] = nt;
+  }
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int3 w = lane < nw ? wsum[lane] : make_int3(0, 0, 0);
+    int3 wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int a = __shfl_up_sync(0xFFFFFFFFu, wi.x, off), b = __shfl_up_sync(0xFFFFFFFFu, wi.y, off),
+                c = __shfl_up_sync(0xFFFFFFFFu, wi.z, off);
+      if (lane >= off) {
+        wi.x += a;
+        wi.y += b;
+        wi.z += c;
+      }
+    }
+    if (lane < nw) wsum[lane] = make_int3(wi.x - w.x, wi.y - w.y, wi.z - w.z);  // exclusive, per warp
+    if (lane == 31) *tot = wi;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = r.offsets[e];
-    for (int b = 0; b < nblocks; ++b) {
+  const int3 base = wsum[warp];
+  __syncthreads();
+  return make_int3(base.x + inc.x - x.x, base.y + inc.y - x.y, base.z + inc.z - x.z);
+}
+
+// Sum of n counters strided by E (per-block expert counts), loads batched for overlap.
+__device__ __forceinline__ int strided_sum(const int* p, int E, int n) {
+  int s = 0, b = 0;
+  for (; b + 8 <= n; b += 8) {
+    int t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t[i] = p[(size_t)(b + i) * E];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += t[i];
+  }
+  for (; b < n; ++b) s += p[(size_t)b * E];
+  return s;
+}
+
+// Totals, exclusive offsets, per-block starting positions, active list and tile table,
+// one thread per expert and block-wide scans (blockDim.x >= E).
+__device__ void scan_groups(const RouteView& r, int E, int nblocks, int tile) {
+  __shared__ int3 totals;
+  const int e = threadIdx.x;
+  const int tot = e < E ? strided_sum(r.block_counts + e, E, nblocks) : 0;
+  const int3 x = make_int3(tot, (tot + tile - 1) / tile, tot > 0 ? 1 : 0);
+  const int3 ex = block_scan3(x, &totals);
+  if (e < E) {
+    r.counts[e] = tot;
+    r.offsets[e] = ex.x;
+    if (tot > 0) r.active[ex.z] = e;
+    for (int s = 0; s < x.y; ++s) {
+      r.tiles[3 * (ex.y + s)] = e;
+      r.tiles[3 * (ex.y + s) + 1] = ex.x + s * tile;
+      r.tiles[3 * (ex.y + s) + 2] = min(tile, tot - s * tile);
+    }
+    // starting position of block b's pairs of expert e
+    int run = ex.x, b = 0;
+    for (; b + 8 <= nblocks; b += 8) {
+      int t[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) t[i] = r.block_counts[(size_t)(b + i) * E + e];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        r.block_start[(size_t)(b + i) * E + e] = run;
+        run += t[i];
+      }
+    }
+    for (; b < nblocks; ++b) {
       const int c = r.block_counts[(size_t)b * E + e];
       r.block_start[(size_t)b * E + e] = run;
       run += c;
     }
+  }
+  if (threadIdx.x == 0) {
+    r.offsets[E] = totals.x;
+    r.meta[0] = totals.z;
+    r.meta[1] = totals.y;
   }
   __syncthreads();
 }
