@@ -45,16 +45,19 @@ struct GemvArgs {
   int nslots;
   int stages;
   float ts;
+  int csplit;      // > 1: cluster mode (row tile q = cluster q, partials reduced over DSMEM)
   float* ws_part;  // [grid][2][M][128]
   int* ws_cnt;     // [NT]
   int* status;
 };
 
+constexpr int kMaxCsplit = 8;  // portable cluster size
+
 struct SmemLayout {
-  size_t bars, stages, xs, sums, red, lut, misc, total;
+  size_t bars, stages, xs, sums, red, cbuf, lut, misc, total;
 };
 
-__host__ __device__ inline SmemLayout gemv_smem_layout(int stage_bytes, int S, int M, int nslots) {
+__host__ __device__ inline SmemLayout gemv_smem_layout(int stage_bytes, int S, int M, int nslots, int csplit) {
   // stage_bytes: bytes of one chunk stage
   const int kCW = consumer_warps(M);
   SmemLayout L;
@@ -71,6 +74,8 @@ __host__ __device__ inline SmemLayout gemv_smem_layout(int stage_bytes, int S, i
   o += (size_t)M * nslots * 16 * 4;  // {scale, Z, X, 0} per 16-input quarter
   L.red = o;
   o += (size_t)kCW * M * 128 * 4;
+  L.cbuf = o;  // cluster mode: every rank's partial of the row tile, in rank 0's CTA
+  o += csplit > 1 ? (size_t)csplit * M * 128 * 4 : 0;
   L.lut = o;
   o += 256 * 4;  // E4M3 -> fp32
   L.misc = o;
@@ -120,21 +125,23 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
   extern __shared__ __align__(128) uint8_t smem[];
   using SG = Stage<FMT>;
   const int S = a.stages, nslots = a.nslots;
-  const SmemLayout L = gemv_smem_layout(Stage<FMT>::bytes(consumer_warps(M) / 4), S, M, nslots);
+  const SmemLayout L = gemv_smem_layout(Stage<FMT>::bytes(consumer_warps(M) / 4), S, M, nslots, a.csplit);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + S;
   uint8_t* stages = smem + L.stages;
   uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.xs);
   float* sums = reinterpret_cast<float*>(smem + L.sums);
   float* red = reinterpret_cast<float*>(smem + L.red);
+  float* cbuf = reinterpret_cast<float*>(smem + L.cbuf);
   float* lut = reinterpret_cast<float*>(smem + L.lut);
   int* flag = reinterpret_cast<int*>(smem + L.misc);
+  const bool clustered = a.csplit > 1;
 
   const int64_t U = a.U;
   const int64_t G = gridDim.x;
   const int64_t b = blockIdx.x;
   const int64_t u0 = b * U / G, u1 = (b + 1) * U / G;
-  if (u0 >= u1) return;
+  if (u0 >= u1 && !clustered) return;
   const int64_t len = u1 - u0;
   const int KG = a.KG;
   const int sbase = len >= KG ? 0 : (int)(u0 % KG);
@@ -142,14 +149,15 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
 
   constexpr int C = kGroups;  // units per chunk: one per unit group
   const int SB = Stage<FMT>::bytes(C);
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kCW);  // every consumer warp releases each chunk once
-    }
-    fence_mbar_init();
+  for (int s = tid; s < S; s += blockDim.x) {
+    mbar_init(&full[s], 1);
+    mbar_init(&empty[s], kCW);  // every consumer warp releases each chunk once
   }
+  if (tid < S) fence_mbar_init();
   __syncthreads();
+  // The next kernel may start streaming its weights while this one runs; it reads
+  // activations and the workspace only after this grid has completed (pdl_wait).
+  if (tid == 0) pdl_launch_dependents();
 
   // All loop indices below are 32-bit and advanced incrementally (the host
   // guarantees fewer than 2^31 units): 64-bit division in the per-unit path costs
@@ -185,6 +193,8 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
         }
       }
     }
+    __syncwarp();  // lane 0 rejoins the warp before the cluster barrier
+    if (clustered) cluster_sync_all();  // every thread of the cluster takes the one barrier
     return;
   }
 
@@ -193,6 +203,7 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
     lut[2 * tid] = v.x;
     lut[2 * tid + 1] = v.y;
   }
+  pdl_wait();  // activations, residual and workspace may come from the preceding kernel
   stage_x<FMT, M, kCT>(a, xs, sums, sbase, nslots, tid);
   named_sync(1, kCT);
 
@@ -208,6 +219,9 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
   const uint8_t* xq_base = reinterpret_cast<const uint8_t*>(xs) + kq * 32;
   const float* sq_base = sums + kq * 4;
   uint32_t u = uu0;
+  const uint32_t crank = clustered ? cluster_rank() : 0;
+  uint32_t part_q0 = 0, part_q1 = 0;  // row tiles this CTA holds only part of
+  int nparts = 0;
   while (u < uu1) {
     const uint32_t q = u / (uint32_t)KG;
     const uint32_t seg_end = min(uu1, (q + 1) * (uint32_t)KG);
@@ -255,49 +269,80 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
       for (int w2 = 0; w2 < kCW; ++w2) v += red[w2 * M * 128 + e];
       if (whole)
         finish_out<M>(a, q, e, v);
+      else if (clustered)  // into rank 0's buffer, slot = this CTA's rank
+        st_cluster_f32(cluster_map(cbuf + (size_t)crank * M * 128 + e, 0), v);
       else
         a.ws_part[(size_t)((b * 2 + slot_ws) * M) * 128 + e] = v;
     }
-    if (!whole) {
-      // Publish the partial (CTA barrier, then one gpu-scope fence before the ticket);
-      // the CTA that takes the last ticket sums all partials of the row tile in CTA
-      // order.  Its first contributor may hold the tile as its last segment (slot 1);
-      // every later contributor starts inside the tile (slot 0).
-      named_sync(1, kCT);
-      const int64_t qk = (int64_t)q * KG;
-      const int64_t bf = owner_cta(qk, U, G), bl = owner_cta(qk + KG - 1, U, G);
-      if (tid == 0) {
-        __threadfence();
-        const int old = atomicAdd(&a.ws_cnt[q], 1);
-        __threadfence();
-        *flag = (old == (int)(bl - bf)) ? 1 : 0;
-      }
-      named_sync(1, kCT);
-      if (*flag) {
-        const int first_sl = (bf * U / G < qk) ? 1 : 0;
-        const int nc = (int)(bl - bf + 1);
-        const float* part = a.ws_part + (size_t)(bf * 2) * M * 128;
-        for (int e = tid; e < M * 128; e += kCT) {
-          float v = __ldcg(part + (size_t)first_sl * M * 128 + e);
-          int c = 1;
-          for (; c + 4 <= nc; c += 4) {  // independent loads, summed in order
-            const float v0 = __ldcg(part + (size_t)(2 * c) * M * 128 + e);
-            const float v1 = __ldcg(part + (size_t)(2 * c + 2) * M * 128 + e);
-            const float v2 = __ldcg(part + (size_t)(2 * c + 4) * M * 128 + e);
-            const float v3 = __ldcg(part + (size_t)(2 * c + 6) * M * 128 + e);
-            v += v0;
-            v += v1;
-            v += v2;
-            v += v3;
-          }
-          for (; c < nc; ++c) v += __ldcg(part + (size_t)(2 * c) * M * 128 + e);
-          finish_out<M>(a, q, e, v);
-        }
-        if (tid == 0) a.ws_cnt[q] = 0;
+    if (!whole && !clustered) {  // the same on every thread
+      if (nparts == 0)
+        part_q0 = q;
+      else
+        part_q1 = q;
+      ++nparts;
+    }
+    named_sync(1, kCT);  // `red` is rewritten by the next segment
+    u = seg_end;
+  }
+
+  // Row tiles split across CTAs (at most two per CTA: its first and its last): one ticket
+  // each, taken after all of this CTA's work, so no ticket latency stalls the stream.  The
+  // CTA that takes a tile's last ticket sums the tile's partials in CTA order (its first
+  // contributor may hold the tile as its last segment, slot 1; every later contributor
+  // starts inside the tile, slot 0) and writes the output.
+  if (nparts > 0) {  // uniform: every consumer thread reaches the barriers below
+    if (tid == 0) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (i >= nparts) break;
+        const uint32_t q = i ? part_q1 : part_q0;
+        const int64_t qk = (int64_t)q * KG;
+        const int64_t bf = owner_cta(qk, U, G), bl = owner_cta(qk + KG - 1, U, G);
+        const int old = ticket_add(&a.ws_cnt[q], 1);
+        flag[i] = (old == (int)(bl - bf)) ? 1 : 0;
       }
     }
     named_sync(1, kCT);
-    u = seg_end;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if (i >= nparts || !flag[i]) continue;
+      const uint32_t q = i ? part_q1 : part_q0;
+      const int64_t qk = (int64_t)q * KG;
+      const int64_t bf = owner_cta(qk, U, G), bl = owner_cta(qk + KG - 1, U, G);
+      const int first_sl = (bf * U / G < qk) ? 1 : 0;
+      const int nc = (int)(bl - bf + 1);
+      const float* part = a.ws_part + (size_t)(bf * 2) * M * 128;
+      for (int e = tid; e < M * 128; e += kCT) {
+        float v = __ldcg(part + (size_t)first_sl * M * 128 + e);
+        int c = 1;
+        for (; c + 4 <= nc; c += 4) {  // independent loads, summed in order
+          const float v0 = __ldcg(part + (size_t)(2 * c) * M * 128 + e);
+          const float v1 = __ldcg(part + (size_t)(2 * c + 2) * M * 128 + e);
+          const float v2 = __ldcg(part + (size_t)(2 * c + 4) * M * 128 + e);
+          const float v3 = __ldcg(part + (size_t)(2 * c + 6) * M * 128 + e);
+          v += v0;
+          v += v1;
+          v += v2;
+          v += v3;
+        }
+        for (; c < nc; ++c) v += __ldcg(part + (size_t)(2 * c) * M * 128 + e);
+        finish_out<M>(a, q, e, v);
+      }
+      if (tid == 0) a.ws_cnt[q] = 0;
+    }
+  }
+  if (clustered) {
+    // Row tile q = this cluster: rank 0 sums the ranks' partials in rank order.
+    __syncwarp();
+    cluster_sync_all();
+    if (crank == 0) {
+      const uint32_t q = (uint32_t)(b / a.csplit);
+      for (int e = tid; e < M * 128; e += kCT) {
+        float v = cbuf[e];
+        for (int r = 1; r < a.csplit; ++r) v += cbuf[(size_t)r * M * 128 + e];
+        finish_out<M>(a, q, e, v);
+      }
+    }
   }
 }
 
@@ -319,25 +364,38 @@ bool plan_gemv(const Geometry& g, int m, const DeviceInfo& dev, GemvPlan* p) {
   if (U >= (int64_t(1) << 31)) return false;
   const size_t budget = (size_t)dev.max_smem_optin;
   int64_t G = std::min<int64_t>(dev.sms, U);
+  int csplit = 1;
+  if (g.nt < dev.sms && g.nt * 8 >= (int64_t)dev.sms * 7) {
+    // Nearly one row tile per SM: every CTA takes one whole row tile -- no partials,
+    // tickets or finishing pass, for a few idle SMs.
+    G = g.nt;
+  } else if (g.nt * 2 <= dev.sms) {
+    // Few row tiles: split each across a cluster of csplit CTAs (equal K ranges); the
+    // partials meet in the first CTA's shared memory instead of going through tickets.
+    csplit = (int)std::min<int64_t>(kMaxCsplit, std::min<int64_t>(dev.sms / g.nt, g.kg));
+    if (csplit > 1) G = g.nt * csplit;
+  }
   for (;;) {
     const int64_t len = (U + G - 1) / G;
     const int nslots = (int)std::min<int64_t>(len, g.kg);
-    const SmemLayout L0 = gemv_smem_layout(sbytes, 2, m, nslots);
+    const SmemLayout L0 = gemv_smem_layout(sbytes, 2, m, nslots, csplit);
     if (L0.total <= budget || G >= U) {
       if (L0.total > budget) return false;
       int S = (int)std::min<int64_t>((len + C - 1) / C, (int64_t)kMaxStages);
       S = std::max(S, 2);
-      while (S > 2 && gemv_smem_layout(sbytes, S, m, nslots).total > budget) --S;
+      while (S > 2 && gemv_smem_layout(sbytes, S, m, nslots, csplit).total > budget) --S;
       p->grid = (int)G;
       p->nslots = nslots;
       p->stages = S;
-      p->smem = gemv_smem_layout(sbytes, S, m, nslots).total;
+      p->smem = gemv_smem_layout(sbytes, S, m, nslots, csplit).total;
+      p->csplit = csplit;
       p->units = U;
       p->off_cnt = kWsHeader;
       p->off_part = kWsHeader + (((size_t)g.nt * 4 + 255) & ~(size_t)255);
       p->ws_bytes = p->off_part + (size_t)G * 2 * m * 128 * 4;
       return true;
     }
+    if (csplit > 1) return false;  // cluster mode keeps its grid
     G = std::min<int64_t>(U, G * 2);
   }
 }
@@ -355,7 +413,26 @@ static int launch_t(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
       return QG_ERR_CUDA;
     configured.fetch_or(bit);
   }
-  gemv_kernel<FMT, M><<<p.grid, consumer_warps(M) * 32 + 32, p.smem, s>>>(a);
+  // Programmatic serialization: this launch may begin while the preceding kernel in the
+  // stream finishes (the kernel waits for it before reading anything that kernel writes).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.grid);
+  cfg.blockDim = dim3((unsigned)(consumer_warps(M) * 32 + 32));
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (p.csplit > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)p.csplit;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  if (cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, M>, a) != cudaSuccess) return QG_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
@@ -388,6 +465,7 @@ int launch_gemv(const Geometry& g, const qg_weight* w, const void* x, int m, int
   a.nslots = p.nslots;
   a.stages = p.stages;
   a.ts = (g.fmt == FMT_NVFP4) ? w->tensor_scale : 1.0f;
+  a.csplit = p.csplit;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   a.status = reinterpret_cast<int*>(wsb);
   a.ws_cnt = reinterpret_cast<int*>(wsb + p.off_cnt);

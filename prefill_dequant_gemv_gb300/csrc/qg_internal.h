@@ -37,6 +37,7 @@ struct GemvPlan {
   size_t ws_bytes;   // workspace bytes
   size_t off_cnt, off_part;  // workspace offsets
   int64_t units;
+  int csplit;        // > 1: each row tile split across a cluster of csplit CTAs
 };
 bool plan_gemv(const Geometry& g, int m, const DeviceInfo& dev, GemvPlan* p);
 

@@ -79,6 +79,41 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel in the stream (launched with the
+// programmatic-serialization attribute) start its CTAs once every CTA of this grid has
+// called this or exited; and, in a dependent kernel, wait until the preceding grid has
+// completed and its memory is visible.  Both are no-ops without such a dependency.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Ticket: atomic add with release (this CTA's writes, ordered before it by a CTA barrier)
+// and acquire (the other CTAs' writes released by their tickets) semantics at GPU scope.
+__device__ __forceinline__ int ticket_add(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Thread-block clusters: this CTA's rank, a shared::cluster address of `p` in the CTA of
+// rank `rank`, a store there, and the full cluster barrier (every thread of every CTA of
+// the cluster must execute it, warp-uniformly; release/acquire orders the remote stores).
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_u32(p)), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Named barrier over `nthreads` threads (a multiple of 32) with id 1..15.
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
