@@ -7,11 +7,17 @@
 // One CTA computes a 128-row x 256-token output tile over the whole K:
 //   warp 0      producer: per 64-deep stage, bulk-copies the packed weight tile (codes,
 //               scales, Q6_K d) and TMA-loads the 256 x 64 activation tile (128-byte swizzle)
-//   warps 2..9  decode the stage's 128 x 64 weights to bf16 in the tensor cores' 128-byte
-//               swizzled K-major layout (E2M1 x block scale is exact in bf16), then run the
-//               epilogue (TMEM -> registers -> bf16 output, tensor scale and residual)
-//   warp 1      allocates 256 TMEM columns and issues tcgen05.mma (M=128, N=256, K=16,
-//               bf16 x bf16 -> fp32) from one lane; completion is committed to mbarriers.
+//   warps 2..9  decode the stage's 128 x 64 weights to bf16 (E2M1 x block scale is exact in
+//               bf16) straight into tensor memory (tcgen05.st: row r -> TMEM lane r), the
+//               MMA's A operand, then run the epilogue (TMEM -> registers -> bf16 output,
+//               tensor scale and residual)
+//   warp 1      allocates all 512 TMEM columns (accumulator 0-255, A ring 256-415) and
+//               issues tcgen05.mma (M=128, N=256, K=16, A from TMEM, B from shared memory,
+//               fp32 accumulate) from one lane; completion is committed to mbarriers.
+// A single accumulator chain at N = 256 with A in tensor memory keeps the tensor pipe ~90%
+// busy (consecutive MMAs into one accumulator wait on each other; at N = 256 that wait is
+// barely longer than the MMA itself), and the decoded weights cost no shared-memory
+// bandwidth.
 // Every wait is bounded (QG_ERR_TIMEOUT in the workspace status word) and TMEM is freed
 // on every path.
 #include <cuda.h>
@@ -29,15 +35,16 @@
 namespace qg {
 
 constexpr int kPfBN = 256;                                   // tokens per tile (MMA N)
-constexpr int kPfStages = 4;
+constexpr int kPfStages = 5;
 constexpr int kPfDeqWarps = 8;
 constexpr int kPfThreads = (2 + kPfDeqWarps) * 32;           // 320
-constexpr int kATile = 128 * 128;                            // 128 rows x 64 bf16
 constexpr int kBTile = kPfBN * 128;                          // 256 tokens x 64 bf16
 constexpr int kRawMax = 7168;                                // >= Q6_K tile 6144 + 512 + 256
-constexpr int kPfStageBytes = kATile + kBTile + kRawMax;     // 56320, a multiple of 1024
+constexpr int kPfStageBytes = kBTile + kRawMax;              // 39936, a multiple of 1024
 constexpr int kPfSmem = 1024 + kPfStages * kPfStageBytes + 256;
-constexpr uint32_t kPfTmemCols = 256;
+constexpr uint32_t kPfTmemCols = 512;
+constexpr uint32_t kPfA0 = 256;                              // A stage s at columns 256 + 32 s
+static_assert(kPfA0 + 32 * kPfStages <= kPfTmemCols, "tensor memory");
 
 struct PrefillArgs {
   const uint8_t* codes;
@@ -99,12 +106,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint8_t* st = smem + s * kPfStageBytes;
         const int64_t tile = (int64_t)tile_n * KG + kt;
         mbar_arrive_expect_tx(&full[s], kRaw + kBTile);
-        bulk_g2s(st + kATile + kBTile, a.codes + tile * F::TB, F::TB, &full[s]);
-        bulk_g2s(st + kATile + kBTile + F::TB, a.scales + tile * (128 * F::SB), 128 * F::SB, &full[s]);
+        bulk_g2s(st + kBTile, a.codes + tile * F::TB, F::TB, &full[s]);
+        bulk_g2s(st + kBTile + F::TB, a.scales + tile * (128 * F::SB), 128 * F::SB, &full[s]);
         if (FMT == FMT_Q6K)
-          bulk_g2s(st + kATile + kBTile + F::TB + 128 * F::SB, a.aux + ((int64_t)tile_n * (KG / 4) + kt / 4) * 256,
-                   256, &full[s]);
-        tma_load_2d(st + kATile, &tmx, kt * 64, t0, &full[s]);
+          bulk_g2s(st + kBTile + F::TB + 128 * F::SB, a.aux + ((int64_t)tile_n * (KG / 4) + kt / 4) * 256, 256,
+                   &full[s]);
+        tma_load_2d(st, &tmx, kt * 64, t0, &full[s]);
         ++issued;
         if (++s == kPfStages) {
           s = 0;
@@ -123,11 +130,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int kt = 0; kt < KG; ++kt) {
         if (!mbar_wait_bounded(&afull[s], ph, a.status) || !mbar_wait_bounded(&full[s], ph, a.status)) break;
         tc_fence_after();
-        const uint32_t abase = smem_u32(smem + s * kPfStageBytes);
-        const uint32_t bbase = abase + kATile;
+        const uint32_t ta = tmem + kPfA0 + 32u * (uint32_t)s;
+        const uint32_t bbase = smem_u32(smem + s * kPfStageBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ss(tmem, sw128_desc(abase + kk * 32), sw128_desc(bbase + kk * 32), idesc, (kt | kk) ? 1u : 0u);
+          mma_bf16_ts(tmem, ta + kk * 8, sw128_desc(bbase + kk * 32), idesc, (kt | kk) ? 1u : 0u);
         mma_commit(&empty[s]);
         if (++s == kPfStages) {
           s = 0;
@@ -138,9 +145,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     __syncwarp();
   } else {
-    // decode warps
-    const int dt = tid - 64;
-    const int r = dt & 127, h = dt >> 7;
+    // decode warps: warp w may only touch TMEM lanes 32*(w%4)..; it decodes rows
+    // 32*(w%4)+lane, inputs 32h..32h+31 of each stage (h = 0 for warps 2-5, 1 for 6-9)
+    const int r = (warp & 3) * 32 + lane, h = (warp - 2) >> 2;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -149,9 +157,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         ok = false;
         break;
       }
+      // slot s's previous A was read by MMAs that completed before the producer refilled the
+      // slot (empty -> producer -> full): order this thread's TMEM writes after them
+      tc_fence_after();
       uint8_t* st = smem + s * kPfStageBytes;
-      decode_stage<FMT>(st + kATile + kBTile, st, r, h);
-      fence_proxy_async_smem();
+      uint32_t o[16];
+      decode_regs<FMT>(st + kBTile, r, h, o);
+      tmem_st16(tmem + lane_base + kPfA0 + 32u * (uint32_t)s + 16u * (uint32_t)h, o);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[s]);
       if (++s == kPfStages) {

@@ -1,40 +1,41 @@
-// Mixture-of-experts layer for many tokens (TurboEXL3 article §4.1, "Prefill: decode once,
-// multiply many times"): after the route (route.cu) groups every (token, expert) pair by
-// expert and cuts each expert's run into tiles of at most 192 pairs,
+// Tensor-core GEMMs with on-chip dequantisation (TurboEXL3 article §4.1, "Prefill: decode
+// once, multiply many times"): every packed 128 x 64 weight tile is decoded once per
+// token tile into the tensor cores' operand and multiplied by up to 192 tokens; the decoded
+// weights never reach device memory.  One kernel body serves the two GEMMs of the MoE layer:
 //
-//   gate/up  one grouped tensor-core GEMM over the tile table: each work item is (tile,
-//            128 features); it decodes the expert's gate rows f.. and up rows F+f.. of every
-//            64-deep stage once into tensor memory, multiplies both by the tile's tokens
-//            gathered straight from x (no grouped copy of x is written), and its epilogue
-//            runs the mid step -- h = bf16(silu(gate) * up) in fp32 (§4.1 "Mid") -- so the
-//            gate/up outputs never reach device memory
-//   down     the same GEMM body on h (rows already in grouped order), fp32 outputs per pair
-//   finish   out[t] = bf16( sum_j p[t, j] * down[pos(t, j)] + shared[t] ) (§4.1 "Finish")
+//   MoE gate/up     one grouped GEMM over the router's tile table (tiles of <= 192 pairs of one
+//                   expert): a work item is (tile, 128 features f..f+127), whose two row tiles
+//                   are the expert's gate rows f.. and up rows F+f..; the token rows are
+//                   gathered straight from x by index; the epilogue is the mid step
+//                   h = bf16(silu(gate) * up) in fp32 (§4.1 "Mid"), so the gate/up outputs
+//                   never reach device memory
+//   MoE down        the same on h (rows already in grouped order), two row tiles per item,
+//                   fp32 outputs per (token, expert) pair for the finish
+// The MoE shared expert runs as extra token tiles of the gate/up and down GEMMs.  Tile widths are ragged: the MMA's N is the tile's token count
+// rounded up to 16.
 //
-// The shared expert runs as extra tiles of both GEMMs (every token, in 192-token tiles).
-// Tile widths are ragged: the MMA's N is the tile's pair count rounded up to 16, so an
-// expert with 160 tokens costs 160 columns, not 192.
-//
-// The GEMM is persistent (one CTA per SM walks the work items) and warp-specialised:
-//   warp 0       raw-weight producer: bulk copies of the packed tiles into a deep ring
-//   warp 1       TMEM allocation and the tcgen05.mma issuer (one lane)
-//   warps 2-9    decode a stage's tiles into the bf16 A operand ring in tensor memory
-//                (tcgen05.st), so the decoded weights cost no shared-memory bandwidth
-//   warps 10-17  epilogue: TMEM -> registers -> h (bf16) or per-pair outputs (fp32)
-//   warps 18-21  gather: cp.async of the tile's activation rows, by row index, into the
-//                128-byte swizzled operand ring; each thread's copies arrive on the
-//                stage's mbarrier when they land, and the MMA thread fences the generic
-//                proxy writes before the tensor cores read them
-// The three rings (raw, decoded A, gathered B) have their own full/empty mbarriers, so HBM
-// latency on the weights, L2 latency on the gathers and the decode overlap one another and
-// the tensor cores.  The down GEMM double-buffers its accumulator in TMEM so an item's
-// epilogue overlaps the next item's main loop.  Every wait is bounded (QG_ERR_TIMEOUT in
-// the workspace status word) and TMEM is freed on every path.
+// Persistent and warp-specialised (one CTA per SM walks the work items):
+//   warp 0       raw-weight producer: bulk copies of both packed tiles of a stage into a
+//                deep shared-memory ring
+//   warp 1       allocates all 512 TMEM columns; one lane issues the tcgen05.mma
+//   warps 2-9    decode each stage's two tiles into the bf16 A operand in tensor memory
+//                (tcgen05.st), so decoded weights cost no shared-memory bandwidth
+//   warps 10-17  epilogue: TMEM -> registers -> outputs
+//   warps 18-21  token rows: one TMA load per stage when the rows are contiguous, else a
+//                cp.async gather by row index into the 128-byte swizzled ring; each
+//                thread's copies arrive on the stage's mbarrier when they land, and the MMA
+//                thread fences these generic-proxy writes before the tensor cores read them
+// Two accumulators (one per row tile, 192 columns each) are two independent MMA chains per
+// 16-deep step: consecutive MMAs into one accumulator wait on each other, so a single chain
+// at N <= 192 leaves the tensor pipe idle part of the time, while two interleaved chains keep
+// it full.  Every wait is bounded (QG_ERR_TIMEOUT in the workspace status word) and TMEM is
+// freed on every path.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "qg_common.cuh"
 #include "qg_decode_tile.cuh"
@@ -45,84 +46,103 @@
 
 namespace qg {
 
-constexpr int kMpDecWarps = 8;  // two per TMEM lane quarter, one per half of a stage's 64 inputs
-constexpr int kMpEpiWarps = 8;  // two per TMEM lane quarter, alternate 16-column chunks
-constexpr int kMpGatWarps = 4;
-constexpr int kMpGatThreads = kMpGatWarps * 32;
-constexpr int kMpWarps = 2 + kMpDecWarps + kMpEpiWarps + kMpGatWarps;  // 22
-constexpr int kMpThreads = kMpWarps * 32;                               // 704
-constexpr int kMpEpiWarp0 = 2 + kMpDecWarps;                            // 10
-constexpr int kMpGatWarp0 = kMpEpiWarp0 + kMpEpiWarps;                  // 18
-constexpr int kMpTile = kRouteTile;  // pairs per tile = largest MMA N
-constexpr int kMpSmemCap = 232448;   // opt-in shared memory per block on sm_100-family GPUs
+constexpr int kTcDecWarps = 8;  // two per TMEM lane quarter, one per half of a stage's 64 inputs
+constexpr int kTcEpiWarps = 8;  // two per TMEM lane quarter, alternate 16-column chunks
+constexpr int kTcGatWarps = 4;
+constexpr int kTcGatThreads = kTcGatWarps * 32;
+constexpr int kTcWarps = 2 + kTcDecWarps + kTcEpiWarps + kTcGatWarps;  // 22
+constexpr int kTcThreads = kTcWarps * 32;                               // 704
+constexpr int kTcEpiWarp0 = 2 + kTcDecWarps;                            // 10
+constexpr int kTcGatWarp0 = kTcEpiWarp0 + kTcEpiWarps;                  // 18
+constexpr int kTcTile = kRouteTile;  // tokens per tile = largest MMA N (192)
+constexpr int kTcSmemCap = 232448;   // opt-in shared memory per block on sm_100-family GPUs
 
-// Tensor memory (512 columns x 128 lanes of 32 bits) holds the accumulators and the decoded
-// weight operand A:
-//   gate/up: gate accumulator [0, 192), up accumulator [192, 384), A ring of 2 stages x 64
-//            columns (gate rows' 64 inputs in 32 columns, then the up rows')
-//   down:    two accumulators [0, 192) and [192, 384), A ring of 4 stages x 32 columns
-// so shared memory holds only the raw packed tiles and the gathered activation rows.
-template <int FMT, bool DUAL>
-struct MpCfg {
+enum TcEpilogue { kEpiSwiglu = 0, kEpiPairF32 = 1 };
+
+// Tensor memory (512 columns x 128 lanes of 32 bits): accumulators of the two row tiles in
+// columns [0, 192) and [192, 384); A ring of 2 stages x 64 columns (first tile's 64 inputs in
+// 32 columns, then the second's) in [384, 512).  Shared memory: the gathered token rows
+// (6 stages) and the raw packed tiles.
+template <int FMT>
+struct TcCfg {
   using F = Fmt<FMT>;
   static constexpr int RAW1 = F::TB + 128 * F::SB + (FMT == FMT_Q6K ? 256 : 0);  // one packed tile
-  static constexpr int RAWB = (DUAL ? 2 : 1) * RAW1;
-  static constexpr int B = kMpTile * 128;      // gathered rows, 128-byte swizzled
+  static constexpr int RAWB = 2 * RAW1;
+  static constexpr int B = kTcTile * 128;
   static constexpr int BS = 6;
-  static constexpr int ACC = DUAL ? 1 : 2;      // accumulator buffers
-  static constexpr uint32_t ACC_COLS = DUAL ? 2 * kMpTile : kMpTile;
-  static constexpr int AS = DUAL ? 2 : 4;       // A stages in TMEM
-  static constexpr uint32_t A_COLS = DUAL ? 64 : 32;
-  static constexpr uint32_t A0 = 2 * kMpTile;  // first A column
+  static constexpr int AS = 2;
+  static constexpr uint32_t A_COLS = 64;
+  static constexpr uint32_t A0 = 2 * kTcTile;
   static_assert(A0 + AS * A_COLS <= 512, "tensor memory");
-  static constexpr int FIT = (kMpSmemCap - 1024 - 512 - BS * B) / RAWB;
+  static constexpr int FIT = (kTcSmemCap - 1024 - 512 - BS * B) / RAWB;
   static constexpr int RS = FIT > 16 ? 16 : FIT;
   static constexpr int OFF_RAW = BS * B;
   static constexpr int OFF_BAR = OFF_RAW + RS * RAWB;
-  static constexpr int NBAR = 2 * RS + 2 * AS + 2 * BS + 2 * 2 + 1;
+  static constexpr int NBAR = 2 * RS + 2 * AS + 2 * BS + 2 + 1;
   static constexpr int SMEM = 1024 + OFF_BAR + NBAR * 8 + 16;
   static_assert(RS >= 4, "raw ring too shallow");
-  static_assert(SMEM <= kMpSmemCap, "shared memory");
+  static_assert(SMEM <= kTcSmemCap, "shared memory");
 };
 
-struct MpArgs {
-  const uint8_t* codes;  // routed experts, concatenated (stride per expert below)
+struct TcArgs {
+  // routed experts (MoE), concatenated; unused when meta is null
+  const uint8_t* codes;
   const uint8_t* scales;
   const uint8_t* aux;
   int64_t cstride, sstride, astride;
-  const uint8_t* sh_codes;  // shared expert (used when n_sh_tiles > 0)
+  float ts;
+  // the MoE shared expert: every token in kTcTile-token tiles
+  const uint8_t* sh_codes;
   const uint8_t* sh_scales;
   const uint8_t* sh_aux;
-  float ts, sh_ts;
-  const __nv_bfloat16* in;  // gate/up: x [T][ldi]; down: h [R][ldi]
+  float sh_ts;
+  int n_sh_tiles;
+  int sh_in_off, sh_out_off;  // input / output row of token 0 of the shared-expert tiles
+  const __nv_bfloat16* in;    // token rows [*][ldi], K inputs each
   int64_t ldi;
   int64_t K;
   int KG;
-  void* out;  // gate/up: h bf16 [R][ldo]; down: d fp32 [R][ldo]
+  int NT;     // 128-row tiles of the weight
+  int QN;     // items per token tile
+  int T;      // tokens
+  int topk;   // routed gate/up: input row = pair / topk
+  void* out;  // kEpiSwiglu: bf16 h [*][ldo]; kEpiPairF32: fp32 [*][ldo]
   int64_t ldo;
-  int64_t n_out;  // features of the output (F for gate/up, H for down)
-  int QN;         // 128-feature blocks per tile (gate/up: F/128; down: ceil(H/128))
-  int T, topk, n_sh_tiles;
-  const int* meta;
+  int64_t n_out;
+  int64_t F;  // kEpiSwiglu: rows of the gate half (up rows start at F)
+  const int* meta;  // router: [1] = routed tiles
   const int* tiles;
   const int* pair_list;
   int* status;
 };
 
-struct MpItem {
+struct TcItem {
   const uint8_t* codes;
   const uint8_t* scales;
   const uint8_t* aux;
   const int* in_list;  // routed gate/up: grouped position -> pair; row = pair / topk
   float ts;
-  int q, count, in_base, out_base;
+  int rt0, rt1;        // the two row tiles
+  bool second;         // rt1 exists (else rt1 == rt0 and its outputs are dropped)
+  int count, in_base, out_base, feat0;
 };
 
-template <bool DUAL>
-__device__ __forceinline__ MpItem mp_item(const MpArgs& a, int n_rt, int i) {
-  MpItem it;
+template <int EPI>
+__device__ __forceinline__ TcItem tc_item(const TcArgs& a, int n_rt, int i) {
+  TcItem it;
   const int ti = i / a.QN;
-  it.q = i - ti * a.QN;
+  const int q = i - ti * a.QN;
+  if (EPI == kEpiSwiglu) {
+    it.rt0 = q;
+    it.rt1 = q + a.QN;
+    it.second = true;
+    it.feat0 = q * 128;
+  } else {
+    it.rt0 = 2 * q;
+    it.second = 2 * q + 1 < a.NT;
+    it.rt1 = it.second ? 2 * q + 1 : 2 * q;
+    it.feat0 = 2 * q * 128;
+  }
   if (ti < n_rt) {
     const int e = a.tiles[3 * ti], first = a.tiles[3 * ti + 1];
     it.count = a.tiles[3 * ti + 2];
@@ -131,24 +151,24 @@ __device__ __forceinline__ MpItem mp_item(const MpArgs& a, int n_rt, int i) {
     it.aux = a.aux ? a.aux + (int64_t)e * a.astride : nullptr;
     it.ts = a.ts;
     it.out_base = first;
-    it.in_list = DUAL ? a.pair_list + first : nullptr;
+    it.in_list = EPI == kEpiSwiglu ? a.pair_list + first : nullptr;
     it.in_base = first;
   } else {
-    const int t0 = (ti - n_rt) * kMpTile;
-    it.count = min(kMpTile, a.T - t0);
+    const int t0 = (ti - n_rt) * kTcTile;
+    it.count = min(kTcTile, a.T - t0);
     it.codes = a.sh_codes;
     it.scales = a.sh_scales;
     it.aux = a.sh_aux;
     it.ts = a.sh_ts;
-    it.out_base = a.T * a.topk + t0;
+    it.out_base = a.sh_out_off + t0;
     it.in_list = nullptr;
-    it.in_base = DUAL ? t0 : a.T * a.topk + t0;
+    it.in_base = a.sh_in_off + t0;
   }
   return it;
 }
 
 template <int FMT>
-__device__ __forceinline__ void mp_load_tile(uint8_t* dst, const MpItem& it, int row_tile, int KG, int kt,
+__device__ __forceinline__ void tc_load_tile(uint8_t* dst, const TcItem& it, int row_tile, int KG, int kt,
                                              uint64_t* bar) {
   using F = Fmt<FMT>;
   const int64_t tile = (int64_t)row_tile * KG + kt;
@@ -158,9 +178,9 @@ __device__ __forceinline__ void mp_load_tile(uint8_t* dst, const MpItem& it, int
     bulk_g2s(dst + F::TB + 128 * F::SB, it.aux + ((int64_t)row_tile * (KG / 4) + kt / 4) * 256, 256, bar);
 }
 
-template <int FMT, bool DUAL>
-__global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a) {
-  using C = MpCfg<FMT, DUAL>;
+template <int FMT, int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmb, const TcArgs a) {
+  using C = TcCfg<FMT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sB = smem;
@@ -172,12 +192,12 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
   uint64_t* b_full = a_empty + C::AS;
   uint64_t* b_empty = b_full + C::BS;
   uint64_t* t_full = b_empty + C::BS;
-  uint64_t* t_empty = t_full + 2;
-  uint64_t* fin = t_empty + 2;
+  uint64_t* t_empty = t_full + 1;
+  uint64_t* fin = t_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_rt = a.meta[1];
+  const int n_rt = a.meta ? a.meta[1] : 0;
   const int n_items = (n_rt + a.n_sh_tiles) * a.QN;
   const int G = gridDim.x, b = blockIdx.x;
   const int KG = a.KG;
@@ -185,20 +205,18 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
   if (tid == 0) {
     for (int s = 0; s < C::RS; ++s) {
       mbar_init(&r_full[s], 1);
-      mbar_init(&r_empty[s], kMpDecWarps);
+      mbar_init(&r_empty[s], kTcDecWarps);
     }
     for (int s = 0; s < C::AS; ++s) {
-      mbar_init(&a_full[s], kMpDecWarps);
+      mbar_init(&a_full[s], kTcDecWarps);
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < C::BS; ++s) {
-      mbar_init(&b_full[s], kMpGatThreads);  // one cp.async completion arrival per gather thread
+      mbar_init(&b_full[s], kTcGatThreads);  // one cp.async completion arrival per gather thread
       mbar_init(&b_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&t_full[s], 1);
-      mbar_init(&t_empty[s], kMpEpiWarps);
-    }
+    mbar_init(t_full, 1);
+    mbar_init(t_empty, kTcEpiWarps);
     mbar_init(fin, 1);
     fence_mbar_init();
   }
@@ -217,7 +235,7 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
       uint32_t gs = 0;
       bool ok = true;
       for (int i = b; ok && i < n_items; i += G) {
-        const MpItem it = mp_item<DUAL>(a, n_rt, i);
+        const TcItem it = tc_item<EPI>(a, n_rt, i);
         for (int kt = 0; kt < KG; ++kt, ++gs) {
           const uint32_t s = gs % C::RS;
           if (gs >= (uint32_t)C::RS && !mbar_wait_bounded(&r_empty[s], ((gs / C::RS) & 1u) ^ 1u, a.status)) {
@@ -226,8 +244,8 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
           }
           uint8_t* dst = sR + s * C::RAWB;
           mbar_arrive_expect_tx(&r_full[s], C::RAWB);
-          mp_load_tile<FMT>(dst, it, it.q, KG, kt, &r_full[s]);
-          if (DUAL) mp_load_tile<FMT>(dst + C::RAW1, it, it.q + a.QN, KG, kt, &r_full[s]);
+          tc_load_tile<FMT>(dst, it, it.rt0, KG, kt, &r_full[s]);
+          tc_load_tile<FMT>(dst + C::RAW1, it, it.rt1, KG, kt, &r_full[s]);
         }
       }
       // leave no copy in flight into this CTA's shared memory
@@ -240,17 +258,14 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
       uint32_t gs = 0, itc = 0;
       bool ok = true;
       for (int i = b; ok && i < n_items; i += G, ++itc) {
-        const MpItem it = mp_item<DUAL>(a, n_rt, i);
+        const TcItem it = tc_item<EPI>(a, n_rt, i);
         const int N = (it.count + 15) & ~15;
         const uint32_t idesc = idesc_bf16_f32(128, N);
-        const uint32_t acc = DUAL ? 0u : (itc & 1u);
-        if (itc >= (uint32_t)C::ACC &&
-            !mbar_wait_bounded(&t_empty[acc], ((itc / C::ACC) & 1u) ^ 1u, a.status)) {
+        if (itc >= 1u && !mbar_wait_bounded(t_empty, (itc & 1u) ^ 1u, a.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d0 = tmem + acc * C::ACC_COLS;
         for (int kt = 0; kt < KG; ++kt, ++gs) {
           const uint32_t sa = gs % C::AS, sb = gs % C::BS;
           if (!mbar_wait_bounded(&a_full[sa], (gs / C::AS) & 1u, a.status) ||
@@ -268,20 +283,20 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t accum = (kt | kk) ? 1u : 0u;
             const uint64_t bd = sw128_desc(bbase + kk * 32);
-            mma_bf16_ts(d0, ta + kk * 8, bd, idesc, accum);
-            if (DUAL) mma_bf16_ts(tmem + kMpTile, ta + 32 + kk * 8, bd, idesc, accum);
+            mma_bf16_ts(tmem, ta + kk * 8, bd, idesc, accum);
+            mma_bf16_ts(tmem + kTcTile, ta + 32 + kk * 8, bd, idesc, accum);
           }
           mma_commit(&a_empty[sa]);
           mma_commit(&b_empty[sb]);
         }
         if (!ok) break;
-        mma_commit(&t_full[acc]);
+        mma_commit(t_full);
       }
       mma_commit(fin);  // every MMA issued so far is complete when this arrives
       mbar_wait_bounded(fin, 0, a.status);
     }
     __syncwarp();
-  } else if (warp < kMpEpiWarp0) {
+  } else if (warp < kTcEpiWarp0) {
     // ------------------------------------------------------------ decode
     // Warp w may only touch TMEM lanes 32*(w%4)..: it decodes rows 32*(w%4)+lane, inputs
     // 32h..32h+31 of each 64-deep stage (h = 0 for warps 2-5, 1 for warps 6-9).
@@ -303,10 +318,8 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
         uint32_t o[16];
         decode_regs<FMT>(raw, r, h, o);
         tmem_st16(ta, o);
-        if (DUAL) {
-          decode_regs<FMT>(raw + C::RAW1, r, h, o);
-          tmem_st16(ta + 32, o);
-        }
+        decode_regs<FMT>(raw + C::RAW1, r, h, o);
+        tmem_st16(ta + 32, o);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -316,25 +329,24 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
         }
       }
     }
-  } else if (warp < kMpGatWarp0) {
+  } else if (warp < kTcGatWarp0) {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3, half = (warp - kMpEpiWarp0) >> 2;
+    const int quarter = warp & 3, half = (warp - kTcEpiWarp0) >> 2;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     uint32_t itc = 0;
     for (int i = b; i < n_items; i += G, ++itc) {
-      const MpItem it = mp_item<DUAL>(a, n_rt, i);
+      const TcItem it = tc_item<EPI>(a, n_rt, i);
       const int N = (it.count + 15) & ~15;
-      const uint32_t acc = DUAL ? 0u : (itc & 1u);
-      if (!mbar_wait_bounded(&t_full[acc], (itc / C::ACC) & 1u, a.status)) break;
+      if (!mbar_wait_bounded(t_full, itc & 1u, a.status)) break;
       tc_fence_after();
-      const int64_t n = (int64_t)it.q * 128 + quarter * 32 + lane;
+      const int r = quarter * 32 + lane;
       for (int c = 16 * half; c < N; c += 32) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_base + acc * C::ACC_COLS + (uint32_t)c, v);
-        if (DUAL) {
-          uint32_t u[16];
-          tmem_ld16(tmem + lane_base + kMpTile + (uint32_t)c, u);
-          tmem_ld_wait();
+        uint32_t v[16], u[16];
+        tmem_ld16(tmem + lane_base + (uint32_t)c, v);
+        tmem_ld16(tmem + lane_base + kTcTile + (uint32_t)c, u);
+        tmem_ld_wait();
+        if (EPI == kEpiSwiglu) {
+          const int64_t n = it.feat0 + r;  // < F: F is a multiple of 128
           __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(a.out) + (int64_t)(it.out_base + c) * a.ldo + n;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -347,36 +359,44 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
             }
           }
         } else {
-          tmem_ld_wait();
-          if (n < a.n_out) {
-            float* dout = static_cast<float*>(a.out) + (int64_t)(it.out_base + c) * a.ldo + n;
+          const int64_t n0 = (int64_t)it.rt0 * 128 + r, n1 = (int64_t)it.rt1 * 128 + r;
+          const bool w0 = n0 < a.n_out, w1 = it.second && n1 < a.n_out;
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c + j < it.count) dout[(int64_t)j * a.ldo] = it.ts * __uint_as_float(v[j]);
+          for (int j = 0; j < 16; ++j) {
+            if (c + j < it.count) {
+              float* o = static_cast<float*>(a.out) + (int64_t)(it.out_base + c + j) * a.ldo;
+              if (w0) o[n0] = it.ts * __uint_as_float(v[j]);
+              if (w1) o[n1] = it.ts * __uint_as_float(u[j]);
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&t_empty[acc]);
+      if (lane == 0) mbar_arrive(t_empty);
     }
   } else {
-    // ------------------------------------------------------------ activation gather
-    // Each thread copies 16-byte chunks of the stage's rows and arrives on the stage's
-    // barrier when its copies land (cp.async.mbarrier.arrive.noinc), so the gather runs up
-    // to BS stages ahead without waiting on its own loads.
-    const int gt = tid - kMpGatWarp0 * 32;
+    // ------------------------------------------------------------ token rows
+    // Contiguous rows (dense GEMM, MoE down, shared-expert tiles): one 2-D TMA load of
+    // 64 inputs x 192 rows per stage (128-byte swizzle; rows past the tensor read as zero),
+    // issued by the first gather thread with the stage's byte count, the other threads
+    // arriving plainly.  Routed gate/up tiles: each thread copies 16-byte chunks of the rows
+    // by index and arrives on the stage's barrier when its copies land
+    // (cp.async.mbarrier.arrive.noinc), so the gather runs up to BS stages ahead without
+    // waiting on its own loads.
+    const int gt = tid - kTcGatWarp0 * 32;
     const int c8 = gt & 7, rs = gt >> 3;  // 16-byte chunk of a 128-byte row; row within 16
     uint32_t gs = 0;
     bool ok = true;
     for (int i = b; ok && i < n_items; i += G) {
-      const MpItem it = mp_item<DUAL>(a, n_rt, i);
+      const TcItem it = tc_item<EPI>(a, n_rt, i);
       const int N = (it.count + 15) & ~15;
-      int row[kMpTile / 16];
+      const bool gather = it.in_list != nullptr;
+      int row[kTcTile / 16];
 #pragma unroll
-      for (int ii = 0; ii < kMpTile / 16; ++ii) {
+      for (int ii = 0; ii < kTcTile / 16; ++ii) {
         const int j = rs + 16 * ii;
-        row[ii] = j < it.count ? (it.in_list ? it.in_list[j] / a.topk : it.in_base + j) : -1;
+        row[ii] = (gather && j < it.count) ? it.in_list[j] / a.topk : -1;
       }
       for (int kt = 0; kt < KG; ++kt, ++gs) {
         const uint32_t s = gs % C::BS;
@@ -385,10 +405,19 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
           break;
         }
         uint8_t* dst = sB + s * C::B;
+        if (!gather) {
+          if (gt == 0) {
+            mbar_arrive_expect_tx(&b_full[s], C::B);
+            tma_load_2d(dst, &tmb, kt * 64, it.in_base, &b_full[s]);
+          } else {
+            mbar_arrive(&b_full[s]);
+          }
+          continue;
+        }
         const int64_t k0 = (int64_t)kt * 64 + c8 * 8;
         const uint32_t kb = k0 + 8 <= a.K ? 16u : (k0 < a.K ? (uint32_t)(a.K - k0) * 2u : 0u);
 #pragma unroll
-        for (int ii = 0; ii < kMpTile / 16; ++ii) {
+        for (int ii = 0; ii < kTcTile / 16; ++ii) {
           const int j = rs + 16 * ii;
           if (j < N) {
             const bool live = row[ii] >= 0 && kb > 0;
@@ -399,6 +428,10 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
         cp_async_arrive_noinc(&b_full[s]);
       }
     }
+    // leave no copy in flight into this CTA's shared memory: cp.async here, TMA below
+    if (gt == 0)
+      for (uint32_t g2 = gs > (uint32_t)C::BS ? gs - C::BS : 0; g2 < gs; ++g2)
+        mbar_wait_bounded(&b_full[g2 % C::BS], (g2 / C::BS) & 1u, a.status);
     cp_async_wait_all();  // no copy in flight into shared memory past this point
   }
 
@@ -411,7 +444,7 @@ __global__ void __launch_bounds__(kMpThreads, 1) moe_gemm_kernel(const MpArgs a)
 }
 
 // out[t][n] = bf16( sum_j w[t][j] * d[pos(t, j)][n] + d[T*topk + t][n] ), fixed order, four
-// features per thread.
+// features per thread (TurboEXL3 article §4.1 "Finish").
 __global__ void __launch_bounds__(256) moe_finish4_kernel(const float* d, int64_t ldd, const float* w,
                                                           const int* pair_pos, int T, int topk, int has_shared,
                                                           int64_t H, __nv_bfloat16* out, int64_t ldo) {
@@ -446,33 +479,64 @@ __global__ void __launch_bounds__(256) moe_finish4_kernel(const float* d, int64_
 // ---------------------------------------------------------------- host side
 namespace {
 
-template <int FMT, bool DUAL>
-int launch_mp(const MpArgs& a, const DeviceInfo& dev, cudaStream_t s) {
-  using C = MpCfg<FMT, DUAL>;
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeFn g_encode = nullptr;
+
+// The token-row operand as a 2-D TMA tensor: rows x K bf16, row stride ldi elements, box of
+// 64 inputs x 192 rows, 128-byte swizzle (the MMA's K-major operand layout), zero fill.
+bool encode_rows(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ldi) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeFn>(fn);
+  });
+  if (!g_encode) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ldi * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kTcTile};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT, int EPI>
+int launch_tc(const CUtensorMap& map, const TcArgs& a, int grid, const DeviceInfo& dev, cudaStream_t s) {
+  using C = TcCfg<FMT>;
   static std::atomic<unsigned long long> configured{0};
   if (C::SMEM > dev.max_smem_optin) return QG_ERR_UNSUPPORTED;
   int devid = 0;
   if (cudaGetDevice(&devid) != cudaSuccess) return QG_ERR_CUDA;
   const unsigned long long bit = 1ull << (devid & 63);
   if (!(configured.load() & bit)) {
-    if (cudaFuncSetAttribute((const void*)moe_gemm_kernel<FMT, DUAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute((const void*)tc_gemm_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM) != cudaSuccess)
       return QG_ERR_CUDA;
     configured.fetch_or(bit);
   }
-  moe_gemm_kernel<FMT, DUAL><<<dev.sms, kMpThreads, C::SMEM, s>>>(a);
+  tc_gemm_kernel<FMT, EPI><<<grid, kTcThreads, C::SMEM, s>>>(map, a);
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
-template <bool DUAL>
-int launch_mp_fmt(int fmt, const MpArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+template <int EPI>
+int launch_tc_fmt(int fmt, int64_t in_rows, const TcArgs& a, int grid, const DeviceInfo& dev, cudaStream_t s) {
+  CUtensorMap map;
+  if (!encode_rows(&map, a.in, in_rows, a.K, a.ldi)) return QG_ERR_CUDA;
   switch (fmt) {
-    case FMT_MLX: return launch_mp<FMT_MLX, DUAL>(a, dev, s);
-    case FMT_MXFP4: return launch_mp<FMT_MXFP4, DUAL>(a, dev, s);
-    case FMT_NVFP4: return launch_mp<FMT_NVFP4, DUAL>(a, dev, s);
-    default: return launch_mp<FMT_Q6K, DUAL>(a, dev, s);
+    case FMT_MLX: return launch_tc<FMT_MLX, EPI>(map, a, grid, dev, s);
+    case FMT_MXFP4: return launch_tc<FMT_MXFP4, EPI>(map, a, grid, dev, s);
+    case FMT_NVFP4: return launch_tc<FMT_NVFP4, EPI>(map, a, grid, dev, s);
+    default: return launch_tc<FMT_Q6K, EPI>(map, a, grid, dev, s);
   }
 }
+
+int tiles_of(int64_t t) { return (int)((t + kTcTile - 1) / kTcTile); }
 
 }  // namespace
 
@@ -487,38 +551,42 @@ int launch_moe_prefill(const qg_moe_layer* m, const Geometry& gu, const Geometry
   size_t cb = 0, sb = 0, ab = 0;
   qg_packed_sizes(m->fmt, gu.n, gu.k, &cb, &sb, &ab);
 
-  MpArgs a{};
+  TcArgs a{};
   a.codes = static_cast<const uint8_t*>(m->gu_codes);
   a.scales = static_cast<const uint8_t*>(m->gu_scales);
   a.aux = static_cast<const uint8_t*>(m->gu_aux);
   a.cstride = (int64_t)cb;
   a.sstride = (int64_t)sb;
   a.astride = (int64_t)ab;
-  a.n_sh_tiles = m->has_shared ? (int)((T + kMpTile - 1) / kMpTile) : 0;
+  a.ts = (m->fmt == FMT_NVFP4) ? m->tensor_scale : 1.0f;
+  a.n_sh_tiles = m->has_shared ? tiles_of(T) : 0;
   a.sh_codes = m->has_shared ? static_cast<const uint8_t*>(m->shared_gate_up.codes) : nullptr;
   a.sh_scales = m->has_shared ? static_cast<const uint8_t*>(m->shared_gate_up.scales) : nullptr;
   a.sh_aux = m->has_shared ? static_cast<const uint8_t*>(m->shared_gate_up.aux) : nullptr;
-  a.ts = (m->fmt == FMT_NVFP4) ? m->tensor_scale : 1.0f;
   a.sh_ts = (m->has_shared && m->fmt == FMT_NVFP4) ? m->shared_gate_up.tensor_scale : 1.0f;
+  a.sh_in_off = 0;                  // the shared expert reads x rows
+  a.sh_out_off = (int)(T * topk);   // and writes h rows after the routed pairs
   a.in = static_cast<const __nv_bfloat16*>(x);
   a.ldi = ldx;
   a.K = gu.k;
   a.KG = (int)gu.kg;
-  a.out = w + L.h;
-  a.ldo = L.ld_h;
-  a.n_out = F;
+  a.NT = (int)gu.nt;
   a.QN = F / 128;
   a.T = (int)T;
   a.topk = topk;
+  a.out = w + L.h;
+  a.ldo = L.ld_h;
+  a.n_out = F;
+  a.F = F;
   a.meta = rv.meta;
   a.tiles = rv.tiles;
   a.pair_list = rv.pair_list;
   a.status = reinterpret_cast<int*>(w);
-  int st = launch_mp_fmt<true>(m->fmt, a, dev, s);
+  int st = launch_tc_fmt<kEpiSwiglu>(m->fmt, T, a, dev.sms, dev, s);
   if (st != QG_OK) return st;
 
   qg_packed_sizes(m->fmt, dn.n, dn.k, &cb, &sb, &ab);
-  MpArgs d = a;
+  TcArgs d = a;
   d.codes = static_cast<const uint8_t*>(m->dn_codes);
   d.scales = static_cast<const uint8_t*>(m->dn_scales);
   d.aux = static_cast<const uint8_t*>(m->dn_aux);
@@ -529,15 +597,19 @@ int launch_moe_prefill(const qg_moe_layer* m, const Geometry& gu, const Geometry
   d.sh_scales = m->has_shared ? static_cast<const uint8_t*>(m->shared_down.scales) : nullptr;
   d.sh_aux = m->has_shared ? static_cast<const uint8_t*>(m->shared_down.aux) : nullptr;
   d.sh_ts = (m->has_shared && m->fmt == FMT_NVFP4) ? m->shared_down.tensor_scale : 1.0f;
+  d.sh_in_off = (int)(T * topk);  // the shared expert's h rows
+  d.sh_out_off = (int)(T * topk);
   d.in = reinterpret_cast<const __nv_bfloat16*>(w + L.h);
   d.ldi = L.ld_h;
   d.K = dn.k;
   d.KG = (int)dn.kg;
+  d.NT = (int)dn.nt;
+  d.QN = (int)((dn.nt + 1) / 2);
+  d.pair_list = nullptr;
   d.out = w + L.d;
   d.ldo = L.ld_d;
   d.n_out = dn.n;
-  d.QN = (int)dn.nt;
-  st = launch_mp_fmt<false>(m->fmt, d, dev, s);
+  st = launch_tc_fmt<kEpiPairF32>(m->fmt, T * topk + T, d, dev.sms, dev, s);
   if (st != QG_OK) return st;
 
   const int64_t H = dn.n;
