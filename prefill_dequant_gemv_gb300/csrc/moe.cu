@@ -62,8 +62,20 @@ struct GroupedArgs {
   int* status;
 };
 
+// Per-group description: weight base, rows (input row index, output row index), count.
+struct GroupInfo {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const uint8_t* aux;
+  float ts;
+  int m;
+  int in_row[kGMaxRows];
+  int out_row[kGMaxRows];
+};
+constexpr int kGInfoCache = 8;
+
 struct GroupedSmem {
-  size_t bars, stages, xs, sums, red, lut, misc, total;
+  size_t bars, stages, xs, sums, red, lut, misc, ginfo, total;
 };
 
 __host__ __device__ inline GroupedSmem grouped_smem(int stage_bytes, int S, int nrows, int KG) {
@@ -85,20 +97,11 @@ __host__ __device__ inline GroupedSmem grouped_smem(int stage_bytes, int S, int 
   o += 256 * 4;
   L.misc = o;
   o += 64;
+  L.ginfo = o;  // descriptors of the first kGInfoCache groups this CTA touches
+  o += (size_t)kGInfoCache * sizeof(GroupInfo);
   L.total = o;
   return L;
 }
-
-// Per-group description: weight base, rows (input row index, output row index), count.
-struct GroupInfo {
-  const uint8_t* codes;
-  const uint8_t* scales;
-  const uint8_t* aux;
-  float ts;
-  int m;
-  int in_row[kGMaxRows];
-  int out_row[kGMaxRows];
-};
 
 __device__ __forceinline__ GroupInfo group_info(const GroupedArgs& a, int g, int n_active) {
   GroupInfo gi;
@@ -147,6 +150,19 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   float* red = reinterpret_cast<float*>(smem + L.red);
   float* lut = reinterpret_cast<float*>(smem + L.lut);
   int* flag = reinterpret_cast<int*>(smem + L.misc);
+  GroupInfo* ginfo = reinterpret_cast<GroupInfo*>(smem + L.ginfo);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int s = tid; s < S; s += blockDim.x) {
+    mbar_init(&full[s], 1);
+    mbar_init(&empty[s], kGCW);
+  }
+  if (tid < S) fence_mbar_init();
+  __syncthreads();
+  // The next launch of the chain may start its prologue now; everything below reads the
+  // router's (or the previous step's) outputs, so wait for the preceding kernel first.
+  if (tid == 0) pdl_launch_dependents();
+  pdl_wait();
 
   const int n_active = a.meta[0];
   const int n_groups = n_active + (a.has_shared ? 1 : 0);
@@ -161,16 +177,6 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   const int64_t c0 = b * NCH / G, c1 = (b + 1) * NCH / G;
   const uint32_t uu0 = (uint32_t)(c0 * kGC), uu1 = (uint32_t)(c1 * kGC);
   const int nch = (int)(c1 - c0);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kGCW);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
 
   if (warp == kGCW) {  // producer: chunks never span two groups
     if (lane == 0) {
@@ -225,6 +231,10 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
     lut[2 * tid] = v.x;
     lut[2 * tid + 1] = v.y;
   }
+  // The groups this CTA touches: their descriptors (a chain of dependent loads each) are
+  // read once here, in parallel with the staging, instead of at every segment.
+  const int g_first = (int)(uu0 / (uint32_t)upg);
+  if (tid < kGInfoCache && g_first + tid < n_groups) ginfo[tid] = group_info(a, g_first + tid, n_active);
   // stage every input row over all of K
   for (int it = tid; it < a.nrows * KG * 4; it += kGCT) {
     const int kq = it & 3, sl = (it >> 2) % KG, row = (it >> 2) / KG;
@@ -250,6 +260,9 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   int s = 0;
   uint32_t ph = 0;
   uint32_t u = uu0;
+  int nparts = 0;  // segments of row tiles this CTA holds only part of (at most 2)
+  int pg0 = 0, pq0 = 0, pg1 = 0, pq1 = 0;
+  uint32_t ps0 = 0, pe0 = 0, ps1 = 0, pe1 = 0;
   while (u < uu1) {
     const uint32_t g = u / (uint32_t)upg;
     const uint32_t l = u - g * (uint32_t)upg;
@@ -257,7 +270,7 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
     const uint32_t seg_start = g * upg + q * KG;
     const uint32_t seg_end_full = (q == (uint32_t)(NT - 1)) ? (g + 1) * upg : seg_start + KG;
     const uint32_t seg_end = min(uu1, seg_end_full);
-    const GroupInfo gi = group_info(a, (int)g, n_active);
+    const GroupInfo gi = ((int)g - g_first < kGInfoCache) ? ginfo[(int)g - g_first] : group_info(a, (int)g, n_active);
     float acc[4][kGMaxRows];
 #pragma unroll
     for (int rt = 0; rt < 4; ++rt)
@@ -319,40 +332,62 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
         a.ws_part[(size_t)((b * 2 + slot_ws) * kGMaxRows) * 128 + e] = v;
       }
     }
-    if (!whole) {
-      named_sync(1, kGCT);
-      const int64_t seg = (int64_t)g * NT + q;
-      // contributors own chunks of this segment
-      const int64_t cs = seg_start / kGC, ce = (seg_end_full - 1) / kGC;
-      const int64_t bf = ((cs + 1) * G - 1) / NCH, bl = ((ce + 1) * G - 1) / NCH;
-      if (tid == 0) {
-        __threadfence();
-        const int old = atomicAdd(&a.ws_cnt[seg], 1);
-        __threadfence();
-        *flag = (old == (int)(bl - bf)) ? 1 : 0;
+    if (!whole) {  // the same on every thread: settled after all of this CTA's work
+      if (nparts == 0) {
+        pg0 = (int)g; pq0 = (int)q; ps0 = seg_start; pe0 = seg_end_full;
+      } else {
+        pg1 = (int)g; pq1 = (int)q; ps1 = seg_start; pe1 = seg_end_full;
       }
-      named_sync(1, kGCT);
-      if (*flag) {
-        const int first_sl = ((bf * NCH / G) * kGC < (int64_t)seg_start) ? 1 : 0;
-        const int nc = (int)(bl - bf + 1);
-        const float* part = a.ws_part + (size_t)(bf * 2) * kGMaxRows * 128;
-        for (int e = tid; e < M * 128; e += kGCT) {
-          float v = __ldcg(part + (size_t)first_sl * kGMaxRows * 128 + e);
-          for (int c = 1; c < nc; ++c) v += __ldcg(part + (size_t)(2 * c) * kGMaxRows * 128 + e);
-          const int64_t n = (int64_t)q * 128 + (e & 127);
-          if (n < a.n) a.out[(int64_t)gi.out_row[e >> 7] * a.ldo + n] = v;
-        }
-        if (tid == 0) a.ws_cnt[seg] = 0;
-      }
+      ++nparts;
     }
     named_sync(1, kGCT);
     u = seg_end;
+  }
+
+  // Row tiles split across CTAs (at most two per CTA): one ticket each, taken after all of
+  // this CTA's work; the CTA that takes a segment's last ticket sums its partials in CTA
+  // order (the first contributor may hold it as its last segment, slot 1).
+  if (nparts > 0) {  // uniform: every consumer thread reaches the barriers below
+    if (tid == 0) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (i >= nparts) break;
+        const int pg = i ? pg1 : pg0, pq = i ? pq1 : pq0;
+        const uint32_t ps = i ? ps1 : ps0, pe = i ? pe1 : pe0;
+        const int64_t cs = ps / kGC, ce = (pe - 1) / kGC;
+        const int64_t bf = ((cs + 1) * G - 1) / NCH, bl = ((ce + 1) * G - 1) / NCH;
+        const int old = ticket_add(&a.ws_cnt[(int64_t)pg * NT + pq], 1);
+        flag[i] = (old == (int)(bl - bf)) ? 1 : 0;
+      }
+    }
+    named_sync(1, kGCT);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if (i >= nparts || !flag[i]) continue;
+      const int pg = i ? pg1 : pg0, pq = i ? pq1 : pq0;
+      const uint32_t ps = i ? ps1 : ps0, pe = i ? pe1 : pe0;
+      const GroupInfo gi = (pg - g_first < kGInfoCache) ? ginfo[pg - g_first] : group_info(a, pg, n_active);
+      const int64_t cs = ps / kGC, ce = (pe - 1) / kGC;
+      const int64_t bf = ((cs + 1) * G - 1) / NCH, bl = ((ce + 1) * G - 1) / NCH;
+      const int first_sl = ((bf * NCH / G) * kGC < (int64_t)ps) ? 1 : 0;
+      const int nc = (int)(bl - bf + 1);
+      const float* part = a.ws_part + (size_t)(bf * 2) * kGMaxRows * 128;
+      for (int e = tid; e < gi.m * 128; e += kGCT) {
+        float v = __ldcg(part + (size_t)first_sl * kGMaxRows * 128 + e);
+        for (int c = 1; c < nc; ++c) v += __ldcg(part + (size_t)(2 * c) * kGMaxRows * 128 + e);
+        const int64_t n = (int64_t)pq * 128 + (e & 127);
+        if (n < a.n) a.out[(int64_t)gi.out_row[e >> 7] * a.ldo + n] = v;
+      }
+      if (tid == 0) a.ws_cnt[(int64_t)pg * NT + pq] = 0;
+    }
   }
 }
 
 // h[r][f] = bf16( silu(gu[r][f]) * gu[r][F + f] ) for the rows that exist this call.
 __global__ void __launch_bounds__(256) mid_kernel(const float* gu, int64_t ldg, __nv_bfloat16* h, int64_t ldh, int F,
                                                   int T, int topk, int has_shared) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int rows = T * topk + (has_shared ? T : 0);
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (int64_t)rows * F) return;
@@ -366,6 +401,8 @@ __global__ void __launch_bounds__(256) mid_kernel(const float* gu, int64_t ldg, 
 __global__ void __launch_bounds__(256) finish_kernel(const float* d, int64_t ldd, const float* w, const int* pair_pos,
                                                      int T, int topk, int has_shared, int64_t H, __nv_bfloat16* out,
                                                      int64_t ldo) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (int64_t)T * H) return;
   const int t = (int)(idx / H);
@@ -378,6 +415,23 @@ __global__ void __launch_bounds__(256) finish_kernel(const float* d, int64_t ldd
 
 // ---------------------------------------------------------------- host side
 namespace {
+// Launch with programmatic stream serialization: the kernel may begin while the preceding
+// kernel of the stream finishes; it waits (griddepcontrol.wait) before reading its outputs.
+template <typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 int grouped_stage_bytes(int fmt) {
   switch (fmt) {
     case FMT_MLX: return Stage<FMT_MLX>::bytes(kGC);
@@ -439,14 +493,15 @@ static int launch_grouped(int fmt, const GroupedArgs& a0, int nrows, int KG, con
       return QG_ERR_CUDA;
     configured[fmt].fetch_or(bit);
   }
-  const int grid = dev.sms;
+  const dim3 grid(dev.sms), block(kGThreads);
+  cudaError_t e;
   switch (fmt) {
-    case FMT_MLX: grouped_gemv_kernel<FMT_MLX><<<grid, kGThreads, smem, s>>>(a); break;
-    case FMT_MXFP4: grouped_gemv_kernel<FMT_MXFP4><<<grid, kGThreads, smem, s>>>(a); break;
-    case FMT_NVFP4: grouped_gemv_kernel<FMT_NVFP4><<<grid, kGThreads, smem, s>>>(a); break;
-    default: grouped_gemv_kernel<FMT_Q6K><<<grid, kGThreads, smem, s>>>(a); break;
+    case FMT_MLX: e = launch_pdl(grouped_gemv_kernel<FMT_MLX>, grid, block, smem, s, a); break;
+    case FMT_MXFP4: e = launch_pdl(grouped_gemv_kernel<FMT_MXFP4>, grid, block, smem, s, a); break;
+    case FMT_NVFP4: e = launch_pdl(grouped_gemv_kernel<FMT_NVFP4>, grid, block, smem, s, a); break;
+    default: e = launch_pdl(grouped_gemv_kernel<FMT_Q6K>, grid, block, smem, s, a); break;
   }
-  return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+  return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? QG_OK : QG_ERR_CUDA;
 }
 
 int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
@@ -495,9 +550,10 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
   const int F = (int)dn.k;
   const int rows = (int)(T * topk + (m->has_shared ? T : 0));
   __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(w + L.h);
-  mid_kernel<<<(unsigned)(((int64_t)rows * F + 255) / 256), 256, 0, s>>>(
-      reinterpret_cast<const float*>(w + L.gu), L.ld_gu, h, L.ld_h, F, (int)T, topk, m->has_shared);
-  if (cudaGetLastError() != cudaSuccess) return QG_ERR_CUDA;
+  if (launch_pdl(mid_kernel, dim3((unsigned)(((int64_t)rows * F + 255) / 256)), dim3(256), 0, s,
+                 (const float*)reinterpret_cast<const float*>(w + L.gu), (int64_t)L.ld_gu, h, (int64_t)L.ld_h, F,
+                 (int)T, topk, (int)m->has_shared) != cudaSuccess)
+    return QG_ERR_CUDA;
 
   qg_packed_sizes(m->fmt, dn.n, dn.k, &cb, &sb, &ab);
   GroupedArgs d = a;
@@ -523,9 +579,11 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
   st = launch_grouped(m->fmt, d, rows, (int)dn.kg, dev, s);
   if (st != QG_OK) return st;
 
-  finish_kernel<<<(unsigned)((T * dn.n + 255) / 256), 256, 0, s>>>(
-      reinterpret_cast<const float*>(w + L.d), L.ld_d, topk_w, rv.pair_pos, (int)T, topk, m->has_shared, dn.n,
-      static_cast<__nv_bfloat16*>(out), ldo);
+  if (launch_pdl(finish_kernel, dim3((unsigned)((T * dn.n + 255) / 256)), dim3(256), 0, s,
+                 (const float*)reinterpret_cast<const float*>(w + L.d), (int64_t)L.ld_d, topk_w,
+                 (const int*)rv.pair_pos, (int)T, topk, (int)m->has_shared, (int64_t)dn.n,
+                 static_cast<__nv_bfloat16*>(out), ldo) != cudaSuccess)
+    return QG_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
