@@ -11,9 +11,10 @@
 
 namespace qg {
 
-// Consumer warps: 16 for 1-2 rows; 12 for 3-4 rows, whose accumulators need the
-// 128 registers a 13-warp CTA allows (warps are allocated in groups of four).
-__host__ __device__ constexpr int consumer_warps(int m) { return m >= 3 ? 12 : 16; }
+// Consumer warps: 16 for 1-3 rows (96 registers a thread); 12 for 4 rows, whose
+// accumulators and activations need the 128 registers a 13-warp CTA allows (warps are
+// allocated in groups of four).
+__host__ __device__ constexpr int consumer_warps(int m) { return m >= 4 ? 12 : 16; }
 constexpr int kMaxStages = 48;
 
 // One pipeline stage holds a chunk of C consecutive units (tile index = unit index,
@@ -113,19 +114,24 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
     wd[rt][1] = v.y;
     if (FMT == FMT_Q6K) hw[rt] = *reinterpret_cast<const uint32_t*>(st + ((rt * 3 + 2) * 32 + lane) * 16 + kq * 4);
   }
-  float P[4][M][2];
+  // Activations of the quarter for every row m (both code words), then one 32-row group
+  // at a time: decode, accumulate, fold -- so only one group's partials are live.
+  uint4 X[M][2];
 #pragma unroll
-  for (int rt = 0; rt < 4; ++rt)
+  for (int m = 0; m < M; ++m) {
+    X[m][0] = *reinterpret_cast<const uint4*>(xr[m]);
+    X[m][1] = *reinterpret_cast<const uint4*>(xr[m] + 4);
+  }
+  float4 zq[M];
 #pragma unroll
-    for (int m = 0; m < M; ++m) P[rt][m][0] = P[rt][m][1] = 0.0f;
-
+  for (int m = 0; m < M; ++m) zq[m] = *reinterpret_cast<const float4*>(zr[m]);
 #pragma unroll
-  for (int wi = 0; wi < 2; ++wi) {
-    uint4 X[M];
+  for (int rt = 0; rt < 4; ++rt) {
+    float P[M][2];
 #pragma unroll
-    for (int m = 0; m < M; ++m) X[m] = *reinterpret_cast<const uint4*>(xr[m] + wi * 4);
+    for (int m = 0; m < M; ++m) P[m][0] = P[m][1] = 0.0f;
 #pragma unroll
-    for (int rt = 0; rt < 4; ++rt) {
+    for (int wi = 0; wi < 2; ++wi) {
       const uint32_t w = wd[rt][wi];
       uint32_t o0, o1, o2, o3;
       if (FMT == FMT_MXFP4 || FMT == FMT_NVFP4) {
@@ -149,43 +155,38 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
       }
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        float p0 = P[rt][m][0], p1 = P[rt][m][1];
-        p0 = hfma_lo(o0, X[m].x, p0);
-        p1 = hfma_hi(o0, X[m].x, p1);
-        p0 = hfma_lo(o1, X[m].y, p0);
-        p1 = hfma_hi(o1, X[m].y, p1);
-        p0 = hfma_lo(o2, X[m].z, p0);
-        p1 = hfma_hi(o2, X[m].z, p1);
-        p0 = hfma_lo(o3, X[m].w, p0);
-        p1 = hfma_hi(o3, X[m].w, p1);
-        P[rt][m][0] = p0;
-        P[rt][m][1] = p1;
+        const uint4 x = X[m][wi];
+        float p0 = P[m][0], p1 = P[m][1];
+        p0 = hfma_lo(o0, x.x, p0);
+        p1 = hfma_hi(o0, x.x, p1);
+        p0 = hfma_lo(o1, x.y, p0);
+        p1 = hfma_hi(o1, x.y, p1);
+        p0 = hfma_lo(o2, x.z, p0);
+        p1 = hfma_hi(o2, x.z, p1);
+        p0 = hfma_lo(o3, x.w, p0);
+        p1 = hfma_hi(o3, x.w, p1);
+        P[m][0] = p0;
+        P[m][1] = p1;
       }
     }
-  }
-  // Fold the quarter's partial with the block scale (once per block and row).
-  float4 zq[M];
-#pragma unroll
-  for (int m = 0; m < M; ++m) zq[m] = *reinterpret_cast<const float4*>(zr[m]);
-#pragma unroll
-  for (int rt = 0; rt < 4; ++rt) {
+    // Fold the quarter's partial with the block scale (once per block and row).
     const int row = rt * 32 + lane;
     const uint8_t* sp = scl + row * F::SB;
     if (FMT == FMT_NVFP4) {
       const float S = e4m3_lut[sp[kq]];
 #pragma unroll
-      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * zq[m].x, P[rt][m][0] + P[rt][m][1], acc[rt][m]);
+      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * zq[m].x, P[m][0] + P[m][1], acc[rt][m]);
     } else if (FMT == FMT_MXFP4) {
       const float S = e8m0_f32(sp[kq >> 1]);
 #pragma unroll
-      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * zq[m].x, P[rt][m][0] + P[rt][m][1], acc[rt][m]);
+      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * zq[m].x, P[m][0] + P[m][1], acc[rt][m]);
     } else if (FMT == FMT_MLX) {
       const uint32_t sw = *reinterpret_cast<const uint32_t*>(sp);
       const float s = __half2float(__ushort_as_half((unsigned short)(sw & 0xFFFFu)));
       const float bias = __half2float(__ushort_as_half((unsigned short)(sw >> 16)));
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        const float dot = fmaf(zq[m].x, P[rt][m][0] + P[rt][m][1], -zq[m].y);
+        const float dot = fmaf(zq[m].x, P[m][0] + P[m][1], -zq[m].y);
         acc[rt][m] = fmaf(s, dot, fmaf(bias, zq[m].z, acc[rt][m]));
       }
     } else {
@@ -194,7 +195,7 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
       const float ds = d * sc;
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        const float dot = fmaf(zq[m].x, P[rt][m][0] + P[rt][m][1], -zq[m].y);
+        const float dot = fmaf(zq[m].x, P[m][0] + P[m][1], -zq[m].y);
         acc[rt][m] = fmaf(ds, dot, acc[rt][m]);
       }
     }
