@@ -33,7 +33,7 @@ __device__ __forceinline__ void cx(float& va, int& ia, float& vb, int& ib) {
 // sorts its 16 once (bitonic network, fixed register indices), then k rounds of a warp
 // tournament on the lanes' heads pick the winners in descending order; lane j keeps the
 // j-th winner and the k lanes compute the softmax over the kept logits in parallel.
-__device__ void warp_topk(const float* lg, int E, int k, int32_t* ids, float* wts) {
+__device__ void warp_topk(const float* lg, int E, int k, int32_t* ids, float* wts, int* ids_copy = nullptr) {
   const int lane = threadIdx.x & 31;
   float v[16];
   int id[16];
@@ -93,6 +93,7 @@ __device__ void warp_topk(const float* lg, int E, int k, int32_t* ids, float* wt
   if (lane < k) {
     ids[lane] = mine_id;
     wts[lane] = z / sum;
+    if (ids_copy) ids_copy[lane] = mine_id;
   }
 }
 
@@ -101,6 +102,12 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* logits, in
   const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
   warp_topk(logits + t * E, E, k, ids + t * k, wts + t * k);
+}
+
+// Clear a shared array with 16-byte stores (bytes a multiple of 16, 16-byte aligned).
+__device__ __forceinline__ void zero_shared(void* p, int bytes) {
+  uint4* q = static_cast<uint4*>(p);
+  for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x) q[i] = make_uint4(0, 0, 0, 0);
 }
 
 // Per-block histogram of the experts of pairs [b*kRouteBlock, ...).
@@ -215,12 +222,12 @@ __device__ void scan_groups(const RouteView& r, int E, int nblocks, int tile) {
 // Stable placement of the pairs of block b: rank among equal experts = earlier pairs of
 // the block with the same expert (warp match + per-warp counts), in pair order.
 __device__ void block_scatter(const int32_t* ids, int64_t P, int E, int b, const RouteView& r) {
-  __shared__ unsigned short wc[kRouteBlock / 32][kMaxExperts];  // pairs per (warp, expert)
+  __shared__ __align__(16) unsigned short wc[kRouteBlock / 32][kMaxExperts];  // pairs per (warp, expert)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t p = (int64_t)b * kRouteBlock + tid;
   const bool valid = tid < kRouteBlock && p < P;
   const int e = valid ? ids[p] : -1;
-  for (int i = tid; i < (kRouteBlock / 32) * E; i += blockDim.x) wc[i / E][i % E] = 0;
+  zero_shared(&wc[0][0], sizeof(wc));
   __syncthreads();
   const unsigned mask = __match_any_sync(0xFFFFFFFFu, e);
   const int rank_in_warp = __popc(mask & ((1u << lane) - 1u));
@@ -247,17 +254,58 @@ __global__ void __launch_bounds__(kRouteBlock) route_scatter_kernel(const int32_
   block_scatter(ids, P, E, blockIdx.x, r);
 }
 
-// Decode-sized routing (T*k <= kRouteBlock, T <= 32): every phase in one CTA.
+// Decode-sized routing (T*k <= kRouteBlock, T <= 32): every phase in one CTA, with the
+// histogram, the scan and the placement in shared memory; only the results go to device
+// memory.
 __global__ void __launch_bounds__(kRouteBlock) route_small_kernel(const float* logits, int T, int E, int k,
                                                                   int32_t* ids, float* wts, int tile, RouteView r) {
-  const int warp = threadIdx.x >> 5;
-  for (int t = warp; t < T; t += kRouteBlock / 32) warp_topk(logits + (int64_t)t * E, E, k, ids + t * k, wts + t * k);
-  __threadfence_block();
+  __shared__ int s_ids[kRouteBlock];
+  __shared__ int hist[kMaxExperts];
+  __shared__ int off[kMaxExperts];
+  __shared__ int3 totals;
+  __shared__ __align__(16) unsigned short wc[kRouteBlock / 32][kMaxExperts];  // pairs per (warp, expert)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < E; e += blockDim.x) hist[e] = 0;
+  zero_shared(&wc[0][0], sizeof(wc));
+  if (warp < T) warp_topk(logits + (int64_t)warp * E, E, k, ids + warp * k, wts + warp * k, s_ids + warp * k);
   __syncthreads();
-  const int64_t P = (int64_t)T * k;
-  block_count(ids, P, E, 0, r.block_counts);
-  scan_groups(r, E, 1, tile);
-  block_scatter(ids, P, E, 0, r);
+  // pairs p = t*k + j: histogram (order-free integer counts) and rank within the warp
+  const int P = T * k;
+  const bool valid = tid < P;
+  const int e = valid ? s_ids[tid] : -1;
+  if (valid) atomicAdd(&hist[e], 1);
+  const unsigned mask = __match_any_sync(0xFFFFFFFFu, e);
+  const int rank_in_warp = __popc(mask & ((1u << lane) - 1u));
+  if (valid && rank_in_warp == 0) wc[warp][e] = (unsigned short)__popc(mask);
+  __syncthreads();
+  // totals, exclusive offsets, active list and tile table (one thread per expert)
+  const int tot = tid < E ? hist[tid] : 0;
+  const int3 ex = block_scan3(make_int3(tot, (tot + tile - 1) / tile, tot > 0 ? 1 : 0), &totals);
+  if (tid < E) {
+    r.counts[tid] = tot;
+    r.offsets[tid] = ex.x;
+    off[tid] = ex.x;
+    if (tot > 0) r.active[ex.z] = tid;
+    for (int s = 0; s * tile < tot; ++s) {
+      r.tiles[3 * (ex.y + s)] = tid;
+      r.tiles[3 * (ex.y + s) + 1] = ex.x + s * tile;
+      r.tiles[3 * (ex.y + s) + 2] = min(tile, tot - s * tile);
+    }
+  }
+  if (tid == 0) {
+    r.offsets[E] = totals.x;
+    r.meta[0] = totals.z;
+    r.meta[1] = totals.y;
+  }
+  __syncthreads();
+  // stable placement: experts ascending, pairs ascending within an expert
+  if (valid) {
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += wc[w][e];
+    const int pos = off[e] + before + rank_in_warp;
+    r.pair_list[pos] = tid;
+    r.pair_pos[tid] = pos;
+  }
 }
 
 RouteView route_view(void* ws, int64_t T, int E, int k) {
