@@ -27,7 +27,7 @@
 
 namespace qg {
 
-constexpr int kGCW = 12;              // consumer warps (rows per group up to 4 -> 128 registers)
+constexpr int kGCW = 16;              // consumer warps (4 units per chunk, 96 registers a thread)
 constexpr int kGCT = kGCW * 32;
 constexpr int kGC = kGCW / 4;         // units per chunk
 constexpr int kGThreads = kGCT + 32;
