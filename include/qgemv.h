@@ -77,7 +77,7 @@ typedef enum {
   QG_ERR_MISALIGNED = 3,         /* pointer not 16-byte aligned or leading dimension not a multiple of 8 */
   QG_ERR_WORKSPACE_TOO_SMALL = 4,
   QG_ERR_CUDA = 5,               /* a CUDA runtime call or a launch failed */
-  QG_ERR_TIMEOUT = 6             /* a bounded device-side wait gave up (reported via qg_read_device_status) */
+  QG_ERR_TIMEOUT = 6             /* a bounded device-side wait gave up (reported via qg_workspace_status) */
 } qg_status;
 
 typedef enum { QG_OUT_F32 = 0, QG_OUT_BF16 = 1 } qg_out_dtype;
@@ -235,6 +235,13 @@ qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t t, int64_t 
 #define QG_STATIC_WORKSPACE_BYTES (4u << 20)
 qg_status qgemv_static_ws(const qg_weight* w, const void* x, int m_rows, int64_t ldx,
                           const void* residual, int64_t ldr, void* y, int64_t ldy, void* stream);
+
+/* Self-test of the shared failure path: launches one CTA whose mbarrier wait nothing will
+ * complete; after the library's wait limit (2 s) the kernel records QG_ERR_TIMEOUT in the
+ * workspace's status word and returns -- no fault, no hang, the context stays usable.
+ * Read the result with qg_workspace_status.  The pages have no counterpart; it exists to
+ * test failure detection.  workspace: device, 16-byte aligned, >= 4 bytes. */
+qg_status qg_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -63,6 +63,7 @@ _SIGNATURES = {
     "qmoe_route": (_I, [_P, _I64, _I, _I, _P, _P, _P, _SZ, _P]),
     "qmoe_workspace_size": (_SZ, [ctypes.POINTER(qg_moe_layer), _I64, _I]),
     "qmoe_ffn": (_I, [ctypes.POINTER(qg_moe_layer), _P, _I64, _I64, _I, _P, _P, _P, _I64, _P, _SZ, _P]),
+    "qg_selftest_wait_timeout": (_I, [_P, _SZ, _P]),
 }
 
 
@@ -167,6 +168,12 @@ def qgemv_static_ws(w: qg_weight, x_ptr: int, m: int, ldx: int, res_ptr: Optiona
     """qgemv without a workspace argument, for callers that cannot allocate device memory
     (its scratch is a fixed array inside the library, shared by all calls)."""
     _check(lib().qgemv_static_ws(ctypes.byref(w), x_ptr, m, ldx, res_ptr, ldr, y_ptr, ldy, stream), "qgemv_static_ws")
+
+
+def qg_selftest_wait_timeout(ws_ptr: int, ws_bytes: int, stream: int = 0):
+    """Launch the bounded-wait self-test (its wait runs out after the library's limit and
+    records QG_ERR_TIMEOUT in the workspace status word)."""
+    _check(lib().qg_selftest_wait_timeout(ws_ptr, ws_bytes, stream), "qg_selftest_wait_timeout")
 
 
 # ------------------------------------------------------------------ torch helpers

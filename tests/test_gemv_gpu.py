@@ -120,3 +120,24 @@ def test_gemv_full_size_sampled_rows(q, name, ms):
         x = wl.activations(m, k, seed=m)
         res = wl.activations(m, n, seed=m, stream="residual") if cfg["residual"] else None
         _check(q, w, x, res, m, pw=pw, rows=rows)
+
+
+# The three ways a GEMV is cut across the SMs (152 on GB300): one whole 128-row tile per CTA
+# (row tiles close to the SM count: 136 here), row tiles split over thread-block clusters
+# with the partials summed in the first CTA's shared memory (few row tiles: 20 here), and
+# stream-K with tickets (more row tiles than SMs: 160 here).  Every output is checked, twice
+# in a row on one workspace (bit-identical).
+PARTITIONS = [("whole_row_tiles", wl.NVFP4, 136 * 128, 256), ("cluster_split", wl.MXFP4, 20 * 128 - 37, 1024),
+              ("stream_k", wl.MLX_AFFINE4_G64, 160 * 128, 512), ("stream_k_q6k", wl.Q6K, 170 * 128 - 5, 512)]
+
+
+@pytest.mark.parametrize("name,fmt,n,k", PARTITIONS)
+@pytest.mark.parametrize("m", [1, 4])
+def test_gemv_partition_modes(q, name, fmt, n, k, m):
+    w, x, res = wl.gemv_case(fmt, n, k, m, seed=900 + m, residual=(m == 4))
+    pw = q.PackedWeight.from_logical(w)
+    ws = q.Workspace(q.qg_gemv_workspace_size(fmt, n, k, m))
+    got, _ = _check(q, w, x, res, m, pw=pw, ws=ws)
+    got2, _ = _check(q, w, x, res, m, pw=pw, ws=ws)
+    assert np.array_equal(got, got2)
+    assert ws.status() == 0
