@@ -20,8 +20,8 @@
 //   warp 1       allocates all 512 TMEM columns; one lane issues the tcgen05.mma
 //   warps 2-9    decode each stage's two tiles into the bf16 A operand in tensor memory
 //                (tcgen05.st), so decoded weights cost no shared-memory bandwidth
-//   warps 10-17  epilogue: TMEM -> registers -> outputs
-//   warps 18-21  token rows: one TMA load per stage when the rows are contiguous, else a
+//   warps 10-21  epilogue: TMEM -> registers -> outputs
+//   warps 22-25  token rows: one TMA load per stage when the rows are contiguous, else a
 //                cp.async gather by row index into the 128-byte swizzled ring; each
 //                thread's copies arrive on the stage's mbarrier when they land, and the MMA
 //                thread fences these generic-proxy writes before the tensor cores read them
@@ -47,13 +47,13 @@
 namespace qg {
 
 constexpr int kTcDecWarps = 8;  // two per TMEM lane quarter, one per half of a stage's 64 inputs
-constexpr int kTcEpiWarps = 8;  // two per TMEM lane quarter, alternate 16-column chunks
+constexpr int kTcEpiWarps = 12;  // three per TMEM lane quarter, every third 16-column chunk
 constexpr int kTcGatWarps = 4;
 constexpr int kTcGatThreads = kTcGatWarps * 32;
-constexpr int kTcWarps = 2 + kTcDecWarps + kTcEpiWarps + kTcGatWarps;  // 22
-constexpr int kTcThreads = kTcWarps * 32;                               // 704
+constexpr int kTcWarps = 2 + kTcDecWarps + kTcEpiWarps + kTcGatWarps;  // 26
+constexpr int kTcThreads = kTcWarps * 32;                               // 832
 constexpr int kTcEpiWarp0 = 2 + kTcDecWarps;                            // 10
-constexpr int kTcGatWarp0 = kTcEpiWarp0 + kTcEpiWarps;                  // 18
+constexpr int kTcGatWarp0 = kTcEpiWarp0 + kTcEpiWarps;                  // 22
 constexpr int kTcTile = kRouteTile;  // tokens per tile = largest MMA N (192)
 constexpr int kTcSmemCap = 232448;   // opt-in shared memory per block on sm_100-family GPUs
 
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
     }
   } else if (warp < kTcGatWarp0) {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3, half = (warp - kTcEpiWarp0) >> 2;
+    const int quarter = warp & 3, third = (warp - kTcEpiWarp0) >> 2;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     uint32_t itc = 0;
     for (int i = b; i < n_items; i += G, ++itc) {
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
       if (!mbar_wait_bounded(t_full, itc & 1u, a.status)) break;
       tc_fence_after();
       const int r = quarter * 32 + lane;
-      for (int c = 16 * half; c < N; c += 32) {
+      for (int c = 16 * third; c < N; c += 48) {
         uint32_t v[16], u[16];
         tmem_ld16(tmem + lane_base + (uint32_t)c, v);
         tmem_ld16(tmem + lane_base + kTcTile + (uint32_t)c, u);
