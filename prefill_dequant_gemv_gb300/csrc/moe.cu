@@ -6,13 +6,15 @@
 //   gate/up  grouped GEMV: every active expert's 2F x H weights are read from HBM once
 //            for all the tokens that chose it (§4.2: "two tokens that chose the same
 //            expert share one decode of its weights"), fp32 results per (token, expert)
-//   mid      h = bf16( silu(gate) * up ) in fp32 (§4.1 "Mid": SwiGLU in 32-bit)
-//   down     grouped GEMV on h, fp32 results per (token, expert)
+//   down     grouped GEMV on h = bf16( silu(gate) * up ) (§4.1 "Mid": SwiGLU in 32-bit),
+//            which each CTA computes from the fp32 gate/up rows while staging its inputs
+//            (only the rows of the experts it works on), so the mid step needs no launch of
+//            its own; fp32 results per (token, expert)
 //   finish   out[t] = bf16( sum_j p[t, j] * down_{e_j}[t] + shared[t] ) (§4.1 "Finish")
 //
 // The grouped GEMV is the dense GEMV's stream-K pipeline (qg_gemv_core.cuh) over a unit
 // space of (group, 128-row tile, 64-input group) with groups = active experts (ascending)
-// then the shared expert; each group is padded to whole chunks so a chunk never spans two
+// then the shared expert once per token; each group is padded to whole chunks so a chunk never spans two
 // experts' weights.
 #include <cuda_runtime.h>
 
@@ -45,16 +47,17 @@ struct GroupedArgs {
   int64_t n, k;
   int NT, KG;
   int T, topk;
-  int mode;  // 0: input rows are tokens; 1: input rows are grouped pairs, shared rows after
+  int mode;  // 0: input rows are tokens (x); 1: input rows are grouped pairs, shared rows
+             // after, computed as SwiGLU of the fp32 gate/up rows gu
   const __nv_bfloat16* x;
   int64_t ldx;
-  int nrows;  // staged input rows
+  const float* gu;
+  int64_t ldg;
+  int nrows;  // input rows (staging slots)
   float* out;
   int64_t ldo;
   const int* meta;
-  const int* offsets;
-  const int* active;
-  const int* pair_list;
+  const int* groups;  // router's group table (kGroupInts ints per active expert)
   int has_shared;
   int stages;
   float* ws_part;
@@ -105,34 +108,44 @@ __host__ __device__ inline GroupedSmem grouped_smem(int stage_bytes, int S, int 
 
 __device__ __forceinline__ GroupInfo group_info(const GroupedArgs& a, int g, int n_active) {
   GroupInfo gi;
-  if (g < n_active) {
-    const int e = a.active[g];
-    const int first = a.offsets[e];
+  if (g < n_active) {  // one 32-byte entry of the router's group table
+    const int4* ge = reinterpret_cast<const int4*>(a.groups + (size_t)g * kGroupInts);
+    const int4 h = ge[0], rows = ge[1];
+    const int e = h.x, first = h.y;
     gi.codes = a.codes + (int64_t)e * a.cstride;
     gi.scales = a.scales + (int64_t)e * a.sstride;
     gi.aux = a.aux ? a.aux + (int64_t)e * a.astride : nullptr;
     gi.ts = a.ts;
-    gi.m = min(kGMaxRows, a.offsets[e + 1] - first);
+    gi.m = min(kGMaxRows, h.z);
+    const int tok[kGroupRows] = {rows.x, rows.y, rows.z, rows.w};
 #pragma unroll
     for (int i = 0; i < kGMaxRows; ++i) {
-      const int pos = first + min(i, gi.m - 1);
-      gi.out_row[i] = pos;
-      gi.in_row[i] = a.mode == 0 ? a.pair_list[pos] / a.topk : pos;
+      const int j = min(i, gi.m - 1);
+      gi.out_row[i] = first + j;
+      gi.in_row[i] = a.mode == 0 ? tok[j] : first + j;
     }
-  } else {  // shared expert: every token
+  } else {  // shared expert, token t = g - n_active
+    const int t = g - n_active;
     gi.codes = a.sh_codes;
     gi.scales = a.sh_scales;
     gi.aux = a.sh_aux;
     gi.ts = a.sh_ts;
-    gi.m = a.T;
+    gi.m = 1;
 #pragma unroll
     for (int i = 0; i < kGMaxRows; ++i) {
-      const int t = min(i, a.T - 1);
       gi.out_row[i] = a.T * a.topk + t;
       gi.in_row[i] = a.mode == 0 ? t : a.T * a.topk + t;
     }
   }
   return gi;
+}
+
+// Two SwiGLU outputs bf16( silu(g) * u ), silu(g) = g / (1 + e^-g) in IEEE fp32 (§4.1
+// "Mid"), packed as a bf16 pair (first in the low half).
+__device__ __forceinline__ uint32_t swiglu_bf16x2(float g0, float u0, float g1, float u1) {
+  const float h0 = g0 / (1.0f + expf(-g0)) * u0, h1 = g1 / (1.0f + expf(-g1)) * u1;
+  const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+  return *reinterpret_cast<const uint32_t*>(&b);
 }
 
 template <int FMT>
@@ -165,7 +178,10 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   pdl_wait();
 
   const int n_active = a.meta[0];
-  const int n_groups = n_active + (a.has_shared ? 1 : 0);
+  // The shared expert runs as one single-row group per token: its weights are read once per
+  // token (the repeats hit L2) but every chunk then costs the same, so the equal split of
+  // chunks over CTAs stays balanced (a 4-row chunk costs ~2.4 one-row chunks).
+  const int n_groups = n_active + (a.has_shared ? a.T : 0);
   const int upg_real = NT * KG;
   const int cpg = (upg_real + kGC - 1) / kGC;  // chunks per group
   const int upg = cpg * kGC;                   // padded units per group
@@ -193,7 +209,7 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
         if (g != gcur) {
           gcur = g;
           if (g < n_active) {
-            const int e = a.active[g];
+            const int e = a.groups[(size_t)g * kGroupInts];
             bc = a.codes + (int64_t)e * a.cstride;
             bs = a.scales + (int64_t)e * a.sstride;
             ba = a.aux ? a.aux + (int64_t)e * a.astride : nullptr;
@@ -231,23 +247,44 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
     lut[2 * tid] = v.x;
     lut[2 * tid + 1] = v.y;
   }
-  // The groups this CTA touches: their descriptors (a chain of dependent loads each) are
-  // read once here, in parallel with the staging, instead of at every segment.
+  // The groups this CTA touches: their descriptors are read once here instead of at every
+  // segment.
   const int g_first = (int)(uu0 / (uint32_t)upg);
+  const int g_span = (int)((uu1 - 1) / (uint32_t)upg) - g_first + 1;
   if (tid < kGInfoCache && g_first + tid < n_groups) ginfo[tid] = group_info(a, g_first + tid, n_active);
-  // stage every input row over all of K
-  for (int it = tid; it < a.nrows * KG * 4; it += kGCT) {
-    const int kq = it & 3, sl = (it >> 2) % KG, row = (it >> 2) / KG;
+  // Stage the input rows over all of K.  Mode 0: every token row of x.  Mode 1: the rows of
+  // the groups this CTA touches (all rows if it touches more than kGInfoCache groups), each
+  // computed as h = bf16( silu(g) * u ) from the fp32 gate/up outputs.
+  const bool by_group = a.mode == 1 && g_span <= kGInfoCache;
+  if (a.mode == 1) named_sync(1, kGCT);  // the row lists come from the descriptors
+  const int nslot = by_group ? g_span * kGMaxRows : a.nrows;
+  for (int it = tid; it < nslot * KG * 4; it += kGCT) {
+    const int kq = it & 3, sl = (it >> 2) % KG, slot = (it >> 2) / KG;
+    int row = slot;
+    if (by_group) {
+      const GroupInfo& gs = ginfo[slot / kGMaxRows];
+      if (slot % kGMaxRows >= gs.m) continue;
+      row = gs.in_row[slot % kGMaxRows];
+    }
     const int64_t k0 = (int64_t)sl * 64 + kq * 16;
     uint32_t u[8];
-    if (k0 < a.k) {
+    if (k0 >= a.k) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) u[i] = 0;
+    } else if (a.mode == 0) {
       const uint4* src = reinterpret_cast<const uint4*>(a.x + (int64_t)row * a.ldx + k0);
       const uint4 r0 = src[0], r1 = src[1];
       u[0] = r0.x; u[1] = r0.y; u[2] = r0.z; u[3] = r0.w;
       u[4] = r1.x; u[5] = r1.y; u[6] = r1.z; u[7] = r1.w;
     } else {
+      const float4* gp = reinterpret_cast<const float4*>(a.gu + (int64_t)row * a.ldg + k0);
+      const float4* up = reinterpret_cast<const float4*>(a.gu + (int64_t)row * a.ldg + a.k + k0);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) u[i] = 0;
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 g4 = __ldcg(gp + q4), u4 = __ldcg(up + q4);
+        u[2 * q4] = swiglu_bf16x2(g4.x, u4.x, g4.y, u4.y);
+        u[2 * q4 + 1] = swiglu_bf16x2(g4.z, u4.z, g4.w, u4.w);
+      }
     }
     const float4 z = stage_quarter<FMT>(u, xs + (size_t)(row * KG + sl) * 32 + kq * 8);
     reinterpret_cast<float4*>(sums)[(size_t)(row * KG + sl) * 4 + kq] = z;
@@ -383,55 +420,56 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   }
 }
 
-// h[r][f] = bf16( silu(gu[r][f]) * gu[r][F + f] ) for the rows that exist this call.
-__global__ void __launch_bounds__(256) mid_kernel(const float* gu, int64_t ldg, __nv_bfloat16* h, int64_t ldh, int F,
-                                                  int T, int topk, int has_shared) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const int rows = T * topk + (has_shared ? T : 0);
-  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (int64_t)rows * F) return;
-  const int r = (int)(idx / F), f = (int)(idx % F);
-  const float g = gu[r * ldg + f], up = gu[r * ldg + F + f];
-  const float silu = g / (1.0f + expf(-g));
-  h[r * ldh + f] = __float2bfloat16_rn(silu * up);
-}
-
-// out[t][n] = bf16( sum_j w[t][j] * d[pos(t, j)][n] + d[T*topk + t][n] ), fixed order.
+// out[t][n] = bf16( sum_j w[t][j] * d[pos(t, j)][n] + d[T*topk + t][n] ), fixed order, four
+// features per thread; every load of a thread is issued before the first multiply-add.
 __global__ void __launch_bounds__(256) finish_kernel(const float* d, int64_t ldd, const float* w, const int* pair_pos,
                                                      int T, int topk, int has_shared, int64_t H, __nv_bfloat16* out,
                                                      int64_t ldo) {
   pdl_launch_dependents();
   pdl_wait();
+  const int64_t H4 = H / 4;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (int64_t)T * H) return;
-  const int t = (int)(idx / H);
-  const int64_t n = idx % H;
-  float acc = 0.0f;
-  for (int j = 0; j < topk; ++j) acc = fmaf(w[t * topk + j], d[(int64_t)pair_pos[t * topk + j] * ldd + n], acc);
-  if (has_shared) acc += d[(int64_t)(T * topk + t) * ldd + n];
-  out[t * ldo + n] = __float2bfloat16_rn(acc);
+  if (idx >= (int64_t)T * H4) return;
+  const int t = (int)(idx / H4);
+  const int64_t n = (idx % H4) * 4;
+  int pos[kMaxTopk];
+  float p[kMaxTopk];
+#pragma unroll
+  for (int j = 0; j < kMaxTopk; ++j) {
+    pos[j] = j < topk ? pair_pos[t * topk + j] : 0;
+    p[j] = j < topk ? w[t * topk + j] : 0.0f;
+  }
+  float4 v[kMaxTopk];
+#pragma unroll
+  for (int j = 0; j < kMaxTopk; ++j)
+    v[j] = j < topk ? __ldcg(reinterpret_cast<const float4*>(d + (int64_t)pos[j] * ldd + n)) : make_float4(0, 0, 0, 0);
+  const float4 sh = has_shared ? __ldcg(reinterpret_cast<const float4*>(d + (int64_t)(T * topk + t) * ldd + n))
+                               : make_float4(0, 0, 0, 0);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < kMaxTopk; ++j) {
+    if (j < topk) {
+      acc.x = fmaf(p[j], v[j].x, acc.x);
+      acc.y = fmaf(p[j], v[j].y, acc.y);
+      acc.z = fmaf(p[j], v[j].z, acc.z);
+      acc.w = fmaf(p[j], v[j].w, acc.w);
+    }
+  }
+  if (has_shared) {
+    acc.x += sh.x;
+    acc.y += sh.y;
+    acc.z += sh.z;
+    acc.w += sh.w;
+  }
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 pk;
+  pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(out + (int64_t)t * ldo + n) = pk;
 }
 
 // ---------------------------------------------------------------- host side
 namespace {
-// Launch with programmatic stream serialization: the kernel may begin while the preceding
-// kernel of the stream finishes; it waits (griddepcontrol.wait) before reading its outputs.
-template <typename... Args>
-cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
 int grouped_stage_bytes(int fmt) {
   switch (fmt) {
     case FMT_MLX: return Stage<FMT_MLX>::bytes(kGC);
@@ -455,12 +493,12 @@ MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, i
   // needs neither the split-K tickets and partials nor the fp32 gate/up rows
   const bool decode = T <= kGMaxRows;
   const int64_t nt_max = std::max(gu.nt, dn.nt);
-  L.cnt = take(decode ? (size_t)(E + 1) * nt_max * 4 : 0);
+  L.cnt = take(decode ? (size_t)(E + kGMaxRows) * nt_max * 4 : 0);  // tickets per (group, row tile)
   L.part = take(decode ? (size_t)grid * 2 * kGMaxRows * 128 * 4 : 0);
   L.ld_gu = (gu.n + 7) / 8 * 8;
   L.gu = take(decode ? (size_t)R * L.ld_gu * 4 : 0);
   L.ld_h = (dn.k + 7) / 8 * 8;
-  L.h = take((size_t)R * L.ld_h * 2);
+  L.h = take(decode ? 0 : (size_t)R * L.ld_h * 2);  // decode: h never leaves the down GEMV
   L.ld_d = (dn.n + 7) / 8 * 8;
   L.d = take((size_t)R * L.ld_d * 4);
   L.total = o;
@@ -538,23 +576,14 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
   a.out = reinterpret_cast<float*>(w + L.gu);
   a.ldo = L.ld_gu;
   a.meta = rv.meta;
-  a.offsets = rv.offsets;
-  a.active = rv.active;
-  a.pair_list = rv.pair_list;
+  a.groups = rv.groups;
   a.ws_part = reinterpret_cast<float*>(w + L.part);
   a.ws_cnt = reinterpret_cast<int*>(w + L.cnt);
   a.status = reinterpret_cast<int*>(w);
   int st = launch_grouped(m->fmt, a, (int)T, (int)gu.kg, dev, s);
   if (st != QG_OK) return st;
 
-  const int F = (int)dn.k;
   const int rows = (int)(T * topk + (m->has_shared ? T : 0));
-  __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(w + L.h);
-  if (launch_pdl(mid_kernel, dim3((unsigned)(((int64_t)rows * F + 255) / 256)), dim3(256), 0, s,
-                 (const float*)reinterpret_cast<const float*>(w + L.gu), (int64_t)L.ld_gu, h, (int64_t)L.ld_h, F,
-                 (int)T, topk, (int)m->has_shared) != cudaSuccess)
-    return QG_ERR_CUDA;
-
   qg_packed_sizes(m->fmt, dn.n, dn.k, &cb, &sb, &ab);
   GroupedArgs d = a;
   d.codes = static_cast<const uint8_t*>(m->dn_codes);
@@ -572,14 +601,15 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
   d.NT = (int)dn.nt;
   d.KG = (int)dn.kg;
   d.mode = 1;
-  d.x = h;
-  d.ldx = L.ld_h;
+  d.x = nullptr;
+  d.gu = reinterpret_cast<const float*>(w + L.gu);
+  d.ldg = L.ld_gu;
   d.out = reinterpret_cast<float*>(w + L.d);
   d.ldo = L.ld_d;
   st = launch_grouped(m->fmt, d, rows, (int)dn.kg, dev, s);
   if (st != QG_OK) return st;
 
-  if (launch_pdl(finish_kernel, dim3((unsigned)((T * dn.n + 255) / 256)), dim3(256), 0, s,
+  if (launch_pdl(finish_kernel, dim3((unsigned)((T * (dn.n / 4) + 255) / 256)), dim3(256), 0, s,
                  (const float*)reinterpret_cast<const float*>(w + L.d), (int64_t)L.ld_d, topk_w,
                  (const int*)rv.pair_pos, (int)T, topk, (int)m->has_shared, (int64_t)dn.n,
                  static_cast<__nv_bfloat16*>(out), ldo) != cudaSuccess)

@@ -10,8 +10,13 @@ constexpr int kMaxExperts = 512;
 constexpr int kMaxTopk = 16;
 constexpr int kRouteTile = 192;  // pairs per grouped-prefill tile (the tensor-core N)
 
+// Group table entry (8 ints) of active expert z (ascending experts): expert, first grouped
+// position, pair count, 0, then the tokens of its first kGroupRows pairs.
+constexpr int kGroupRows = 4;
+constexpr int kGroupInts = 8;
+
 struct RouteLayout {
-  size_t meta, counts, offsets, active, pair_list, pair_pos, tiles, block_counts, block_start, total;
+  size_t meta, counts, offsets, active, pair_list, pair_pos, tiles, groups, zidx, block_counts, block_start, total;
   int64_t max_tiles, nblocks;
 };
 
@@ -33,6 +38,8 @@ __host__ __device__ inline RouteLayout route_layout(int64_t T, int E, int k) {
   L.pair_list = take((size_t)P * 4);      // grouped position -> pair t*k + j
   L.pair_pos = take((size_t)P * 4);       // pair -> grouped position
   L.tiles = take((size_t)L.max_tiles * 12);  // (expert, first position, count)
+  L.groups = take((size_t)E * kGroupInts * 4);  // group table, one entry per active expert
+  L.zidx = take((size_t)E * 4);                 // expert -> its index in the active list
   L.block_counts = take((size_t)L.nblocks * E * 4);
   L.block_start = take((size_t)L.nblocks * E * 4);
   L.total = o;
@@ -47,6 +54,8 @@ struct RouteView {
   int* pair_list;
   int* pair_pos;
   int* tiles;
+  int* groups;
+  int* zidx;
   int* block_counts;
   int* block_start;
 };

@@ -4,6 +4,7 @@
 // forever, so a broken pipeline ends the kernel with an error the host can read.
 #pragma once
 
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace qg {
@@ -85,6 +86,23 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // completed and its memory is visible.  Both are no-ops without such a dependency.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch with programmatic stream serialization: the kernel may begin while the preceding
+// kernel of the stream finishes; it waits (griddepcontrol.wait) before reading its outputs.
+template <typename... Args, typename... Pass>
+cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Pass... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args>(args)...);
+}
 
 // Ticket: atomic add with release (this CTA's writes, ordered before it by a CTA barrier)
 // and acquire (the other CTAs' writes released by their tickets) semantics at GPU scope.

@@ -13,80 +13,83 @@
 
 #include "qg_internal.h"
 #include "qg_route.h"
+#include "qg_sync.cuh"
 
 namespace qg {
 
 constexpr int kRouteBlock = 1024;  // pairs per grouping block (one thread per pair)
 
-// Compare-exchange for a descending order by value, ties to the lower expert index.
-__device__ __forceinline__ void cx(float& va, int& ia, float& vb, int& ib) {
-  const bool swap = vb > va || (vb == va && ib < ia);
-  const float tv = swap ? vb : va, tw = swap ? va : vb;
-  const int ti = swap ? ib : ia, tj = swap ? ia : ib;
-  va = tv;
-  vb = tw;
-  ia = ti;
-  ib = tj;
+// Order-preserving 32-bit key of an fp32 logit: larger logit, larger key; -0 ties with +0
+// and NaN sorts below every number (a stable descending sort of the values puts NaN last)
+// but above key 0, which marks padding and experts already taken.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 1u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
 }
 
-// Warp-level top-k of one token's logits (E <= 512): lane l holds logits l, l+32, ...,
-// sorts its 16 once (bitonic network, fixed register indices), then k rounds of a warp
-// tournament on the lanes' heads pick the winners in descending order; lane j keeps the
-// j-th winner and the k lanes compute the softmax over the kept logits in parallel.
+// Largest key of a lane's 16 (ties to the lower slot, i.e. the lower expert index): a
+// 4-level tree over fixed register indices.
+__device__ __forceinline__ void lane_best(const uint32_t (&key)[16], uint32_t& bk, int& bi) {
+  uint32_t k8[8];
+  int i8[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool hi = key[2 * i + 1] > key[2 * i];
+    k8[i] = hi ? key[2 * i + 1] : key[2 * i];
+    i8[i] = hi ? 2 * i + 1 : 2 * i;
+  }
+#pragma unroll
+  for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const bool hi = k8[i + w] > k8[i] || (k8[i + w] == k8[i] && i8[i + w] < i8[i]);
+      k8[i] = hi ? k8[i + w] : k8[i];
+      i8[i] = hi ? i8[i + w] : i8[i];
+    }
+  bk = k8[0];
+  bi = i8[0];
+}
+
+// Warp-level top-k of one token's logits (E <= 512): lane l holds the keys of logits l,
+// l+32, ... (16 registers; the expert of slot i is l + 32 i).  Each of k rounds takes the
+// warp maximum of the lanes' best keys and the warp minimum of the experts holding it (two
+// single-instruction warp reductions); the winner's lane clears that slot and finds its
+// next best.  Lane j keeps the j-th winner and the k lanes compute the softmax over the kept
+// logits in parallel.
 __device__ void warp_topk(const float* lg, int E, int k, int32_t* ids, float* wts, int* ids_copy = nullptr) {
   const int lane = threadIdx.x & 31;
-  float v[16];
-  int id[16];
+  uint32_t key[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int e = lane + 32 * i;
-    v[i] = e < E ? lg[e] : -INFINITY;
-    id[i] = e < E ? e : 0x7FFFFFFF;
+    key[i] = e < E ? order_key(lg[e]) : 0u;
   }
-  // bitonic sort of 16 (descending)
-#pragma unroll
-  for (int size = 2; size <= 16; size <<= 1)
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1)
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          if ((i & size) == 0) cx(v[i], id[i], v[j], id[j]);
-          else cx(v[j], id[j], v[i], id[i]);
-        }
-      }
-  float mine = 0.0f, top = 0.0f;
+  uint32_t bk;
+  int bi;
+  lane_best(key, bk, bi);
+  uint32_t mine = 0u, top = 0u;
   int mine_id = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = v[0];
-    int bi = id[0];
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (j == 0) top = bv;
+    const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, bk);
+    const int win = (int)__reduce_min_sync(0xFFFFFFFFu, bk == kmax ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
+    if (j == 0) top = kmax;
     if (lane == j) {
-      mine = bv;
-      mine_id = bi;
+      mine = kmax;
+      mine_id = win;
     }
-    if ((bi & 31) == lane && bi == id[0]) {  // the winner's lane advances its head
+    if ((win & 31) == lane) {  // the winner's lane takes the slot out and finds its next best
 #pragma unroll
-      for (int i = 0; i < 15; ++i) {
-        v[i] = v[i + 1];
-        id[i] = id[i + 1];
-      }
-      v[15] = -INFINITY;
-      id[15] = 0x7FFFFFFF;
+      for (int i = 0; i < 16; ++i) key[i] = (i == (win >> 5)) ? 0u : key[i];
+      lane_best(key, bk, bi);
     }
   }
   // softmax over the k kept logits (descending order), shifted by the largest
-  const float z = lane < k ? expf(mine - top) : 0.0f;
+  const float z = lane < k ? expf(key_value(mine) - key_value(top)) : 0.0f;
   float sum = z;
 #pragma unroll
   for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
@@ -187,7 +190,12 @@ __device__ void scan_groups(const RouteView& r, int E, int nblocks, int tile) {
   if (e < E) {
     r.counts[e] = tot;
     r.offsets[e] = ex.x;
-    if (tot > 0) r.active[ex.z] = e;
+    if (tot > 0) {
+      r.active[ex.z] = e;
+      r.zidx[e] = ex.z;
+      int4* g = reinterpret_cast<int4*>(r.groups + (size_t)ex.z * kGroupInts);
+      g[0] = make_int4(e, ex.x, tot, 0);
+    }
     for (int s = 0; s < x.y; ++s) {
       r.tiles[3 * (ex.y + s)] = e;
       r.tiles[3 * (ex.y + s) + 1] = ex.x + s * tile;
@@ -221,7 +229,7 @@ __device__ void scan_groups(const RouteView& r, int E, int nblocks, int tile) {
 
 // Stable placement of the pairs of block b: rank among equal experts = earlier pairs of
 // the block with the same expert (warp match + per-warp counts), in pair order.
-__device__ void block_scatter(const int32_t* ids, int64_t P, int E, int b, const RouteView& r) {
+__device__ void block_scatter(const int32_t* ids, int64_t P, int E, int k, int b, const RouteView& r) {
   __shared__ __align__(16) unsigned short wc[kRouteBlock / 32][kMaxExperts];  // pairs per (warp, expert)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t p = (int64_t)b * kRouteBlock + tid;
@@ -239,6 +247,8 @@ __device__ void block_scatter(const int32_t* ids, int64_t P, int E, int b, const
     const int pos = r.block_start[(size_t)b * E + e] + before + rank_in_warp;
     r.pair_list[pos] = (int)p;
     r.pair_pos[p] = pos;
+    const int rank = pos - r.offsets[e];
+    if (rank < kGroupRows) r.groups[(size_t)r.zidx[e] * kGroupInts + 4 + rank] = (int)(p / k);
   }
   __syncthreads();
 }
@@ -249,9 +259,9 @@ __global__ void __launch_bounds__(kRouteBlock) route_count_kernel(const int32_t*
 __global__ void __launch_bounds__(kRouteBlock) route_scan_kernel(int E, int nblocks, int tile, RouteView r) {
   scan_groups(r, E, nblocks, tile);
 }
-__global__ void __launch_bounds__(kRouteBlock) route_scatter_kernel(const int32_t* ids, int64_t P, int E,
+__global__ void __launch_bounds__(kRouteBlock) route_scatter_kernel(const int32_t* ids, int64_t P, int E, int k,
                                                                     RouteView r) {
-  block_scatter(ids, P, E, blockIdx.x, r);
+  block_scatter(ids, P, E, k, blockIdx.x, r);
 }
 
 // Decode-sized routing (T*k <= kRouteBlock, T <= 32): every phase in one CTA, with the
@@ -262,11 +272,16 @@ __global__ void __launch_bounds__(kRouteBlock) route_small_kernel(const float* l
   __shared__ int s_ids[kRouteBlock];
   __shared__ int hist[kMaxExperts];
   __shared__ int off[kMaxExperts];
+  __shared__ int zid[kMaxExperts];
   __shared__ int3 totals;
   __shared__ __align__(16) unsigned short wc[kRouteBlock / 32][kMaxExperts];  // pairs per (warp, expert)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The consumers of the routing wait for this grid to complete before reading it; the
+  // logits may come from the preceding kernel.
+  if (tid == 0) pdl_launch_dependents();
   for (int e = tid; e < E; e += blockDim.x) hist[e] = 0;
   zero_shared(&wc[0][0], sizeof(wc));
+  pdl_wait();
   if (warp < T) warp_topk(logits + (int64_t)warp * E, E, k, ids + warp * k, wts + warp * k, s_ids + warp * k);
   __syncthreads();
   // pairs p = t*k + j: histogram (order-free integer counts) and rank within the warp
@@ -285,7 +300,12 @@ __global__ void __launch_bounds__(kRouteBlock) route_small_kernel(const float* l
     r.counts[tid] = tot;
     r.offsets[tid] = ex.x;
     off[tid] = ex.x;
-    if (tot > 0) r.active[ex.z] = tid;
+    zid[tid] = ex.z;
+    if (tot > 0) {
+      r.active[ex.z] = tid;
+      r.zidx[tid] = ex.z;
+      reinterpret_cast<int4*>(r.groups + (size_t)ex.z * kGroupInts)[0] = make_int4(tid, ex.x, tot, 0);
+    }
     for (int s = 0; s * tile < tot; ++s) {
       r.tiles[3 * (ex.y + s)] = tid;
       r.tiles[3 * (ex.y + s) + 1] = ex.x + s * tile;
@@ -305,6 +325,8 @@ __global__ void __launch_bounds__(kRouteBlock) route_small_kernel(const float* l
     const int pos = off[e] + before + rank_in_warp;
     r.pair_list[pos] = tid;
     r.pair_pos[tid] = pos;
+    const int rank = before + rank_in_warp;
+    if (rank < kGroupRows) r.groups[(size_t)zid[e] * kGroupInts + 4 + rank] = tid / k;
   }
 }
 
@@ -319,6 +341,8 @@ RouteView route_view(void* ws, int64_t T, int E, int k) {
   v.pair_list = reinterpret_cast<int*>(b + L.pair_list);
   v.pair_pos = reinterpret_cast<int*>(b + L.pair_pos);
   v.tiles = reinterpret_cast<int*>(b + L.tiles);
+  v.groups = reinterpret_cast<int*>(b + L.groups);
+  v.zidx = reinterpret_cast<int*>(b + L.zidx);
   v.block_counts = reinterpret_cast<int*>(b + L.block_counts);
   v.block_start = reinterpret_cast<int*>(b + L.block_start);
   return v;
@@ -329,13 +353,15 @@ int launch_route(const float* logits, int64_t T, int E, int k, int32_t* ids, flo
   RouteView r = route_view(ws, T, E, k);
   const int64_t P = T * k;
   if (P <= kRouteBlock && T <= 32) {
-    route_small_kernel<<<1, kRouteBlock, 0, s>>>(logits, (int)T, E, k, ids, wts, kRouteTile, r);
+    if (launch_pdl(route_small_kernel, dim3(1), dim3(kRouteBlock), 0, s, logits, (int)T, E, k, ids, wts,
+                   (int)kRouteTile, r) != cudaSuccess)
+      return QG_ERR_CUDA;
   } else {
     const int64_t nb = (P + kRouteBlock - 1) / kRouteBlock;
     route_topk_kernel<<<(unsigned)((T + 7) / 8), 256, 0, s>>>(logits, T, E, k, ids, wts);
     route_count_kernel<<<(unsigned)nb, kRouteBlock, 0, s>>>(ids, P, E, r);
     route_scan_kernel<<<1, kRouteBlock, 0, s>>>(E, (int)nb, kRouteTile, r);
-    route_scatter_kernel<<<(unsigned)nb, kRouteBlock, 0, s>>>(ids, P, E, r);
+    route_scatter_kernel<<<(unsigned)nb, kRouteBlock, 0, s>>>(ids, P, E, k, r);
   }
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }

@@ -45,11 +45,18 @@ def test_route_ties_go_to_lower_index(q):
     lg[:, 10] = 1.0
     lg[:, 20] = 1.0
     lg[2, :] = 0.5
+    # -0 ties with +0 (lower index first); NaN sorts below every number
+    lg[3, :] = -1.0
+    lg[3, 7] = -0.0
+    lg[3, 2] = 0.0
+    lg[3, 9] = np.nan
     lt = torch.from_numpy(lg).cuda()
     ids, w, _ = q.route(lt, 3)
     torch.cuda.synchronize()
     rid, rp = oracle.route(lg, 3)
     assert np.array_equal(ids.cpu().numpy(), rid)
+    assert list(rid[3]) == [2, 7, 0]
+    assert np.allclose(w.cpu().numpy(), rp, rtol=2e-6, atol=1e-7)
 
 
 @pytest.mark.parametrize("fmt", [wl.MXFP4, wl.NVFP4, wl.MLX_AFFINE4_G64, wl.Q6K])
