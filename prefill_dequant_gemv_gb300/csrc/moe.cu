@@ -29,7 +29,7 @@
 
 namespace qg {
 
-constexpr int kGCW = 16;              // consumer warps (4 units per chunk, 96 registers a thread)
+constexpr int kGCW = 12;              // consumer warps (3 units per chunk, 128 registers a thread: no spills)
 constexpr int kGCT = kGCW * 32;
 constexpr int kGC = kGCW / 4;         // units per chunk
 constexpr int kGThreads = kGCT + 32;
