@@ -207,9 +207,10 @@ size_t qmoe_workspace_size(const qg_moe_layer* layer, int64_t t, int topk);
  *   out[t] = bf16( sum_j topk_w[t][j] * down_e(h) + shared(h) ),
  *   h = bf16(silu(gate) * up) per (token, expert), gate = rows 0..F-1 and up = rows
  *   F..2F-1 of the expert's 2F x H gate/up weight.
- * 1..4 tokens (decode / speculative verify; TurboEXL3 article §4.2): five launches --
+ * 1..4 tokens (decode / speculative verify; TurboEXL3 article §4.2): three launches --
  *   gate/up as one grouped GEMV over the active experts that reads each expert's weights
- *   once for all its tokens, with the shared expert as extra groups; mid; down; finish.
+ *   once for all its tokens, with the shared expert as extra groups; down, whose blocks
+ *   compute the mid (h = bf16(silu(gate) * up)) while staging their inputs; finish.
  * More tokens (prefill; §4.1): three launches -- one grouped tensor-core GEMM over the
  *   router's tile table for gate/up whose epilogue runs the mid, the same GEMM for down,
  *   and the finish; the shared expert runs as extra tiles of both GEMMs.  Needs
@@ -220,6 +221,26 @@ size_t qmoe_workspace_size(const qg_moe_layer* layer, int64_t t, int topk);
 qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t t, int64_t ldx, int topk,
                    const float* topk_w, const void* route_ws, void* out, int64_t ldo,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* The MoE FFN one stage at a time (the grouped GEMM of the two stages, for callers that
+ * keep h or run something between the stages); the same results as qmoe_ffn, bit for bit.
+ * rows = t * topk + (has_shared ? t : 0).
+ *   QG_MOE_GATE_UP_SWIGLU: in = x bf16 [t][ldi] (H inputs); out = h bf16 [rows][ldo] (F
+ *       columns): row p < t*topk is the p-th (token, slot) pair in the router's grouped order
+ *       (experts ascending, tokens ascending within an expert), h = bf16(silu(gate) * up)
+ *       with the gate/up rows of that pair's expert; row t*topk + i is token i's shared-expert
+ *       h.  topk_w may be NULL.
+ *   QG_MOE_DOWN_COMBINE: in = h [rows][ldi] as above; out = bf16 [t][ldo] (H columns),
+ *       out[i] = bf16( sum_j topk_w[i][j] * down_e(h of pair (i, j)) + shared down(h) ).
+ * route_ws from qmoe_route on the same t, n_experts and topk.  The workspace holds
+ * qgemm_grouped_workspace_size bytes (the qmoe_ffn size), zero-filled before first use.
+ * Same limits and errors as qmoe_ffn; stage values other than the two return
+ * QG_ERR_INVALID_ARG. */
+typedef enum { QG_MOE_GATE_UP_SWIGLU = 1, QG_MOE_DOWN_COMBINE = 2 } qg_moe_stage;
+size_t qgemm_grouped_workspace_size(const qg_moe_layer* layer, int64_t t, int topk, int stage);
+qg_status qgemm_grouped(const qg_moe_layer* layer, int stage, const void* in, int64_t t, int64_t ldi, int topk,
+                        const float* topk_w, const void* route_ws, void* out, int64_t ldo,
+                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace-free variant of qgemv, for callers that cannot allocate device memory:
  * plugins hosted by a runtime that owns all of the GPU's memory and gives them no

@@ -63,8 +63,13 @@ _SIGNATURES = {
     "qmoe_route": (_I, [_P, _I64, _I, _I, _P, _P, _P, _SZ, _P]),
     "qmoe_workspace_size": (_SZ, [ctypes.POINTER(qg_moe_layer), _I64, _I]),
     "qmoe_ffn": (_I, [ctypes.POINTER(qg_moe_layer), _P, _I64, _I64, _I, _P, _P, _P, _I64, _P, _SZ, _P]),
+    "qgemm_grouped_workspace_size": (_SZ, [ctypes.POINTER(qg_moe_layer), _I64, _I, _I]),
+    "qgemm_grouped": (_I, [ctypes.POINTER(qg_moe_layer), _I, _P, _I64, _I64, _I, _P, _P, _P, _I64, _P, _SZ, _P]),
     "qg_selftest_wait_timeout": (_I, [_P, _SZ, _P]),
 }
+
+QG_MOE_GATE_UP_SWIGLU = 1
+QG_MOE_DOWN_COMBINE = 2
 
 
 def lib():
@@ -161,6 +166,16 @@ def qmoe_ffn(layer: qg_moe_layer, x_ptr: int, t: int, ldx: int, topk: int, w_ptr
              out_ptr: int, ldo: int, ws_ptr: int, ws_bytes: int, stream: int = 0):
     _check(lib().qmoe_ffn(ctypes.byref(layer), x_ptr, t, ldx, topk, w_ptr, route_ws_ptr, out_ptr, ldo, ws_ptr,
                           ws_bytes, stream), "qmoe_ffn")
+
+
+def qgemm_grouped_workspace_size(layer: qg_moe_layer, t: int, topk: int, stage: int) -> int:
+    return lib().qgemm_grouped_workspace_size(ctypes.byref(layer), t, topk, stage)
+
+
+def qgemm_grouped(layer: qg_moe_layer, stage: int, in_ptr: int, t: int, ldi: int, topk: int, w_ptr: Optional[int],
+                  route_ws_ptr: int, out_ptr: int, ldo: int, ws_ptr: int, ws_bytes: int, stream: int = 0):
+    _check(lib().qgemm_grouped(ctypes.byref(layer), stage, in_ptr, t, ldi, topk, w_ptr, route_ws_ptr, out_ptr, ldo,
+                               ws_ptr, ws_bytes, stream), "qgemm_grouped")
 
 
 def qgemv_static_ws(w: qg_weight, x_ptr: int, m: int, ldx: int, res_ptr: Optional[int], ldr: int, y_ptr: int,
@@ -323,4 +338,23 @@ def moe_ffn(pm: PackedMoE, x, topk_w, route_ws: Workspace, out=None, workspace: 
         workspace = Workspace(qmoe_workspace_size(pm.desc, t, topk), x.device)
     qmoe_ffn(pm.desc, x.data_ptr(), t, x.stride(0), topk, topk_w.data_ptr(), route_ws.ptr, out.data_ptr(),
              out.stride(0), workspace.ptr, workspace.nbytes, _stream_ptr())
+    return out
+
+
+def moe_stage(pm: PackedMoE, stage: int, inp, t: int, topk: int, route_ws: Workspace, topk_w=None, out=None,
+              workspace: Optional[Workspace] = None):
+    """One stage of the MoE FFN (qgemm_grouped): QG_MOE_GATE_UP_SWIGLU takes x bf16 [t, H] and
+    returns h bf16 [t*topk + (t if shared), F] in the router's grouped row order;
+    QG_MOE_DOWN_COMBINE takes that h and topk_w and returns out bf16 [t, H]."""
+    import torch
+    rows = t * topk + (t if pm.desc.has_shared else 0)
+    cols = pm.ffn if stage == QG_MOE_GATE_UP_SWIGLU else pm.hidden
+    n_out = rows if stage == QG_MOE_GATE_UP_SWIGLU else t
+    if out is None:
+        out = torch.empty((n_out, (cols + 7) // 8 * 8), dtype=torch.bfloat16, device=inp.device)[:, :cols]
+    if workspace is None:
+        workspace = Workspace(qgemm_grouped_workspace_size(pm.desc, t, topk, stage), inp.device)
+    qgemm_grouped(pm.desc, stage, inp.data_ptr(), t, inp.stride(0), topk,
+                  None if topk_w is None else topk_w.data_ptr(), route_ws.ptr, out.data_ptr(), out.stride(0),
+                  workspace.ptr, workspace.nbytes, _stream_ptr())
     return out

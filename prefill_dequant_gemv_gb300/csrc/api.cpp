@@ -217,7 +217,42 @@ extern "C" qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t 
     return QG_ERR_WORKSPACE_TOO_SMALL;
   if (t > 4)
     return (qg_status)launch_moe_prefill(layer, gu, dn, x, t, ldx, topk, topk_w, route_ws, out, ldo, workspace, dev,
-                                         stream);
+                                         stream, kMoeAll);
   return (qg_status)launch_moe_decode(layer, gu, dn, x, t, ldx, topk, topk_w, route_ws, out, ldo, workspace, dev,
-                                      stream);
+                                      stream, kMoeAll);
+}
+
+extern "C" size_t qgemm_grouped_workspace_size(const qg_moe_layer* layer, int64_t t, int topk, int stage) {
+  if (stage != QG_MOE_GATE_UP_SWIGLU && stage != QG_MOE_DOWN_COMBINE) return 0;
+  return qmoe_workspace_size(layer, t, topk);
+}
+
+extern "C" qg_status qgemm_grouped(const qg_moe_layer* layer, int stage, const void* in, int64_t t, int64_t ldi,
+                                   int topk, const float* topk_w, const void* route_ws, void* out, int64_t ldo,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  Geometry gu, dn;
+  int st = check_moe(layer, t, topk, &gu, &dn);
+  if (st != QG_OK) return (qg_status)st;
+  if (stage != QG_MOE_GATE_UP_SWIGLU && stage != QG_MOE_DOWN_COMBINE) return QG_ERR_INVALID_ARG;
+  if (!in || !route_ws || !out || !workspace || (stage == QG_MOE_DOWN_COMBINE && !topk_w)) return QG_ERR_INVALID_ARG;
+  if (t > 4 && (layer->ffn % 128 != 0 || layer->hidden % 8 != 0)) return QG_ERR_UNSUPPORTED;
+  if (t * (int64_t)(topk + 1) >= ((int64_t)1 << 31)) return QG_ERR_UNSUPPORTED;
+  // gate/up: in = x [t][H], out = h [rows][F]; down: in = h [rows][F], out = [t][H]
+  const int64_t in_cols = stage == QG_MOE_GATE_UP_SWIGLU ? layer->hidden : layer->ffn;
+  const int64_t out_cols = stage == QG_MOE_GATE_UP_SWIGLU ? layer->ffn : layer->hidden;
+  if (ldi < in_cols || ldo < out_cols) return QG_ERR_INVALID_ARG;
+  if (!aligned16(in) || !aligned16(out) || !aligned16(workspace) || !aligned16(route_ws) ||
+      (topk_w && !aligned16(topk_w)))
+    return QG_ERR_MISALIGNED;
+  if (ldi % 8 || ldo % 8) return QG_ERR_MISALIGNED;
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return QG_ERR_CUDA;
+  if (workspace_bytes < moe_layout(gu, dn, t, layer->n_experts, topk, dev.sms).total)
+    return QG_ERR_WORKSPACE_TOO_SMALL;
+  const int ms = stage == QG_MOE_GATE_UP_SWIGLU ? kMoeGateUp : kMoeDown;
+  if (t > 4)
+    return (qg_status)launch_moe_prefill(layer, gu, dn, in, t, ldi, topk, topk_w, route_ws, out, ldo, workspace, dev,
+                                         stream, ms);
+  return (qg_status)launch_moe_decode(layer, gu, dn, in, t, ldi, topk, topk_w, route_ws, out, ldo, workspace, dev,
+                                      stream, ms);
 }

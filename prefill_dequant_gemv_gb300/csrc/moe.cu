@@ -48,7 +48,7 @@ struct GroupedArgs {
   int NT, KG;
   int T, topk;
   int mode;  // 0: input rows are tokens (x); 1: input rows are grouped pairs, shared rows
-             // after, computed as SwiGLU of the fp32 gate/up rows gu
+             // after: bf16 rows of x, or (gu non-null) the SwiGLU of the fp32 gate/up rows gu
   const __nv_bfloat16* x;
   int64_t ldx;
   const float* gu;
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
     if (k0 >= a.k) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) u[i] = 0;
-    } else if (a.mode == 0) {
+    } else if (a.gu == nullptr) {  // bf16 rows of x (mode 0) or of h (mode 1, staged calls)
       const uint4* src = reinterpret_cast<const uint4*>(a.x + (int64_t)row * a.ldx + k0);
       const uint4 r0 = src[0], r1 = src[1];
       u[0] = r0.x; u[1] = r0.y; u[2] = r0.z; u[3] = r0.w;
@@ -420,6 +420,20 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   }
 }
 
+// h[r][f] = bf16( silu(gu[r][f]) * gu[r][F + f] ) for every row (the staged gate/up call
+// writes h for the caller; the fused chain computes it inside the down GEMV instead).
+__global__ void __launch_bounds__(256) mid_kernel(const float* gu, int64_t ldg, __nv_bfloat16* h, int64_t ldh, int F,
+                                                  int rows) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (int64_t)rows * (F / 2)) return;
+  const int r = (int)(idx / (F / 2)), f = (int)(idx % (F / 2)) * 2;
+  const float2 g = *reinterpret_cast<const float2*>(gu + r * ldg + f);
+  const float2 u = *reinterpret_cast<const float2*>(gu + r * ldg + F + f);
+  *reinterpret_cast<uint32_t*>(h + r * ldh + f) = swiglu_bf16x2(g.x, u.x, g.y, u.y);
+}
+
 // out[t][n] = bf16( sum_j w[t][j] * d[pos(t, j)][n] + d[T*topk + t][n] ), fixed order, four
 // features per thread; every load of a thread is issued before the first multiply-add.
 __global__ void __launch_bounds__(256) finish_kernel(const float* d, int64_t ldd, const float* w, const int* pair_pos,
@@ -544,7 +558,7 @@ static int launch_grouped(int fmt, const GroupedArgs& a0, int nrows, int KG, con
 
 int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
                       int64_t ldx, int topk, const float* topk_w, const void* route_ws, void* out, int64_t ldo,
-                      void* ws, const DeviceInfo& dev, void* stream) {
+                      void* ws, const DeviceInfo& dev, void* stream, int stage) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const RouteView rv = route_view(const_cast<void*>(route_ws), T, m->n_experts, topk);
   const MoeLayout L = moe_layout(gu, dn, T, m->n_experts, topk, dev.sms);
@@ -580,10 +594,21 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
   a.ws_part = reinterpret_cast<float*>(w + L.part);
   a.ws_cnt = reinterpret_cast<int*>(w + L.cnt);
   a.status = reinterpret_cast<int*>(w);
-  int st = launch_grouped(m->fmt, a, (int)T, (int)gu.kg, dev, s);
-  if (st != QG_OK) return st;
-
   const int rows = (int)(T * topk + (m->has_shared ? T : 0));
+  int st = QG_OK;
+  if (stage != kMoeDown) {
+    st = launch_grouped(m->fmt, a, (int)T, (int)gu.kg, dev, s);
+    if (st != QG_OK) return st;
+  }
+  if (stage == kMoeGateUp) {  // h for the caller: out [rows][ldo] bf16
+    const int F = (int)dn.k;
+    if (launch_pdl(mid_kernel, dim3((unsigned)(((int64_t)rows * (F / 2) + 255) / 256)), dim3(256), 0, s,
+                   (const float*)reinterpret_cast<const float*>(w + L.gu), (int64_t)L.ld_gu,
+                   static_cast<__nv_bfloat16*>(out), ldo, F, rows) != cudaSuccess)
+      return QG_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
+  }
+
   qg_packed_sizes(m->fmt, dn.n, dn.k, &cb, &sb, &ab);
   GroupedArgs d = a;
   d.codes = static_cast<const uint8_t*>(m->dn_codes);
@@ -601,9 +626,15 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
   d.NT = (int)dn.nt;
   d.KG = (int)dn.kg;
   d.mode = 1;
-  d.x = nullptr;
-  d.gu = reinterpret_cast<const float*>(w + L.gu);
-  d.ldg = L.ld_gu;
+  if (stage == kMoeDown) {  // h from the caller's gate/up call
+    d.x = static_cast<const __nv_bfloat16*>(x);
+    d.ldx = ldx;
+    d.gu = nullptr;
+  } else {  // fused: SwiGLU of the fp32 gate/up rows while staging
+    d.x = nullptr;
+    d.gu = reinterpret_cast<const float*>(w + L.gu);
+    d.ldg = L.ld_gu;
+  }
   d.out = reinterpret_cast<float*>(w + L.d);
   d.ldo = L.ld_d;
   st = launch_grouped(m->fmt, d, rows, (int)dn.kg, dev, s);

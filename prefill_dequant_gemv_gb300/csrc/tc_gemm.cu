@@ -542,7 +542,7 @@ int tiles_of(int64_t t) { return (int)((t + kTcTile - 1) / kTcTile); }
 
 int launch_moe_prefill(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
                        int64_t ldx, int topk, const float* topk_w, const void* route_ws, void* out, int64_t ldo,
-                       void* ws, const DeviceInfo& dev, void* stream) {
+                       void* ws, const DeviceInfo& dev, void* stream, int stage) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const RouteView rv = route_view(const_cast<void*>(route_ws), T, m->n_experts, topk);
   const MoeLayout L = moe_layout(gu, dn, T, m->n_experts, topk, dev.sms);
@@ -574,16 +574,20 @@ int launch_moe_prefill(const qg_moe_layer* m, const Geometry& gu, const Geometry
   a.QN = F / 128;
   a.T = (int)T;
   a.topk = topk;
-  a.out = w + L.h;
-  a.ldo = L.ld_h;
+  a.out = stage == kMoeGateUp ? out : w + L.h;  // h: the caller's (staged call) or ours
+  a.ldo = stage == kMoeGateUp ? ldo : L.ld_h;
   a.n_out = F;
   a.F = F;
   a.meta = rv.meta;
   a.tiles = rv.tiles;
   a.pair_list = rv.pair_list;
   a.status = reinterpret_cast<int*>(w);
-  int st = launch_tc_fmt<kEpiSwiglu>(m->fmt, T, a, dev.sms, dev, s);
-  if (st != QG_OK) return st;
+  int st = QG_OK;
+  if (stage != kMoeDown) {
+    st = launch_tc_fmt<kEpiSwiglu>(m->fmt, T, a, dev.sms, dev, s);
+    if (st != QG_OK) return st;
+  }
+  if (stage == kMoeGateUp) return QG_OK;
 
   qg_packed_sizes(m->fmt, dn.n, dn.k, &cb, &sb, &ab);
   TcArgs d = a;
@@ -599,8 +603,8 @@ int launch_moe_prefill(const qg_moe_layer* m, const Geometry& gu, const Geometry
   d.sh_ts = (m->has_shared && m->fmt == FMT_NVFP4) ? m->shared_down.tensor_scale : 1.0f;
   d.sh_in_off = (int)(T * topk);  // the shared expert's h rows
   d.sh_out_off = (int)(T * topk);
-  d.in = reinterpret_cast<const __nv_bfloat16*>(w + L.h);
-  d.ldi = L.ld_h;
+  d.in = stage == kMoeDown ? static_cast<const __nv_bfloat16*>(x) : reinterpret_cast<const __nv_bfloat16*>(w + L.h);
+  d.ldi = stage == kMoeDown ? ldx : L.ld_h;
   d.K = dn.k;
   d.KG = (int)dn.kg;
   d.NT = (int)dn.nt;
@@ -609,7 +613,7 @@ int launch_moe_prefill(const qg_moe_layer* m, const Geometry& gu, const Geometry
   d.out = w + L.d;
   d.ldo = L.ld_d;
   d.n_out = dn.n;
-  st = launch_tc_fmt<kEpiPairF32>(m->fmt, T * topk + T, d, dev.sms, dev, s);
+  st = launch_tc_fmt<kEpiPairF32>(m->fmt, T * topk + (m->has_shared ? T : 0), d, dev.sms, dev, s);
   if (st != QG_OK) return st;
 
   const int64_t H = dn.n;

@@ -52,3 +52,33 @@ def moe_tolerance(o, layer, x, lg, topk, out_ref, tokens=None):
             h = inter[(int(t), -1)][2]
             tol[i] += (2e-3 + 2.0 ** -8) * np.linalg.norm(h) * float(np.max(o.row_norms(layer.shared_down)))
     return tol + 2.0 ** -7 * np.abs(out_ref)
+
+
+def grouped_rows(ids, with_shared: bool):
+    """(token, expert) of each row of the staged gate/up output: the (token, slot) pairs with
+    experts ascending and tokens ascending within an expert, then one shared row per token
+    (expert -1)."""
+    t, k = ids.shape
+    pairs = sorted((int(ids[i, j]), i) for i in range(t) for j in range(k))
+    rows = [(i, e) for e, i in pairs]
+    if with_shared:
+        rows += [(i, -1) for i in range(t)]
+    return rows
+
+
+def h_tolerance(o, layer, x, inter, rows):
+    """Per-element bound for the staged h = bf16(silu(g)·u) rows: g and u each within the GEMV
+    bound D = 2e-3·||x_t||·max_n||w_n|| of the gate/up weight, propagated through silu(g)·u
+    (|d silu/dg| <= 1.1), plus one bf16 ulp of h (a rounding flip between the two sides)."""
+    xv = o.bf16_value(x)
+    rn = {}
+    tol = []
+    for t, e in rows:
+        w = layer.shared_gate_up if e < 0 else layer.gate_up[e]
+        if e not in rn:
+            rn[e] = float(np.max(o.row_norms(w)))
+        d = 2e-3 * np.linalg.norm(xv[t]) * rn[e]
+        g, u, h, _ = inter[(t, e)]
+        silu = g / (1.0 + np.exp(-np.clip(g, -80.0, None)))
+        tol.append((1.1 * np.abs(u) + np.abs(silu) + 1.1 * d) * d + 2.0 ** -7 * np.abs(h))
+    return np.array(tol)

@@ -122,3 +122,37 @@ def test_qgemv_rejects_bad_rows_and_strides(q):
     assert L.qgemv(ctypes.byref(w), 0x3008, 1, 256, None, 0, 0x4000, 256, 0x5000, 1 << 20, None) == 3
     assert L.qgemv(ctypes.byref(w), None, 1, 256, None, 0, 0x4000, 256, 0x5000, 1 << 20, None) == 1
     assert L.qgemv(ctypes.byref(w), 0x3000, 1, 128, None, 0, 0x4000, 256, 0x5000, 1 << 20, None) == 1
+
+
+def _moe_desc(q, **kw):
+    d = dict(fmt=wl.MXFP4, n_experts=8, hidden=256, ffn=128, gu_codes=0x10000, gu_scales=0x20000, gu_aux=None,
+             dn_codes=0x30000, dn_scales=0x40000, dn_aux=None, tensor_scale=1.0, has_shared=0)
+    d.update(kw)
+    return q.qg_moe_layer(**d)
+
+
+def test_qgemm_grouped_host_validation(q):
+    """Argument errors of the staged MoE call come back before any device work."""
+    L = q.lib()
+    m = _moe_desc(q)
+    args = dict(stage=q.QG_MOE_GATE_UP_SWIGLU, inp=0x3000, t=4, ldi=256, topk=2, w=0x6000, rws=0x7000, out=0x8000,
+                ldo=128, ws=0x9000, wsb=1 << 24)
+
+    def call(layer=m, **kw):
+        a = dict(args)
+        a.update(kw)
+        return L.qgemm_grouped(ctypes.byref(layer), a["stage"], a["inp"], a["t"], a["ldi"], a["topk"], a["w"],
+                               a["rws"], a["out"], a["ldo"], a["ws"], a["wsb"], None)
+
+    assert call(stage=3) == 1                                   # unknown stage
+    assert call(stage=0) == 1
+    assert call(inp=None) == 1
+    assert call(stage=q.QG_MOE_DOWN_COMBINE, w=None, ldi=128, ldo=256) == 1  # the combine needs topk_w
+    assert call(ldi=128) == 1                                   # gate/up input narrower than H
+    assert call(stage=q.QG_MOE_DOWN_COMBINE, ldi=64, ldo=256) == 1  # down input narrower than F
+    assert call(inp=0x3008) == 3                                # misaligned
+    assert call(ldo=132) == 3                                   # leading dimension not a multiple of 8
+    assert call(topk=9) == 1                                    # more than the experts
+    assert call(layer=_moe_desc(q, n_experts=32), topk=17) == 2  # above the router's limit
+    assert call(t=0) == 1
+    assert L.qgemm_grouped_workspace_size(ctypes.byref(m), 4, 2, 3) == 0

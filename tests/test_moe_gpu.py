@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import workloads as wl
-from tests.gpu_util import dev_bf16, moe_tolerance, qlib, to_f64
+from tests.gpu_util import dev_bf16, grouped_rows, h_tolerance, moe_tolerance, qlib, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -112,3 +112,30 @@ def test_moe_decode_full_config(q):
         err = np.abs(to_f64(out) - ref)
         assert np.all(err <= tol), f"rep {rep}: {np.sum(err > tol)} out of tolerance"
         assert ws.status() == 0
+
+
+@pytest.mark.parametrize("fmt", [wl.MXFP4, wl.Q6K])
+@pytest.mark.parametrize("t,shared", [(1, True), (4, True), (3, False)])
+def test_moe_decode_staged(q, fmt, t, shared):
+    """qgemm_grouped one stage at a time: h against the oracle's h of the same (token,
+    expert), and the combined output bit-identical to the fused qmoe_ffn chain."""
+    E, k = 16, 4
+    H, F = (512, 256) if fmt == wl.Q6K else (256, 128)
+    layer = wl.moe_layer(fmt, E, H, F, seed=320 + fmt, shared=shared)
+    x = wl.moe_tokens(t, H, seed=321)
+    lg = wl.router_logits(t, E, seed=322)
+    pm = q.PackedMoE(layer)
+    ids, w, rws = q.route(torch.from_numpy(lg).cuda(), k)
+    xd = dev_bf16(x)
+    fused = q.moe_ffn(pm, xd, w, rws)
+    h = q.moe_stage(pm, q.QG_MOE_GATE_UP_SWIGLU, xd, t, k, rws)
+    out = q.moe_stage(pm, q.QG_MOE_DOWN_COMBINE, h, t, k, rws, topk_w=w)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), fused.view(torch.int16))
+    _, _, _, _, inter = oracle.moe_forward(layer, x, lg, k, with_intermediates=True)
+    rows = grouped_rows(ids.cpu().numpy(), shared)
+    assert h.shape[0] == len(rows)
+    href = np.stack([inter[r][2] for r in rows])
+    err = np.abs(to_f64(h) - href)
+    tol = h_tolerance(oracle, layer, x, inter, rows)
+    assert np.all(err <= tol), f"{np.sum(err > tol)} h values out of tolerance"

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import workloads as wl
-from tests.gpu_util import dev_bf16, moe_tolerance, qlib, to_f64
+from tests.gpu_util import dev_bf16, grouped_rows, h_tolerance, moe_tolerance, qlib, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -119,3 +119,25 @@ def test_moe_prefill_full_config_sampled(q):
     tokens = np.array([0, 255, 256, 8191])
     ref = oracle.moe_forward(layer, x, lg, c["topk"], tokens=tokens)
     _check(got[tokens], ref, moe_tolerance(oracle, layer, x, lg, c["topk"], ref, tokens=tokens))
+
+
+@pytest.mark.parametrize("fmt,shared", [(wl.MXFP4, True), (wl.NVFP4, False)])
+def test_moe_prefill_staged(q, fmt, shared):
+    """qgemm_grouped one stage at a time on the tensor-core chain: h against the oracle's h,
+    the combined output bit-identical to the fused qmoe_ffn chain."""
+    E, H, F, k, t = 16, 256, 128, 4, 257
+    layer = wl.moe_layer(fmt, E, H, F, seed=430 + fmt, shared=shared)
+    x = wl.moe_tokens(t, H, seed=431)
+    lg = wl.router_logits(t, E, seed=432)
+    pm = q.PackedMoE(layer)
+    ids, w, rws = q.route(torch.from_numpy(lg).cuda(), k)
+    xd = dev_bf16(x)
+    fused = q.moe_ffn(pm, xd, w, rws)
+    h = q.moe_stage(pm, q.QG_MOE_GATE_UP_SWIGLU, xd, t, k, rws)
+    out = q.moe_stage(pm, q.QG_MOE_DOWN_COMBINE, h, t, k, rws, topk_w=w)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), fused.view(torch.int16))
+    _, _, _, _, inter = oracle.moe_forward(layer, x, lg, k, with_intermediates=True)
+    rows = grouped_rows(ids.cpu().numpy(), shared)
+    href = np.stack([inter[r][2] for r in rows])
+    _check(to_f64(h), href, h_tolerance(oracle, layer, x, inter, rows))
