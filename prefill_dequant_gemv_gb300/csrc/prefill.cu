@@ -45,6 +45,7 @@ constexpr int kPfSmem = 1024 + kPfStages * kPfStageBytes + 256;
 constexpr uint32_t kPfTmemCols = 512;
 constexpr uint32_t kPfA0 = 256;                              // A stage s at columns 256 + 32 s
 static_assert(kPfA0 + 32 * kPfStages <= kPfTmemCols, "tensor memory");
+static_assert(kPfBN * 128 * 4 <= kPfStages * kPfStageBytes, "epilogue tile fits in the stage buffers");
 
 struct PrefillArgs {
   const uint8_t* codes;
@@ -173,26 +174,63 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         ph ^= 1u;
       }
     }
-    // epilogue: TMEM lanes 32*(warp%4).. hold output rows; warps 2-5 take tokens 0..127,
-    // warps 6-9 tokens 128..255
-    if (mbar_wait_bounded(done, 0, a.status) && ok) {
+    // Epilogue, two phases over the (now idle) stage buffers.  Phase 1: TMEM lanes
+    // 32*(warp%4).. hold output rows; warps 2-5 take tokens 0..127, warps 6-9 tokens
+    // 128..255; each thread scales its row's accumulators by the tensor scale into a
+    // token-major fp32 tile [256 tokens][128 rows] (a warp writes 128 contiguous bytes per
+    // token).  Phase 2: each thread takes 8 consecutive rows of one token -- adds the
+    // residual, rounds to bf16 once and writes 16 bytes.  The barriers between the phases
+    // are reached by every decode warp, also after a failed wait.
+    const bool go = mbar_wait_bounded(done, 0, a.status) && ok;
+    float* sF = reinterpret_cast<float*>(smem);  // 128 KB, inside stages 0..3
+    if (go) {
       tc_fence_after();
       const int quarter = warp & 3;
       const int col0 = ((warp - 2) >> 2) * (kPfBN / 2);
-      const int64_t n = (int64_t)tile_n * 128 + quarter * 32 + lane;
+      const int row = quarter * 32 + lane;
       for (int c = 0; c < kPfBN / 2; c += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(col0 + c), v);
         tmem_ld_wait();
-        if (n < a.n) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int64_t t = t0 + col0 + c + j;
-            if (t < a.t) {
-              float o = a.ts * __uint_as_float(v[j]);
-              if (a.res) o += __bfloat162float(a.res[t * a.ldr + n]);
-              a.y[t * a.ldy + n] = __float2bfloat16_rn(o);
+        for (int j = 0; j < 32; ++j) sF[(col0 + c + j) * 128 + row] = a.ts * __uint_as_float(v[j]);
+      }
+    }
+    named_sync(1, kPfDeqWarps * 32);
+    if (go) {
+      const int e = tid - 64;  // 0..255
+      const int64_t nb = (int64_t)tile_n * 128;
+#pragma unroll 4
+      for (int i = 0; i < (kPfBN * 16) / (kPfDeqWarps * 32); ++i) {
+        const int item = e + i * kPfDeqWarps * 32;
+        const int tok = item >> 4, f8 = (item & 15) * 8;
+        const int64_t t = t0 + tok, n = nb + f8;
+        if (t >= a.t || n >= a.n) continue;
+        const float4 p0 = *reinterpret_cast<const float4*>(sF + tok * 128 + f8);
+        const float4 p1 = *reinterpret_cast<const float4*>(sF + tok * 128 + f8 + 4);
+        float o[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        if (n + 8 <= a.n) {
+          if (a.res) {
+            const uint4 rv = *reinterpret_cast<const uint4*>(a.res + t * a.ldr + n);
+            const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              o[2 * q] += __uint_as_float(rw[q] << 16);
+              o[2 * q + 1] += __uint_as_float(rw[q] & 0xFFFF0000u);
             }
+          }
+          uint32_t pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[2 * q], o[2 * q + 1]);
+            pk[q] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          *reinterpret_cast<uint4*>(a.y + t * a.ldy + n) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        } else {  // the matrix's last rows
+          for (int q = 0; q < 8 && n + q < a.n; ++q) {
+            float v = o[q];
+            if (a.res) v += __bfloat162float(a.res[t * a.ldr + n + q]);
+            a.y[t * a.ldy + n + q] = __float2bfloat16_rn(v);
           }
         }
       }
