@@ -36,7 +36,8 @@ namespace qg {
 
 constexpr int kPfBN = 256;                                   // tokens per tile (MMA N)
 constexpr int kPfStages = 5;
-constexpr int kPfDeqWarps = 8;
+constexpr int kPfDeqWarps = 8;                               // epilogue warps (and Q6_K decoders)
+__host__ __device__ constexpr int pf_decoders(int fmt) { return fmt == FMT_Q6K ? 8 : 4; }
 constexpr int kPfThreads = (2 + kPfDeqWarps) * 32;           // 320
 constexpr int kBTile = kPfBN * 128;                          // 256 tokens x 64 bf16
 constexpr int kRawMax = 7168;                                // >= Q6_K tile 6144 + 512 + 256
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&afull[s], kPfDeqWarps);
+      mbar_init(&afull[s], pf_decoders(FMT));
       mbar_init(&empty[s], 1);
     }
     mbar_init(done, 1);
@@ -147,13 +148,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncwarp();
   } else {
     // decode warps: warp w may only touch TMEM lanes 32*(w%4)..; it decodes rows
-    // 32*(w%4)+lane, inputs 32h..32h+31 of each stage (h = 0 for warps 2-5, 1 for 6-9)
+    // 32*(w%4)+lane.  4-bit formats: warps 2-5 decode all 64 inputs of each stage and store
+    // them with one 32-column tensor-memory write; Q6_K (heavier extraction): warps 2-9,
+    // inputs 32h..32h+31 (h = 0 for warps 2-5, 1 for 6-9), 16 columns each.
+    constexpr int kDec = pf_decoders(FMT);
     const int r = (warp & 3) * 32 + lane, h = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int kt = 0; kt < KG; ++kt) {
+    for (int kt = 0; kt < (warp < 2 + kDec ? KG : 0); ++kt) {
       if (!mbar_wait_bounded(&full[s], ph, a.status)) {
         ok = false;
         break;
@@ -162,9 +166,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // slot (empty -> producer -> full): order this thread's TMEM writes after them
       tc_fence_after();
       uint8_t* st = smem + s * kPfStageBytes;
-      uint32_t o[16];
-      decode_regs<FMT>(st + kBTile, r, h, o);
-      tmem_st16(tmem + lane_base + kPfA0 + 32u * (uint32_t)s + 16u * (uint32_t)h, o);
+      if (kDec == 4) {
+        uint32_t o[32];
+        decode_regs<FMT>(st + kBTile, r, 0, *reinterpret_cast<uint32_t(*)[16]>(o));
+        decode_regs<FMT>(st + kBTile, r, 1, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
+        tmem_st32(tmem + lane_base + kPfA0 + 32u * (uint32_t)s, o);
+      } else {
+        uint32_t o[16];
+        decode_regs<FMT>(st + kBTile, r, h, o);
+        tmem_st16(tmem + lane_base + kPfA0 + 32u * (uint32_t)s + 16u * (uint32_t)h, o);
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
