@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&afull[s], pf_decoders(FMT));
+      mbar_init(&afull[s], 4);  // the four decode warps of the stage's group
       mbar_init(&empty[s], 1);
     }
     mbar_init(done, 1);
@@ -148,16 +148,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncwarp();
   } else {
     // decode warps: warp w may only touch TMEM lanes 32*(w%4)..; it decodes rows
-    // 32*(w%4)+lane.  4-bit formats: warps 2-5 decode all 64 inputs of each stage and store
-    // them with one 32-column tensor-memory write; Q6_K (heavier extraction): warps 2-9,
-    // inputs 32h..32h+31 (h = 0 for warps 2-5, 1 for 6-9), 16 columns each.
-    constexpr int kDec = pf_decoders(FMT);
-    const int r = (warp & 3) * 32 + lane, h = (warp - 2) >> 2;
+    // 32*(w%4)+lane, all 64 inputs of a stage, stored with one 32-column tensor-memory write
+    // (fewer, wider writes contend less with the MMAs).  4-bit formats: warps 2-5 take every
+    // stage; Q6_K (heavier extraction): warps 2-5 the even stages, warps 6-9 the odd ones.
+    constexpr int kGroups = pf_decoders(FMT) / 4;
+    const int r = (warp & 3) * 32 + lane, grp = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    int s = 0;
-    uint32_t ph = 0;
     bool ok = true;
-    for (int kt = 0; kt < (warp < 2 + kDec ? KG : 0); ++kt) {
+    for (int kt = grp < kGroups ? grp : KG; kt < KG; kt += kGroups) {
+      const int s = kt % kPfStages;
+      const uint32_t ph = (uint32_t)(kt / kPfStages) & 1u;
       if (!mbar_wait_bounded(&full[s], ph, a.status)) {
         ok = false;
         break;
@@ -166,24 +166,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // slot (empty -> producer -> full): order this thread's TMEM writes after them
       tc_fence_after();
       uint8_t* st = smem + s * kPfStageBytes;
-      if (kDec == 4) {
-        uint32_t o[32];
-        decode_regs<FMT>(st + kBTile, r, 0, *reinterpret_cast<uint32_t(*)[16]>(o));
-        decode_regs<FMT>(st + kBTile, r, 1, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
-        tmem_st32(tmem + lane_base + kPfA0 + 32u * (uint32_t)s, o);
-      } else {
-        uint32_t o[16];
-        decode_regs<FMT>(st + kBTile, r, h, o);
-        tmem_st16(tmem + lane_base + kPfA0 + 32u * (uint32_t)s + 16u * (uint32_t)h, o);
-      }
+      uint32_t o[32];
+      decode_regs<FMT>(st + kBTile, r, 0, *reinterpret_cast<uint32_t(*)[16]>(o));
+      decode_regs<FMT>(st + kBTile, r, 1, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
+      tmem_st32(tmem + lane_base + kPfA0 + 32u * (uint32_t)s, o);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&afull[s]);
-      if (++s == kPfStages) {
-        s = 0;
-        ph ^= 1u;
-      }
     }
     // Epilogue, two phases over the (now idle) stage buffers.  Phase 1: TMEM lanes
     // 32*(warp%4).. hold output rows; warps 2-5 take tokens 0..127, warps 6-9 tokens

@@ -18,10 +18,11 @@
 //   warp 0       raw-weight producer: bulk copies of both packed tiles of a stage into a
 //                deep shared-memory ring
 //   warp 1       allocates all 512 TMEM columns; one lane issues the tcgen05.mma
-//   warps 2-5    decode each stage's two tiles into the bf16 A operand in tensor memory
-//                (tcgen05.st), so decoded weights cost no shared-memory bandwidth
-//   warps 6-17   epilogue: TMEM -> registers -> outputs
-//   warps 18-25  token rows: one TMA load per stage when the rows are contiguous, else a
+//   warps 2-9    decode each stage's two tiles into the bf16 A operand in tensor memory
+//                (tcgen05.st; warps 2-5 the even stages, 6-9 the odd ones), so decoded
+//                weights cost no shared-memory bandwidth
+//   warps 10-21  epilogue: TMEM -> registers -> outputs
+//   warps 22-29  token rows: one TMA load per stage when the rows are contiguous, else a
 //                cp.async gather by row index into the 128-byte swizzled ring; each
 //                thread's copies arrive on the stage's mbarrier when they land, and the MMA
 //                thread fences these generic-proxy writes before the tensor cores read them
@@ -46,14 +47,14 @@
 
 namespace qg {
 
-constexpr int kTcDecWarps = 4;  // one per TMEM lane quarter, both row tiles of a stage
+constexpr int kTcDecWarps = 8;  // two groups of four (one per TMEM lane quarter), alternate stages
 constexpr int kTcEpiWarps = 12;  // three per TMEM lane quarter, every third 16-column chunk
 constexpr int kTcGatWarps = 8;  // the gathered token rows keep 256 threads busy
 constexpr int kTcGatThreads = kTcGatWarps * 32;
-constexpr int kTcWarps = 2 + kTcDecWarps + kTcEpiWarps + kTcGatWarps;  // 26
-constexpr int kTcThreads = kTcWarps * 32;                               // 832
-constexpr int kTcEpiWarp0 = 2 + kTcDecWarps;                            // 6
-constexpr int kTcGatWarp0 = kTcEpiWarp0 + kTcEpiWarps;                  // 18
+constexpr int kTcWarps = 2 + kTcDecWarps + kTcEpiWarps + kTcGatWarps;  // 30
+constexpr int kTcThreads = kTcWarps * 32;                               // 960
+constexpr int kTcEpiWarp0 = 2 + kTcDecWarps;                            // 10
+constexpr int kTcGatWarp0 = kTcEpiWarp0 + kTcEpiWarps;                  // 22
 constexpr int kTcTile = kRouteTile;  // tokens per tile = largest MMA N (192)
 constexpr int kTcSmemCap = 232448;   // opt-in shared memory per block on sm_100-family GPUs
 
@@ -205,10 +206,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   if (tid == 0) {
     for (int s = 0; s < C::RS; ++s) {
       mbar_init(&r_full[s], 1);
-      mbar_init(&r_empty[s], kTcDecWarps);
+      mbar_init(&r_empty[s], 4);  // the four decode warps of the stage's group
     }
     for (int s = 0; s < C::AS; ++s) {
-      mbar_init(&a_full[s], kTcDecWarps);
+      mbar_init(&a_full[s], 4);
       mbar_init(&a_empty[s], 1);
     }
     for (int s = 0; s < C::BS; ++s) {
@@ -299,15 +300,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   } else if (warp < kTcEpiWarp0) {
     // ------------------------------------------------------------ decode
     // Warp w may only touch TMEM lanes 32*(w%4)..: it decodes rows 32*(w%4)+lane, all 64
-    // inputs of each stage of both row tiles, each tile stored with one 32-column
-    // tensor-memory write (four warps with wide writes contend less with the MMAs reading
-    // tensor memory than eight with 16-column writes: 911 -> 881 us for the 8192-token FFN).
-    const int r = (warp & 3) * 32 + lane;
+    // inputs of both row tiles of every other stage (warps 2-5 the even stages, 6-9 the odd
+    // ones), each tile stored with one 32-column tensor-memory write (wide writes contend
+    // less with the MMAs reading tensor memory than 16-column ones: 911 -> 866 us for the
+    // 8192-token FFN).
+    const int r = (warp & 3) * 32 + lane, grp = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     uint32_t gs = 0;
     bool ok = true;
     for (int i = b; ok && i < n_items; i += G) {
       for (int kt = 0; kt < KG; ++kt, ++gs) {
+        if ((int)(gs & 1u) != grp) continue;
         const uint32_t sr = gs % C::RS, sa = gs % C::AS;
         if (!mbar_wait_bounded(&r_full[sr], (gs / C::RS) & 1u, a.status) ||
             (gs >= (uint32_t)C::AS && !mbar_wait_bounded(&a_empty[sa], ((gs / C::AS) & 1u) ^ 1u, a.status))) {
