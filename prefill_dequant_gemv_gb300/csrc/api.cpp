@@ -144,6 +144,11 @@ extern "C" qg_status qgemm(const qg_weight* w, const void* x, int64_t m, int64_t
   if (ldx % 8 || ldy % 8 || (residual && ldr % 8)) return QG_ERR_MISALIGNED;
   if (workspace_bytes < kWsHeader) return QG_ERR_WORKSPACE_TOO_SMALL;
   if ((m + 255) / 256 > 65535 || g.nt > 0x7FFFFFFF) return QG_ERR_UNSUPPORTED;
+  if (m <= kSmallGemmMaxRows) {
+    DeviceInfo dev;
+    if (!current_device_info(&dev)) return QG_ERR_CUDA;
+    return (qg_status)launch_gemm_small(g, w, x, m, ldx, residual, ldr, y, ldy, workspace, dev, stream);
+  }
   return (qg_status)launch_prefill(g, w, x, m, ldx, residual, ldr, y, ldy, workspace, stream);
 }
 

@@ -23,6 +23,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -58,8 +59,16 @@ struct PrefillArgs {
   int64_t n, t;
   int KG;
   float ts;
+  int ks;  // CTAs per cluster splitting K (1: no split)
   int* status;
 };
+
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+  return v;
+}
 
 template <int FMT>
 __global__ void __launch_bounds__(kPfThreads, 1)
@@ -79,6 +88,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int tile_n = blockIdx.x;
   const int t0 = blockIdx.y * kPfBN;
   const int KG = a.KG;
+  // split K: this CTA's 64-deep stages [kt0, kt1) (the host keeps ks <= KG)
+  const int ks = a.ks;
+  const int rank = ks > 1 ? (int)cluster_rank() : 0;
+  const int kt0 = (int)((int64_t)rank * KG / ks), kt1 = (int)((int64_t)(rank + 1) * KG / ks);
+  const int nst = kt1 - kt0;
 
   if (tid == 0) {
     for (int s = 0; s < kPfStages; ++s) {
@@ -103,8 +117,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       int issued = 0;
-      for (int kt = 0; kt < KG; ++kt) {
-        if (kt >= kPfStages && !mbar_wait_bounded(&empty[s], ph ^ 1u, a.status)) break;
+      for (int kt = kt0; kt < kt1; ++kt) {
+        if (kt - kt0 >= kPfStages && !mbar_wait_bounded(&empty[s], ph ^ 1u, a.status)) break;
         uint8_t* st = smem + s * kPfStageBytes;
         const int64_t tile = (int64_t)tile_n * KG + kt;
         mbar_arrive_expect_tx(&full[s], kRaw + kBTile);
@@ -124,19 +138,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int i = (issued > kPfStages ? issued - kPfStages : 0); i < issued; ++i)
         mbar_wait_bounded(&full[i % kPfStages], (uint32_t)(i / kPfStages) & 1u, a.status);
     }
+    __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
       constexpr uint32_t idesc = idesc_bf16_f32(128, kPfBN);
       int s = 0;
       uint32_t ph = 0;
-      for (int kt = 0; kt < KG; ++kt) {
-        if (!mbar_wait_bounded(&afull[s], ph, a.status) || !mbar_wait_bounded(&full[s], ph, a.status)) break;
+      // the decoders waited for the stage's landing before arriving on afull, so this one
+      // wait covers both operands
+      for (int kt = kt0; kt < kt1; ++kt) {
+        if (!mbar_wait_bounded(&afull[s], ph, a.status)) break;
         tc_fence_after();
         const uint32_t ta = tmem + kPfA0 + 32u * (uint32_t)s;
         const uint32_t bbase = smem_u32(smem + s * kPfStageBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ts(tmem, ta + kk * 8, sw128_desc(bbase + kk * 32), idesc, (kt | kk) ? 1u : 0u);
+          mma_bf16_ts(tmem, ta + kk * 8, sw128_desc(bbase + kk * 32), idesc, ((kt - kt0) | kk) ? 1u : 0u);
         mma_commit(&empty[s]);
         if (++s == kPfStages) {
           s = 0;
@@ -146,7 +163,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mma_commit(done);  // also drains whatever was issued if the loop stopped early
     }
     __syncwarp();
-  } else {
+  }
+  bool go = false;  // decode warps: every wait succeeded and the accumulator is complete
+  float* sF = reinterpret_cast<float*>(smem);  // epilogue tile, 128 KB inside stages 0..3
+  if (warp >= 2) {
     // decode warps: warp w may only touch TMEM lanes 32*(w%4)..; it decodes rows
     // 32*(w%4)+lane, all 64 inputs of a stage, stored with one 32-column tensor-memory write
     // (fewer, wider writes contend less with the MMAs).  4-bit formats: warps 2-5 take every
@@ -155,9 +175,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int r = (warp & 3) * 32 + lane, grp = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = true;
-    for (int kt = grp < kGroups ? grp : KG; kt < KG; kt += kGroups) {
-      const int s = kt % kPfStages;
-      const uint32_t ph = (uint32_t)(kt / kPfStages) & 1u;
+    for (int j = grp < kGroups ? grp : nst; j < nst; j += kGroups) {
+      const int s = j % kPfStages;
+      const uint32_t ph = (uint32_t)(j / kPfStages) & 1u;
       if (!mbar_wait_bounded(&full[s], ph, a.status)) {
         ok = false;
         break;
@@ -179,11 +199,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // 32*(warp%4).. hold output rows; warps 2-5 take tokens 0..127, warps 6-9 tokens
     // 128..255; each thread scales its row's accumulators by the tensor scale into a
     // token-major fp32 tile [256 tokens][128 rows] (a warp writes 128 contiguous bytes per
-    // token).  Phase 2: each thread takes 8 consecutive rows of one token -- adds the
-    // residual, rounds to bf16 once and writes 16 bytes.  The barriers between the phases
-    // are reached by every decode warp, also after a failed wait.
-    const bool go = mbar_wait_bounded(done, 0, a.status) && ok;
-    float* sF = reinterpret_cast<float*>(smem);  // 128 KB, inside stages 0..3
+    // token).  Phase 2 (below, after a barrier of the CTA or, with K split, of the cluster):
+    // each thread takes 8 consecutive rows of one token -- sums the K-split partial tiles in
+    // rank order, adds the residual, rounds to bf16 once and writes 16 bytes.  The barriers
+    // are reached by every thread, also after a failed wait.
+    go = mbar_wait_bounded(done, 0, a.status) && ok;
     if (go) {
       tc_fence_after();
       const int quarter = warp & 3;
@@ -197,46 +217,60 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int j = 0; j < 32; ++j) sF[(col0 + c + j) * 128 + row] = a.ts * __uint_as_float(v[j]);
       }
     }
-    named_sync(1, kPfDeqWarps * 32);
-    if (go) {
-      const int e = tid - 64;  // 0..255
-      const int64_t nb = (int64_t)tile_n * 128;
-#pragma unroll 4
-      for (int i = 0; i < (kPfBN * 16) / (kPfDeqWarps * 32); ++i) {
-        const int item = e + i * kPfDeqWarps * 32;
-        const int tok = item >> 4, f8 = (item & 15) * 8;
-        const int64_t t = t0 + tok, n = nb + f8;
-        if (t >= a.t || n >= a.n) continue;
-        const float4 p0 = *reinterpret_cast<const float4*>(sF + tok * 128 + f8);
-        const float4 p1 = *reinterpret_cast<const float4*>(sF + tok * 128 + f8 + 4);
-        float o[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-        if (n + 8 <= a.n) {
-          if (a.res) {
-            const uint4 rv = *reinterpret_cast<const uint4*>(a.res + t * a.ldr + n);
-            const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              o[2 * q] += __uint_as_float(rw[q] << 16);
-              o[2 * q + 1] += __uint_as_float(rw[q] & 0xFFFF0000u);
-            }
-          }
-          uint32_t pk[4];
+  }
+  __syncwarp();
+  if (ks > 1) cluster_sync_all();
+  else __syncthreads();
+  if (go) {
+    const int e = tid - 64;  // 0..255
+    const int64_t nb = (int64_t)tile_n * 128;
+    for (int item = rank + ks * e; item < kPfBN * 16; item += ks * kPfDeqWarps * 32) {
+      const int tok = item >> 4, f8 = (item & 15) * 8;
+      const int64_t t = t0 + tok, n = nb + f8;
+      if (t >= a.t || n >= a.n) continue;
+      float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int q = 0; q < ks; ++q) {
+        float4 p0, p1;
+        if (ks > 1) {
+          const uint32_t ad = cluster_map(sF + tok * 128 + f8, (uint32_t)q);
+          p0 = ld_cluster_f32x4(ad);
+          p1 = ld_cluster_f32x4(ad + 16);
+        } else {
+          p0 = *reinterpret_cast<const float4*>(sF + tok * 128 + f8);
+          p1 = *reinterpret_cast<const float4*>(sF + tok * 128 + f8 + 4);
+        }
+        o[0] += p0.x; o[1] += p0.y; o[2] += p0.z; o[3] += p0.w;
+        o[4] += p1.x; o[5] += p1.y; o[6] += p1.z; o[7] += p1.w;
+      }
+      if (n + 8 <= a.n) {
+        if (a.res) {
+          const uint4 rv = *reinterpret_cast<const uint4*>(a.res + t * a.ldr + n);
+          const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[2 * q], o[2 * q + 1]);
-            pk[q] = *reinterpret_cast<const uint32_t*>(&b2);
+            o[2 * q] += __uint_as_float(rw[q] << 16);
+            o[2 * q + 1] += __uint_as_float(rw[q] & 0xFFFF0000u);
           }
-          *reinterpret_cast<uint4*>(a.y + t * a.ldy + n) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        } else {  // the matrix's last rows
-          for (int q = 0; q < 8 && n + q < a.n; ++q) {
-            float v = o[q];
-            if (a.res) v += __bfloat162float(a.res[t * a.ldr + n + q]);
-            a.y[t * a.ldy + n + q] = __float2bfloat16_rn(v);
-          }
+        }
+        uint32_t pk[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(o[2 * q], o[2 * q + 1]);
+          pk[q] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        *reinterpret_cast<uint4*>(a.y + t * a.ldy + n) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      } else {  // the matrix's last rows
+        for (int q = 0; q < 8 && n + q < a.n; ++q) {
+          float v = o[q];
+          if (a.res) v += __bfloat162float(a.res[t * a.ldr + n + q]);
+          a.y[t * a.ldy + n + q] = __float2bfloat16_rn(v);
         }
       }
     }
   }
+  // with K split, the other CTAs of the cluster may still read this CTA's tile
+  __syncwarp();
+  if (ks > 1) cluster_sync_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -266,6 +300,18 @@ EncodeFn encode_fn() {
 }
 }  // namespace
 
+bool encode_token_rows(CUtensorMap* map, const void* x, int64_t rows, int64_t k, int64_t ldx, int box_rows) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ldx * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int launch_prefill(const Geometry& g, const qg_weight* w, const void* x, int64_t t, int64_t ldx, const void* res,
                    int64_t ldr, void* y, int64_t ldy, void* ws, void* stream) {
   EncodeFn enc = encode_fn();
@@ -292,37 +338,52 @@ int launch_prefill(const Geometry& g, const qg_weight* w, const void* x, int64_t
   a.KG = (int)g.kg;
   a.ts = (g.fmt == FMT_NVFP4) ? w->tensor_scale : 1.0f;
   a.status = static_cast<int*>(ws);
-  const dim3 grid((unsigned)g.nt, (unsigned)((t + kPfBN - 1) / kPfBN));
-  if (grid.y > 65535u) return QG_ERR_UNSUPPORTED;
+  DeviceInfo info;
+  int devid = 0;
+  if (cudaGetDevice(&devid) != cudaSuccess || !device_info(devid, &info)) return QG_ERR_CUDA;
+  const int64_t tt = (t + kPfBN - 1) / kPfBN;
+  if (tt > 65535) return QG_ERR_UNSUPPORTED;
+  // split K over a cluster of up to 8 CTAs when the output tiles fill less than half the GPU
+  a.ks = 1;
+  if (g.nt * tt * 2 <= info.sms) a.ks = (int)std::min<int64_t>(std::min<int64_t>(8, info.sms / (g.nt * tt)), g.kg);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   static std::atomic<unsigned long long> configured[5];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return QG_ERR_CUDA;
-  const unsigned long long bit = 1ull << (dev & 63);
-  auto config = [&](const void* fn) -> bool {
-    if (configured[g.fmt].load() & bit) return true;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem) != cudaSuccess) return false;
-    configured[g.fmt].fetch_or(bit);
-    return true;
-  };
+  const unsigned long long bit = 1ull << (devid & 63);
+  const void* fn = nullptr;
   switch (g.fmt) {
-    case FMT_MLX:
-      if (!config((const void*)prefill_kernel<FMT_MLX>)) return QG_ERR_CUDA;
-      prefill_kernel<FMT_MLX><<<grid, kPfThreads, kPfSmem, s>>>(map, a);
-      break;
-    case FMT_MXFP4:
-      if (!config((const void*)prefill_kernel<FMT_MXFP4>)) return QG_ERR_CUDA;
-      prefill_kernel<FMT_MXFP4><<<grid, kPfThreads, kPfSmem, s>>>(map, a);
-      break;
-    case FMT_NVFP4:
-      if (!config((const void*)prefill_kernel<FMT_NVFP4>)) return QG_ERR_CUDA;
-      prefill_kernel<FMT_NVFP4><<<grid, kPfThreads, kPfSmem, s>>>(map, a);
-      break;
-    default:
-      if (!config((const void*)prefill_kernel<FMT_Q6K>)) return QG_ERR_CUDA;
-      prefill_kernel<FMT_Q6K><<<grid, kPfThreads, kPfSmem, s>>>(map, a);
-      break;
+    case FMT_MLX: fn = (const void*)prefill_kernel<FMT_MLX>; break;
+    case FMT_MXFP4: fn = (const void*)prefill_kernel<FMT_MXFP4>; break;
+    case FMT_NVFP4: fn = (const void*)prefill_kernel<FMT_NVFP4>; break;
+    default: fn = (const void*)prefill_kernel<FMT_Q6K>; break;
   }
+  if (!(configured[g.fmt].load() & bit)) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem) != cudaSuccess)
+      return QG_ERR_CUDA;
+    configured[g.fmt].fetch_or(bit);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)g.nt, (unsigned)tt, (unsigned)a.ks);
+  cfg.blockDim = dim3(kPfThreads);
+  cfg.dynamicSmemBytes = kPfSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  if (a.ks > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)a.ks;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e;
+  switch (g.fmt) {
+    case FMT_MLX: e = cudaLaunchKernelEx(&cfg, prefill_kernel<FMT_MLX>, map, a); break;
+    case FMT_MXFP4: e = cudaLaunchKernelEx(&cfg, prefill_kernel<FMT_MXFP4>, map, a); break;
+    case FMT_NVFP4: e = cudaLaunchKernelEx(&cfg, prefill_kernel<FMT_NVFP4>, map, a); break;
+    default: e = cudaLaunchKernelEx(&cfg, prefill_kernel<FMT_Q6K>, map, a); break;
+  }
+  if (e != cudaSuccess) return QG_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 

@@ -1,6 +1,7 @@
 // Host-side internals shared by the C ABI entry points and the kernel launchers.
 #pragma once
 
+#include <cuda.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -46,6 +47,14 @@ int launch_gemv(const Geometry& g, const qg_weight* w, const void* x, int m, int
                 const void* res, int64_t ldr, void* y, int64_t ldy, void* ws, const GemvPlan& p,
                 void* stream);
 int launch_dequant(const Geometry& g, const qg_weight* w, int out_dtype, void* out, int64_t ldo, void* stream);
+// The token rows as a 2-D TMA tensor (rows x k bf16, row stride ldx elements): box of 64
+// inputs x box_rows rows, 128-byte swizzle, zero fill.
+bool encode_token_rows(CUtensorMap* map, const void* x, int64_t rows, int64_t k, int64_t ldx, int box_rows);
+// Tensor-core GEMM for 5..kSmallGemmMaxRows token rows, one token tile (split K over a
+// cluster when the row tiles are few); more rows take the 256-token-tile prefill GEMM.
+constexpr int64_t kSmallGemmMaxRows = 128;
+int launch_gemm_small(const Geometry& g, const qg_weight* w, const void* x, int64_t t, int64_t ldx, const void* res,
+                      int64_t ldr, void* y, int64_t ldy, void* ws, const DeviceInfo& dev, void* stream);
 int launch_prefill(const Geometry& g, const qg_weight* w, const void* x, int64_t t, int64_t ldx, const void* res,
                    int64_t ldr, void* y, int64_t ldy, void* ws, void* stream);
 
