@@ -8,16 +8,15 @@
 //   warp 0      producer: per 64-deep stage, bulk-copies the packed weight tile and TMA-loads
 //               the NB x 64 activation tile (128-byte swizzle) into an 8-stage ring
 //   warp 1      allocates the 512 TMEM columns and issues tcgen05.mma M=128 N=NB K=16 (A from
-//               TMEM, B from shared memory); the 4 K-steps of stage j go to accumulators
-//               (4j + kk) mod NACC, so consecutive MMAs never wait on each other (consecutive
-//               MMAs into one accumulator cost ~130 cycles whatever N is)
+//               TMEM, B from shared memory) into one accumulator, with every operand prepared
+//               ahead (one thread issues an MMA every ~48 cycles at best)
 //   warps 2-9   decode in two groups of four, alternate pairs of stages, each row's 64 inputs
 //               per stage written with one 32-column tcgen05.st; then the epilogue
-// With few tokens the MMAs are short and the MMA thread's own barrier traffic sets the pace
-// (each wait or commit costs about as much as issuing an MMA), so stages travel in pairs:
-// one readiness wait and one commit (freeing both stages' buffers and A slots) per pair.
-// Epilogue: every thread of warps 2-5 sums its row's NACC accumulators in a fixed order
-// into a token-major fp32 tile in its CTA's idle stage buffers; after a cluster barrier each
+// With few tokens the MMAs are short and the MMA thread's own instruction stream sets the
+// pace, so stages travel in pairs -- one readiness wait and one commit (freeing both stages'
+// buffers and A slots) per pair -- and the descriptors are prepared outside the issue.
+// Epilogue: every thread of warps 2-5 scales its row of the accumulator into a token-major
+// fp32 tile in its CTA's idle stage buffers; after a cluster barrier each
 // CTA takes every ks-th group of 8 rows of one token, adds the ks partial tiles in rank order
 // (distributed shared memory), the residual, rounds to bf16 once and writes 16 bytes.  No
 // workspace, no atomics: results are deterministic.  Every wait is bounded (QG_ERR_TIMEOUT in
@@ -46,9 +45,8 @@ struct SmCfg {
   static constexpr int B = NB * 128;                                 // NB token rows x 64 bf16
   static constexpr int STAGE = ((B + kSmRawMax) + 1023) & ~1023;     // B tile 1024-byte aligned
   static constexpr int S = kSmAS;  // stage ring = A ring: stage j uses buffer and A slot j % 8
-  static constexpr int NACC = (256 / NB) > 8 ? 8 : (256 / NB);       // accumulators of NB columns
   static constexpr int SMEM = 1024 + S * STAGE + 1024;
-  static_assert(NACC * NB <= (int)kSmA0, "accumulators");
+  static_assert(NB <= (int)kSmA0, "accumulator");
   static_assert(NB * 128 * 4 <= S * STAGE, "epilogue tile fits in the stage buffers");
   static_assert(SMEM <= 232448, "shared memory");
 };
@@ -142,22 +140,23 @@ __global__ void __launch_bounds__(kSmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
       constexpr uint32_t idesc = idesc_bf16_f32(128, NB);
+      const uint32_t lo0 = sw128_desc_lo(smem_u32(smem));  // stage s: lo0 + s * STAGE / 16
       // the decoders waited for each stage's landing before arriving on afull, so one wait
       // per pair covers both its A and its B
       for (int q = 0; 2 * q < nst; ++q) {
         const int pq = q % (C::S / 2);
         if (!mbar_wait_bounded(&afull[pq], (uint32_t)(q / (C::S / 2)) & 1u, a.status)) break;
         tc_fence_after();
-        for (int j = 2 * q; j < 2 * q + 2 && j < nst; ++j) {
-          const int s = j % C::S;
-          const uint32_t ta = tmem + kSmA0 + 32u * (uint32_t)s;
-          const uint32_t bbase = smem_u32(smem + s * C::STAGE);
+        const uint32_t s0 = 2u * (uint32_t)pq;  // the pair's stages s0, s0 + 1
+        const uint32_t ta = tmem + kSmA0 + 32u * s0, lo = lo0 + s0 * (uint32_t)(C::STAGE / 16);
+        if (q == 0) mma_bf16_ts_fast<false>(tmem, ta, lo, idesc);
+        else mma_bf16_ts_fast<true>(tmem, ta, lo, idesc);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int step = 4 * j + kk;
-            mma_bf16_ts(tmem + (uint32_t)((step % C::NACC) * NB), ta + kk * 8, sw128_desc(bbase + kk * 32), idesc,
-                        step >= C::NACC ? 1u : 0u);
-          }
+        for (int kk = 1; kk < 4; ++kk) mma_bf16_ts_fast<true>(tmem, ta + 8u * kk, lo + 2u * kk, idesc);
+        if (2 * q + 1 < nst) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ts_fast<true>(tmem, ta + 32u + 8u * kk, lo + (uint32_t)(C::STAGE / 16) + 2u * kk, idesc);
         }
         mma_commit(&empty[pq]);
       }
@@ -197,26 +196,19 @@ __global__ void __launch_bounds__(kSmThreads, 1)
       __syncwarp();
       if (lane == 0 && ok) mbar_arrive(&afull[pq]);
     }
-    // Phase 1 (warps 2-5): this row's accumulators, summed in a fixed order, scaled by the
-    // tensor scale, into the token-major fp32 tile [NB tokens][128 rows].
+    // Phase 1 (warps 2-5): this row of the accumulator, scaled by the tensor scale, into the
+    // token-major fp32 tile [NB tokens][128 rows].
     const bool go = mbar_wait_bounded(done, 0, a.status);
     float* sF = reinterpret_cast<float*>(smem);
     if (go && warp < 6) {
       tc_fence_after();
-      const int nacc = 4 * nst < C::NACC ? 4 * nst : C::NACC;
 #pragma unroll 1
       for (int c = 0; c < NB; c += 16) {
-        float sum[16];
-        for (int i = 0; i < 16; ++i) sum[i] = 0.0f;
-        for (int q = 0; q < nacc; ++q) {
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_base + (uint32_t)(q * NB + c), v);
-          tmem_ld_wait();
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_base + (uint32_t)c, v);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) sum[i] += __uint_as_float(v[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) sF[(c + i) * 128 + r] = a.ts * sum[i];
+        for (int i = 0; i < 16; ++i) sF[(c + i) * 128 + r] = a.ts * __uint_as_float(v[i]);
       }
     }
   }

@@ -142,18 +142,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
       constexpr uint32_t idesc = idesc_bf16_f32(128, kPfBN);
+      const uint32_t lo0 = sw128_desc_lo(smem_u32(smem));  // stage s: lo0 + s * kPfStageBytes / 16
       int s = 0;
       uint32_t ph = 0;
       // the decoders waited for the stage's landing before arriving on afull, so this one
-      // wait covers both operands
+      // wait covers both operands; the MMAs' operands are prepared outside the issue
       for (int kt = kt0; kt < kt1; ++kt) {
         if (!mbar_wait_bounded(&afull[s], ph, a.status)) break;
         tc_fence_after();
         const uint32_t ta = tmem + kPfA0 + 32u * (uint32_t)s;
-        const uint32_t bbase = smem_u32(smem + s * kPfStageBytes);
+        const uint32_t lo = lo0 + (uint32_t)s * (uint32_t)(kPfStageBytes / 16);
+        if (kt == kt0) mma_bf16_ts_fast<false>(tmem, ta, lo, idesc);
+        else mma_bf16_ts_fast<true>(tmem, ta, lo, idesc);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ts(tmem, ta + kk * 8, sw128_desc(bbase + kk * 32), idesc, ((kt - kt0) | kk) ? 1u : 0u);
+        for (int kk = 1; kk < 4; ++kk) mma_bf16_ts_fast<true>(tmem, ta + 8u * kk, lo + 2u * kk, idesc);
         mma_commit(&empty[s]);
         if (++s == kPfStages) {
           s = 0;

@@ -76,6 +76,25 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Low and high 32-bit halves of sw128_desc(smem_addr): the high half is the same for every
+// tile; advancing the low half by 2 moves the start 32 bytes (the next 16-wide K slice).
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t smem_addr) { return ((smem_addr & 0x3FFFFu) >> 4) | (1u << 16); }
+constexpr uint32_t kSw128DescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+
+// mma_bf16_ts with the accumulate decision fixed at compile time and the B descriptor given
+// as its two halves.  Only one thread issues MMAs, and a short MMA is issued faster than the
+// thread can compute its operands: measured on GB300 with operands prepared ahead, one thread
+// issues an M=128 K=16 MMA every ~48 cycles, and a single accumulator chain then keeps the
+// tensor pipe full from N = 128 up -- so the issuing code, not the chain, sets the pace.
+template <bool ACC>
+__device__ __forceinline__ void mma_bf16_ts_fast(uint32_t d_tmem, uint32_t a_tmem, uint32_t bdesc_lo, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b64 bd;\n\tmov.b64 bd, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, %5;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(bdesc_lo), "n"(kSw128DescHi), "r"(idesc), "n"(ACC ? 1 : 0)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
