@@ -14,10 +14,9 @@
 //   warp 1      allocates all 512 TMEM columns (accumulator 0-255, A ring 256-415) and
 //               issues tcgen05.mma (M=128, N=256, K=16, A from TMEM, B from shared memory,
 //               fp32 accumulate) from one lane; completion is committed to mbarriers.
-// A single accumulator chain at N = 256 with A in tensor memory keeps the tensor pipe ~90%
-// busy (consecutive MMAs into one accumulator wait on each other; at N = 256 that wait is
-// barely longer than the MMA itself), and the decoded weights cost no shared-memory
-// bandwidth.
+// With A in tensor memory the decoded weights cost no shared-memory bandwidth; one
+// accumulator chain at N = 256 can keep the tensor pipe full when the issuing thread has its
+// operands ready (its MMA descriptors are prepared outside the issue).
 // Every wait is bounded (QG_ERR_TIMEOUT in the workspace status word) and TMEM is freed
 // on every path.
 #include <cuda.h>

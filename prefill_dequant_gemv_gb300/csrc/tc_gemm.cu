@@ -26,11 +26,9 @@
 //                cp.async gather by row index into the 128-byte swizzled ring; each
 //                thread's copies arrive on the stage's mbarrier when they land, and the MMA
 //                thread fences these generic-proxy writes before the tensor cores read them
-// Two accumulators (one per row tile, 192 columns each) are two independent MMA chains per
-// 16-deep step: consecutive MMAs into one accumulator wait on each other, so a single chain
-// at N <= 192 leaves the tensor pipe idle part of the time, while two interleaved chains keep
-// it full.  Every wait is bounded (QG_ERR_TIMEOUT in the workspace status word) and TMEM is
-// freed on every path.
+// Two accumulators (one per row tile, 192 columns each): an item's two row tiles share each
+// stage's token rows, so the B operand is loaded once for both.  Every wait is bounded
+// (QG_ERR_TIMEOUT in the workspace status word) and TMEM is freed on every path.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
