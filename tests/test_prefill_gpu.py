@@ -92,3 +92,33 @@ def test_prefill_full_size_sampled(q):
     tol = oracle.tolerance(w, x[toks], rows=rows)
     err = np.abs(got[np.ix_(toks, rows)] - ref)
     assert np.all(err <= tol), f"{np.sum(err > tol)} out of tolerance"
+
+
+@pytest.mark.parametrize("n,k,t", [(17408, 5120, 128), (5120, 17408, 128), (5120, 17408, 300), (17408, 5120, 16)])
+def test_small_token_gemm_full_size_sampled(q, n, k, t):
+    """The benchmark matrices against one token tile (the small-token GEMM: 136 row tiles over
+    all of K, or 40 row tiles with K split over clusters of 3) and against 300 tokens (the
+    256-token GEMM with K split): sampled rows of every token against the oracle."""
+    w = wl.weight(wl.NVFP4, n, k, seed=0)
+    x = wl.activations(t, k, seed=5)
+    got, _ = _run(q, w, x, None)
+    rng = np.random.default_rng(6)
+    rows = np.unique(np.concatenate([[0, 127, 128, n - 1], rng.integers(0, n, 124)]))
+    ref, _ = oracle.gemv_rows(w, x, rows)
+    tol = oracle.tolerance(w, x, rows=rows)
+    err = np.abs(got[:, rows] - ref)
+    assert np.all(np.isfinite(got))
+    assert np.all(err <= tol), f"{np.sum(err > tol)} out of tolerance"
+
+
+@pytest.mark.parametrize("t", [5, 16, 17, 64, 65, 128, 129, 255, 256, 257])
+def test_token_count_boundaries(q, t):
+    """Every token-tile width of the small-token GEMM (16/32/64/128) and the switch to the
+    256-token GEMM, with a residual, on a weight whose few row tiles split K over clusters."""
+    w, x, res = wl.gemv_case(wl.NVFP4, 384, 1024, t, seed=60 + t, residual=True)
+    ws = q.Workspace(q.qg_gemm_workspace_size(wl.NVFP4, 384, 1024, t))
+    got, _ = _run(q, w, x, res, ws=ws)
+    ref, _ = oracle.gemv(w, x, res)
+    err = np.abs(got - ref)
+    assert np.all(err <= oracle.tolerance(w, x, res))
+    assert ws.status() == 0
