@@ -183,7 +183,8 @@ typedef struct {
   const void* dn_scales;
   const void* dn_aux;
   float tensor_scale;       /* NVFP4 tensor scale of the routed experts, else 1.0f */
-  int32_t has_shared;       /* 1: the shared expert below joins every token with weight 1 */
+  int32_t has_shared;       /* 1: the shared expert below joins every token (weight 1, or its
+                               sigmoid gate when the call passes gate logits) */
   qg_weight shared_gate_up; /* 2F x H */
   qg_weight shared_down;    /* H x F */
 } qg_moe_layer;
@@ -204,7 +205,13 @@ qg_status qmoe_route(const float* logits, int64_t t, int n_experts, int topk,
 size_t qmoe_workspace_size(const qg_moe_layer* layer, int64_t t, int topk);
 
 /* One MoE FFN layer after qmoe_route on the same logits:
- *   out[t] = bf16( sum_j topk_w[t][j] * down_e(h) + shared(h) ),
+ *   out[t] = bf16( sum_j topk_w[t][j] * down_e(h) + g_t * shared(h) ),
+ *   g_t = sigmoid(shared_gate[t]) = 1 / (1 + exp(-shared_gate[t])) in fp32 when the
+ *   shared expert's gate logits are given (TurboEXL3 article §4.2: the shared expert's
+ *   sigmoid gate), else 1.  shared_gate: fp32 [t] on the device, or NULL; non-NULL
+ *   without a shared expert is QG_ERR_INVALID_ARG.  Like the router's logits, the gate
+ *   logit (the 1-output projection of x) is the caller's input.  The gate multiplies the
+ *   shared expert's fp32 down output in the finish, before the single bf16 rounding.
  *   h = bf16(silu(gate) * up) per (token, expert), gate = rows 0..F-1 and up = rows
  *   F..2F-1 of the expert's 2F x H gate/up weight.
  * 1..4 tokens (decode / speculative verify; TurboEXL3 article §4.2): three launches --
@@ -219,7 +226,7 @@ size_t qmoe_workspace_size(const qg_moe_layer* layer, int64_t t, int topk);
  * bytes for this t) must be zero-filled before first use and not be shared by
  * overlapping calls.  Deterministic: no atomics in any sum. */
 qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t t, int64_t ldx, int topk,
-                   const float* topk_w, const void* route_ws, void* out, int64_t ldo,
+                   const float* topk_w, const float* shared_gate, const void* route_ws, void* out, int64_t ldo,
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* The MoE FFN one stage at a time (the grouped GEMM of the two stages, for callers that
@@ -231,7 +238,9 @@ qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t t, int64_t 
  *       with the gate/up rows of that pair's expert; row t*topk + i is token i's shared-expert
  *       h.  topk_w may be NULL.
  *   QG_MOE_DOWN_COMBINE: in = h [rows][ldi] as above; out = bf16 [t][ldo] (H columns),
- *       out[i] = bf16( sum_j topk_w[i][j] * down_e(h of pair (i, j)) + shared down(h) ).
+ *       out[i] = bf16( sum_j topk_w[i][j] * down_e(h of pair (i, j)) + g_i * shared down(h) ),
+ *       g_i from shared_gate as in qmoe_ffn (NULL: 1).  The gate/up stage ignores
+ *       shared_gate.
  * route_ws from qmoe_route on the same t, n_experts and topk.  The workspace holds
  * qgemm_grouped_workspace_size bytes (the qmoe_ffn size), zero-filled before first use.
  * Same limits and errors as qmoe_ffn; stage values other than the two return
@@ -239,7 +248,7 @@ qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t t, int64_t 
 typedef enum { QG_MOE_GATE_UP_SWIGLU = 1, QG_MOE_DOWN_COMBINE = 2 } qg_moe_stage;
 size_t qgemm_grouped_workspace_size(const qg_moe_layer* layer, int64_t t, int topk, int stage);
 qg_status qgemm_grouped(const qg_moe_layer* layer, int stage, const void* in, int64_t t, int64_t ldi, int topk,
-                        const float* topk_w, const void* route_ws, void* out, int64_t ldo,
+                        const float* topk_w, const float* shared_gate, const void* route_ws, void* out, int64_t ldo,
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace-free variant of qgemv, for callers that cannot allocate device memory:

@@ -23,5 +23,5 @@ from .formats import (  # noqa: F401
     bits_per_weight, q6k_half_operand_bits, dequant_operand_bf16,
 )
 from .gemv import gemv, gemv_rows, row_norms, tolerance  # noqa: F401
-from .moe import route, silu, swiglu_bf16, moe_forward, expert_ffn  # noqa: F401
+from .moe import route, sigmoid, silu, swiglu_bf16, moe_forward, expert_ffn  # noqa: F401
 from .layout import unpack, packed_sizes  # noqa: F401

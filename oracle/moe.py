@@ -14,9 +14,11 @@ Steps, in the order of the TurboEXL3 article §4.1 (prefill chain) and §4.2
    16-bit input of the down projection (§4.1 "Mid").
 4. Down: the expert's H x F projection of h, fp64.
 5. Finish: the score-weighted sum of each token's k expert outputs plus the
-   shared expert's output with weight 1 (reading: the pages name a sigmoid gate
-   for the shared expert but give no gate weights), rounded to bf16 once
-   (§4.1 "Finish", §4.2).
+   shared expert's output times its sigmoid gate, rounded to bf16 once (§4.1
+   "Finish"; §4.2 names the shared expert's sigmoid gate, a multiply and an add).
+   Reading: the gate is sigmoid(l_t) of one logit per token, which the caller
+   supplies as it supplies the router's logits; without gate logits the shared
+   expert enters with weight 1.
 """
 from __future__ import annotations
 
@@ -37,6 +39,13 @@ def route(logits, topk: int):
     z = np.exp(sel - sel[:, :1])
     p = z / z.sum(axis=1, keepdims=True)
     return order.astype(np.int64), p
+
+
+def sigmoid(l) -> np.ndarray:
+    """sigmoid(l) = 1 / (1 + exp(-l)) in fp64."""
+    l = np.asarray(l, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-l))
 
 
 def silu(g) -> np.ndarray:
@@ -62,10 +71,12 @@ def expert_ffn(gu_w32: np.ndarray, dn_w32: np.ndarray, x64: np.ndarray):
     return g, u, h, d
 
 
-def moe_forward(layer, x_bits, logits, topk: int, tokens=None, with_intermediates: bool = False):
+def moe_forward(layer, x_bits, logits, topk: int, tokens=None, with_intermediates: bool = False,
+                shared_gate=None):
     """out bits-exact fp64 values [len(tokens), H] for the selected tokens (all by default).
 
-    out[t] = RN_bf16( sum_j p[t, j] * down_{e_j}(h_{t, e_j}) + shared(h_{t, s}) )."""
+    out[t] = RN_bf16( sum_j p[t, j] * down_{e_j}(h_{t, e_j}) + g_t * shared(h_{t, s}) ),
+    g_t = sigmoid(shared_gate[t]) (fp32 logits [T]) or 1 when shared_gate is None."""
     x64_all = bf16_value(x_bits)
     ids, p = route(logits, topk)
     tokens = np.arange(x64_all.shape[0]) if tokens is None else np.asarray(tokens, dtype=np.int64)
@@ -82,7 +93,11 @@ def moe_forward(layer, x_bits, logits, topk: int, tokens=None, with_intermediate
                 inter[(int(tokens[r]), int(e))] = (g[i], u[i], h[i], d[i])
     if layer.shared_gate_up is not None:
         g, u, h, d = expert_ffn(dequant(layer.shared_gate_up), dequant(layer.shared_down), x64_all[tokens])
-        acc += d
+        if shared_gate is None:
+            acc += d
+        else:
+            lg = np.asarray(shared_gate, dtype=np.float32)[tokens]
+            acc += sigmoid(lg)[:, None] * d
         if with_intermediates:
             for i, t in enumerate(tokens):
                 inter[(int(t), -1)] = (g[i], u[i], h[i], d[i])

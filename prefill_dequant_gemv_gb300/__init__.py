@@ -62,9 +62,9 @@ _SIGNATURES = {
     "qmoe_route_workspace_size": (_SZ, [_I64, _I, _I]),
     "qmoe_route": (_I, [_P, _I64, _I, _I, _P, _P, _P, _SZ, _P]),
     "qmoe_workspace_size": (_SZ, [ctypes.POINTER(qg_moe_layer), _I64, _I]),
-    "qmoe_ffn": (_I, [ctypes.POINTER(qg_moe_layer), _P, _I64, _I64, _I, _P, _P, _P, _I64, _P, _SZ, _P]),
+    "qmoe_ffn": (_I, [ctypes.POINTER(qg_moe_layer), _P, _I64, _I64, _I, _P, _P, _P, _P, _I64, _P, _SZ, _P]),
     "qgemm_grouped_workspace_size": (_SZ, [ctypes.POINTER(qg_moe_layer), _I64, _I, _I]),
-    "qgemm_grouped": (_I, [ctypes.POINTER(qg_moe_layer), _I, _P, _I64, _I64, _I, _P, _P, _P, _I64, _P, _SZ, _P]),
+    "qgemm_grouped": (_I, [ctypes.POINTER(qg_moe_layer), _I, _P, _I64, _I64, _I, _P, _P, _P, _P, _I64, _P, _SZ, _P]),
     "qg_selftest_wait_timeout": (_I, [_P, _SZ, _P]),
 }
 
@@ -162,10 +162,10 @@ def qmoe_workspace_size(layer: qg_moe_layer, t: int, topk: int) -> int:
     return lib().qmoe_workspace_size(ctypes.byref(layer), t, topk)
 
 
-def qmoe_ffn(layer: qg_moe_layer, x_ptr: int, t: int, ldx: int, topk: int, w_ptr: int, route_ws_ptr: int,
-             out_ptr: int, ldo: int, ws_ptr: int, ws_bytes: int, stream: int = 0):
-    _check(lib().qmoe_ffn(ctypes.byref(layer), x_ptr, t, ldx, topk, w_ptr, route_ws_ptr, out_ptr, ldo, ws_ptr,
-                          ws_bytes, stream), "qmoe_ffn")
+def qmoe_ffn(layer: qg_moe_layer, x_ptr: int, t: int, ldx: int, topk: int, w_ptr: int, gate_ptr: Optional[int],
+             route_ws_ptr: int, out_ptr: int, ldo: int, ws_ptr: int, ws_bytes: int, stream: int = 0):
+    _check(lib().qmoe_ffn(ctypes.byref(layer), x_ptr, t, ldx, topk, w_ptr, gate_ptr, route_ws_ptr, out_ptr, ldo,
+                          ws_ptr, ws_bytes, stream), "qmoe_ffn")
 
 
 def qgemm_grouped_workspace_size(layer: qg_moe_layer, t: int, topk: int, stage: int) -> int:
@@ -173,9 +173,10 @@ def qgemm_grouped_workspace_size(layer: qg_moe_layer, t: int, topk: int, stage: 
 
 
 def qgemm_grouped(layer: qg_moe_layer, stage: int, in_ptr: int, t: int, ldi: int, topk: int, w_ptr: Optional[int],
-                  route_ws_ptr: int, out_ptr: int, ldo: int, ws_ptr: int, ws_bytes: int, stream: int = 0):
-    _check(lib().qgemm_grouped(ctypes.byref(layer), stage, in_ptr, t, ldi, topk, w_ptr, route_ws_ptr, out_ptr, ldo,
-                               ws_ptr, ws_bytes, stream), "qgemm_grouped")
+                  gate_ptr: Optional[int], route_ws_ptr: int, out_ptr: int, ldo: int, ws_ptr: int, ws_bytes: int,
+                  stream: int = 0):
+    _check(lib().qgemm_grouped(ctypes.byref(layer), stage, in_ptr, t, ldi, topk, w_ptr, gate_ptr, route_ws_ptr,
+                               out_ptr, ldo, ws_ptr, ws_bytes, stream), "qgemm_grouped")
 
 
 def qgemv_static_ws(w: qg_weight, x_ptr: int, m: int, ldx: int, res_ptr: Optional[int], ldr: int, y_ptr: int,
@@ -326,9 +327,11 @@ def route(logits, topk: int, workspace: Optional[Workspace] = None):
     return ids, w, workspace
 
 
-def moe_ffn(pm: PackedMoE, x, topk_w, route_ws: Workspace, out=None, workspace: Optional[Workspace] = None):
+def moe_ffn(pm: PackedMoE, x, topk_w, route_ws: Workspace, out=None, workspace: Optional[Workspace] = None,
+            shared_gate=None):
     """One MoE FFN layer for the routed tokens x bf16 [t, H]: 1..4 tokens take the grouped-GEMV
-    decode chain, more tokens the grouped tensor-core prefill chain."""
+    decode chain, more tokens the grouped tensor-core prefill chain.  shared_gate: fp32 [t]
+    gate logits of the shared expert (its output is weighed by their sigmoid), or None."""
     import torch
     t = x.shape[0]
     topk = topk_w.shape[1]
@@ -336,16 +339,18 @@ def moe_ffn(pm: PackedMoE, x, topk_w, route_ws: Workspace, out=None, workspace: 
         out = torch.empty((t, (pm.hidden + 7) // 8 * 8), dtype=torch.bfloat16, device=x.device)[:, :pm.hidden]
     if workspace is None:
         workspace = Workspace(qmoe_workspace_size(pm.desc, t, topk), x.device)
-    qmoe_ffn(pm.desc, x.data_ptr(), t, x.stride(0), topk, topk_w.data_ptr(), route_ws.ptr, out.data_ptr(),
+    qmoe_ffn(pm.desc, x.data_ptr(), t, x.stride(0), topk, topk_w.data_ptr(),
+             None if shared_gate is None else shared_gate.data_ptr(), route_ws.ptr, out.data_ptr(),
              out.stride(0), workspace.ptr, workspace.nbytes, _stream_ptr())
     return out
 
 
 def moe_stage(pm: PackedMoE, stage: int, inp, t: int, topk: int, route_ws: Workspace, topk_w=None, out=None,
-              workspace: Optional[Workspace] = None):
+              workspace: Optional[Workspace] = None, shared_gate=None):
     """One stage of the MoE FFN (qgemm_grouped): QG_MOE_GATE_UP_SWIGLU takes x bf16 [t, H] and
     returns h bf16 [t*topk + (t if shared), F] in the router's grouped row order;
-    QG_MOE_DOWN_COMBINE takes that h and topk_w and returns out bf16 [t, H]."""
+    QG_MOE_DOWN_COMBINE takes that h, topk_w and optionally the shared expert's gate logits and
+    returns out bf16 [t, H]."""
     import torch
     rows = t * topk + (t if pm.desc.has_shared else 0)
     cols = pm.ffn if stage == QG_MOE_GATE_UP_SWIGLU else pm.hidden
@@ -355,6 +360,7 @@ def moe_stage(pm: PackedMoE, stage: int, inp, t: int, topk: int, route_ws: Works
     if workspace is None:
         workspace = Workspace(qgemm_grouped_workspace_size(pm.desc, t, topk, stage), inp.device)
     qgemm_grouped(pm.desc, stage, inp.data_ptr(), t, inp.stride(0), topk,
-                  None if topk_w is None else topk_w.data_ptr(), route_ws.ptr, out.data_ptr(), out.stride(0),
-                  workspace.ptr, workspace.nbytes, _stream_ptr())
+                  None if topk_w is None else topk_w.data_ptr(),
+                  None if shared_gate is None else shared_gate.data_ptr(), route_ws.ptr, out.data_ptr(),
+                  out.stride(0), workspace.ptr, workspace.nbytes, _stream_ptr())
     return out

@@ -202,12 +202,14 @@ extern "C" size_t qmoe_workspace_size(const qg_moe_layer* layer, int64_t t, int 
 }
 
 extern "C" qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t t, int64_t ldx, int topk,
-                              const float* topk_w, const void* route_ws, void* out, int64_t ldo, void* workspace,
-                              size_t workspace_bytes, void* stream) {
+                              const float* topk_w, const float* shared_gate, const void* route_ws, void* out,
+                              int64_t ldo, void* workspace, size_t workspace_bytes, void* stream) {
   Geometry gu, dn;
   int st = check_moe(layer, t, topk, &gu, &dn);
   if (st != QG_OK) return (qg_status)st;
   if (!x || !topk_w || !route_ws || !out || !workspace) return QG_ERR_INVALID_ARG;
+  if (shared_gate && !layer->has_shared) return QG_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(shared_gate) % 4) return QG_ERR_MISALIGNED;
   // the prefill chain pairs gate rows f.. with up rows F+f.. inside one 128-row tile and
   // finishes four features at a time
   if (t > 4 && (layer->ffn % 128 != 0 || layer->hidden % 8 != 0)) return QG_ERR_UNSUPPORTED;
@@ -221,10 +223,10 @@ extern "C" qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t 
   if (workspace_bytes < moe_layout(gu, dn, t, layer->n_experts, topk, dev.sms).total)
     return QG_ERR_WORKSPACE_TOO_SMALL;
   if (t > 4)
-    return (qg_status)launch_moe_prefill(layer, gu, dn, x, t, ldx, topk, topk_w, route_ws, out, ldo, workspace, dev,
-                                         stream, kMoeAll);
-  return (qg_status)launch_moe_decode(layer, gu, dn, x, t, ldx, topk, topk_w, route_ws, out, ldo, workspace, dev,
-                                      stream, kMoeAll);
+    return (qg_status)launch_moe_prefill(layer, gu, dn, x, t, ldx, topk, topk_w, shared_gate, route_ws, out, ldo,
+                                         workspace, dev, stream, kMoeAll);
+  return (qg_status)launch_moe_decode(layer, gu, dn, x, t, ldx, topk, topk_w, shared_gate, route_ws, out, ldo,
+                                      workspace, dev, stream, kMoeAll);
 }
 
 extern "C" size_t qgemm_grouped_workspace_size(const qg_moe_layer* layer, int64_t t, int topk, int stage) {
@@ -233,13 +235,16 @@ extern "C" size_t qgemm_grouped_workspace_size(const qg_moe_layer* layer, int64_
 }
 
 extern "C" qg_status qgemm_grouped(const qg_moe_layer* layer, int stage, const void* in, int64_t t, int64_t ldi,
-                                   int topk, const float* topk_w, const void* route_ws, void* out, int64_t ldo,
-                                   void* workspace, size_t workspace_bytes, void* stream) {
+                                   int topk, const float* topk_w, const float* shared_gate, const void* route_ws,
+                                   void* out, int64_t ldo, void* workspace, size_t workspace_bytes, void* stream) {
   Geometry gu, dn;
   int st = check_moe(layer, t, topk, &gu, &dn);
   if (st != QG_OK) return (qg_status)st;
   if (stage != QG_MOE_GATE_UP_SWIGLU && stage != QG_MOE_DOWN_COMBINE) return QG_ERR_INVALID_ARG;
   if (!in || !route_ws || !out || !workspace || (stage == QG_MOE_DOWN_COMBINE && !topk_w)) return QG_ERR_INVALID_ARG;
+  if (shared_gate && !layer->has_shared) return QG_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(shared_gate) % 4) return QG_ERR_MISALIGNED;
+  if (stage == QG_MOE_GATE_UP_SWIGLU) shared_gate = nullptr;
   if (t > 4 && (layer->ffn % 128 != 0 || layer->hidden % 8 != 0)) return QG_ERR_UNSUPPORTED;
   if (t * (int64_t)(topk + 1) >= ((int64_t)1 << 31)) return QG_ERR_UNSUPPORTED;
   // gate/up: in = x [t][H], out = h [rows][F]; down: in = h [rows][F], out = [t][H]
@@ -256,8 +261,8 @@ extern "C" qg_status qgemm_grouped(const qg_moe_layer* layer, int stage, const v
     return QG_ERR_WORKSPACE_TOO_SMALL;
   const int ms = stage == QG_MOE_GATE_UP_SWIGLU ? kMoeGateUp : kMoeDown;
   if (t > 4)
-    return (qg_status)launch_moe_prefill(layer, gu, dn, in, t, ldi, topk, topk_w, route_ws, out, ldo, workspace, dev,
-                                         stream, ms);
-  return (qg_status)launch_moe_decode(layer, gu, dn, in, t, ldi, topk, topk_w, route_ws, out, ldo, workspace, dev,
-                                      stream, ms);
+    return (qg_status)launch_moe_prefill(layer, gu, dn, in, t, ldi, topk, topk_w, shared_gate, route_ws, out, ldo,
+                                         workspace, dev, stream, ms);
+  return (qg_status)launch_moe_decode(layer, gu, dn, in, t, ldi, topk, topk_w, shared_gate, route_ws, out, ldo,
+                                      workspace, dev, stream, ms);
 }

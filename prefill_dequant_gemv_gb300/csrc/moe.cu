@@ -434,11 +434,12 @@ __global__ void __launch_bounds__(256) mid_kernel(const float* gu, int64_t ldg, 
   *reinterpret_cast<uint32_t*>(h + r * ldh + f) = swiglu_bf16x2(g.x, u.x, g.y, u.y);
 }
 
-// out[t][n] = bf16( sum_j w[t][j] * d[pos(t, j)][n] + d[T*topk + t][n] ), fixed order, four
-// features per thread; every load of a thread is issued before the first multiply-add.
+// out[t][n] = bf16( sum_j w[t][j] * d[pos(t, j)][n] + g_t * d[T*topk + t][n] ), fixed order,
+// four features per thread (g_t: the shared expert's sigmoid gate, or 1); every load of a
+// thread is issued before the first multiply-add.
 __global__ void __launch_bounds__(256) finish_kernel(const float* d, int64_t ldd, const float* w, const int* pair_pos,
-                                                     int T, int topk, int has_shared, int64_t H, __nv_bfloat16* out,
-                                                     int64_t ldo) {
+                                                     int T, int topk, int has_shared, const float* shared_gate,
+                                                     int64_t H, __nv_bfloat16* out, int64_t ldo) {
   pdl_launch_dependents();
   pdl_wait();
   const int64_t H4 = H / 4;
@@ -470,10 +471,11 @@ __global__ void __launch_bounds__(256) finish_kernel(const float* d, int64_t ldd
     }
   }
   if (has_shared) {
-    acc.x += sh.x;
-    acc.y += sh.y;
-    acc.z += sh.z;
-    acc.w += sh.w;
+    const float g = shared_gate_weight(shared_gate, t);
+    acc.x = fmaf(g, sh.x, acc.x);
+    acc.y = fmaf(g, sh.y, acc.y);
+    acc.z = fmaf(g, sh.z, acc.z);
+    acc.w = fmaf(g, sh.w, acc.w);
   }
   const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
   uint2 pk;
@@ -557,8 +559,8 @@ static int launch_grouped(int fmt, const GroupedArgs& a0, int nrows, int KG, con
 }
 
 int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
-                      int64_t ldx, int topk, const float* topk_w, const void* route_ws, void* out, int64_t ldo,
-                      void* ws, const DeviceInfo& dev, void* stream, int stage) {
+                      int64_t ldx, int topk, const float* topk_w, const float* shared_gate, const void* route_ws,
+                      void* out, int64_t ldo, void* ws, const DeviceInfo& dev, void* stream, int stage) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const RouteView rv = route_view(const_cast<void*>(route_ws), T, m->n_experts, topk);
   const MoeLayout L = moe_layout(gu, dn, T, m->n_experts, topk, dev.sms);
@@ -642,7 +644,7 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
 
   if (launch_pdl(finish_kernel, dim3((unsigned)((T * (dn.n / 4) + 255) / 256)), dim3(256), 0, s,
                  (const float*)reinterpret_cast<const float*>(w + L.d), (int64_t)L.ld_d, topk_w,
-                 (const int*)rv.pair_pos, (int)T, topk, (int)m->has_shared, (int64_t)dn.n,
+                 (const int*)rv.pair_pos, (int)T, topk, (int)m->has_shared, shared_gate, (int64_t)dn.n,
                  static_cast<__nv_bfloat16*>(out), ldo) != cudaSuccess)
     return QG_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;

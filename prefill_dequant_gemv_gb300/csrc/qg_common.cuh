@@ -124,4 +124,13 @@ __device__ __forceinline__ uint32_t i6_op_hi(uint32_t w, uint32_t h) {
   return (w & 0x00F000F0u) | (h & 0x03000300u) | 0x3C003C00u;
 }
 
+// ---------------------------------------------------------------- MoE finish
+// Weight of the shared expert's output for one token: its sigmoid gate
+// 1 / (1 + e^-l) in fp32 from the gate logit l (TurboEXL3 article §4.2), or 1 when the
+// caller passes no gate logits.
+__device__ __forceinline__ float shared_gate_weight(const float* gate_logits, int t) {
+  if (!gate_logits) return 1.0f;
+  return 1.0f / (1.0f + expf(-gate_logits[t]));
+}
+
 }  // namespace qg

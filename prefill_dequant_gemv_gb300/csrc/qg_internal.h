@@ -68,12 +68,14 @@ struct MoeLayout {
 MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, int topk, int grid);
 // MoE chains: the whole FFN (kMoeAll: x -> out), or one stage of it -- kMoeGateUp: x -> h
 // (bf16 [rows][ldo], grouped rows then the shared expert's), kMoeDown: h (x, ldx) -> out.
+// shared_gate: fp32 gate logits [T] of the shared expert (its output is weighed by their
+// sigmoid in the finish) or null (weight 1).
 enum MoeStage { kMoeAll = 0, kMoeGateUp = 1, kMoeDown = 2 };
 int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
-                      int64_t ldx, int topk, const float* topk_w, const void* route_ws, void* out, int64_t ldo,
-                      void* ws, const DeviceInfo& dev, void* stream, int stage);
+                      int64_t ldx, int topk, const float* topk_w, const float* shared_gate, const void* route_ws,
+                      void* out, int64_t ldo, void* ws, const DeviceInfo& dev, void* stream, int stage);
 int launch_moe_prefill(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
-                       int64_t ldx, int topk, const float* topk_w, const void* route_ws, void* out, int64_t ldo,
-                       void* ws, const DeviceInfo& dev, void* stream, int stage);
+                       int64_t ldx, int topk, const float* topk_w, const float* shared_gate, const void* route_ws,
+                       void* out, int64_t ldo, void* ws, const DeviceInfo& dev, void* stream, int stage);
 
 }  // namespace qg

@@ -448,11 +448,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   }
 }
 
-// out[t][n] = bf16( sum_j w[t][j] * d[pos(t, j)][n] + d[T*topk + t][n] ), fixed order, four
-// features per thread (TurboEXL3 article §4.1 "Finish").
+// out[t][n] = bf16( sum_j w[t][j] * d[pos(t, j)][n] + g_t * d[T*topk + t][n] ), fixed order,
+// four features per thread (TurboEXL3 article §4.1 "Finish"; g_t: the shared expert's
+// sigmoid gate, §4.2, or 1).
 __global__ void __launch_bounds__(256) moe_finish4_kernel(const float* d, int64_t ldd, const float* w,
                                                           const int* pair_pos, int T, int topk, int has_shared,
-                                                          int64_t H, __nv_bfloat16* out, int64_t ldo) {
+                                                          const float* shared_gate, int64_t H, __nv_bfloat16* out,
+                                                          int64_t ldo) {
   const int64_t H4 = H / 4;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (int64_t)T * H4) return;
@@ -469,10 +471,11 @@ __global__ void __launch_bounds__(256) moe_finish4_kernel(const float* d, int64_
   }
   if (has_shared) {
     const float4 v = __ldcs(reinterpret_cast<const float4*>(d + (int64_t)(T * topk + t) * ldd + n));
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
+    const float g = shared_gate_weight(shared_gate, t);
+    acc.x = fmaf(g, v.x, acc.x);
+    acc.y = fmaf(g, v.y, acc.y);
+    acc.z = fmaf(g, v.z, acc.z);
+    acc.w = fmaf(g, v.w, acc.w);
   }
   __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
   uint2 pk;
@@ -546,8 +549,8 @@ int tiles_of(int64_t t) { return (int)((t + kTcTile - 1) / kTcTile); }
 }  // namespace
 
 int launch_moe_prefill(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
-                       int64_t ldx, int topk, const float* topk_w, const void* route_ws, void* out, int64_t ldo,
-                       void* ws, const DeviceInfo& dev, void* stream, int stage) {
+                       int64_t ldx, int topk, const float* topk_w, const float* shared_gate, const void* route_ws,
+                       void* out, int64_t ldo, void* ws, const DeviceInfo& dev, void* stream, int stage) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const RouteView rv = route_view(const_cast<void*>(route_ws), T, m->n_experts, topk);
   const MoeLayout L = moe_layout(gu, dn, T, m->n_experts, topk, dev.sms);
@@ -624,7 +627,7 @@ int launch_moe_prefill(const qg_moe_layer* m, const Geometry& gu, const Geometry
   const int64_t H = dn.n;
   const int64_t n4 = T * (H / 4);
   moe_finish4_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
-      reinterpret_cast<const float*>(w + L.d), L.ld_d, topk_w, rv.pair_pos, (int)T, topk, m->has_shared, H,
+      reinterpret_cast<const float*>(w + L.d), L.ld_d, topk_w, rv.pair_pos, (int)T, topk, m->has_shared, shared_gate, H,
       static_cast<__nv_bfloat16*>(out), ldo);
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }

@@ -278,6 +278,39 @@ def check_silu(o, seed=23):
     assert np.allclose(o.silu(g), ref, rtol=1e-14, atol=0)
 
 
+def check_sigmoid(o, seed=24):
+    """sigmoid(0) = 1/2, the symmetry sigmoid(l) + sigmoid(-l) = 1, saturation, and the
+    library routine on random logits."""
+    assert o.sigmoid(np.array([0.0]))[0] == 0.5
+    assert o.sigmoid(np.array([800.0]))[0] == 1.0 and o.sigmoid(np.array([-800.0]))[0] == 0.0
+    l = np.random.default_rng(seed).standard_normal(1000) * 8
+    assert np.allclose(o.sigmoid(l) + o.sigmoid(-l), 1.0, rtol=0, atol=1e-15)
+    ref = torch.sigmoid(torch.from_numpy(l)).numpy()
+    assert np.allclose(o.sigmoid(l), ref, rtol=1e-14, atol=0)
+
+
+def check_moe_shared_gate(o, seed=30):
+    """The shared expert's sigmoid gate scales only the shared expert's output: with the
+    routed-only sum a_r (no shared expert) and the ungated sum a_s, the gated sum is
+    a_r + sigmoid(l) (a_s - a_r) per token; a zero logit halves the shared output, and a
+    very large logit gives the ungated layer."""
+    layer = wl.moe_layer(wl.MXFP4, 6, 64, 32, seed=seed, shared=True)
+    routed = wl.MoELayer(layer.fmt, 6, 64, 32, layer.gate_up, layer.down, None, None)
+    x = wl.moe_tokens(4, 64, seed=seed)
+    lg = wl.router_logits(4, 6, seed=seed)
+    gate = np.array([0.0, 1.5, -2.25, 100.0], np.float32)
+    a_r = o.moe_forward(routed, x, lg, topk=2, with_intermediates=True)[1]
+    a_s = o.moe_forward(layer, x, lg, topk=2, with_intermediates=True)[1]
+    out, a_g = o.moe_forward(layer, x, lg, topk=2, with_intermediates=True, shared_gate=gate)[:2]
+    sg = 1.0 / (1.0 + np.exp(-gate.astype(np.float64)))
+    assert np.allclose(a_g, a_r + sg[:, None] * (a_s - a_r), rtol=1e-12, atol=1e-12)
+    assert np.allclose(a_g[0], a_r[0] + 0.5 * (a_s[0] - a_r[0]), rtol=1e-12, atol=1e-12)
+    assert np.array_equal(a_g[3], a_s[3])
+    assert np.array_equal(out, o.round_to_bf16(a_g))
+    ungated = o.moe_forward(layer, x, lg, topk=2)
+    assert np.array_equal(o.moe_forward(layer, x, lg, topk=2, shared_gate=np.full(4, 100.0, np.float32)), ungated)
+
+
 def check_moe_composition(o, seed=29):
     """The MoE chain against the dense GEMV oracle: top-1 routing (p = 1) through one
     expert equals gate/up GEMV -> SwiGLU -> down GEMV, and relabelling the experts

@@ -135,14 +135,14 @@ def test_qgemm_grouped_host_validation(q):
     """Argument errors of the staged MoE call come back before any device work."""
     L = q.lib()
     m = _moe_desc(q)
-    args = dict(stage=q.QG_MOE_GATE_UP_SWIGLU, inp=0x3000, t=4, ldi=256, topk=2, w=0x6000, rws=0x7000, out=0x8000,
-                ldo=128, ws=0x9000, wsb=1 << 24)
+    args = dict(stage=q.QG_MOE_GATE_UP_SWIGLU, inp=0x3000, t=4, ldi=256, topk=2, w=0x6000, gate=None, rws=0x7000,
+                out=0x8000, ldo=128, ws=0x9000, wsb=1 << 24)
 
     def call(layer=m, **kw):
         a = dict(args)
         a.update(kw)
         return L.qgemm_grouped(ctypes.byref(layer), a["stage"], a["inp"], a["t"], a["ldi"], a["topk"], a["w"],
-                               a["rws"], a["out"], a["ldo"], a["ws"], a["wsb"], None)
+                               a["gate"], a["rws"], a["out"], a["ldo"], a["ws"], a["wsb"], None)
 
     assert call(stage=3) == 1                                   # unknown stage
     assert call(stage=0) == 1
@@ -155,4 +155,11 @@ def test_qgemm_grouped_host_validation(q):
     assert call(topk=9) == 1                                    # more than the experts
     assert call(layer=_moe_desc(q, n_experts=32), topk=17) == 2  # above the router's limit
     assert call(t=0) == 1
+    assert call(gate=0xA000) == 1                               # gate logits without a shared expert
+    sh = _moe_desc(q, has_shared=1,
+                   shared_gate_up=q.qg_weight(fmt=wl.MXFP4, n=256, k=256, codes=0x50000, scales=0x51000,
+                                              tensor_scale=1.0),
+                   shared_down=q.qg_weight(fmt=wl.MXFP4, n=256, k=128, codes=0x52000, scales=0x53000,
+                                           tensor_scale=1.0))
+    assert call(layer=sh, gate=0xA002) == 3                     # misaligned gate logits
     assert L.qgemm_grouped_workspace_size(ctypes.byref(m), 4, 2, 3) == 0

@@ -139,3 +139,31 @@ def test_moe_decode_staged(q, fmt, t, shared):
     err = np.abs(to_f64(h) - href)
     tol = h_tolerance(oracle, layer, x, inter, rows)
     assert np.all(err <= tol), f"{np.sum(err > tol)} h values out of tolerance"
+
+
+@pytest.mark.parametrize("fmt,t", [(wl.MXFP4, 1), (wl.MXFP4, 4), (wl.NVFP4, 3)])
+def test_moe_decode_shared_gate(q, fmt, t):
+    """The shared expert weighed by its sigmoid gate (fp32 logits per token): against the
+    oracle, the staged chain bit-identical to the fused one, and a saturated gate (+100)
+    bit-identical to no gate."""
+    E, H, F, k = 16, 256, 128, 4
+    layer = wl.moe_layer(fmt, E, H, F, seed=330 + t, shared=True)
+    x = wl.moe_tokens(t, H, seed=331)
+    lg = wl.router_logits(t, E, seed=332)
+    gl = wl.shared_gate_logits(t, seed=333)
+    pm = q.PackedMoE(layer)
+    ids, w, rws = q.route(torch.from_numpy(lg).cuda(), k)
+    xd = dev_bf16(x)
+    gd = torch.from_numpy(gl).cuda()
+    out = q.moe_ffn(pm, xd, w, rws, shared_gate=gd)
+    h = q.moe_stage(pm, q.QG_MOE_GATE_UP_SWIGLU, xd, t, k, rws)
+    staged = q.moe_stage(pm, q.QG_MOE_DOWN_COMBINE, h, t, k, rws, topk_w=w, shared_gate=gd)
+    sat = q.moe_ffn(pm, xd, w, rws, shared_gate=torch.full((t,), 100.0, device="cuda"))
+    plain = q.moe_ffn(pm, xd, w, rws)
+    torch.cuda.synchronize()
+    assert torch.equal(staged.view(torch.int16), out.view(torch.int16))
+    assert torch.equal(sat.view(torch.int16), plain.view(torch.int16))
+    ref = oracle.moe_forward(layer, x, lg, k, shared_gate=gl)
+    tol = moe_tolerance(oracle, layer, x, lg, k, ref)
+    err = np.abs(to_f64(out) - ref)
+    assert np.all(err <= tol), f"{np.sum(err > tol)} out of tolerance, worst {np.max(err - tol)}"

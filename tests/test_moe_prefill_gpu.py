@@ -141,3 +141,29 @@ def test_moe_prefill_staged(q, fmt, shared):
     rows = grouped_rows(ids.cpu().numpy(), shared)
     href = np.stack([inter[r][2] for r in rows])
     _check(to_f64(h), href, h_tolerance(oracle, layer, x, inter, rows))
+
+
+@pytest.mark.parametrize("fmt", [wl.MXFP4, wl.Q6K])
+def test_moe_prefill_shared_gate(q, fmt):
+    """The shared expert weighed by its sigmoid gate on the tensor-core chain: against the
+    oracle, staged = fused bit for bit, a saturated gate (+100) = no gate bit for bit."""
+    E, k, t = 16, 4, 200
+    H, F = (512, 256) if fmt == wl.Q6K else (256, 128)
+    layer = wl.moe_layer(fmt, E, H, F, seed=440 + fmt, shared=True)
+    x = wl.moe_tokens(t, H, seed=441)
+    lg = wl.router_logits(t, E, seed=442)
+    gl = wl.shared_gate_logits(t, seed=443)
+    pm = q.PackedMoE(layer)
+    ids, w, rws = q.route(torch.from_numpy(lg).cuda(), k)
+    xd = dev_bf16(x)
+    gd = torch.from_numpy(gl).cuda()
+    out = q.moe_ffn(pm, xd, w, rws, shared_gate=gd)
+    h = q.moe_stage(pm, q.QG_MOE_GATE_UP_SWIGLU, xd, t, k, rws)
+    staged = q.moe_stage(pm, q.QG_MOE_DOWN_COMBINE, h, t, k, rws, topk_w=w, shared_gate=gd)
+    sat = q.moe_ffn(pm, xd, w, rws, shared_gate=torch.full((t,), 100.0, device="cuda"))
+    plain = q.moe_ffn(pm, xd, w, rws)
+    torch.cuda.synchronize()
+    assert torch.equal(staged.view(torch.int16), out.view(torch.int16))
+    assert torch.equal(sat.view(torch.int16), plain.view(torch.int16))
+    ref = oracle.moe_forward(layer, x, lg, k, shared_gate=gl)
+    _check(to_f64(out), ref, moe_tolerance(oracle, layer, x, lg, k, ref))

@@ -161,3 +161,28 @@ def test_moe_swiglu_swapped(monkeypatch):
     orig = MO.swiglu_bf16
     monkeypatch.setattr(MO, "swiglu_bf16", lambda g, u: orig(u, g))
     assert _fails(pins.check_moe_composition, oracle)
+
+
+def test_sigmoid_sign_flipped(monkeypatch):
+    orig = MO.sigmoid
+    monkeypatch.setattr(MO, "sigmoid", lambda l: orig(-np.asarray(l, np.float64)))
+    monkeypatch.setattr(oracle, "sigmoid", lambda l: orig(-np.asarray(l, np.float64)))
+    assert _fails(pins.check_sigmoid, oracle)
+    assert _fails(pins.check_moe_shared_gate, oracle)
+
+
+def test_shared_gate_on_the_routed_sum(monkeypatch):
+    orig = MO.moe_forward
+
+    def bad(layer, x, lg, topk, tokens=None, with_intermediates=False, shared_gate=None):
+        if shared_gate is None or layer.shared_gate_up is None:
+            return orig(layer, x, lg, topk, tokens, with_intermediates)
+        routed = wl.MoELayer(layer.fmt, layer.n_experts, layer.hidden, layer.ffn, layer.gate_up, layer.down, None, None)
+        a_r = orig(routed, x, lg, topk, tokens, True)[1]
+        a_s = orig(layer, x, lg, topk, tokens, True)
+        g = MO.sigmoid(np.asarray(shared_gate, np.float32))[:, None]
+        acc = g * a_r + (a_s[1] - a_r)  # the gate on the routed experts instead of the shared one
+        out = F.round_to_bf16(acc)
+        return (out, acc) + tuple(a_s[2:]) if with_intermediates else out
+    monkeypatch.setattr(oracle, "moe_forward", bad)
+    assert _fails(pins.check_moe_shared_gate, oracle)

@@ -64,6 +64,14 @@ def test_silu():
     pins.check_silu(oracle)
 
 
+def test_sigmoid():
+    pins.check_sigmoid(oracle)
+
+
+def test_moe_shared_gate():
+    pins.check_moe_shared_gate(oracle)
+
+
 def test_moe_chain_composition():
     pins.check_moe_composition(oracle)
 

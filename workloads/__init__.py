@@ -165,6 +165,17 @@ def router_logits(t: int, n_experts: int, seed: int = 0, sets: int = 1) -> np.nd
     return a[0] if sets == 1 else a
 
 
+def shared_gate_logits(t: int, seed: int = 0) -> np.ndarray:
+    """fp32 N(0, 2^2) gate logits [t] of the shared expert (one per token); the first is 0
+    and, from four tokens on, the fourth is +30 (a saturated gate) when t allows."""
+    a = (streams(seed)["logits"].standard_normal(size=t, dtype=np.float32) * np.float32(2.0)).astype(np.float32)
+    if t > 0:
+        a[0] = 0.0
+    if t > 3:
+        a[3] = 30.0
+    return a
+
+
 def moe_tokens(t: int, hidden: int, seed: int = 0) -> np.ndarray:
     """bf16 bits [t, hidden] of the MoE layer input."""
     return activations(t, hidden, seed, stream="x")
