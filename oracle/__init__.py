@@ -14,13 +14,14 @@ the source pages it follows:
   for modern Macs), §2.1 block-scaled formats, §2.2 W4A16, §4.1 prefill chain,
   §4.2 decode chain, §4.4 numerics.
 * "Q6_K operand PR" (perf: Q6_K's zero point in the operands of the Apple7/8
-  register decode tile, #19), "What changed" and its commit message.
+  register decode tile, #19), "What changed" and its commit messages (the 5-bit
+  nibble operand of Q5_K, Q5_1 and Q5_0).
 
 Parity pins for every function live in ``tests/test_oracle_pins.py``.
 """
 from .formats import (  # noqa: F401
     e2m1_value, e8m0_value, e4m3fn_value, bf16_value, bf16_bits_of, round_to_bf16, dequant, dequant_rows,
-    bits_per_weight, q6k_half_operand_bits, dequant_operand_bf16,
+    bits_per_weight, q6k_half_operand_bits, q5_half_operand_bits, dequant_operand_bf16,
 )
 from .gemv import gemv, gemv_rows, row_norms, tolerance  # noqa: F401
 from .moe import route, sigmoid, silu, swiglu_bf16, moe_forward, expert_ffn  # noqa: F401

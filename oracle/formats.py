@@ -11,6 +11,10 @@ Sources:
 * Q6_K operand PR, "What changed": 6-bit codes with zero point 32, a scale per
   16 weights, and the half-precision operand 1 + code/64 whose value minus 1.5
   is exactly (code - 32)/64.
+* Q6_K operand PR, commit "5-bit nibble operand": the 5-bit formats Q5_K, Q5_1
+  and Q5_0 (the last taken "as ZeroAsMin": its zero point as a block minimum);
+  the five-bit operand is the nibble with the fifth bit at bit 8 of the
+  halfword, the half 1 + code/64, exact for codes up to 31.
 
 Readings where the pages are silent (each listed in the design notes):
 * E2M1 bit layout: bit 3 sign, bits 2..1 exponent with bias 1, bit 0 mantissa;
@@ -21,13 +25,19 @@ Readings where the pages are silent (each listed in the design notes):
 * MLX scale and bias are fp16 and w = s * code + b.
 * Q6_K: w = d * sc * (code - 32) with fp16 d per 256 weights and int8 sc per 16.
 * NVFP4: w = RN_fp32(tensor_scale * (E4M3(S) * E2M1(code))), the tensor scale last.
+* The 5-bit formats, which the PR names but does not define, follow the public
+  GGML block definitions: codes 0..31 and 32-weight blocks;
+  Q5_0: w = d * (code - 16), fp16 d per block (5.5 bpw);
+  Q5_1: w = d * code + m, fp16 d and fp16 m per block (6 bpw);
+  Q5_K: w = (d * sc) * code - dmin * mn, a 6-bit scale sc and 6-bit minimum mn per
+  32-weight block and fp16 d, dmin per 256 (5 + 12/32 + 32/256 = 5.5 bpw).
 """
 from __future__ import annotations
 
 import numpy as np
 
-MLX_AFFINE4_G64, MXFP4, NVFP4, Q6K = 1, 2, 3, 4
-BLOCK = {MLX_AFFINE4_G64: 64, MXFP4: 32, NVFP4: 16, Q6K: 16}
+MLX_AFFINE4_G64, MXFP4, NVFP4, Q6K, Q5_0, Q5_1, Q5_K = 1, 2, 3, 4, 5, 6, 7
+BLOCK = {MLX_AFFINE4_G64: 64, MXFP4: 32, NVFP4: 16, Q6K: 16, Q5_0: 32, Q5_1: 32, Q5_K: 32}
 
 
 # ---------------------------------------------------------------- element decoders
@@ -111,6 +121,21 @@ def _exact_values(fmt: int, codes, scales, aux, tensor_scale: float) -> np.ndarr
         sc = np.repeat(np.asarray(scales, dtype=np.int8).astype(np.float64), blk, axis=1)
         d = np.repeat(np.asarray(aux, dtype=np.float16).astype(np.float64), 256, axis=1)
         return d * sc * (codes.astype(np.float64) - 32.0)
+    if fmt == Q5_0:
+        d = np.repeat(np.asarray(scales, dtype=np.float16).astype(np.float64), blk, axis=1)
+        return d * (codes.astype(np.float64) - 16.0)
+    if fmt == Q5_1:
+        d = np.repeat(np.asarray(scales, dtype=np.float16).astype(np.float64), blk, axis=1)
+        m = np.repeat(np.asarray(aux, dtype=np.float16).astype(np.float64), blk, axis=1)
+        return d * codes.astype(np.float64) + m
+    if fmt == Q5_K:
+        sm = np.asarray(scales, dtype=np.uint8).astype(np.float64)  # [N, K/32, 2]: (sc, mn)
+        dd = np.asarray(aux, dtype=np.float16).astype(np.float64)   # [N, K/256, 2]: (d, dmin)
+        sc = np.repeat(sm[:, :, 0], blk, axis=1)
+        mn = np.repeat(sm[:, :, 1], blk, axis=1)
+        d = np.repeat(dd[:, :, 0], 256, axis=1)
+        dmin = np.repeat(dd[:, :, 1], 256, axis=1)
+        return d * sc * codes.astype(np.float64) - dmin * mn
     raise ValueError(f"unknown format {fmt}")
 
 
@@ -132,8 +157,9 @@ def dequant_operand_bf16(w) -> np.ndarray:
     """bf16-exact fp64 values [N, K] of the 16-bit operand a prefill GEMM multiplies
     (TurboEXL3 article §2.2: W4A16 expands each weight to 16 bits).  MXFP4 and NVFP4:
     the E2M1 value times its block scale, without the NVFP4 tensor scale (exact in
-    bf16: at most 6 significant bits); MLX affine and Q6_K: the fp32 weight rounded
-    to bf16 (a second rounding, since these weights carry up to 24 bits)."""
+    bf16: at most 6 significant bits); MLX affine, Q6_K and the 5-bit formats: the fp32
+    weight rounded to bf16 (a second rounding, since these weights carry up to 24
+    bits)."""
     if w.fmt == MXFP4:
         v = e2m1_value(w.codes) * np.repeat(e8m0_value(w.scales), BLOCK[MXFP4], axis=1)
     elif w.fmt == NVFP4:
@@ -154,6 +180,12 @@ def bits_per_weight(fmt: int) -> float:
         return 4 + 8 / 16  # the single fp32 tensor scale is not per weight
     if fmt == Q6K:
         return 6 + 8 / 16 + 16 / 256
+    if fmt == Q5_0:
+        return 5 + 16 / 32
+    if fmt == Q5_1:
+        return 5 + (16 + 16) / 32
+    if fmt == Q5_K:
+        return 5 + (6 + 6) / 32 + (16 + 16) / 256
     raise ValueError(fmt)
 
 
@@ -162,4 +194,12 @@ def q6k_half_operand_bits(code) -> np.ndarray:
     the code's low nibble in mantissa bits 4..7 and its two high bits in bits 8..9
     of a half whose exponent encodes 1.0, i.e. the half 1 + code/64."""
     c = np.asarray(code).astype(np.uint16) & 0x3F
+    return (np.uint16(0x3C00) | ((c & 0xF) << 4) | ((c >> 4) << 8)).astype(np.uint16)
+
+
+def q5_half_operand_bits(code) -> np.ndarray:
+    """fp16 bit pattern of the 5-bit operand of the Q6_K operand PR (commit "5-bit
+    nibble operand"): the low nibble in mantissa bits 4..7 and the fifth bit at bit 8
+    of a half whose exponent encodes 1.0, i.e. the half 1 + code/64."""
+    c = np.asarray(code).astype(np.uint16) & 0x1F
     return (np.uint16(0x3C00) | ((c & 0xF) << 4) | ((c >> 4) << 8)).astype(np.uint16)

@@ -22,7 +22,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 with open(os.path.join(_HERE, "golden", "page_facts.json")) as _f:
     FACTS = json.load(_f)
 
-FMT_KEY = {wl.MLX_AFFINE4_G64: "mlx_affine4_g64", wl.MXFP4: "mxfp4", wl.NVFP4: "nvfp4", wl.Q6K: "q6k"}
+FMT_KEY = {wl.MLX_AFFINE4_G64: "mlx_affine4_g64", wl.MXFP4: "mxfp4", wl.NVFP4: "nvfp4", wl.Q6K: "q6k",
+           wl.Q5_0: "q5_0", wl.Q5_1: "q5_1", wl.Q5_K: "q5_k"}
+Q5 = (wl.Q5_0, wl.Q5_1, wl.Q5_K)
+
+
+def shape_for(fmt, n, k_small):
+    """A test shape: formats with a 256-weight super-block need K = 256."""
+    return (n, 256) if fmt in (wl.Q6K, wl.Q5_K) else (n, k_small)
 
 
 # ----------------------------------------------------------------- exact helpers
@@ -80,6 +87,14 @@ def exact_weight(w, n: int, k: int) -> Fraction:
         return Fraction(float(np.float32(w.tensor_scale))) * torch_e4m3(int(w.scales[n, k // 16])) * e2m1_from_page(c)
     if w.fmt == wl.Q6K:
         return Fraction(float(w.aux[n, k // 256])) * int(w.scales[n, k // 16]) * (c - 32)
+    if w.fmt == wl.Q5_0:  # GGML Q5_0: d (code - 16)
+        return Fraction(float(w.scales[n, k // 32])) * (c - FACTS["_not_from_pages"]["q5_zero_point"]["q5_0"])
+    if w.fmt == wl.Q5_1:  # GGML Q5_1: d code + m
+        return Fraction(float(w.scales[n, k // 32])) * c + Fraction(float(w.aux[n, k // 32]))
+    if w.fmt == wl.Q5_K:  # GGML Q5_K: d sc code - dmin mn
+        sc, mn = int(w.scales[n, k // 32, 0]), int(w.scales[n, k // 32, 1])
+        d, dmin = Fraction(float(w.aux[n, k // 256, 0])), Fraction(float(w.aux[n, k // 256, 1]))
+        return d * sc * c - dmin * mn
     raise ValueError(w.fmt)
 
 
@@ -144,6 +159,11 @@ def check_bpw(o):
     total = c + s + a
     assert total == q["n"] * q["k"] * o.bits_per_weight(wl.Q6K) / 8
     assert round(total / 1e9, 2) == q["gigabytes"], total
+    for fmt in Q5:  # the GGML block sizes (bytes per block of weights)
+        nbytes, nweights = FACTS["_not_from_pages"]["q5_block_bytes"][FMT_KEY[fmt]]
+        assert o.bits_per_weight(fmt) == nbytes * 8 / nweights, fmt
+        c, s, a = o.packed_sizes(fmt, 1024, 2048)
+        assert (c + s + a) * 8 / (1024 * 2048) == nbytes * 8 / nweights, fmt
 
 
 def check_q6k_operand(o):
@@ -160,6 +180,25 @@ def check_q6k_operand(o):
     assert np.array_equal(got, 64.0 * np.tile(diff, 4))
 
 
+def check_q5_operand(o):
+    """The 5-bit operand is 1 + code/64 for every 5-bit code, and Q5_0's dequantisation
+    uses zero point 16 (GGML; the page's "as ZeroAsMin": d (code - 16) = d code - 16 d)."""
+    f = FACTS["q5_operand"]
+    codes = np.arange(f["max_exact_code"] + 1)
+    bits = o.q5_half_operand_bits(codes)
+    assert np.array_equal(bits.view(np.float16).astype(np.float64), f["operand_base"] + codes * f["operand_step"])
+    assert np.array_equal((bits >> f["fifth_bit"]) & 1, codes >> 4)
+    zp = FACTS["_not_from_pages"]["q5_zero_point"]["q5_0"]
+    w = wl.QWeight(wl.Q5_0, 1, 64, codes=np.tile(np.arange(32, dtype=np.uint8), 2)[None, :],
+                   scales=np.ones((1, 2), np.float16))
+    assert np.array_equal(o.dequant(w)[0].astype(np.float64), np.tile(np.arange(32) - zp, 2).astype(np.float64))
+    # ZeroAsMin: the same weights as a Q5_1 block with m = -16 d
+    w1 = wl.QWeight(wl.Q5_1, 1, 64, codes=w.codes, scales=np.full((1, 2), 0.25, np.float16),
+                    aux=np.full((1, 2), -zp * 0.25, np.float16))
+    w0 = wl.QWeight(wl.Q5_0, 1, 64, codes=w.codes, scales=np.full((1, 2), 0.25, np.float16))
+    assert np.array_equal(o.dequant(w1), o.dequant(w0))
+
+
 def check_q6k_old_seed(seed=3):
     """(128 + c) operands seeded with -160 * sum(x) give the same exact dot as (c - 32)."""
     f = FACTS["q6k_old_seed"]
@@ -173,7 +212,7 @@ def check_q6k_old_seed(seed=3):
 
 
 def check_dequant_exact(o, fmt, seed=5):
-    n, k = (8, 256) if fmt == wl.Q6K else (8, 128)
+    n, k = shape_for(fmt, 8, 128)
     w = wl.weight(fmt, n, k, seed)
     got = o.dequant(w)
     for i in range(n):
@@ -184,7 +223,7 @@ def check_dequant_exact(o, fmt, seed=5):
 
 
 def check_gemv_brute_force(o, fmt, m, residual, seed=7):
-    n, k = (16, 256) if fmt == wl.Q6K else (16, 64)
+    n, k = shape_for(fmt, 16, 64)
     w, x, res = wl.gemv_case(fmt, n, k, m, seed=seed, residual=residual)
     y, v = o.gemv(w, x, res)
     w32 = o.dequant(w)
@@ -206,7 +245,7 @@ def check_gemv_brute_force(o, fmt, m, residual, seed=7):
 
 def check_dense_special_case(o, fmt, seed=11):
     """Unit scales reduce every format to a dense matmul of its integer / E2M1 values."""
-    n, k, m = (32, 256, 3) if fmt == wl.Q6K else (32, 128, 3)
+    (n, k), m = shape_for(fmt, 32, 128), 3
     w, x, _ = wl.gemv_case(fmt, n, k, m, seed=seed)
     if fmt == wl.MLX_AFFINE4_G64:
         w.scales = np.ones_like(w.scales)
@@ -219,10 +258,21 @@ def check_dense_special_case(o, fmt, seed=11):
         w.scales = np.full_like(w.scales, 0x38)  # E4M3 1.0
         w.tensor_scale = 1.0
         dense = np.vectorize(lambda c: float(e2m1_from_page(int(c))))(w.codes)
-    else:
+    elif fmt == wl.Q6K:
         w.scales = np.ones_like(w.scales)
         w.aux = np.ones_like(w.aux)
         dense = w.codes.astype(np.float64) - 32.0
+    elif fmt == wl.Q5_0:
+        w.scales = np.ones_like(w.scales)
+        dense = w.codes.astype(np.float64) - 16.0
+    elif fmt == wl.Q5_1:
+        w.scales = np.ones_like(w.scales)
+        w.aux = np.zeros_like(w.aux)
+        dense = w.codes.astype(np.float64)
+    else:  # Q5_K: sc = 1, mn = 0, d = 1
+        w.scales = np.stack([np.ones_like(w.scales[..., 0]), np.zeros_like(w.scales[..., 1])], axis=-1)
+        w.aux = np.ones_like(w.aux)
+        dense = w.codes.astype(np.float64)
     xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64)
     ref = torch.matmul(xt, torch.from_numpy(dense).T).numpy()
     _, v = o.gemv(w, x)
@@ -346,8 +396,8 @@ def check_moe_composition(o, seed=29):
 def check_operand_bf16(o, fmt, seed=31):
     """The bf16 prefill operand: exact for the E2M1 formats (rounding changes nothing and
     the NVFP4 tensor scale times the operand rounds to the fp32 weight); one extra
-    rounding of the fp32 weight for MLX affine and Q6_K."""
-    n, k = (8, 256) if fmt == wl.Q6K else (8, 128)
+    rounding of the fp32 weight for MLX affine, Q6_K and the 5-bit formats."""
+    n, k = shape_for(fmt, 8, 128)
     w = wl.weight(fmt, n, k, seed)
     op = o.dequant_operand_bf16(w)
     w32 = o.dequant(w).astype(np.float64)

@@ -186,3 +186,40 @@ def test_shared_gate_on_the_routed_sum(monkeypatch):
         return (out, acc) + tuple(a_s[2:]) if with_intermediates else out
     monkeypatch.setattr(oracle, "moe_forward", bad)
     assert _fails(pins.check_moe_shared_gate, oracle)
+
+
+def test_q5_0_zero_point_15(monkeypatch):
+    def t(v, fmt, codes, scales, aux, ts):
+        d = np.repeat(np.asarray(scales, np.float16).astype(np.float64), 32, axis=1)
+        return d * (np.asarray(codes, np.float64) - 15.0)
+    _patch_exact(monkeypatch, wl.Q5_0, t)
+    assert _fails(pins.check_q5_operand, oracle)
+    assert _fails(pins.check_dequant_exact, oracle, wl.Q5_0)
+
+
+def test_q5_k_min_added(monkeypatch):
+    def t(v, fmt, codes, scales, aux, ts):
+        sm = np.asarray(scales, np.uint8).astype(np.float64)
+        dd = np.asarray(aux, np.float16).astype(np.float64)
+        return np.repeat(dd[:, :, 0], 256, axis=1) * np.repeat(sm[:, :, 0], 32, axis=1) * np.asarray(codes, np.float64) \
+            + np.repeat(dd[:, :, 1], 256, axis=1) * np.repeat(sm[:, :, 1], 32, axis=1)
+    _patch_exact(monkeypatch, wl.Q5_K, t)
+    assert _fails(pins.check_dequant_exact, oracle, wl.Q5_K)
+
+
+def test_q5_1_scale_and_min_swapped(monkeypatch):
+    def t(v, fmt, codes, scales, aux, ts):
+        d = np.repeat(np.asarray(scales, np.float16).astype(np.float64), 32, axis=1)
+        m = np.repeat(np.asarray(aux, np.float16).astype(np.float64), 32, axis=1)
+        return m * np.asarray(codes, np.float64) + d
+    _patch_exact(monkeypatch, wl.Q5_1, t)
+    assert _fails(pins.check_dense_special_case, oracle, wl.Q5_1)
+    assert _fails(pins.check_dequant_exact, oracle, wl.Q5_1)
+
+
+def test_q5_operand_fifth_bit_at_bit_9(monkeypatch):
+    def bad(code):
+        c = np.asarray(code).astype(np.uint16) & 0x1F
+        return (np.uint16(0x3C00) | ((c & 0xF) << 4) | ((c >> 4) << 9)).astype(np.uint16)
+    monkeypatch.setattr(oracle, "q5_half_operand_bits", bad)
+    assert _fails(pins.check_q5_operand, oracle)

@@ -5,7 +5,7 @@ import oracle
 import workloads as wl
 from tests import pins
 
-ALL_FMTS = [wl.MLX_AFFINE4_G64, wl.MXFP4, wl.NVFP4, wl.Q6K]
+ALL_FMTS = [wl.MLX_AFFINE4_G64, wl.MXFP4, wl.NVFP4, wl.Q6K, wl.Q5_0, wl.Q5_1, wl.Q5_K]
 
 
 def test_e2m1_table_is_the_page_set():
@@ -30,6 +30,10 @@ def test_bits_per_weight_and_q6k_output_layer_bytes():
 
 def test_q6k_half_operand_identity():
     pins.check_q6k_operand(oracle)
+
+
+def test_q5_half_operand_identity():
+    pins.check_q5_operand(oracle)
 
 
 def test_q6k_old_seed_identity():

@@ -20,6 +20,11 @@ workload definitions of the quantized-GEMV benchmark:
   fp32 tensor scale 1/448.
 * Q6_K-style: 6-bit codes uniform in [0, 63]; int8 scale per 16 uniform in
   [-64, 63]; fp16 super-scale d per 256 = fp16(|N(0,1)| * 1e-3).
+* 5-bit formats (codes uniform in [0, 31], 32-weight blocks):
+  Q5_0: fp16 d = fp16(0.02 * U(0.5, 1.5));
+  Q5_1: the same d and fp16 m = fp16(-d * U(12, 20)) (a block minimum near -16 d);
+  Q5_K: 6-bit sc and mn uniform in [0, 63] per block, fp16 d and dmin per 256 =
+  fp16(|N(0,1)| * 1e-3) each.
 * Activations and residuals: fp32 N(0,1) draws rounded to bf16 (round to
   nearest even).  Router logits: fp32 N(0,1).
 """
@@ -36,10 +41,14 @@ MLX_AFFINE4_G64 = 1
 MXFP4 = 2
 NVFP4 = 3
 Q6K = 4
+Q5_0 = 5
+Q5_1 = 6
+Q5_K = 7
 
-FORMAT_NAMES = {MLX_AFFINE4_G64: "mlx_affine4_g64", MXFP4: "mxfp4", NVFP4: "nvfp4", Q6K: "q6k"}
-BLOCK = {MLX_AFFINE4_G64: 64, MXFP4: 32, NVFP4: 16, Q6K: 16}
-SUPER_BLOCK = {Q6K: 256}
+FORMAT_NAMES = {MLX_AFFINE4_G64: "mlx_affine4_g64", MXFP4: "mxfp4", NVFP4: "nvfp4", Q6K: "q6k", Q5_0: "q5_0",
+                Q5_1: "q5_1", Q5_K: "q5_k"}
+BLOCK = {MLX_AFFINE4_G64: 64, MXFP4: 32, NVFP4: 16, Q6K: 16, Q5_0: 32, Q5_1: 32, Q5_K: 32}
+SUPER_BLOCK = {Q6K: 256, Q5_K: 256}
 
 _STREAMS = ("codes", "scales", "aux", "x", "residual", "logits")
 
@@ -66,10 +75,14 @@ def e4m3_bytes_from_f32(a: np.ndarray) -> np.ndarray:
 class QWeight:
     """A quantized N x K weight matrix in logical (unpacked) form.
 
-    codes:  uint8 [N, K], one code per byte (4-bit formats: 0..15, Q6_K: 0..63).
+    codes:  uint8 [N, K], one code per byte (4-bit formats: 0..15, Q6_K: 0..63,
+            5-bit formats: 0..31).
     scales: MLX: float16 [N, K/64] scale s; MXFP4: uint8 [N, K/32] E8M0 bytes;
-            NVFP4: uint8 [N, K/16] E4M3 bytes; Q6_K: int8 [N, K/16].
-    aux:    MLX: float16 [N, K/64] bias b; Q6_K: float16 [N, K/256] d; else None.
+            NVFP4: uint8 [N, K/16] E4M3 bytes; Q6_K: int8 [N, K/16];
+            Q5_0, Q5_1: float16 [N, K/32] d; Q5_K: uint8 [N, K/32, 2] (sc, mn).
+    aux:    MLX: float16 [N, K/64] bias b; Q6_K: float16 [N, K/256] d;
+            Q5_1: float16 [N, K/32] m; Q5_K: float16 [N, K/256, 2] (d, dmin);
+            else None.
     tensor_scale: NVFP4 fp32 tensor scale (1.0 for the other formats).
     """
 
@@ -104,6 +117,18 @@ def _draw_weight(fmt: int, n: int, k: int, rs: dict) -> QWeight:
         sc = rs["scales"].integers(-64, 64, size=(n, k // 16), dtype=np.int8)
         d = (np.abs(rs["aux"].standard_normal(size=(n, k // 256), dtype=np.float32)) * np.float32(1e-3)).astype(np.float16)
         return QWeight(fmt, n, k, codes, sc, d, 1.0)
+    if fmt in (Q5_0, Q5_1):
+        codes = rs["codes"].integers(0, 32, size=(n, k), dtype=np.uint8)
+        d = (0.02 * rs["scales"].uniform(0.5, 1.5, size=(n, k // 32))).astype(np.float16)
+        if fmt == Q5_0:
+            return QWeight(fmt, n, k, codes, d, None, 1.0)
+        m = (-d.astype(np.float64) * rs["aux"].uniform(12.0, 20.0, size=(n, k // 32))).astype(np.float16)
+        return QWeight(fmt, n, k, codes, d, m, 1.0)
+    if fmt == Q5_K:
+        codes = rs["codes"].integers(0, 32, size=(n, k), dtype=np.uint8)
+        sm = rs["scales"].integers(0, 64, size=(n, k // 32, 2), dtype=np.uint8)
+        dd = (np.abs(rs["aux"].standard_normal(size=(n, k // 256, 2), dtype=np.float32)) * np.float32(1e-3)).astype(np.float16)
+        return QWeight(fmt, n, k, codes, sm, dd, 1.0)
     raise ValueError(f"unknown format {fmt}")
 
 
