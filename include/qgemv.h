@@ -16,6 +16,15 @@
  *                           one fp32 tensor scale ts (4.5 bpw)
  *   QG_FMT_Q6K              w = d * sc * (code - 32); code 0..63; int8 sc per 16 weights,
  *                           fp16 d per 256 weights (6.5625 bpw)
+ * and the 5-bit formats the Q6_K operand PR's 5-bit nibble operand serves (Q5_K, Q5_1,
+ * Q5_0), defined as the public GGML blocks (the pages name them without defining them);
+ * code 0..31, 32-weight blocks:
+ *   QG_FMT_Q5_0             w = d * (code - 16); fp16 d per 32 weights (5.5 bpw)
+ *   QG_FMT_Q5_1             w = d * code + m; fp16 d and m per 32 weights (6 bpw)
+ *   QG_FMT_Q5_K             w = (d * sc) * code - dmin * mn; 6-bit sc and mn per 32 weights,
+ *                           fp16 d and dmin per 256 weights (5.5 bpw)
+ * The 5-bit formats run on the dense paths (qgemv, qgemm, qg_dequant); the MoE entry
+ * points take the four formats above and return QG_ERR_UNSUPPORTED for them.
  *
  * Conventions shared by every entry point:
  *   - Matrices are N x K (outputs x inputs).  Activations x are bf16 [m][ldx],
@@ -34,10 +43,10 @@
  *
  * Packed weight layout "T128x64" (written by qg_pack_host, read by every kernel):
  *   Rows are padded to NP = 128*ceil(N/128) and the inputs to KP = KB*ceil(K/KB),
- *   KB = 64 (4-bit formats) or 256 (Q6_K).  Tile (q, g) -- rows 128q..128q+127,
+ *   KB = 256 (Q6_K, Q5_K) or 64 (the others).  Tile (q, g) -- rows 128q..128q+127,
  *   inputs 64g..64g+63 -- has index t = q*KG + g, KG = KP/64.  Padding holds
  *   zero codes and zero scales.
- *   codes : TB bytes per tile at t*TB, TB = 4096 (4-bit) or 6144 (Q6_K).  Row r of
+ *   codes : TB bytes per tile at t*TB, TB = 4096 (4-bit), 6144 (Q6_K) or 5120 (5-bit).  Row r of
  *           the tile (rt = r/32, lane = r%32) owns the 16-byte chunks at byte
  *           ((rt*CH + c)*32 + lane)*16, CH = 2 (4-bit) or 3 (Q6_K).
  *           4-bit, chunk c = 0,1: byte b holds code (64g + 32c + 2b) in its low
@@ -45,13 +54,23 @@
  *           Q6_K: chunks 0,1 hold the low nibbles (code & 15) as above; chunk 2 is
  *           four little-endian 32-bit words, word w holding in nibble j (bits
  *           4j..4j+3) hi(64g+16w+j) | hi(64g+16w+8+j) << 2, hi(code) = code >> 4.
+ *           5-bit: bytes 0..4095 hold the low nibbles (code & 15) as the 4-bit chunks
+ *           (CH = 2); bytes 4096..5119 hold the fifth bits: two little-endian 32-bit
+ *           words per row, word j (0, 1) of row r at byte 4096 + 512j + 4r, holding
+ *           (code >> 4) of input 64g + 32j + 8u + i (u = 0..3, i = 0..7) at bit
+ *           (4i + 4 + u) mod 32.
  *   scales: 128*SB bytes per tile at t*128*SB, SB bytes for row r at r*SB:
  *           NVFP4 (SB=4) byte i = E4M3 scale of inputs 64g+16i..+15;
  *           MXFP4 (SB=2) byte i = E8M0 scale of inputs 64g+32i..+31;
  *           MLX   (SB=4) fp16 s then fp16 b (little-endian) of the 64-input group;
- *           Q6_K  (SB=4) byte i = int8 scale of inputs 64g+16i..+15.
- *   aux   : Q6_K only: fp16 d of inputs 256u..256u+255 for row r of row tile q at
- *           byte (q*(KG/4) + u)*256 + 2r.  NULL for the other formats.
+ *           Q6_K  (SB=4) byte i = int8 scale of inputs 64g+16i..+15;
+ *           Q5_0  (SB=4) fp16 d of inputs 64g+32i..+31 at bytes 2i..2i+1;
+ *           Q5_1  (SB=8) fp16 d then fp16 m of inputs 64g+32i..+31 at bytes 4i..4i+3;
+ *           Q5_K  (SB=3) one little-endian 24-bit value: sc of inputs 64g..64g+31 in bits
+ *                 0..5, its mn in 6..11, sc and mn of 64g+32..64g+63 in 12..17, 18..23.
+ *   aux   : Q6_K: fp16 d of inputs 256u..256u+255 for row r of row tile q at
+ *           byte (q*(KG/4) + u)*256 + 2r.  Q5_K: fp16 d then fp16 dmin of those inputs
+ *           at byte (q*(KG/4) + u)*512 + 4r.  NULL for the other formats.
  */
 #ifndef QGEMV_H
 #define QGEMV_H
@@ -67,7 +86,10 @@ typedef enum {
   QG_FMT_MLX_AFFINE4_G64 = 1,
   QG_FMT_MXFP4 = 2,
   QG_FMT_NVFP4 = 3,
-  QG_FMT_Q6K = 4
+  QG_FMT_Q6K = 4,
+  QG_FMT_Q5_0 = 5,
+  QG_FMT_Q5_1 = 6,
+  QG_FMT_Q5_K = 7
 } qg_format;
 
 typedef enum {
@@ -84,7 +106,7 @@ typedef enum { QG_OUT_F32 = 0, QG_OUT_BF16 = 1 } qg_out_dtype;
 
 /* A packed weight matrix in device memory (layout "T128x64" above).
  * n, k are the logical sizes; k must be a multiple of the format's block (64 MLX,
- * 32 MXFP4, 16 NVFP4, 256 Q6_K).  tensor_scale is used by NVFP4 only and must be
+ * 32 MXFP4, 16 NVFP4, 256 Q6_K, 32 Q5_0 / Q5_1, 256 Q5_K).  tensor_scale is used by NVFP4 only and must be
  * 1.0f for the other formats. */
 typedef struct {
   int32_t fmt;            /* qg_format */
@@ -93,7 +115,7 @@ typedef struct {
   int64_t k;
   const void* codes;      /* device, 16-byte aligned */
   const void* scales;     /* device, 16-byte aligned */
-  const void* aux;        /* device, 16-byte aligned; Q6_K d, NULL otherwise */
+  const void* aux;        /* device, 16-byte aligned; Q6_K d, Q5_K (d, dmin), NULL otherwise */
   float tensor_scale;
   float reserved2;        /* must be 0 */
 } qg_weight;
@@ -108,12 +130,15 @@ qg_status qg_packed_sizes(int fmt, int64_t n, int64_t k,
                           size_t* codes_bytes, size_t* scales_bytes, size_t* aux_bytes);
 
 /* Host-side packer: logical row-major arrays -> packed layout (host memory).
- *   logical_codes  : uint8 [n][k], one code per byte (0..15, or 0..63 for Q6_K)
+ *   logical_codes  : uint8 [n][k], one code per byte (0..15; 0..63 Q6_K; 0..31 5-bit)
  *   logical_scales : MLX fp16 s [n][k/64]; MXFP4 uint8 E8M0 [n][k/32];
- *                    NVFP4 uint8 E4M3 [n][k/16]; Q6_K int8 sc [n][k/16]
- *   logical_aux    : MLX fp16 b [n][k/64]; Q6_K fp16 d [n][k/256]; NULL otherwise
- *   codes/scales/aux: outputs sized by qg_packed_sizes (aux NULL unless Q6_K).
- * Codes out of range return QG_ERR_INVALID_ARG.  No GPU needed. */
+ *                    NVFP4 uint8 E4M3 [n][k/16]; Q6_K int8 sc [n][k/16];
+ *                    Q5_0 / Q5_1 fp16 d [n][k/32]; Q5_K uint8 (sc, mn) [n][k/32][2]
+ *   logical_aux    : MLX fp16 b [n][k/64]; Q6_K fp16 d [n][k/256]; Q5_1 fp16 m [n][k/32];
+ *                    Q5_K fp16 (d, dmin) [n][k/256][2]; NULL otherwise
+ *   codes/scales/aux: outputs sized by qg_packed_sizes (aux NULL unless Q6_K or Q5_K).
+ * Codes (or Q5_K sc / mn above 63) out of range return QG_ERR_INVALID_ARG.  No GPU
+ * needed. */
 qg_status qg_pack_host(int fmt, int64_t n, int64_t k,
                        const uint8_t* logical_codes, const void* logical_scales, const void* logical_aux,
                        void* codes, void* scales, void* aux);
@@ -122,7 +147,8 @@ qg_status qg_pack_host(int fmt, int64_t n, int64_t k,
  *   QG_OUT_F32 : the exact weight rounded once to fp32 (NVFP4 includes the tensor scale).
  *   QG_OUT_BF16: the operand the prefill GEMM feeds the tensor cores: for MXFP4 /
  *                NVFP4 the block-scaled E2M1 value without the tensor scale (exact in
- *                bf16); for MLX / Q6_K the fp32 weight rounded to bf16. */
+ *                bf16); for MLX / Q6_K / the 5-bit formats the fp32 weight rounded to
+ *                bf16. */
 qg_status qg_dequant(const qg_weight* w, int out_dtype, void* out, int64_t ldo, void* stream);
 
 /* Workspace bytes qgemv needs for this shape on the current device (split-K

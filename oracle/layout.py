@@ -26,9 +26,10 @@ behind a shared helper.  The specification ("T128x64"):
   byte offset (q * (KG / 4) + u) * 256 + 2 r.
 * 5-bit formats (Q5_0, Q5_1, Q5_K): TB = 5120.  Bytes 0..4095 hold the low nibbles
   (code & 15) exactly as the 4-bit formats' chunks (CH = 2); bytes 4096..5119 hold
-  the fifth bits, 8 bytes per row at 4096 + 8 r: two little-endian 32-bit words,
-  word j in {0, 1} holding bit (code >> 4) of column g*64 + 32j + 8u + i (u in
-  0..3, i in 0..7) at bit (4i + 4 + u) mod 32.  KB = 256 for Q5_K, 64 otherwise.
+  the fifth bits: two little-endian 32-bit words per row, word j in {0, 1} of row r
+  at byte 4096 + 512 j + 4 r, holding bit (code >> 4) of column g*64 + 32j + 8u + i
+  (u in 0..3, i in 0..7) at bit (4i + 4 + u) mod 32.  KB = 256 for Q5_K, 64
+  otherwise.
   - Q5_0 (SB = 4): fp16 d of columns g*64 + 32i .. +31 at bytes 2i..2i+1;
   - Q5_1 (SB = 8): fp16 d then fp16 m of columns g*64 + 32i .. +31 at bytes
     4i..4i+3;
@@ -94,7 +95,7 @@ def unpack(fmt: int, n: int, k: int, codes: np.ndarray, scales: np.ndarray, aux=
         hrow = hsel.transpose(0, 2, 3, 1, 4, 5).reshape(np_, kp).astype(np.uint8)
         logical = (logical | (hrow << 4)).astype(np.uint8)
     if fmt in _Q5:
-        fb = tiles[:, :, 4096:].reshape(nt, kg, 128, 2, 4).astype(np.uint32)  # [q, g, row, j, byte]
+        fb = tiles[:, :, 4096:].reshape(nt, kg, 2, 128, 4).transpose(0, 1, 3, 2, 4).astype(np.uint32)  # [q, g, row, j, byte]
         w32 = fb[..., 0] | (fb[..., 1] << 8) | (fb[..., 2] << 16) | (fb[..., 3] << 24)
         u = np.arange(4, dtype=np.uint32)[:, None]
         i = np.arange(8, dtype=np.uint32)[None, :]

@@ -19,7 +19,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqgemv.so")
 
-FMT_MLX_AFFINE4_G64, FMT_MXFP4, FMT_NVFP4, FMT_Q6K = 1, 2, 3, 4
+FMT_MLX_AFFINE4_G64, FMT_MXFP4, FMT_NVFP4, FMT_Q6K, FMT_Q5_0, FMT_Q5_1, FMT_Q5_K = 1, 2, 3, 4, 5, 6, 7
 OUT_F32, OUT_BF16 = 0, 1
 STATUS = {0: "QG_OK", 1: "QG_ERR_INVALID_ARG", 2: "QG_ERR_UNSUPPORTED", 3: "QG_ERR_MISALIGNED",
           4: "QG_ERR_WORKSPACE_TOO_SMALL", 5: "QG_ERR_CUDA", 6: "QG_ERR_TIMEOUT"}
@@ -103,7 +103,8 @@ def qg_packed_sizes(fmt: int, n: int, k: int):
 
 
 def qg_pack_host(fmt: int, n: int, k: int, codes: np.ndarray, scales: np.ndarray, aux: Optional[np.ndarray]):
-    """Pack logical host arrays; returns (codes, scales, aux) uint8 numpy arrays (aux empty unless Q6_K)."""
+    """Pack logical host arrays; returns (codes, scales, aux) uint8 numpy arrays (aux empty unless Q6_K or
+    Q5_K)."""
     cb, sb, ab = qg_packed_sizes(fmt, n, k)
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
     scales = np.ascontiguousarray(scales)

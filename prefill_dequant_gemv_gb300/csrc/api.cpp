@@ -43,7 +43,7 @@ static int check_weight(const qg_weight* w, Geometry* g) {
   if (w->reserved != 0 || w->reserved2 != 0.0f) return QG_ERR_INVALID_ARG;
   if (!geometry(w->fmt, w->n, w->k, g)) return QG_ERR_INVALID_ARG;
   if (!w->codes || !w->scales) return QG_ERR_INVALID_ARG;
-  if (w->fmt == QG_FMT_Q6K && !w->aux) return QG_ERR_INVALID_ARG;
+  if ((w->fmt == QG_FMT_Q6K || w->fmt == QG_FMT_Q5_K) && !w->aux) return QG_ERR_INVALID_ARG;
   if (w->fmt != QG_FMT_NVFP4 && w->tensor_scale != 1.0f) return QG_ERR_INVALID_ARG;
   if (!aligned16(w->codes) || !aligned16(w->scales) || (w->aux && !aligned16(w->aux))) return QG_ERR_MISALIGNED;
   return QG_OK;
@@ -172,6 +172,7 @@ static int check_moe(const qg_moe_layer* m, int64_t t, int topk, Geometry* gu, G
   if (!m || t < 1 || topk < 1) return QG_ERR_INVALID_ARG;
   if (m->n_experts < 1 || topk > m->n_experts) return QG_ERR_INVALID_ARG;
   if (m->n_experts > kMaxExperts || topk > kMaxTopk) return QG_ERR_UNSUPPORTED;
+  if (is_q5(m->fmt)) return QG_ERR_UNSUPPORTED;  // the 5-bit formats run on the dense paths only
   if (!geometry(m->fmt, 2 * m->ffn, m->hidden, gu) || !geometry(m->fmt, m->hidden, m->ffn, dn))
     return QG_ERR_INVALID_ARG;
   if (!m->gu_codes || !m->gu_scales || !m->dn_codes || !m->dn_scales) return QG_ERR_INVALID_ARG;

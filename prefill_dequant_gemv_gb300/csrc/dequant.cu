@@ -4,7 +4,7 @@
 // each operand back into the weight, so a bit-exact comparison of its output with
 // the CPU oracle checks the layout reader and every decoder of the fast path.
 //   fp32: the exact weight rounded once (TurboEXL3 article §2.1 formats; Q6_K
-//         operand PR #19 zero point 32).
+//         operand PR #19 zero point 32 and its 5-bit formats).
 //   bf16: the prefill tensor-core operand: e2m1 * block scale (without the NVFP4
 //         tensor scale; exact in bf16) or the fp32 weight rounded to bf16.
 #include <cuda_runtime.h>
@@ -70,20 +70,13 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantArgs a) {
       // the GEMV's f16 operands: op0 = (n0, n4) and op2 = (n2, n6) are 1 + code/1024,
       // op1 = (n1, n5) and op3 = (n3, n7) are 1 + code/64
       uint32_t op[4];
-      const uint32_t r = rot8(wd);
-      if (FMT == FMT_MLX) {
-        op[0] = i4_op_lo(wd);
-        op[1] = i4_op_hi(wd);
-        op[2] = i4_op_lo(r);
-        op[3] = i4_op_hi(r);
-      } else {
-        const uint32_t hw = *reinterpret_cast<const uint32_t*>(tc + ((rt * 3 + 2) * 32 + lane) * 16 + kq * 4);
-        const uint32_t hh = q6k_hi_for(hw, wi), hr = rot8(hh);
-        op[0] = i6_op_lo(wd, hh);
-        op[1] = i6_op_hi(wd, hh);
-        op[2] = i6_op_lo(r, hr);
-        op[3] = i6_op_hi(r, hr);
-      }
+      uint32_t hh = 0;
+      if (FMT == FMT_Q6K)
+        hh = q6k_hi_for(*reinterpret_cast<const uint32_t*>(tc + ((rt * 3 + 2) * 32 + lane) * 16 + kq * 4), wi);
+      else if (fmt_q5(FMT))
+        hh = q5_hi_for(*reinterpret_cast<const uint32_t*>(tc + kQ5Plane + (kq >> 1) * 512 + row * 4),
+                       2 * (kq & 1) + wi);
+      int_ops<FMT>(wd, hh, op);
       float code[8];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -99,6 +92,10 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantArgs a) {
           const float s = __half2float(__ushort_as_half((unsigned short)(sw & 0xFFFFu)));
           const float bias = __half2float(__ushort_as_half((unsigned short)(sw >> 16)));
           o[j] = fmaf(s, code[j], bias);
+        } else if (fmt_q5(FMT)) {
+          const float2 sb = q5_affine<FMT>(sp, a.aux + (q * (a.kg / 4) + g / 4) * fmt_aux(FMT) + row * fmt_aux_row(FMT),
+                                           kq >> 1);
+          o[j] = fmaf(sb.x, code[j], sb.y);  // one rounding of the exact value
         } else {
           const float sc = (float)(int8_t)sp[kq];
           const float d = __half2float(*reinterpret_cast<const __half*>(a.aux + (q * (a.kg / 4) + g / 4) * 256 + row * 2));
@@ -142,6 +139,9 @@ int launch_dequant(const Geometry& g, const qg_weight* w, int out_dtype, void* o
     case FMT_MLX: dequant_kernel<FMT_MLX><<<(unsigned)blocks, threads, 0, s>>>(a); break;
     case FMT_MXFP4: dequant_kernel<FMT_MXFP4><<<(unsigned)blocks, threads, 0, s>>>(a); break;
     case FMT_NVFP4: dequant_kernel<FMT_NVFP4><<<(unsigned)blocks, threads, 0, s>>>(a); break;
+    case FMT_Q50: dequant_kernel<FMT_Q50><<<(unsigned)blocks, threads, 0, s>>>(a); break;
+    case FMT_Q51: dequant_kernel<FMT_Q51><<<(unsigned)blocks, threads, 0, s>>>(a); break;
+    case FMT_Q5K: dequant_kernel<FMT_Q5K><<<(unsigned)blocks, threads, 0, s>>>(a); break;
     default: dequant_kernel<FMT_Q6K><<<(unsigned)blocks, threads, 0, s>>>(a); break;
   }
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kSmThreads, 1)
     gemm_small_kernel(const __grid_constant__ CUtensorMap tmx, const SmallArgs a) {
   using F = Fmt<FMT>;
   using C = SmCfg<NB>;
-  constexpr int kRaw = F::TB + 128 * F::SB + (FMT == FMT_Q6K ? 256 : 0);
+  constexpr int kRaw = F::TB + 128 * F::SB + fmt_aux(FMT);  // tile, scales, aux of its 256 inputs
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // full[s]: stage s landed; pair barriers (pair q = stages 2q, 2q+1 uses index q % 4):
@@ -126,9 +126,9 @@ __global__ void __launch_bounds__(kSmThreads, 1)
         mbar_arrive_expect_tx(&full[s], kRaw + C::B);
         bulk_g2s(st + C::B, a.codes + tile * F::TB, F::TB, &full[s]);
         bulk_g2s(st + C::B + F::TB, a.scales + tile * (128 * F::SB), 128 * F::SB, &full[s]);
-        if (FMT == FMT_Q6K)
-          bulk_g2s(st + C::B + F::TB + 128 * F::SB, a.aux + ((int64_t)tile_n * (a.KG / 4) + kt / 4) * 256, 256,
-                   &full[s]);
+        if (fmt_aux(FMT))
+          bulk_g2s(st + C::B + F::TB + 128 * F::SB,
+                   a.aux + ((int64_t)tile_n * (a.KG / 4) + kt / 4) * fmt_aux(FMT), fmt_aux(FMT), &full[s]);
         tma_load_2d(st, &tmx, kt * 64, t0, &full[s]);
         ++issued;
       }
@@ -317,6 +317,9 @@ int launch_small_nb(int fmt, const CUtensorMap& map, const SmallArgs& a, dim3 gr
     case FMT_MLX: return launch_small_t<FMT_MLX, NB>(map, a, grid, s);
     case FMT_MXFP4: return launch_small_t<FMT_MXFP4, NB>(map, a, grid, s);
     case FMT_NVFP4: return launch_small_t<FMT_NVFP4, NB>(map, a, grid, s);
+    case FMT_Q50: return launch_small_t<FMT_Q50, NB>(map, a, grid, s);
+    case FMT_Q51: return launch_small_t<FMT_Q51, NB>(map, a, grid, s);
+    case FMT_Q5K: return launch_small_t<FMT_Q5K, NB>(map, a, grid, s);
     default: return launch_small_t<FMT_Q6K, NB>(map, a, grid, s);
   }
 }

@@ -353,6 +353,9 @@ static int stage_bytes_of(int fmt, int m) {
     case FMT_MLX: return Stage<FMT_MLX>::bytes(C);
     case FMT_MXFP4: return Stage<FMT_MXFP4>::bytes(C);
     case FMT_NVFP4: return Stage<FMT_NVFP4>::bytes(C);
+    case FMT_Q50: return Stage<FMT_Q50>::bytes(C);
+    case FMT_Q51: return Stage<FMT_Q51>::bytes(C);
+    case FMT_Q5K: return Stage<FMT_Q5K>::bytes(C);
     default: return Stage<FMT_Q6K>::bytes(C);
   }
 }
@@ -475,6 +478,9 @@ int launch_gemv(const Geometry& g, const qg_weight* w, const void* x, int m, int
     case FMT_MLX: return launch_m<FMT_MLX>(a, m, p, s);
     case FMT_MXFP4: return launch_m<FMT_MXFP4>(a, m, p, s);
     case FMT_NVFP4: return launch_m<FMT_NVFP4>(a, m, p, s);
+    case FMT_Q50: return launch_m<FMT_Q50>(a, m, p, s);
+    case FMT_Q51: return launch_m<FMT_Q51>(a, m, p, s);
+    case FMT_Q5K: return launch_m<FMT_Q5K>(a, m, p, s);
     default: return launch_m<FMT_Q6K>(a, m, p, s);
   }
 }

@@ -45,7 +45,7 @@ extern "C" qg_status qgemv_static_ws(const qg_weight* w, const void* x, int m, i
   if (w->reserved != 0 || w->reserved2 != 0.0f) return QG_ERR_INVALID_ARG;
   if (!qg::geometry(w->fmt, w->n, w->k, &g)) return QG_ERR_INVALID_ARG;
   if (!w->codes || !w->scales) return QG_ERR_INVALID_ARG;
-  if (w->fmt == QG_FMT_Q6K && !w->aux) return QG_ERR_INVALID_ARG;
+  if ((w->fmt == QG_FMT_Q6K || w->fmt == QG_FMT_Q5_K) && !w->aux) return QG_ERR_INVALID_ARG;
   if (w->fmt != QG_FMT_NVFP4 && w->tensor_scale != 1.0f) return QG_ERR_INVALID_ARG;
   if (!aligned16(w->codes) || !aligned16(w->scales) || (w->aux && !aligned16(w->aux))) return QG_ERR_MISALIGNED;
   if (m < 1 || m > 4) return QG_ERR_UNSUPPORTED;

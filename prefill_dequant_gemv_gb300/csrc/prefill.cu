@@ -37,7 +37,7 @@ namespace qg {
 constexpr int kPfBN = 256;                                   // tokens per tile (MMA N)
 constexpr int kPfStages = 5;
 constexpr int kPfDeqWarps = 8;                               // epilogue warps (and Q6_K decoders)
-__host__ __device__ constexpr int pf_decoders(int fmt) { return fmt == FMT_Q6K ? 8 : 4; }
+__host__ __device__ constexpr int pf_decoders(int fmt) { return fmt == FMT_Q6K || fmt_q5(fmt) ? 8 : 4; }
 constexpr int kPfThreads = (2 + kPfDeqWarps) * 32;           // 320
 constexpr int kBTile = kPfBN * 128;                          // 256 tokens x 64 bf16
 constexpr int kRawMax = 7168;                                // >= Q6_K tile 6144 + 512 + 256
@@ -73,7 +73,7 @@ template <int FMT>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmx, const PrefillArgs a) {
   using F = Fmt<FMT>;
-  constexpr int kRaw = F::TB + 128 * F::SB + (FMT == FMT_Q6K ? 256 : 0);
+  constexpr int kRaw = F::TB + 128 * F::SB + fmt_aux(FMT);  // tile, scales, aux of its 256 inputs
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPfStages * kPfStageBytes);
@@ -123,9 +123,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         mbar_arrive_expect_tx(&full[s], kRaw + kBTile);
         bulk_g2s(st + kBTile, a.codes + tile * F::TB, F::TB, &full[s]);
         bulk_g2s(st + kBTile + F::TB, a.scales + tile * (128 * F::SB), 128 * F::SB, &full[s]);
-        if (FMT == FMT_Q6K)
-          bulk_g2s(st + kBTile + F::TB + 128 * F::SB, a.aux + ((int64_t)tile_n * (KG / 4) + kt / 4) * 256, 256,
-                   &full[s]);
+        if (fmt_aux(FMT))
+          bulk_g2s(st + kBTile + F::TB + 128 * F::SB,
+                   a.aux + ((int64_t)tile_n * (KG / 4) + kt / 4) * fmt_aux(FMT), fmt_aux(FMT), &full[s]);
         tma_load_2d(st, &tmx, kt * 64, t0, &full[s]);
         ++issued;
         if (++s == kPfStages) {
@@ -348,13 +348,16 @@ int launch_prefill(const Geometry& g, const qg_weight* w, const void* x, int64_t
   a.ks = 1;
   if (g.nt * tt * 2 <= info.sms) a.ks = (int)std::min<int64_t>(std::min<int64_t>(8, info.sms / (g.nt * tt)), g.kg);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  static std::atomic<unsigned long long> configured[5];
+  static std::atomic<unsigned long long> configured[8];
   const unsigned long long bit = 1ull << (devid & 63);
   const void* fn = nullptr;
   switch (g.fmt) {
     case FMT_MLX: fn = (const void*)prefill_kernel<FMT_MLX>; break;
     case FMT_MXFP4: fn = (const void*)prefill_kernel<FMT_MXFP4>; break;
     case FMT_NVFP4: fn = (const void*)prefill_kernel<FMT_NVFP4>; break;
+    case FMT_Q50: fn = (const void*)prefill_kernel<FMT_Q50>; break;
+    case FMT_Q51: fn = (const void*)prefill_kernel<FMT_Q51>; break;
+    case FMT_Q5K: fn = (const void*)prefill_kernel<FMT_Q5K>; break;
     default: fn = (const void*)prefill_kernel<FMT_Q6K>; break;
   }
   if (!(configured[g.fmt].load() & bit)) {
@@ -382,6 +385,9 @@ int launch_prefill(const Geometry& g, const qg_weight* w, const void* x, int64_t
     case FMT_MLX: e = cudaLaunchKernelEx(&cfg, prefill_kernel<FMT_MLX>, map, a); break;
     case FMT_MXFP4: e = cudaLaunchKernelEx(&cfg, prefill_kernel<FMT_MXFP4>, map, a); break;
     case FMT_NVFP4: e = cudaLaunchKernelEx(&cfg, prefill_kernel<FMT_NVFP4>, map, a); break;
+    case FMT_Q50: e = cudaLaunchKernelEx(&cfg, prefill_kernel<FMT_Q50>, map, a); break;
+    case FMT_Q51: e = cudaLaunchKernelEx(&cfg, prefill_kernel<FMT_Q51>, map, a); break;
+    case FMT_Q5K: e = cudaLaunchKernelEx(&cfg, prefill_kernel<FMT_Q5K>, map, a); break;
     default: e = cudaLaunchKernelEx(&cfg, prefill_kernel<FMT_Q6K>, map, a); break;
   }
   if (e != cudaSuccess) return QG_ERR_CUDA;

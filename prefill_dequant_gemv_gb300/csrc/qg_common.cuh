@@ -11,6 +11,9 @@
 //    the constant 1 (and Q6_K's zero point 32) is removed once per block with the
 //    block's input sums instead of once per weight.  This is the PR's half operand
 //    1 + code/64, whose offset the PR removes by subtracting 1.5.
+//  * 5-bit codes (Q5_0, Q5_1, Q5_K; the PR's 5-bit nibble operand): the nibble with
+//    the fifth bit just above it, 1 + code/1024 or 1 + code/64 (exact for codes to 31);
+//    zero points and minimums are a per-block affine term, as for MLX.
 // Products are formed with the mixed-precision FMA f32 += f16 * f16 (exact
 // products, fp32 accumulation).
 #pragma once
@@ -21,13 +24,27 @@
 
 namespace qg {
 
-enum : int { FMT_MLX = 1, FMT_MXFP4 = 2, FMT_NVFP4 = 3, FMT_Q6K = 4 };
+enum : int { FMT_MLX = 1, FMT_MXFP4 = 2, FMT_NVFP4 = 3, FMT_Q6K = 4, FMT_Q50 = 5, FMT_Q51 = 6, FMT_Q5K = 7 };
 
+// TB: code bytes per 128 x 64 tile; CH: 512-byte chunks per 32 rows (the 5-bit formats'
+// fifth-bit plane follows the two nibble chunks at byte kQ5Plane); SB: scale bytes per row.
 template <int FMT> struct Fmt;
 template <> struct Fmt<FMT_MLX>   { static constexpr int TB = 4096, CH = 2, SB = 4; };
 template <> struct Fmt<FMT_MXFP4> { static constexpr int TB = 4096, CH = 2, SB = 2; };
 template <> struct Fmt<FMT_NVFP4> { static constexpr int TB = 4096, CH = 2, SB = 4; };
 template <> struct Fmt<FMT_Q6K>   { static constexpr int TB = 6144, CH = 3, SB = 4; };
+template <> struct Fmt<FMT_Q50>   { static constexpr int TB = 5120, CH = 2, SB = 4; };
+template <> struct Fmt<FMT_Q51>   { static constexpr int TB = 5120, CH = 2, SB = 8; };
+template <> struct Fmt<FMT_Q5K>   { static constexpr int TB = 5120, CH = 2, SB = 3; };
+constexpr int kQ5Plane = 4096;  // 5-bit formats: word j of row r at kQ5Plane + 512 j + 4 r
+
+__host__ __device__ constexpr bool fmt_q5(int f) { return f == FMT_Q50 || f == FMT_Q51 || f == FMT_Q5K; }
+// Integer codes (decoded through the operand classes below) rather than E2M1.
+__host__ __device__ constexpr bool fmt_int(int f) { return f == FMT_MLX || f == FMT_Q6K || fmt_q5(f); }
+// Aux bytes per row tile and 256 inputs (four tiles): Q6_K fp16 d, Q5_K fp16 (d, dmin).
+__host__ __device__ constexpr int fmt_aux(int f) { return f == FMT_Q6K ? 256 : f == FMT_Q5K ? 512 : 0; }
+// Aux bytes of one row inside that record.
+__host__ __device__ constexpr int fmt_aux_row(int f) { return f == FMT_Q6K ? 2 : f == FMT_Q5K ? 4 : 0; }
 
 // ------------------------------------------------------------------ loads
 // Weight stream: read once, never reused by this SM -> no L1 allocation.
@@ -122,6 +139,67 @@ __device__ __forceinline__ uint32_t i6_op_lo(uint32_t w, uint32_t h) {
 }
 __device__ __forceinline__ uint32_t i6_op_hi(uint32_t w, uint32_t h) {
   return (w & 0x00F000F0u) | (h & 0x03000300u) | 0x3C003C00u;
+}
+// 5-bit codes: the fifth bit sits just above its nibble (bit 4 for class 1024, bit 8 for
+// class 64: the PR's "fifth bit at bit 8 of each halfword").  The layout stores the fifth
+// bit of input 8u + i of a 32-input half at bit (4i + 4 + u) mod 32 of the row's word, so
+// rotating that word right by u (one funnel shift) puts code i's bit at 4i + 4.
+__device__ __forceinline__ uint32_t q5_hi_for(uint32_t hw, int u) { return __funnelshift_r(hw, hw, u & 3); }
+__device__ __forceinline__ uint32_t i5_op_lo(uint32_t w, uint32_t h) {
+  return (w & 0x000F000Fu) | (h & 0x00100010u) | 0x3C003C00u;
+}
+__device__ __forceinline__ uint32_t i5_op_hi(uint32_t w, uint32_t h) {
+  return (w & 0x00F000F0u) | (h & 0x01000100u) | 0x3C003C00u;
+}
+
+// The four operands of one code word of an integer format: op0 = (n0, n4) and op2 =
+// (n2, n6) of class 1024, op1 = (n1, n5) and op3 = (n3, n7) of class 64.  `h`: the
+// high-bit word aligned for this code word (q6k_hi_for / q5_hi_for); unused for MLX.
+template <int FMT>
+__device__ __forceinline__ void int_ops(uint32_t w, uint32_t h, uint32_t (&op)[4]) {
+  const uint32_t r = rot8(w);
+  if (FMT == FMT_MLX) {
+    op[0] = i4_op_lo(w);
+    op[1] = i4_op_hi(w);
+    op[2] = i4_op_lo(r);
+    op[3] = i4_op_hi(r);
+  } else if (FMT == FMT_Q6K) {
+    const uint32_t hr = rot8(h);
+    op[0] = i6_op_lo(w, h);
+    op[1] = i6_op_hi(w, h);
+    op[2] = i6_op_lo(r, hr);
+    op[3] = i6_op_hi(r, hr);
+  } else {
+    const uint32_t hr = rot8(h);
+    op[0] = i5_op_lo(w, h);
+    op[1] = i5_op_hi(w, h);
+    op[2] = i5_op_lo(r, hr);
+    op[3] = i5_op_hi(r, hr);
+  }
+}
+
+// Per-block affine map of the 5-bit formats, w = s * code + bias (GGML blocks):
+//   Q5_0: s = d, bias = -16 d (the zero point as a minimum, "ZeroAsMin");
+//   Q5_1: s = d, bias = m;  Q5_K: s = d * sc, bias = -(dmin * mn).
+// sp: the row's SB scale bytes of the tile; ap: the row's aux record (Q5_K d, dmin);
+// blk: the 32-input block of the tile (0, 1).  s and bias are exact in fp32.
+template <int FMT>
+__device__ __forceinline__ float2 q5_affine(const uint8_t* sp, const uint8_t* ap, int blk) {
+  if (FMT == FMT_Q50) {
+    const float d = __half2float(*reinterpret_cast<const __half*>(sp + 2 * blk));
+    return make_float2(d, -16.0f * d);
+  } else if (FMT == FMT_Q51) {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(sp + 4 * blk);
+    return make_float2(__half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))),
+                       __half2float(__ushort_as_half((unsigned short)(v >> 16))));
+  } else {
+    const uint32_t v = (uint32_t)sp[0] | ((uint32_t)sp[1] << 8) | ((uint32_t)sp[2] << 16);
+    const float sc = (float)((v >> (12 * blk)) & 63u), mn = (float)((v >> (12 * blk + 6)) & 63u);
+    const uint32_t dd = *reinterpret_cast<const uint32_t*>(ap);
+    const float d = __half2float(__ushort_as_half((unsigned short)(dd & 0xFFFFu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(dd >> 16)));
+    return make_float2(d * sc, -(dmin * mn));
+  }
 }
 
 // ---------------------------------------------------------------- MoE finish

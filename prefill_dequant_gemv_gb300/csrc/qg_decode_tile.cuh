@@ -18,8 +18,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Decode one code word of row r: word wg (0..7) of the row's 64-input stage holds inputs
-// 8wg..8wg+7 (4-bit formats; Q6_K low nibbles, with the high bits from the tile's third
-// chunk); the result is four bf16x2 words in input order (low half = lower input).
+// 8wg..8wg+7 (4-bit formats; Q6_K and 5-bit low nibbles, with the high bits from the
+// tile's third chunk or fifth-bit plane); the result is four bf16x2 words in input order
+// (low half = lower input).  Raw stage layout: codes, then 128 rows' scales, then the
+// rows' aux records (Q6_K, Q5_K).
 template <int FMT>
 __device__ __forceinline__ void decode_word(const uint8_t* raw, int r, int wg, uint32_t w, uint32_t* o) {
   using F = Fmt<FMT>;
@@ -45,21 +47,15 @@ __device__ __forceinline__ void decode_word(const uint8_t* raw, int r, int wg, u
     }
   } else {
     uint32_t op[4];
-    const uint32_t rw = rot8(w);
-    if (FMT == FMT_MLX) {
-      op[0] = i4_op_lo(w);
-      op[1] = i4_op_hi(w);
-      op[2] = i4_op_lo(rw);
-      op[3] = i4_op_hi(rw);
-    } else {
+    uint32_t hh = 0;
+    if (FMT == FMT_Q6K) {
       const int quarter = wg >> 1;
       const uint32_t hw = *reinterpret_cast<const uint32_t*>(raw + ((rt * 3 + 2) * 32 + lane) * 16 + quarter * 4);
-      const uint32_t hh = q6k_hi_for(hw, wg & 1), hr = rot8(hh);
-      op[0] = i6_op_lo(w, hh);
-      op[1] = i6_op_hi(w, hh);
-      op[2] = i6_op_lo(rw, hr);
-      op[3] = i6_op_hi(rw, hr);
+      hh = q6k_hi_for(hw, wg & 1);
+    } else if (fmt_q5(FMT)) {
+      hh = q5_hi_for(*reinterpret_cast<const uint32_t*>(raw + kQ5Plane + (wg >> 2) * 512 + r * 4), wg & 3);
     }
+    int_ops<FMT>(w, hh, op);
     float code[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -74,6 +70,10 @@ __device__ __forceinline__ void decode_word(const uint8_t* raw, int r, int wg, u
       const float bias = __half2float(__ushort_as_half((unsigned short)(sw >> 16)));
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] = fmaf(s, code[j], bias);
+    } else if (fmt_q5(FMT)) {  // the fp32 weight, one rounding: fma of the exact s * code and bias
+      const float2 sb = q5_affine<FMT>(sp, raw + F::TB + 128 * F::SB + r * fmt_aux_row(FMT), wg >> 2);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = fmaf(sb.x, code[j], sb.y);
     } else {
       const float sc = (float)(int8_t)sp[wg >> 1];
       const float d = __half2float(*reinterpret_cast<const __half*>(raw + F::TB + 128 * F::SB + r * 2));

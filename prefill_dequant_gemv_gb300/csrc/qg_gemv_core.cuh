@@ -24,7 +24,7 @@ constexpr int kMaxStages = 48;
 template <int FMT> struct Stage {
   static constexpr int CODE = Fmt<FMT>::TB;            // per unit
   static constexpr int SCALE = 128 * Fmt<FMT>::SB;     // per unit
-  static constexpr int AUX = (FMT == FMT_Q6K) ? 256 : 0;  // per 4 units (Q6_K d)
+  static constexpr int AUX = fmt_aux(FMT);             // per 4 units (Q6_K d, Q5_K d and dmin)
   __host__ __device__ static constexpr int bytes(int C) { return C * (CODE + SCALE) + 2 * AUX; }
 };
 
@@ -50,7 +50,7 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t v, float& lo, float& hi) 
 // (16x0,16x4) (x1,x5) (16x2,16x6) (x3,x7).
 template <int FMT>
 __device__ __forceinline__ float4 stage_quarter(const uint32_t (&u)[8], uint32_t* dst) {
-  constexpr bool kInt = (FMT == FMT_MLX || FMT == FMT_Q6K);
+  constexpr bool kInt = fmt_int(FMT);
   uint32_t mb = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) mb = max(mb, max(u[i] & 0x7FFFu, (u[i] >> 16) & 0x7FFFu));
@@ -113,6 +113,8 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
     wd[rt][0] = v.x;
     wd[rt][1] = v.y;
     if (FMT == FMT_Q6K) hw[rt] = *reinterpret_cast<const uint32_t*>(st + ((rt * 3 + 2) * 32 + lane) * 16 + kq * 4);
+    if (fmt_q5(FMT))  // the row's fifth-bit word of this quarter's 32-input half
+      hw[rt] = *reinterpret_cast<const uint32_t*>(st + kQ5Plane + (kq >> 1) * 512 + (rt * 32 + lane) * 4);
   }
   // Activations of the quarter for every row m (both code words), then one 32-row group
   // at a time: decode, accumulate, fold -- so only one group's partials are live.
@@ -139,19 +141,14 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
         o1 = e2m1x2_h2<1>(w);
         o2 = e2m1x2_h2<2>(w);
         o3 = e2m1x2_h2<3>(w);
-      } else if (FMT == FMT_MLX) {
-        const uint32_t r = rot8(w);
-        o0 = i4_op_lo(w);
-        o1 = i4_op_hi(w);
-        o2 = i4_op_lo(r);
-        o3 = i4_op_hi(r);
       } else {
-        const uint32_t h = q6k_hi_for(hw[rt], wi);
-        const uint32_t r = rot8(w), hr = rot8(h);
-        o0 = i6_op_lo(w, h);
-        o1 = i6_op_hi(w, h);
-        o2 = i6_op_lo(r, hr);
-        o3 = i6_op_hi(r, hr);
+        uint32_t op[4];
+        const uint32_t h = FMT == FMT_Q6K ? q6k_hi_for(hw[rt], wi) : fmt_q5(FMT) ? q5_hi_for(hw[rt], 2 * (kq & 1) + wi) : 0u;
+        int_ops<FMT>(w, h, op);
+        o0 = op[0];
+        o1 = op[1];
+        o2 = op[2];
+        o3 = op[3];
       }
 #pragma unroll
       for (int m = 0; m < M; ++m) {
@@ -189,7 +186,7 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
         const float dot = fmaf(zq[m].x, P[m][0] + P[m][1], -zq[m].y);
         acc[rt][m] = fmaf(s, dot, fmaf(bias, zq[m].z, acc[rt][m]));
       }
-    } else {
+    } else if (FMT == FMT_Q6K) {
       const float sc = (float)(int8_t)sp[kq];
       const float d = __half2float(*reinterpret_cast<const __half*>(aux + row * 2));
       const float ds = d * sc;
@@ -197,6 +194,13 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
       for (int m = 0; m < M; ++m) {
         const float dot = fmaf(zq[m].x, P[m][0] + P[m][1], -zq[m].y);
         acc[rt][m] = fmaf(ds, dot, acc[rt][m]);
+      }
+    } else {  // 5-bit: w = s * code + bias over the quarter's 32-input block
+      const float2 sb = q5_affine<FMT>(sp, aux + row * fmt_aux_row(FMT), kq >> 1);
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const float dot = fmaf(zq[m].x, P[m][0] + P[m][1], -zq[m].y);
+        acc[rt][m] = fmaf(sb.x, dot, fmaf(sb.y, zq[m].z, acc[rt][m]));
       }
     }
   }

@@ -20,6 +20,8 @@ struct Geometry {
 };
 bool geometry(int fmt, int64_t n, int64_t k, Geometry* g);
 int format_block(int fmt);  // k must be a multiple of this (64, 32, 16, 256); 0 if unknown
+bool is_q5(int fmt);        // one of the 5-bit formats
+int aux_group_bytes(int fmt);  // aux bytes per row tile and 256 inputs (Q6_K, Q5_K), else 0
 
 // Per-device attributes, cached once per device.
 struct DeviceInfo {

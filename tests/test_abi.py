@@ -45,7 +45,8 @@ def test_status_strings(q):
     assert q.qg_status_str(99) == "QG_ERR_UNKNOWN"
 
 
-@pytest.mark.parametrize("fmt,bpw", [(wl.MLX_AFFINE4_G64, 4.5), (wl.MXFP4, 4.25), (wl.NVFP4, 4.5), (wl.Q6K, 6.5625)])
+@pytest.mark.parametrize("fmt,bpw", [(wl.MLX_AFFINE4_G64, 4.5), (wl.MXFP4, 4.25), (wl.NVFP4, 4.5), (wl.Q6K, 6.5625),
+                                     (wl.Q5_0, 5.5), (wl.Q5_1, 6.0), (wl.Q5_K, 5.5)])
 def test_packed_sizes_match_spec_and_bpw(q, fmt, bpw):
     for n, k in [(1024, 2048), (300, 768), (17408, 5120)]:
         assert q.qg_packed_sizes(fmt, n, k) == oracle.packed_sizes(fmt, n, k)
@@ -57,7 +58,7 @@ def test_q6k_output_layer_is_1_04_gb(q):
     assert round(sum(q.qg_packed_sizes(wl.Q6K, 248320, 5120)) / 1e9, 2) == 1.04
 
 
-@pytest.mark.parametrize("fmt", [wl.MLX_AFFINE4_G64, wl.MXFP4, wl.NVFP4, wl.Q6K])
+@pytest.mark.parametrize("fmt", [wl.MLX_AFFINE4_G64, wl.MXFP4, wl.NVFP4, wl.Q6K, wl.Q5_0, wl.Q5_1, wl.Q5_K])
 @pytest.mark.parametrize("shape", [(128, 256), (300, 768), (1, 256), (129, 512)])
 def test_pack_round_trip_through_oracle_reader(q, fmt, shape):
     n, k = shape
@@ -74,12 +75,15 @@ def test_pack_round_trip_through_oracle_reader(q, fmt, shape):
 
 
 def test_pack_ragged_k_for_small_blocks(q):
-    # NVFP4 K = 208 (13 blocks of 16) and MXFP4 K = 96 pad to whole 64-input groups
-    for fmt, k in [(wl.NVFP4, 208), (wl.MXFP4, 96)]:
+    # NVFP4 K = 208 (13 blocks of 16), MXFP4, Q5_0 and Q5_1 K = 96 pad to whole 64-input groups
+    for fmt, k in [(wl.NVFP4, 208), (wl.MXFP4, 96), (wl.Q5_0, 96), (wl.Q5_1, 160)]:
         w = wl.weight(fmt, 130, k, seed=3)
-        c, s, a = q.qg_pack_host(fmt, 130, k, w.codes, w.scales, None)
-        lc, ls, _ = oracle.unpack(fmt, 130, k, c, s)
-        assert np.array_equal(lc, w.codes) and np.array_equal(ls, w.scales)
+        c, s, a = q.qg_pack_host(fmt, 130, k, w.codes, w.scales, w.aux)
+        lc, ls, la = oracle.unpack(fmt, 130, k, c, s)
+        assert np.array_equal(lc, w.codes)
+        assert np.array_equal(ls.view(np.uint8), np.asarray(w.scales).view(np.uint8))
+        if w.aux is not None:
+            assert np.array_equal(la.view(np.uint16), w.aux.view(np.uint16))
 
 
 def test_pack_rejects_bad_input(q):
@@ -93,6 +97,17 @@ def test_pack_rejects_bad_input(q):
         q.qg_packed_sizes(wl.NVFP4, 128, 100)  # K not a multiple of 16
     with pytest.raises(q.QGError):
         q.qg_packed_sizes(9, 128, 128)  # unknown format
+    w5 = wl.weight(wl.Q5_K, 128, 256, seed=2)
+    bad5 = w5.codes.copy()
+    bad5[0, 0] = 32
+    with pytest.raises(q.QGError):
+        q.qg_pack_host(wl.Q5_K, 128, 256, bad5, w5.scales, w5.aux)  # 5-bit code above 31
+    sm = w5.scales.copy()
+    sm[1, 2, 1] = 64
+    with pytest.raises(q.QGError):
+        q.qg_pack_host(wl.Q5_K, 128, 256, w5.codes, sm, w5.aux)  # 6-bit minimum above 63
+    with pytest.raises(q.QGError):
+        q.qg_packed_sizes(wl.Q5_K, 128, 128)  # K not a multiple of 256
 
 
 def _desc(q, **kw):
@@ -156,6 +171,7 @@ def test_qgemm_grouped_host_validation(q):
     assert call(layer=_moe_desc(q, n_experts=32), topk=17) == 2  # above the router's limit
     assert call(t=0) == 1
     assert call(gate=0xA000) == 1                               # gate logits without a shared expert
+    assert call(layer=_moe_desc(q, fmt=wl.Q5_0)) == 2           # the 5-bit formats run on the dense paths only
     sh = _moe_desc(q, has_shared=1,
                    shared_gate_up=q.qg_weight(fmt=wl.MXFP4, n=256, k=256, codes=0x50000, scales=0x51000,
                                               tensor_scale=1.0),

@@ -10,13 +10,16 @@ from tests.gpu_util import dev_bf16, qlib, to_f64
 
 pytestmark = pytest.mark.gpu
 
-ALL = [wl.MLX_AFFINE4_G64, wl.MXFP4, wl.NVFP4, wl.Q6K]
+ALL = [wl.MLX_AFFINE4_G64, wl.MXFP4, wl.NVFP4, wl.Q6K, wl.Q5_0, wl.Q5_1, wl.Q5_K]
 # several 128 x 64 tiles, ragged row tails, padded K (NVFP4 208 = 13 blocks, MXFP4 96)
 SMALL = {
     wl.MLX_AFFINE4_G64: [(300, 640), (128, 64), (1000, 1280)],
     wl.MXFP4: [(300, 640), (257, 96), (1024, 2048)],
     wl.NVFP4: [(300, 208), (1000, 1280), (129, 512)],
     wl.Q6K: [(300, 768), (129, 256), (640, 1536)],
+    wl.Q5_0: [(300, 640), (257, 96), (1000, 1280)],
+    wl.Q5_1: [(300, 160), (129, 512), (640, 1536)],
+    wl.Q5_K: [(300, 768), (129, 256), (640, 1536)],
 }
 
 
@@ -105,12 +108,17 @@ FULL = [
     ("nvfp4_down_5120x17408", (1, 4)),
     ("q6k_5120x6144", (1, 4)),
     ("q6k_output_248320x5120", (1, 4)),
+    ("q5_k_gate_up_17408x5120", (1, 4)),
+    ("q5_k_down_5120x17408", (1, 3)),
+    ("q5_k_out_5120x6144", (2,)),
+    ("q5_0_gate_up_17408x5120", (1, 4)),
+    ("q5_1_gate_up_17408x5120", (1, 2)),
 ]
 
 
 @pytest.mark.parametrize("name,ms", FULL)
 def test_gemv_full_size_sampled_rows(q, name, ms):
-    cfg = wl.WORKLOADS[name]
+    cfg = wl.WORKLOADS.get(name) or wl.WORKLOADS_Q5[name]
     fmt, n, k = cfg["fmt"], cfg["n"], cfg["k"]
     w = wl.weight(fmt, n, k, seed=0)
     pw = q.PackedWeight.from_logical(w)
@@ -128,7 +136,9 @@ def test_gemv_full_size_sampled_rows(q, name, ms):
 # stream-K with tickets (more row tiles than SMs: 160 here).  Every output is checked, twice
 # in a row on one workspace (bit-identical).
 PARTITIONS = [("whole_row_tiles", wl.NVFP4, 136 * 128, 256), ("cluster_split", wl.MXFP4, 20 * 128 - 37, 1024),
-              ("stream_k", wl.MLX_AFFINE4_G64, 160 * 128, 512), ("stream_k_q6k", wl.Q6K, 170 * 128 - 5, 512)]
+              ("stream_k", wl.MLX_AFFINE4_G64, 160 * 128, 512), ("stream_k_q6k", wl.Q6K, 170 * 128 - 5, 512),
+              ("stream_k_q5k", wl.Q5_K, 170 * 128 - 5, 512), ("cluster_split_q5_1", wl.Q5_1, 20 * 128 - 9, 1056),
+              ("whole_row_tiles_q5_0", wl.Q5_0, 136 * 128 - 100, 288)]
 
 
 @pytest.mark.parametrize("name,fmt,n,k", PARTITIONS)

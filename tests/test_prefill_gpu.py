@@ -10,7 +10,7 @@ from tests.gpu_util import dev_bf16, qlib, to_f64
 
 pytestmark = pytest.mark.gpu
 
-ALL = [wl.MLX_AFFINE4_G64, wl.MXFP4, wl.NVFP4, wl.Q6K]
+ALL = [wl.MLX_AFFINE4_G64, wl.MXFP4, wl.NVFP4, wl.Q6K, wl.Q5_0, wl.Q5_1, wl.Q5_K]
 # (n, k, tokens): several 128-row tiles, ragged rows, ragged token tiles (256 per tile),
 # K that is not a multiple of the 64-deep stage for the small-block formats
 SHAPES = {
@@ -18,6 +18,9 @@ SHAPES = {
     wl.MXFP4: [(300, 640, 260), (1024, 2048, 96), (257, 96, 33)],
     wl.NVFP4: [(300, 208, 300), (1000, 1280, 600), (129, 512, 7)],
     wl.Q6K: [(300, 768, 130), (640, 1536, 257), (129, 256, 5)],
+    wl.Q5_0: [(300, 640, 5), (256, 1024, 300), (129, 96, 17)],
+    wl.Q5_1: [(300, 160, 260), (1024, 2048, 96), (257, 512, 33)],
+    wl.Q5_K: [(300, 768, 130), (640, 1536, 257), (129, 256, 5)],
 }
 
 
@@ -122,3 +125,18 @@ def test_token_count_boundaries(q, t):
     err = np.abs(got - ref)
     assert np.all(err <= oracle.tolerance(w, x, res))
     assert ws.status() == 0
+
+
+@pytest.mark.parametrize("fmt,t", [(wl.Q5_K, 128), (wl.Q5_0, 1000), (wl.Q5_1, 40)])
+def test_prefill_q5_full_size_sampled(q, fmt, t):
+    """The 5-bit formats at the 17408 x 5120 gate/up size against one small-token tile, several
+    256-token tiles and 40 tokens: every token of sampled rows against the oracle."""
+    n, k = 17408, 5120
+    w = wl.weight(fmt, n, k, seed=0)
+    x = wl.activations(t, k, seed=7)
+    got, _ = _run(q, w, x, None)
+    rng = np.random.default_rng(8)
+    rows = np.unique(np.concatenate([[0, 127, 128, n - 1], rng.integers(0, n, 60)]))
+    ref, _ = oracle.gemv_rows(w, x, rows)
+    err = np.abs(got[:, rows] - ref)
+    assert np.all(err <= oracle.tolerance(w, x, rows=rows)), f"{fmt} t={t}"

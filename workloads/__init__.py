@@ -214,6 +214,14 @@ WORKLOADS = {
     "q6k_output_248320x5120": dict(fmt=Q6K, n=248320, k=5120, ms=(1, 2, 3, 4), residual=False),
     "q6k_5120x6144": dict(fmt=Q6K, n=5120, k=6144, ms=(1, 2, 3, 4), residual=False),
 }
+# The 5-bit GEMVs of the Q6_K operand PR's 5-bit commit (its q5k / q50 / q51 rows).
+WORKLOADS_Q5 = {
+    "q5_k_gate_up_17408x5120": dict(fmt=Q5_K, n=17408, k=5120, ms=(1, 2, 3, 4), residual=False),
+    "q5_k_down_5120x17408": dict(fmt=Q5_K, n=5120, k=17408, ms=(1, 2, 3, 4), residual=True),
+    "q5_k_out_5120x6144": dict(fmt=Q5_K, n=5120, k=6144, ms=(1, 2, 3, 4), residual=False),
+    "q5_0_gate_up_17408x5120": dict(fmt=Q5_0, n=17408, k=5120, ms=(1, 2, 3, 4), residual=False),
+    "q5_1_gate_up_17408x5120": dict(fmt=Q5_1, n=17408, k=5120, ms=(1, 2, 3, 4), residual=False),
+}
 MOE_DECODE = dict(fmt=MXFP4, n_experts=512, hidden=2048, ffn=512, topk=10, tokens=4, shared=True)
 PREFILL = dict(fmt=NVFP4, n=17408, k=5120, tokens=8192, tile=128)
 MOE_PREFILL = dict(fmt=MXFP4, n_experts=512, hidden=2048, ffn=512, topk=10, tokens=8192, shared=True)
