@@ -193,8 +193,10 @@ __device__ __forceinline__ float2 q5_affine(const uint8_t* sp, const uint8_t* ap
     return make_float2(__half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))),
                        __half2float(__ushort_as_half((unsigned short)(v >> 16))));
   } else {
-    const uint32_t v = (uint32_t)sp[0] | ((uint32_t)sp[1] << 8) | ((uint32_t)sp[2] << 16);
-    const float sc = (float)((v >> (12 * blk)) & 63u), mn = (float)((v >> (12 * blk + 6)) & 63u);
+    const uint32_t v = ((uint32_t)sp[0] | ((uint32_t)sp[1] << 8) | ((uint32_t)sp[2] << 16)) >> (12 * blk);
+    // 6-bit integers to float exactly: (2^23 + i) - 2^23, cheaper than an integer conversion
+    const float sc = __uint_as_float(0x4B000000u | (v & 63u)) - 8388608.0f;
+    const float mn = __uint_as_float(0x4B000000u | ((v >> 6) & 63u)) - 8388608.0f;
     const uint32_t dd = *reinterpret_cast<const uint32_t*>(ap);
     const float d = __half2float(__ushort_as_half((unsigned short)(dd & 0xFFFFu)));
     const float dmin = __half2float(__ushort_as_half((unsigned short)(dd >> 16)));
