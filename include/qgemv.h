@@ -47,13 +47,14 @@
  *   inputs 64g..64g+63 -- has index t = q*KG + g, KG = KP/64.  Padding holds
  *   zero codes and zero scales.
  *   codes : TB bytes per tile at t*TB, TB = 4096 (4-bit), 6144 (Q6_K) or 5120 (5-bit).  Row r of
- *           the tile (rt = r/32, lane = r%32) owns the 16-byte chunks at byte
- *           ((rt*CH + c)*32 + lane)*16, CH = 2 (4-bit) or 3 (Q6_K).
- *           4-bit, chunk c = 0,1: byte b holds code (64g + 32c + 2b) in its low
+ *           the tile (rt = r/32, lane = r%32):
+ *           4-bit (and the 5-bit low nibbles): 16-byte chunks c = 0,1 at byte
+ *           ((rt*2 + c)*32 + lane)*16; byte b holds code (64g + 32c + 2b) in its low
  *           nibble and code (64g + 32c + 2b + 1) in its high nibble.
- *           Q6_K: chunks 0,1 hold the low nibbles (code & 15) as above; chunk 2 is
- *           four little-endian 32-bit words, word w holding in nibble j (bits
- *           4j..4j+3) hi(64g+16w+j) | hi(64g+16w+8+j) << 2, hi(code) = code >> 4.
+ *           Q6_K: the 16 inputs 64g + 16kq .. +15 (kq = 0..3) are three little-endian
+ *           32-bit words, word c (0..2) at byte ((rt*4 + kq)*3 + c)*128 + 4*lane; byte j
+ *           of word c holds in bits 2..7 the code of input 64g + 16kq + 4c + j and in bits
+ *           0..1 bits 2c..2c+1 of the code of input 64g + 16kq + 12 + j.
  *           5-bit: bytes 0..4095 hold the low nibbles (code & 15) as the 4-bit chunks
  *           (CH = 2); bytes 4096..5119 hold the fifth bits: two little-endian 32-bit
  *           words per row, word j (0, 1) of row r at byte 4096 + 512j + 4r, holding

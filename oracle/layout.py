@@ -9,13 +9,14 @@ behind a shared helper.  The specification ("T128x64"):
   t = q * KG + g with KG = KP / 64.  Padding holds zero codes and zero scales.
 * codes: TB bytes per tile (4096 for 4-bit formats, 6144 for Q6_K) at offset
   t * TB.  Row r of the tile (rt = r // 32, lane = r % 32) owns the 16-byte
-  chunks at ((rt * CH + c) * 32 + lane) * 16, CH = 2 (4-bit) or 3 (Q6_K).
+  chunks at ((rt * 2 + c) * 32 + lane) * 16 (4-bit and 5-bit formats).
   - 4-bit formats, chunk c in {0, 1}: byte b holds code (g*64 + c*32 + 2b) in
     its low nibble and code (g*64 + c*32 + 2b + 1) in its high nibble.
-  - Q6_K: chunks 0 and 1 hold the low nibbles (code & 15) as above; chunk 2 is
-    four little-endian 32-bit words, word w in 0..3 holding in its nibble j
-    (bits 4j..4j+3) hi(g*64 + 16w + j) | hi(g*64 + 16w + 8 + j) << 2, with
-    hi(code) = code >> 4.
+  - Q6_K (TB = 6144): row r's 16-column quarter kq (columns g*64 + 16 kq ..)
+    is three little-endian 32-bit words, word c in 0..2 at byte offset
+    ((rt * 4 + kq) * 3 + c) * 128 + lane * 4; byte j of word c holds in bits
+    2..7 the code of column 16 kq + 4c + j and in bits 0..1 bits 2c..2c+1 of the
+    code of column 16 kq + 12 + j.
 * scales: 128 * SB bytes per tile at offset t * 128 * SB, SB bytes per row:
   - NVFP4 (SB = 4): byte i = E4M3 scale of columns g*64 + 16i .. +15;
   - MXFP4 (SB = 2): byte i = E8M0 scale of columns g*64 + 32i .. +31;
@@ -73,27 +74,24 @@ def unpack(fmt: int, n: int, k: int, codes: np.ndarray, scales: np.ndarray, aux=
     np_, kp, nt, kg = _geometry(fmt, n, k)
     codes = np.frombuffer(np.ascontiguousarray(codes).tobytes(), dtype=np.uint8)
     scales = np.frombuffer(np.ascontiguousarray(scales).tobytes(), dtype=np.uint8)
-    ch = 3 if fmt == Q6K else 2
     tb = 6144 if fmt == Q6K else 5120 if fmt in _Q5 else 4096
     tiles = codes.reshape(nt, kg, tb)
-    # chunk bytes indexed [q, g, rt, c, lane, b]
-    cb = tiles[:, :, :4 * ch * 512].reshape(nt, kg, 4, ch, 32, 16)
-    lo = cb[:, :, :, :2] & 0x0F
-    hi = cb[:, :, :, :2] >> 4
-    nib = np.stack([lo, hi], axis=-1)  # [q, g, rt, c, lane, b, 2]
-    # -> [q, rt, lane, g, c, b, 2] -> rows x columns
-    logical = nib.transpose(0, 2, 4, 1, 3, 5, 6).reshape(np_, kp).astype(np.uint8)
     if fmt == Q6K:
-        words = cb[:, :, :, 2].reshape(nt, kg, 4, 32, 4, 4)  # [q, g, rt, lane, w, byte]
-        words = words.astype(np.uint32)
-        w32 = words[..., 0] | (words[..., 1] << 8) | (words[..., 2] << 16) | (words[..., 3] << 24)
-        j = np.arange(8, dtype=np.uint32)
-        nibs = (w32[..., None] >> (4 * j)) & 0xF  # [q, g, rt, lane, w, j]
-        h_first = nibs & 3  # code 16w + j
-        h_second = nibs >> 2  # code 16w + 8 + j
-        hsel = np.concatenate([h_first, h_second], axis=-1)  # [q, g, rt, lane, w, 16]
-        hrow = hsel.transpose(0, 2, 3, 1, 4, 5).reshape(np_, kp).astype(np.uint8)
-        logical = (logical | (hrow << 4)).astype(np.uint8)
+        # bytes indexed [q, g, rt, kq, c, lane, j]
+        qb = tiles.reshape(nt, kg, 4, 4, 3, 32, 4)
+        main = qb >> 2  # codes of columns 16 kq + 4c + j
+        low = (qb[..., 0, :, :] & 3) | ((qb[..., 1, :, :] & 3) << 2) | ((qb[..., 2, :, :] & 3) << 4)  # 12 + j
+        cols = np.concatenate([main.transpose(0, 1, 2, 3, 5, 4, 6).reshape(nt, kg, 4, 4, 32, 12),
+                               low.reshape(nt, kg, 4, 4, 32, 4)], axis=-1)  # [q, g, rt, kq, lane, 16]
+        logical = cols.transpose(0, 2, 4, 1, 3, 5).reshape(np_, kp).astype(np.uint8)
+    else:
+        # chunk bytes indexed [q, g, rt, c, lane, b]
+        cb = tiles[:, :, :4096].reshape(nt, kg, 4, 2, 32, 16)
+        lo = cb & 0x0F
+        hi = cb >> 4
+        nib = np.stack([lo, hi], axis=-1)  # [q, g, rt, c, lane, b, 2]
+        # -> [q, rt, lane, g, c, b, 2] -> rows x columns
+        logical = nib.transpose(0, 2, 4, 1, 3, 5, 6).reshape(np_, kp).astype(np.uint8)
     if fmt in _Q5:
         fb = tiles[:, :, 4096:].reshape(nt, kg, 2, 128, 4).transpose(0, 1, 3, 2, 4).astype(np.uint32)  # [q, g, row, j, byte]
         w32 = fb[..., 0] | (fb[..., 1] << 8) | (fb[..., 2] << 16) | (fb[..., 3] << 24)

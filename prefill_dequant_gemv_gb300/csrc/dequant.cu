@@ -38,14 +38,30 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantArgs a) {
   const int row = (int)(n % 128), rt = row / 32, lane = row % 32;
   const int64_t t = q * a.kg + g;
   const uint8_t* tc = a.codes + t * F::TB;
-  const uint2 v = *reinterpret_cast<const uint2*>(tc + ((rt * F::CH + (kq >> 1)) * 32 + lane) * 16 + (kq & 1) * 8);
   const uint8_t* sp = a.scales + t * 128 * F::SB + row * F::SB;
   float w[16];
+  if constexpr (FMT == FMT_Q6K) {  // one quarter: three words, eight operands (input pairs (4c, 4c+2), (4c+1, 4c+3))
+    const uint8_t* qb = tc + q6k_word_offset(rt, kq, 0, lane);
+    uint32_t op[8];
+    q6k_ops(*reinterpret_cast<const uint32_t*>(qb), *reinterpret_cast<const uint32_t*>(qb + 128),
+            *reinterpret_cast<const uint32_t*>(qb + 256), op);
+    const float sc = (float)(int8_t)sp[kq];
+    const float d = __half2float(*reinterpret_cast<const __half*>(a.aux + (q * (a.kg / 4) + g / 4) * 256 + row * 2));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 e = __half22float2(*reinterpret_cast<const __half2*>(&op[j]));
+      const float mul = j < 6 ? 256.0f : 1024.0f;
+      const int base = (j >> 1) * 4 + (j & 1);
+      w[base] = (d * sc) * ((e.x - 1.0f) * mul - 32.0f);
+      w[base + 2] = (d * sc) * ((e.y - 1.0f) * mul - 32.0f);
+    }
+  } else {
+  const uint2 v = *reinterpret_cast<const uint2*>(tc + ((rt * F::CH + (kq >> 1)) * 32 + lane) * 16 + (kq & 1) * 8);
 #pragma unroll
   for (int wi = 0; wi < 2; ++wi) {
     const uint32_t wd = wi ? v.y : v.x;
     float* o = w + wi * 8;
-    if (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
+    if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
       float S;
       if (FMT == FMT_NVFP4) {
         const uint32_t sw = *reinterpret_cast<const uint32_t*>(sp);
@@ -71,9 +87,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantArgs a) {
       // op1 = (n1, n5) and op3 = (n3, n7) are 1 + code/64
       uint32_t op[4];
       uint32_t hh = 0;
-      if (FMT == FMT_Q6K)
-        hh = q6k_hi_for(*reinterpret_cast<const uint32_t*>(tc + ((rt * 3 + 2) * 32 + lane) * 16 + kq * 4), wi);
-      else if (fmt_q5(FMT))
+      if (fmt_q5(FMT))
         hh = q5_hi_for(*reinterpret_cast<const uint32_t*>(tc + kQ5Plane + (kq >> 1) * 512 + row * 4),
                        2 * (kq & 1) + wi);
       int_ops<FMT>(wd, hh, op);
@@ -103,6 +117,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantArgs a) {
         }
       }
     }
+  }
   }
   if (n >= a.n) return;
   const int64_t k0 = g * 64 + kq * 16;

@@ -93,7 +93,6 @@ extern "C" qg_status qg_pack_host(int fmt, int64_t n, int64_t k, const uint8_t* 
   memset(so, 0, sb);
   if (ab) memset(ao, 0, ab);
 
-  const int ch = q6k ? 3 : 2;
   for (int64_t r = 0; r < n; ++r) {
     const int64_t q = r / 128;
     const int row = (int)(r % 128), rt = row / 32, lane = row % 32;
@@ -102,14 +101,19 @@ extern "C" qg_status qg_pack_host(int fmt, int64_t n, int64_t k, const uint8_t* 
       const int64_t gi = c / 64;
       const int kk = (int)(c % 64);
       uint8_t* tile = co + (size_t)(q * g.kg + gi) * g.tile_bytes;
-      const int chunk = kk / 32, byte = (kk % 32) / 2, high = kk & 1;
       const uint8_t code = src[c];
-      tile[((rt * ch + chunk) * 32 + lane) * 16 + byte] |= (uint8_t)((code & 15) << (4 * high));
-      if (q6k) {
-        const int w = kk / 16, j = kk % 16;
-        const int bit = 4 * (j % 8) + (j < 8 ? 0 : 2);  // nibble j%8, low or high bit pair
-        tile[((rt * ch + 2) * 32 + lane) * 16 + w * 4 + bit / 8] |= (uint8_t)((code >> 4) << (bit % 8));
+      if (q6k) {  // quarter kq, words of ((rt*4 + kq)*3 + w)*128 + lane*4
+        const int kq = kk / 16, i = kk % 16;
+        uint8_t* qw = tile + ((rt * 4 + kq) * 3) * 128 + lane * 4;
+        if (i < 12) {
+          qw[(i / 4) * 128 + i % 4] |= (uint8_t)(code << 2);  // bits 2..7 of byte i%4 of word i/4
+        } else {
+          for (int w = 0; w < 3; ++w) qw[w * 128 + (i - 12)] |= (uint8_t)((code >> (2 * w)) & 3);
+        }
+        continue;
       }
+      const int chunk = kk / 32, byte = (kk % 32) / 2, high = kk & 1;
+      tile[((rt * 2 + chunk) * 32 + lane) * 16 + byte] |= (uint8_t)((code & 15) << (4 * high));
       if (q5) {  // fifth bit of input 32j + 8u + i at bit (4i + 4 + u) mod 32 of word j
         const int j = kk / 32, u = (kk % 32) / 8, i = kk % 8;
         const int bit = (4 * i + 4 + u) % 32;

@@ -7,10 +7,11 @@
 //    is exact in f16.
 //  * Integer codes (MLX affine, Q6_K): the zero point and the integer-to-float
 //    conversion live in the operand's bit pattern.  The code is placed in the
-//    mantissa of 1.0 (f16), giving the exact operand 1 + code/1024 or 1 + code/64;
-//    the constant 1 (and Q6_K's zero point 32) is removed once per block with the
-//    block's input sums instead of once per weight.  This is the PR's half operand
-//    1 + code/64, whose offset the PR removes by subtracting 1.5.
+//    mantissa of 1.0 (f16), giving the exact operand 1 + code/1024, 1 + code/256 or
+//    1 + code/64; the constant 1 (and Q6_K's zero point 32) is removed once per block
+//    with the block's input sums instead of once per weight.  This is the PR's half
+//    operand 1 + code/64, whose offset the PR removes by subtracting 1.5; Q6_K keeps
+//    its 6-bit codes byte-aligned so that most operands take one mask.
 //  * 5-bit codes (Q5_0, Q5_1, Q5_K; the PR's 5-bit nibble operand): the nibble with
 //    the fifth bit just above it, 1 + code/1024 or 1 + code/64 (exact for codes to 31);
 //    zero points and minimums are a per-block affine term, as for MLX.
@@ -87,13 +88,6 @@ __device__ __forceinline__ float e8m0_f32(uint32_t e) {
 // Byte rotations of a 32-bit word (one PRMT each).
 __device__ __forceinline__ uint32_t rot8(uint32_t w)  { return __byte_perm(w, w, 0x0321); }
 
-// Q6_K high-bit word for the low-nibble word `half` (0: codes 16w..16w+7, 1: codes
-// 16w+8..16w+15) of the layout's chunk-2 word: after this shift, the high bits of
-// the code in nibble i of the low word sit at bits 4i+4..4i+5 (mod 32), so the same
-// byte rotations align them above the rotated nibble.
-__device__ __forceinline__ uint32_t q6k_hi_for(uint32_t hw, int half) {
-  return half ? __funnelshift_l(hw, hw, 2) : __funnelshift_l(hw, hw, 4);
-}
 
 // ---------------------------------------------------------------- f16 operands
 // Mixed-precision FMA: c + a.half * b.half in fp32 (the f16 x f16 product is exact
@@ -131,15 +125,30 @@ __device__ __forceinline__ uint32_t e2m1x2_h2(uint32_t wd) {
 // accumulator, and the constants are removed per block with precomputed sums.
 __device__ __forceinline__ uint32_t i4_op_lo(uint32_t w) { return (w & 0x000F000Fu) | 0x3C003C00u; }
 __device__ __forceinline__ uint32_t i4_op_hi(uint32_t w) { return (w & 0x00F000F0u) | 0x3C003C00u; }
-// Q6_K: the two high bits of each code sit just above its nibble (bits 4..5 for
-// class 1024, 8..9 for class 64); `h` is the high-bit word aligned by q6k_hi_for and
-// rotated like the low word.
-__device__ __forceinline__ uint32_t i6_op_lo(uint32_t w, uint32_t h) {
-  return (w & 0x000F000Fu) | (h & 0x00300030u) | 0x3C003C00u;
+// Q6_K (zero point 32 in the operand, as the PR does, with byte-aligned codes): a tile row's
+// 16-input quarter is three 32-bit words; byte j of word c holds the code of input 4c + j in
+// bits 2..7 and bits 2c..2c+1 of the code of input 12 + j in bits 0..1.  Word c of quarter
+// kq of row (rt, lane) sits at q6k_word_offset(rt, kq, c, lane): a warp reads 128 bytes.
+__host__ __device__ constexpr int q6k_word_offset(int rt, int kq, int c, int lane) {
+  return ((rt * 4 + kq) * 3 + c) * 128 + lane * 4;
 }
-__device__ __forceinline__ uint32_t i6_op_hi(uint32_t w, uint32_t h) {
-  return (w & 0x00F000F0u) | (h & 0x03000300u) | 0x3C003C00u;
+// The quarter's eight operands: (x0,x2) (x1,x3) (x4,x6) (x5,x7) (x8,x10) (x9,x11) are
+// 1 + code/256 (the code in mantissa bits 2..7, straight from the word or its byte
+// rotation), (x12,x14) (x13,x15) are 1 + code/1024 (the code gathered from the three words'
+// low bit pairs into mantissa bits 0..5).
+__device__ __forceinline__ void q6k_ops(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t (&op)[8]) {
+  constexpr uint32_t K = 0x3C003C00u, M6 = 0x00FC00FCu, M2 = 0x03030303u;
+  op[0] = (w0 & M6) | K;
+  op[1] = (rot8(w0) & M6) | K;
+  op[2] = (w1 & M6) | K;
+  op[3] = (rot8(w1) & M6) | K;
+  op[4] = (w2 & M6) | K;
+  op[5] = (rot8(w2) & M6) | K;
+  const uint32_t t = (w0 & M2) + (w1 & M2) * 4u + (w2 & M2) * 16u;  // disjoint fields: + is |
+  op[6] = (t & 0x003F003Fu) | K;
+  op[7] = (rot8(t) & 0x003F003Fu) | K;
 }
+
 // 5-bit codes: the fifth bit sits just above its nibble (bit 4 for class 1024, bit 8 for
 // class 64: the PR's "fifth bit at bit 8 of each halfword").  The layout stores the fifth
 // bit of input 8u + i of a 32-input half at bit (4i + 4 + u) mod 32 of the row's word, so
@@ -152,23 +161,18 @@ __device__ __forceinline__ uint32_t i5_op_hi(uint32_t w, uint32_t h) {
   return (w & 0x00F000F0u) | (h & 0x01000100u) | 0x3C003C00u;
 }
 
-// The four operands of one code word of an integer format: op0 = (n0, n4) and op2 =
-// (n2, n6) of class 1024, op1 = (n1, n5) and op3 = (n3, n7) of class 64.  `h`: the
-// high-bit word aligned for this code word (q6k_hi_for / q5_hi_for); unused for MLX.
+// The four operands of one code word of MLX affine or a 5-bit format: op0 = (n0, n4) and
+// op2 = (n2, n6) of class 1024, op1 = (n1, n5) and op3 = (n3, n7) of class 64.  `h`: the
+// fifth-bit word aligned for this code word (q5_hi_for); unused for MLX.
 template <int FMT>
 __device__ __forceinline__ void int_ops(uint32_t w, uint32_t h, uint32_t (&op)[4]) {
+  static_assert(FMT == FMT_MLX || fmt_q5(FMT), "nibble-word formats only");
   const uint32_t r = rot8(w);
   if (FMT == FMT_MLX) {
     op[0] = i4_op_lo(w);
     op[1] = i4_op_hi(w);
     op[2] = i4_op_lo(r);
     op[3] = i4_op_hi(r);
-  } else if (FMT == FMT_Q6K) {
-    const uint32_t hr = rot8(h);
-    op[0] = i6_op_lo(w, h);
-    op[1] = i6_op_hi(w, h);
-    op[2] = i6_op_lo(r, hr);
-    op[3] = i6_op_hi(r, hr);
   } else {
     const uint32_t hr = rot8(h);
     op[0] = i5_op_lo(w, h);

@@ -73,7 +73,25 @@ __device__ __forceinline__ float4 stage_quarter(const uint32_t (&u)[8], uint32_t
     return *reinterpret_cast<uint32_t*>(&h);
   };
   float4 z = make_float4(inv, 0.0f, 0.0f, 0.0f);
-  if (kInt) {
+  if (FMT == FMT_Q6K) {
+    // operand order of q6k_ops: (x0,x2) (x1,x3) (x4,x6) (x5,x7) (x8,x10) (x9,x11) of class 256
+    // (activations x4), (x12,x14) (x13,x15) of class 1024 (activations x16)
+    const float* q = v;
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(h2(4.0f * q[0], 4.0f * q[2]), h2(4.0f * q[1], 4.0f * q[3]),
+                                                  h2(4.0f * q[4], 4.0f * q[6]), h2(4.0f * q[5], 4.0f * q[7]));
+    reinterpret_cast<uint4*>(dst)[1] = make_uint4(h2(4.0f * q[8], 4.0f * q[10]), h2(4.0f * q[9], 4.0f * q[11]),
+                                                  h2(16.0f * q[12], 16.0f * q[14]), h2(16.0f * q[13], 16.0f * q[15]));
+    float x4 = 0.0f, x16 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 12; ++i) x4 += q[i];
+#pragma unroll
+    for (int i = 12; i < 16; ++i) x16 += q[i];
+    const float xsum = (x4 + x16) * inv;              // X, unscaled
+    const float xop = fmaf(4.0f, x4, 16.0f * x16) * inv;  // the operands' constant part, unscaled
+    z.x = 64.0f * inv;
+    z.y = fmaf(64.0f, xop, 32.0f * xsum);  // and the zero point 32
+    z.z = xsum;
+  } else if (kInt) {
     float x16 = 0.0f, x1 = 0.0f;
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
@@ -86,7 +104,7 @@ __device__ __forceinline__ float4 stage_quarter(const uint32_t (&u)[8], uint32_t
     const float xsum = (x16 + x1) * inv;           // X, unscaled
     const float xop = fmaf(16.0f, x16, x1) * inv;  // the operands' constant part, unscaled
     z.x = 64.0f * inv;
-    z.y = (FMT == FMT_Q6K) ? fmaf(64.0f, xop, 32.0f * xsum) : 64.0f * xop;
+    z.y = 64.0f * xop;
     z.z = xsum;
   } else {
 #pragma unroll
@@ -109,10 +127,17 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
   uint32_t hw[4];
 #pragma unroll
   for (int rt = 0; rt < 4; ++rt) {
-    const uint2 v = *reinterpret_cast<const uint2*>(st + ((rt * F::CH + (kq >> 1)) * 32 + lane) * 16 + (kq & 1) * 8);
-    wd[rt][0] = v.x;
-    wd[rt][1] = v.y;
-    if (FMT == FMT_Q6K) hw[rt] = *reinterpret_cast<const uint32_t*>(st + ((rt * 3 + 2) * 32 + lane) * 16 + kq * 4);
+    if (FMT != FMT_Q6K) {
+      const uint2 v = *reinterpret_cast<const uint2*>(st + ((rt * F::CH + (kq >> 1)) * 32 + lane) * 16 + (kq & 1) * 8);
+      wd[rt][0] = v.x;
+      wd[rt][1] = v.y;
+    }
+    if (FMT == FMT_Q6K) {  // the row's three words of this quarter
+      const uint8_t* qb = st + q6k_word_offset(rt, kq, 0, lane);
+      wd[rt][0] = *reinterpret_cast<const uint32_t*>(qb);
+      wd[rt][1] = *reinterpret_cast<const uint32_t*>(qb + 128);
+      hw[rt] = *reinterpret_cast<const uint32_t*>(qb + 256);
+    }
     if (fmt_q5(FMT))  // the row's fifth-bit word of this quarter's 32-input half
       hw[rt] = *reinterpret_cast<const uint32_t*>(st + kQ5Plane + (kq >> 1) * 512 + (rt * 32 + lane) * 4);
   }
@@ -132,18 +157,25 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
     float P[M][2];
 #pragma unroll
     for (int m = 0; m < M; ++m) P[m][0] = P[m][1] = 0.0f;
+    uint32_t q6[8];
+    if (FMT == FMT_Q6K) q6k_ops(wd[rt][0], wd[rt][1], hw[rt], q6);
 #pragma unroll
     for (int wi = 0; wi < 2; ++wi) {
       const uint32_t w = wd[rt][wi];
       uint32_t o0, o1, o2, o3;
-      if (FMT == FMT_MXFP4 || FMT == FMT_NVFP4) {
+      if constexpr (FMT == FMT_Q6K) {
+        o0 = q6[4 * wi];
+        o1 = q6[4 * wi + 1];
+        o2 = q6[4 * wi + 2];
+        o3 = q6[4 * wi + 3];
+      } else if constexpr (FMT == FMT_MXFP4 || FMT == FMT_NVFP4) {
         o0 = e2m1x2_h2<0>(w);
         o1 = e2m1x2_h2<1>(w);
         o2 = e2m1x2_h2<2>(w);
         o3 = e2m1x2_h2<3>(w);
       } else {
         uint32_t op[4];
-        const uint32_t h = FMT == FMT_Q6K ? q6k_hi_for(hw[rt], wi) : fmt_q5(FMT) ? q5_hi_for(hw[rt], 2 * (kq & 1) + wi) : 0u;
+        const uint32_t h = fmt_q5(FMT) ? q5_hi_for(hw[rt], 2 * (kq & 1) + wi) : 0u;
         int_ops<FMT>(w, h, op);
         o0 = op[0];
         o1 = op[1];
