@@ -12,10 +12,11 @@
 //            its own; fp32 results per (token, expert)
 //   finish   out[t] = bf16( sum_j p[t, j] * down_{e_j}[t] + shared[t] ) (§4.1 "Finish")
 //
-// The grouped GEMV is the dense GEMV's stream-K pipeline (qg_gemv_core.cuh) over a unit
-// space of (group, 128-row tile, 64-input group) with groups = active experts (ascending)
-// then the shared expert once per token; each group is padded to whole chunks so a chunk never spans two
-// experts' weights.
+// The grouped GEMV runs the dense GEMV's decode (qg_gemv_core.cuh) over segments (group,
+// 128-row tile, 1/P of the inputs) with groups = active experts (ascending) then the shared
+// expert once per token; each CTA takes an equal share of whole segments, its 12 consumer
+// warps hand each segment's partials to a reducer warp (two buffers, so they run on), and
+// the P parts of an output are summed by whoever reads it next, in part order.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -32,7 +33,7 @@ namespace qg {
 constexpr int kGCW = 12;              // consumer warps (3 units per chunk, 128 registers a thread: no spills)
 constexpr int kGCT = kGCW * 32;
 constexpr int kGC = kGCW / 4;         // units per chunk
-constexpr int kGThreads = kGCT + 32;
+constexpr int kGThreads = kGCT + 64;  // + the producer warp and the reducer warp
 constexpr int kGMaxRows = 4;
 
 struct GroupedArgs {
@@ -46,22 +47,24 @@ struct GroupedArgs {
   float ts, sh_ts;
   int64_t n, k;
   int NT, KG;
+  int P;  // input parts: a segment is (group, 128-row tile, 1/P of the inputs)
   int T, topk;
   int mode;  // 0: input rows are tokens (x); 1: input rows are grouped pairs, shared rows
              // after: bf16 rows of x, or (gu non-null) the SwiGLU of the fp32 gate/up rows gu
   const __nv_bfloat16* x;
   int64_t ldx;
-  const float* gu;
+  const float* gu;      // gu_parts partial sums of the gate/up rows, gu_pstride floats apart
   int64_t ldg;
+  int gu_parts;
+  int64_t gu_pstride;
   int nrows;  // input rows (staging slots)
-  float* out;
+  float* out;  // P partial outputs, out_pstride floats apart
   int64_t ldo;
+  int64_t out_pstride;
   const int* meta;
   const int* groups;  // router's group table (kGroupInts ints per active expert)
   int has_shared;
   int stages;
-  float* ws_part;
-  int* ws_cnt;
   int* status;
 };
 
@@ -81,11 +84,14 @@ struct GroupedSmem {
   size_t bars, stages, xs, sums, red, lut, misc, ginfo, total;
 };
 
+// Shared memory: mbarriers (full[S], empty[S], rfull[2], rempty[2]), the stage ring, the
+// staged activations, two reduction buffers (one per segment in flight), the E4M3 table
+// and the descriptors of the first groups the CTA touches.
 __host__ __device__ inline GroupedSmem grouped_smem(int stage_bytes, int S, int nrows, int KG) {
   GroupedSmem L;
   size_t o = 0;
   L.bars = o;
-  o += (size_t)2 * S * 8;
+  o += (size_t)(2 * S + 4) * 8;
   o = (o + 127) & ~(size_t)127;
   L.stages = o;
   o += (size_t)S * stage_bytes;
@@ -95,7 +101,7 @@ __host__ __device__ inline GroupedSmem grouped_smem(int stage_bytes, int S, int 
   L.sums = o;
   o += (size_t)nrows * KG * 64;   // {scale, Z, X, 0} per 16-input quarter
   L.red = o;
-  o += (size_t)kGCW * kGMaxRows * 128 * 4;
+  o += (size_t)2 * kGCW * kGMaxRows * 128 * 4;
   L.lut = o;
   o += 256 * 4;
   L.misc = o;
@@ -152,17 +158,18 @@ template <int FMT>
 __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const GroupedArgs a) {
   using SG = Stage<FMT>;
   extern __shared__ __align__(128) uint8_t smem[];
-  const int S = a.stages, KG = a.KG, NT = a.NT;
+  const int S = a.stages, KG = a.KG, NT = a.NT, P = a.P;
   const int SBY = SG::bytes(kGC);
   const GroupedSmem L = grouped_smem(SBY, S, a.nrows, KG);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + S;
+  uint64_t* rfull = empty + S;  // [2]: a segment's 12 partials are in red[buf]
+  uint64_t* rempty = rfull + 2;  // [2]: the reducer has consumed red[buf]
   uint8_t* stages = smem + L.stages;
   uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.xs);
   float* sums = reinterpret_cast<float*>(smem + L.sums);
   float* red = reinterpret_cast<float*>(smem + L.red);
   float* lut = reinterpret_cast<float*>(smem + L.lut);
-  int* flag = reinterpret_cast<int*>(smem + L.misc);
   GroupInfo* ginfo = reinterpret_cast<GroupInfo*>(smem + L.ginfo);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -170,74 +177,117 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
     mbar_init(&full[s], 1);
     mbar_init(&empty[s], kGCW);
   }
-  if (tid < S) fence_mbar_init();
+  if (tid < 2) {
+    mbar_init(&rfull[tid], kGCW);
+    mbar_init(&rempty[tid], 1);
+  }
+  if (tid < S + 2) fence_mbar_init();
   __syncthreads();
   // The next launch of the chain may start its prologue now; everything below reads the
   // router's (or the previous step's) outputs, so wait for the preceding kernel first.
   if (tid == 0) pdl_launch_dependents();
   pdl_wait();
 
+  // Segments: (group, row tile q, input part p), p-major inside a row tile; groups are the
+  // active experts, then the shared expert once per token.  Each CTA takes a contiguous,
+  // equal share of whole segments: no row tile is split across CTAs, so there are no
+  // tickets or partials to combine here -- the P parts are summed by the consumer of the
+  // outputs (the down GEMV's staging, the mid, the finish), in part order.
   const int n_active = a.meta[0];
-  // The shared expert runs as one single-row group per token: its weights are read once per
-  // token (the repeats hit L2) but every chunk then costs the same, so the equal split of
-  // chunks over CTAs stays balanced (a 4-row chunk costs ~2.4 one-row chunks).
   const int n_groups = n_active + (a.has_shared ? a.T : 0);
-  const int upg_real = NT * KG;
-  const int cpg = (upg_real + kGC - 1) / kGC;  // chunks per group
-  const int upg = cpg * kGC;                   // padded units per group
-  const int64_t NCH = (int64_t)n_groups * cpg;
-  // Only as many CTAs as chunks take part, so every participating CTA owns at least one
-  // chunk and the contributors to a split row tile are consecutive CTAs.
-  const int64_t G = min((int64_t)gridDim.x, NCH), b = blockIdx.x;
+  const int spg = NT * P;
+  const int64_t n_seg = (int64_t)n_groups * spg;
+  const int64_t G = min((int64_t)gridDim.x, n_seg), b = blockIdx.x;
   if (b >= G) return;
-  const int64_t c0 = b * NCH / G, c1 = (b + 1) * NCH / G;
-  const uint32_t uu0 = (uint32_t)(c0 * kGC), uu1 = (uint32_t)(c1 * kGC);
-  const int nch = (int)(c1 - c0);
+  const int sg0 = (int)(b * n_seg / G), sg1 = (int)((b + 1) * n_seg / G);
+  const int nck = (KG + kGC - 1) / kGC;  // chunks per row tile; part p takes chunks [p*nck/P, (p+1)*nck/P)
+  auto seg_units = [&](int sg, int& g, int& q, int& p, int& k0, int& k1) {
+    g = sg / spg;
+    const int r = sg - g * spg;
+    q = r / P;
+    p = r - q * P;
+    k0 = kGC * (p * nck / P);
+    k1 = min(KG, kGC * ((p + 1) * nck / P));
+  };
 
-  if (warp == kGCW) {  // producer: chunks never span two groups
+  if (warp == kGCW) {  // producer: the segments' units, chunks never span two segments
     if (lane == 0) {
-      int s = 0;
+      int s = 0, j = 0;
       uint32_t ph = 0;
-      int gcur = -1;  // the group whose weight bases are loaded (reloaded only on a change)
-      const uint8_t *bc = nullptr, *bs = nullptr, *ba = nullptr;
-      for (int j = 0; j < nch; ++j) {
-        if (j >= S && !mbar_wait_bounded(&empty[s], ph ^ 1u, a.status)) break;
-        const int64_t c = c0 + j;
-        const int g = (int)(c / cpg);
-        const int l0 = (int)(c % cpg) * kGC;
-        const int nu = min(kGC, upg_real - l0);
-        if (g != gcur) {
-          gcur = g;
-          if (g < n_active) {
-            const int e = a.groups[(size_t)g * kGroupInts];
-            bc = a.codes + (int64_t)e * a.cstride;
-            bs = a.scales + (int64_t)e * a.sstride;
-            ba = a.aux ? a.aux + (int64_t)e * a.astride : nullptr;
-          } else {
-            bc = a.sh_codes;
-            bs = a.sh_scales;
-            ba = a.sh_aux;
+      bool ok = true;
+      for (int sg = sg0; ok && sg < sg1; ++sg) {
+        int g, q, p, k0, k1;
+        seg_units(sg, g, q, p, k0, k1);
+        const uint8_t *bc, *bs, *ba;
+        if (g < n_active) {
+          const int e = a.groups[(size_t)g * kGroupInts];
+          bc = a.codes + (int64_t)e * a.cstride;
+          bs = a.scales + (int64_t)e * a.sstride;
+          ba = a.aux ? a.aux + (int64_t)e * a.astride : nullptr;
+        } else {
+          bc = a.sh_codes;
+          bs = a.sh_scales;
+          ba = a.sh_aux;
+        }
+        for (int kc = k0; kc < k1; kc += kGC, ++j) {
+          if (j >= S && !mbar_wait_bounded(&empty[s], ph ^ 1u, a.status)) {
+            ok = false;
+            break;
+          }
+          const int l0 = q * KG + kc;  // unit index within the group
+          const int nu = min(kGC, k1 - kc);
+          uint8_t* dst = stages + (size_t)s * SBY;
+          uint32_t bytes = (uint32_t)nu * (SG::CODE + SG::SCALE);
+          int aux_a = 0, aux_n = 0;
+          if (SG::AUX) {
+            aux_a = l0 >> 2;
+            aux_n = ((l0 + nu - 1) >> 2) - aux_a + 1;
+            bytes += (uint32_t)aux_n * SG::AUX;
+          }
+          mbar_arrive_expect_tx(&full[s], bytes);
+          bulk_g2s(dst, bc + (size_t)l0 * SG::CODE, (uint32_t)nu * SG::CODE, &full[s]);
+          bulk_g2s(dst + kGC * SG::CODE, bs + (size_t)l0 * SG::SCALE, (uint32_t)nu * SG::SCALE, &full[s]);
+          if (SG::AUX)
+            bulk_g2s(dst + kGC * (SG::CODE + SG::SCALE), ba + (size_t)aux_a * SG::AUX, (uint32_t)aux_n * SG::AUX,
+                     &full[s]);
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
           }
         }
-        uint8_t* dst = stages + (size_t)s * SBY;
-        uint32_t bytes = (uint32_t)nu * (SG::CODE + SG::SCALE);
-        int aux_a = 0, aux_n = 0;
-        if (SG::AUX) {
-          aux_a = l0 >> 2;
-          aux_n = ((l0 + nu - 1) >> 2) - aux_a + 1;
-          bytes += (uint32_t)aux_n * SG::AUX;
-        }
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s(dst, bc + (size_t)l0 * SG::CODE, (uint32_t)nu * SG::CODE, &full[s]);
-        bulk_g2s(dst + kGC * SG::CODE, bs + (size_t)l0 * SG::SCALE, (uint32_t)nu * SG::SCALE, &full[s]);
-        if (SG::AUX)
-          bulk_g2s(dst + kGC * (SG::CODE + SG::SCALE), ba + (size_t)aux_a * SG::AUX, (uint32_t)aux_n * SG::AUX,
-                   &full[s]);
-        if (++s == S) {
-          s = 0;
-          ph ^= 1u;
+      }
+    }
+    return;
+  }
+
+  // The groups this CTA touches: their descriptors are read once here.
+  const int g_first = sg0 / spg;
+  const int g_span = (sg1 - 1) / spg - g_first + 1;
+  if (tid < kGInfoCache && g_first + tid < n_groups) ginfo[tid] = group_info(a, g_first + tid, n_active);
+
+  if (warp == kGCW + 1) {  // reducer: each segment's 12 warp partials, summed in warp order
+    __syncwarp();
+    named_sync(2, kGCT + 32);  // descriptors ready
+    bool ok = true;
+    for (int sg = sg0; sg < sg1; ++sg) {
+      const int i = sg - sg0, buf = i & 1;
+      if (ok && !mbar_wait_bounded(&rfull[buf], (uint32_t)(i >> 1) & 1u, a.status)) ok = false;
+      if (ok) {
+        int g, q, p, k0, k1;
+        seg_units(sg, g, q, p, k0, k1);
+        const GroupInfo gi = (g - g_first < kGInfoCache) ? ginfo[g - g_first] : group_info(a, g, n_active);
+        const float* rb = red + (size_t)buf * kGCW * kGMaxRows * 128;
+        float* outp = a.out + (int64_t)p * a.out_pstride;
+        for (int e = lane; e < gi.m * 128; e += 32) {
+          float v = 0.0f;
+#pragma unroll
+          for (int w2 = 0; w2 < kGCW; ++w2) v += rb[w2 * kGMaxRows * 128 + e];
+          const int64_t n = (int64_t)q * 128 + (e & 127);
+          if (n < a.n) outp[(int64_t)gi.out_row[e >> 7] * a.ldo + n] = v * gi.ts;
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rempty[buf]);  // also on failure, so no consumer waits forever
     }
     return;
   }
@@ -247,16 +297,11 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
     lut[2 * tid] = v.x;
     lut[2 * tid + 1] = v.y;
   }
-  // The groups this CTA touches: their descriptors are read once here instead of at every
-  // segment.
-  const int g_first = (int)(uu0 / (uint32_t)upg);
-  const int g_span = (int)((uu1 - 1) / (uint32_t)upg) - g_first + 1;
-  if (tid < kGInfoCache && g_first + tid < n_groups) ginfo[tid] = group_info(a, g_first + tid, n_active);
+  named_sync(2, kGCT + 32);  // descriptors ready (consumers and reducer)
   // Stage the input rows over all of K.  Mode 0: every token row of x.  Mode 1: the rows of
   // the groups this CTA touches (all rows if it touches more than kGInfoCache groups), each
-  // computed as h = bf16( silu(g) * u ) from the fp32 gate/up outputs.
+  // computed as h = bf16( silu(g) * u ) from the fp32 gate/up outputs (their parts summed).
   const bool by_group = a.mode == 1 && g_span <= kGInfoCache;
-  if (a.mode == 1) named_sync(1, kGCT);  // the row lists come from the descriptors
   const int nslot = by_group ? g_span * kGMaxRows : a.nrows;
   for (int it = tid; it < nslot * KG * 4; it += kGCT) {
     const int kq = it & 3, sl = (it >> 2) % KG, slot = (it >> 2) / KG;
@@ -277,11 +322,17 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
       u[0] = r0.x; u[1] = r0.y; u[2] = r0.z; u[3] = r0.w;
       u[4] = r1.x; u[5] = r1.y; u[6] = r1.z; u[7] = r1.w;
     } else {
-      const float4* gp = reinterpret_cast<const float4*>(a.gu + (int64_t)row * a.ldg + k0);
-      const float4* up = reinterpret_cast<const float4*>(a.gu + (int64_t)row * a.ldg + a.k + k0);
+      const float* gp = a.gu + (int64_t)row * a.ldg + k0;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        const float4 g4 = __ldcg(gp + q4), u4 = __ldcg(up + q4);
+        float4 g4 = __ldcg(reinterpret_cast<const float4*>(gp) + q4);
+        float4 u4 = __ldcg(reinterpret_cast<const float4*>(gp + a.k) + q4);
+        for (int pp = 1; pp < a.gu_parts; ++pp) {
+          const float4 gx = __ldcg(reinterpret_cast<const float4*>(gp + pp * a.gu_pstride) + q4);
+          const float4 ux = __ldcg(reinterpret_cast<const float4*>(gp + pp * a.gu_pstride + a.k) + q4);
+          g4.x += gx.x; g4.y += gx.y; g4.z += gx.z; g4.w += gx.w;
+          u4.x += ux.x; u4.y += ux.y; u4.z += ux.z; u4.w += ux.w;
+        }
         u[2 * q4] = swiglu_bf16x2(g4.x, u4.x, g4.y, u4.y);
         u[2 * q4 + 1] = swiglu_bf16x2(g4.z, u4.z, g4.w, u4.w);
       }
@@ -293,21 +344,12 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
 
   const int ug = warp >> 2, kq = warp & 3;
   bool ok = true;
-  uint32_t i = (uint32_t)ug;  // relative unit index; one per chunk
   int s = 0;
   uint32_t ph = 0;
-  uint32_t u = uu0;
-  int nparts = 0;  // segments of row tiles this CTA holds only part of (at most 2)
-  int pg0 = 0, pq0 = 0, pg1 = 0, pq1 = 0;
-  uint32_t ps0 = 0, pe0 = 0, ps1 = 0, pe1 = 0;
-  while (u < uu1) {
-    const uint32_t g = u / (uint32_t)upg;
-    const uint32_t l = u - g * (uint32_t)upg;
-    const uint32_t q = min(l / (uint32_t)KG, (uint32_t)(NT - 1));
-    const uint32_t seg_start = g * upg + q * KG;
-    const uint32_t seg_end_full = (q == (uint32_t)(NT - 1)) ? (g + 1) * upg : seg_start + KG;
-    const uint32_t seg_end = min(uu1, seg_end_full);
-    const GroupInfo gi = ((int)g - g_first < kGInfoCache) ? ginfo[(int)g - g_first] : group_info(a, (int)g, n_active);
+  for (int sg = sg0; sg < sg1; ++sg) {
+    int g, q, p, k0, k1;
+    seg_units(sg, g, q, p, k0, k1);
+    const GroupInfo gi = (g - g_first < kGInfoCache) ? ginfo[g - g_first] : group_info(a, g, n_active);
     float acc[4][kGMaxRows];
 #pragma unroll
     for (int rt = 0; rt < 4; ++rt)
@@ -315,17 +357,13 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
       for (int m = 0; m < kGMaxRows; ++m) acc[rt][m] = 0.0f;
     const uint32_t* xr[kGMaxRows];
     const float* zr[kGMaxRows];
-    for (; ok && uu0 + i < seg_end; i += kGC) {
-      if (!mbar_wait_bounded(&full[s], ph, a.status)) {
-        ok = false;
-        break;
-      }
-      const uint32_t uu = uu0 + i;
-      const int ul = (int)(uu - g * upg);
-      if (ul < upg_real) {  // padding units carry no data
-        const int kg = ul % KG;
+    for (int kc = k0; kc < k1; kc += kGC) {
+      if (ok && !mbar_wait_bounded(&full[s], ph, a.status)) ok = false;
+      const int kg = kc + ug;
+      if (ok && kg < k1) {
+        const int ul = q * KG + kg;  // unit within the group
         const uint8_t* st = stages + (size_t)s * SBY;
-        const int l0 = ul - ug;  // first unit of this chunk within the group
+        const int l0 = q * KG + kc;  // first unit of this chunk
         const uint8_t* aux = st + kGC * (SG::CODE + SG::SCALE) + ((ul >> 2) - (l0 >> 2)) * SG::AUX;
 #pragma unroll
         for (int m = 0; m < kGMaxRows; ++m) {
@@ -348,96 +386,48 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
         ph ^= 1u;
       }
     }
+    // Hand the warp's partial to the reducer (two buffers: the warps run on into the next
+    // segment while the reducer sums this one).
+    const int i = sg - sg0, buf = i & 1;
+    if (i >= 2 && ok && !mbar_wait_bounded(&rempty[buf], (uint32_t)((i >> 1) - 1) & 1u, a.status)) ok = false;
+    float* rb = red + ((size_t)buf * kGCW + warp) * kGMaxRows * 128;
 #pragma unroll
     for (int rt = 0; rt < 4; ++rt)
 #pragma unroll
-      for (int m = 0; m < kGMaxRows; ++m) red[(warp * kGMaxRows + m) * 128 + rt * 32 + lane] = acc[rt][m];
-    named_sync(1, kGCT);
-
-    const int M = gi.m;
-    const bool whole = (u == seg_start) && (seg_end == seg_end_full);
-    const int slot_ws = (u == uu0) ? 0 : 1;
-    for (int e = tid; e < M * 128; e += kGCT) {
-      float v = 0.0f;
-#pragma unroll 4
-      for (int w2 = 0; w2 < kGCW; ++w2) v += red[w2 * kGMaxRows * 128 + e];
-      v *= gi.ts;
-      if (whole) {
-        const int64_t n = (int64_t)q * 128 + (e & 127);
-        if (n < a.n) a.out[(int64_t)gi.out_row[e >> 7] * a.ldo + n] = v;
-      } else {
-        a.ws_part[(size_t)((b * 2 + slot_ws) * kGMaxRows) * 128 + e] = v;
-      }
-    }
-    if (!whole) {  // the same on every thread: settled after all of this CTA's work
-      if (nparts == 0) {
-        pg0 = (int)g; pq0 = (int)q; ps0 = seg_start; pe0 = seg_end_full;
-      } else {
-        pg1 = (int)g; pq1 = (int)q; ps1 = seg_start; pe1 = seg_end_full;
-      }
-      ++nparts;
-    }
-    named_sync(1, kGCT);
-    u = seg_end;
+      for (int m = 0; m < kGMaxRows; ++m) rb[m * 128 + rt * 32 + lane] = acc[rt][m];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rfull[buf]);
   }
-
-  // Row tiles split across CTAs (at most two per CTA): one ticket each, taken after all of
-  // this CTA's work; the CTA that takes a segment's last ticket sums its partials in CTA
-  // order (the first contributor may hold it as its last segment, slot 1).
-  if (nparts > 0) {  // uniform: every consumer thread reaches the barriers below
-    if (tid == 0) {
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (i >= nparts) break;
-        const int pg = i ? pg1 : pg0, pq = i ? pq1 : pq0;
-        const uint32_t ps = i ? ps1 : ps0, pe = i ? pe1 : pe0;
-        const int64_t cs = ps / kGC, ce = (pe - 1) / kGC;
-        const int64_t bf = ((cs + 1) * G - 1) / NCH, bl = ((ce + 1) * G - 1) / NCH;
-        const int old = ticket_add(&a.ws_cnt[(int64_t)pg * NT + pq], 1);
-        flag[i] = (old == (int)(bl - bf)) ? 1 : 0;
-      }
-    }
-    named_sync(1, kGCT);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      if (i >= nparts || !flag[i]) continue;
-      const int pg = i ? pg1 : pg0, pq = i ? pq1 : pq0;
-      const uint32_t ps = i ? ps1 : ps0, pe = i ? pe1 : pe0;
-      const GroupInfo gi = (pg - g_first < kGInfoCache) ? ginfo[pg - g_first] : group_info(a, pg, n_active);
-      const int64_t cs = ps / kGC, ce = (pe - 1) / kGC;
-      const int64_t bf = ((cs + 1) * G - 1) / NCH, bl = ((ce + 1) * G - 1) / NCH;
-      const int first_sl = ((bf * NCH / G) * kGC < (int64_t)ps) ? 1 : 0;
-      const int nc = (int)(bl - bf + 1);
-      const float* part = a.ws_part + (size_t)(bf * 2) * kGMaxRows * 128;
-      for (int e = tid; e < gi.m * 128; e += kGCT) {
-        float v = __ldcg(part + (size_t)first_sl * kGMaxRows * 128 + e);
-        for (int c = 1; c < nc; ++c) v += __ldcg(part + (size_t)(2 * c) * kGMaxRows * 128 + e);
-        const int64_t n = (int64_t)pq * 128 + (e & 127);
-        if (n < a.n) a.out[(int64_t)gi.out_row[e >> 7] * a.ldo + n] = v;
-      }
-      if (tid == 0) a.ws_cnt[(int64_t)pg * NT + pq] = 0;
-    }
-  }
+  // the reducer still reads red: it returns on its own; nothing here waits for it
 }
 
 // h[r][f] = bf16( silu(gu[r][f]) * gu[r][F + f] ) for every row (the staged gate/up call
 // writes h for the caller; the fused chain computes it inside the down GEMV instead).
-__global__ void __launch_bounds__(256) mid_kernel(const float* gu, int64_t ldg, __nv_bfloat16* h, int64_t ldh, int F,
-                                                  int rows) {
+__global__ void __launch_bounds__(256) mid_kernel(const float* gu, int64_t ldg, int parts, int64_t pstride,
+                                                  __nv_bfloat16* h, int64_t ldh, int F, int rows) {
   pdl_launch_dependents();
   pdl_wait();
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (int64_t)rows * (F / 2)) return;
   const int r = (int)(idx / (F / 2)), f = (int)(idx % (F / 2)) * 2;
-  const float2 g = *reinterpret_cast<const float2*>(gu + r * ldg + f);
-  const float2 u = *reinterpret_cast<const float2*>(gu + r * ldg + F + f);
+  float2 g = *reinterpret_cast<const float2*>(gu + r * ldg + f);
+  float2 u = *reinterpret_cast<const float2*>(gu + r * ldg + F + f);
+  for (int p = 1; p < parts; ++p) {  // the gate/up GEMV's input parts, summed in order
+    const float2 gp = *reinterpret_cast<const float2*>(gu + p * pstride + r * ldg + f);
+    const float2 up = *reinterpret_cast<const float2*>(gu + p * pstride + r * ldg + F + f);
+    g.x += gp.x;
+    g.y += gp.y;
+    u.x += up.x;
+    u.y += up.y;
+  }
   *reinterpret_cast<uint32_t*>(h + r * ldh + f) = swiglu_bf16x2(g.x, u.x, g.y, u.y);
 }
 
 // out[t][n] = bf16( sum_j w[t][j] * d[pos(t, j)][n] + g_t * d[T*topk + t][n] ), fixed order,
 // four features per thread (g_t: the shared expert's sigmoid gate, or 1); every load of a
 // thread is issued before the first multiply-add.
-__global__ void __launch_bounds__(256) finish_kernel(const float* d, int64_t ldd, const float* w, const int* pair_pos,
+__global__ void __launch_bounds__(256) finish_kernel(const float* d, int64_t ldd, int parts, int64_t pstride,
+                                                     const float* w, const int* pair_pos,
                                                      int T, int topk, int has_shared, const float* shared_gate,
                                                      int64_t H, __nv_bfloat16* out, int64_t ldo) {
   pdl_launch_dependents();
@@ -458,8 +448,28 @@ __global__ void __launch_bounds__(256) finish_kernel(const float* d, int64_t ldd
 #pragma unroll
   for (int j = 0; j < kMaxTopk; ++j)
     v[j] = j < topk ? __ldcg(reinterpret_cast<const float4*>(d + (int64_t)pos[j] * ldd + n)) : make_float4(0, 0, 0, 0);
-  const float4 sh = has_shared ? __ldcg(reinterpret_cast<const float4*>(d + (int64_t)(T * topk + t) * ldd + n))
-                               : make_float4(0, 0, 0, 0);
+  float4 sh = has_shared ? __ldcg(reinterpret_cast<const float4*>(d + (int64_t)(T * topk + t) * ldd + n))
+                         : make_float4(0, 0, 0, 0);
+  for (int p = 1; p < parts; ++p) {  // the down GEMV's input parts, summed in order
+    const float* dp = d + p * pstride;
+#pragma unroll
+    for (int j = 0; j < kMaxTopk; ++j) {
+      if (j < topk) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(dp + (int64_t)pos[j] * ldd + n));
+        v[j].x += x.x;
+        v[j].y += x.y;
+        v[j].z += x.z;
+        v[j].w += x.w;
+      }
+    }
+    if (has_shared) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(dp + (int64_t)(T * topk + t) * ldd + n));
+      sh.x += x.x;
+      sh.y += x.y;
+      sh.z += x.z;
+      sh.w += x.w;
+    }
+  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < kMaxTopk; ++j) {
@@ -496,6 +506,16 @@ int grouped_stage_bytes(int fmt) {
 }
 }  // namespace
 
+// Input parts of a decode GEMV: the fewest that give every CTA about four whole segments
+// (group, row tile, part) at the most groups the routing can produce, so equal shares of
+// whole segments stay balanced; parts are whole chunks of kGC units, so at most one part
+// per row tile -- the last -- leaves warps idle in its last chunk.
+static int grouped_parts(int64_t max_groups, int64_t nt, int64_t kg, int sms) {
+  const int64_t nck = (kg + kGC - 1) / kGC;
+  int64_t p = (4 * (int64_t)sms + max_groups * nt - 1) / (max_groups * nt);
+  return (int)std::max<int64_t>(1, std::min<int64_t>(p, nck));
+}
+
 MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, int topk, int grid) {
   MoeLayout L;
   const int64_t R = T * topk + T;
@@ -506,17 +526,19 @@ MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, i
     return at;
   };
   // the prefill chain (more than kGMaxRows tokens) fuses the mid into the gate/up GEMM and
-  // needs neither the split-K tickets and partials nor the fp32 gate/up rows
+  // needs no fp32 gate/up rows; its down outputs are one part
   const bool decode = T <= kGMaxRows;
-  const int64_t nt_max = std::max(gu.nt, dn.nt);
-  L.cnt = take(decode ? (size_t)(E + kGMaxRows) * nt_max * 4 : 0);  // tickets per (group, row tile)
-  L.part = take(decode ? (size_t)grid * 2 * kGMaxRows * 128 * 4 : 0);
+  const int64_t max_groups = std::min<int64_t>(E, T * topk) + T;
+  L.p_gu = decode ? grouped_parts(max_groups, gu.nt, gu.kg, grid) : 1;
+  L.p_dn = decode ? grouped_parts(max_groups, dn.nt, dn.kg, grid) : 1;
   L.ld_gu = (gu.n + 7) / 8 * 8;
-  L.gu = take(decode ? (size_t)R * L.ld_gu * 4 : 0);
+  L.pst_gu = R * L.ld_gu;
+  L.gu = take(decode ? (size_t)L.p_gu * R * L.ld_gu * 4 : 0);
   L.ld_h = (dn.k + 7) / 8 * 8;
   L.h = take(decode ? 0 : (size_t)R * L.ld_h * 2);  // decode: h never leaves the down GEMV
   L.ld_d = (dn.n + 7) / 8 * 8;
-  L.d = take((size_t)R * L.ld_d * 4);
+  L.pst_dn = R * L.ld_d;
+  L.d = take((size_t)L.p_dn * R * L.ld_d * 4);
   L.total = o;
   return L;
 }
@@ -531,7 +553,7 @@ static int launch_grouped(int fmt, const GroupedArgs& a0, int nrows, int KG, con
   a.stages = S;
   a.nrows = nrows;
   const size_t smem = grouped_smem(sb, S, nrows, KG).total;
-  static std::atomic<unsigned long long> configured[5];
+  static std::atomic<unsigned long long> configured[8];
   int devid = 0;
   if (cudaGetDevice(&devid) != cudaSuccess) return QG_ERR_CUDA;
   const unsigned long long bit = 1ull << (devid & 63);
@@ -591,10 +613,10 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
   a.ldx = ldx;
   a.out = reinterpret_cast<float*>(w + L.gu);
   a.ldo = L.ld_gu;
+  a.P = L.p_gu;
+  a.out_pstride = L.pst_gu;
   a.meta = rv.meta;
   a.groups = rv.groups;
-  a.ws_part = reinterpret_cast<float*>(w + L.part);
-  a.ws_cnt = reinterpret_cast<int*>(w + L.cnt);
   a.status = reinterpret_cast<int*>(w);
   const int rows = (int)(T * topk + (m->has_shared ? T : 0));
   int st = QG_OK;
@@ -605,7 +627,7 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
   if (stage == kMoeGateUp) {  // h for the caller: out [rows][ldo] bf16
     const int F = (int)dn.k;
     if (launch_pdl(mid_kernel, dim3((unsigned)(((int64_t)rows * (F / 2) + 255) / 256)), dim3(256), 0, s,
-                   (const float*)reinterpret_cast<const float*>(w + L.gu), (int64_t)L.ld_gu,
+                   (const float*)reinterpret_cast<const float*>(w + L.gu), (int64_t)L.ld_gu, L.p_gu, L.pst_gu,
                    static_cast<__nv_bfloat16*>(out), ldo, F, rows) != cudaSuccess)
       return QG_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
@@ -636,14 +658,18 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
     d.x = nullptr;
     d.gu = reinterpret_cast<const float*>(w + L.gu);
     d.ldg = L.ld_gu;
+    d.gu_parts = L.p_gu;
+    d.gu_pstride = L.pst_gu;
   }
   d.out = reinterpret_cast<float*>(w + L.d);
   d.ldo = L.ld_d;
+  d.P = L.p_dn;
+  d.out_pstride = L.pst_dn;
   st = launch_grouped(m->fmt, d, rows, (int)dn.kg, dev, s);
   if (st != QG_OK) return st;
 
   if (launch_pdl(finish_kernel, dim3((unsigned)((T * (dn.n / 4) + 255) / 256)), dim3(256), 0, s,
-                 (const float*)reinterpret_cast<const float*>(w + L.d), (int64_t)L.ld_d, topk_w,
+                 (const float*)reinterpret_cast<const float*>(w + L.d), (int64_t)L.ld_d, L.p_dn, L.pst_dn, topk_w,
                  (const int*)rv.pair_pos, (int)T, topk, (int)m->has_shared, shared_gate, (int64_t)dn.n,
                  static_cast<__nv_bfloat16*>(out), ldo) != cudaSuccess)
     return QG_ERR_CUDA;

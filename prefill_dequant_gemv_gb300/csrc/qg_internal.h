@@ -64,8 +64,10 @@ constexpr size_t kWsHeader = 256;  // status word + reserved
 
 // Mixture-of-experts decode workspace (after the status header).
 struct MoeLayout {
-  size_t cnt, part, gu, h, d, total;
+  size_t gu, h, d, total;
   int64_t ld_gu, ld_h, ld_d;
+  int p_gu, p_dn;            // decode: input parts of the gate/up and down GEMVs (outputs per part)
+  int64_t pst_gu, pst_dn;    // floats between two parts' outputs
 };
 MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, int topk, int grid);
 // MoE chains: the whole FFN (kMoeAll: x -> out), or one stage of it -- kMoeGateUp: x -> h
