@@ -256,6 +256,19 @@ qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t t, int64_t 
                    const float* topk_w, const float* shared_gate, const void* route_ws, void* out, int64_t ldo,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Router and FFN in one call: qmoe_route on `logits` (fp32 [t][n_experts], device) followed
+ * by qmoe_ffn, with the same outputs -- topk_ids, topk_w and route_ws as qmoe_route stores
+ * them, out as qmoe_ffn computes it, bit for bit.  At 1..4 tokens the gate/up launch routes
+ * the tokens itself (every CTA computes the same small table; the first also stores the
+ * router's outputs), so the layer takes three launches instead of four (TurboEXL3 article
+ * §4.2: the router's top-k and softmax run inside the FFN chain); needs t * topk <= 64.
+ * More tokens: the router's launches, then the prefill chain.  Same arguments, limits and
+ * errors as qmoe_route and qmoe_ffn together. */
+qg_status qmoe_forward(const qg_moe_layer* layer, const void* x, int64_t t, int64_t ldx, const float* logits,
+                       int topk, const float* shared_gate, int32_t* topk_ids, float* topk_w, void* route_ws,
+                       size_t route_ws_bytes, void* out, int64_t ldo, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
 /* The MoE FFN one stage at a time (the grouped GEMM of the two stages, for callers that
  * keep h or run something between the stages); the same results as qmoe_ffn, bit for bit.
  * rows = t * topk + (has_shared ? t : 0).

@@ -64,6 +64,8 @@ _SIGNATURES = {
     "qmoe_workspace_size": (_SZ, [ctypes.POINTER(qg_moe_layer), _I64, _I]),
     "qmoe_ffn": (_I, [ctypes.POINTER(qg_moe_layer), _P, _I64, _I64, _I, _P, _P, _P, _P, _I64, _P, _SZ, _P]),
     "qgemm_grouped_workspace_size": (_SZ, [ctypes.POINTER(qg_moe_layer), _I64, _I, _I]),
+    "qmoe_forward": (_I, [ctypes.POINTER(qg_moe_layer), _P, _I64, _I64, _P, _I, _P, _P, _P, _P, _SZ, _P, _I64, _P, _SZ,
+                          _P]),
     "qgemm_grouped": (_I, [ctypes.POINTER(qg_moe_layer), _I, _P, _I64, _I64, _I, _P, _P, _P, _P, _I64, _P, _SZ, _P]),
     "qg_selftest_wait_timeout": (_I, [_P, _SZ, _P]),
 }
@@ -167,6 +169,13 @@ def qmoe_ffn(layer: qg_moe_layer, x_ptr: int, t: int, ldx: int, topk: int, w_ptr
              route_ws_ptr: int, out_ptr: int, ldo: int, ws_ptr: int, ws_bytes: int, stream: int = 0):
     _check(lib().qmoe_ffn(ctypes.byref(layer), x_ptr, t, ldx, topk, w_ptr, gate_ptr, route_ws_ptr, out_ptr, ldo,
                           ws_ptr, ws_bytes, stream), "qmoe_ffn")
+
+
+def qmoe_forward(layer: qg_moe_layer, x_ptr: int, t: int, ldx: int, logits_ptr: int, topk: int,
+                 gate_ptr: Optional[int], ids_ptr: int, w_ptr: int, route_ws_ptr: int, route_ws_bytes: int, out_ptr: int,
+                 ldo: int, ws_ptr: int, ws_bytes: int, stream: int = 0):
+    _check(lib().qmoe_forward(ctypes.byref(layer), x_ptr, t, ldx, logits_ptr, topk, gate_ptr, ids_ptr, w_ptr,
+                              route_ws_ptr, route_ws_bytes, out_ptr, ldo, ws_ptr, ws_bytes, stream), "qmoe_forward")
 
 
 def qgemm_grouped_workspace_size(layer: qg_moe_layer, t: int, topk: int, stage: int) -> int:
@@ -344,6 +353,27 @@ def moe_ffn(pm: PackedMoE, x, topk_w, route_ws: Workspace, out=None, workspace: 
              None if shared_gate is None else shared_gate.data_ptr(), route_ws.ptr, out.data_ptr(),
              out.stride(0), workspace.ptr, workspace.nbytes, _stream_ptr())
     return out
+
+
+def moe_forward(pm: PackedMoE, x, logits, topk: int, out=None, workspace: Optional[Workspace] = None,
+                route_ws: Optional[Workspace] = None, shared_gate=None):
+    """Router and MoE FFN in one call (qmoe_forward) for x bf16 [t, H] and fp32 logits [t, E]:
+    returns (out bf16 [t, H], topk_ids int32 [t, topk], topk_w fp32 [t, topk], route workspace)."""
+    import torch
+    t = x.shape[0]
+    e = logits.shape[1]
+    ids = torch.empty((t, topk), dtype=torch.int32, device=x.device)
+    w = torch.empty((t, topk), dtype=torch.float32, device=x.device)
+    if route_ws is None:
+        route_ws = Workspace(qmoe_route_workspace_size(t, e, topk), x.device)
+    if out is None:
+        out = torch.empty((t, (pm.hidden + 7) // 8 * 8), dtype=torch.bfloat16, device=x.device)[:, :pm.hidden]
+    if workspace is None:
+        workspace = Workspace(qmoe_workspace_size(pm.desc, t, topk), x.device)
+    qmoe_forward(pm.desc, x.data_ptr(), t, x.stride(0), logits.data_ptr(), topk,
+                 None if shared_gate is None else shared_gate.data_ptr(), ids.data_ptr(), w.data_ptr(), route_ws.ptr,
+                 route_ws.nbytes, out.data_ptr(), out.stride(0), workspace.ptr, workspace.nbytes, _stream_ptr())
+    return out, ids, w, route_ws
 
 
 def moe_stage(pm: PackedMoE, stage: int, inp, t: int, topk: int, route_ws: Workspace, topk_w=None, out=None,

@@ -267,3 +267,36 @@ extern "C" qg_status qgemm_grouped(const qg_moe_layer* layer, int stage, const v
   return (qg_status)launch_moe_decode(layer, gu, dn, in, t, ldi, topk, topk_w, shared_gate, route_ws, out, ldo,
                                       workspace, dev, stream, ms);
 }
+
+extern "C" qg_status qmoe_forward(const qg_moe_layer* layer, const void* x, int64_t t, int64_t ldx, const float* logits,
+                                  int topk, const float* shared_gate, int32_t* topk_ids, float* topk_w, void* route_ws,
+                                  size_t route_ws_bytes, void* out, int64_t ldo, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  Geometry gu, dn;
+  int st = check_moe(layer, t, topk, &gu, &dn);
+  if (st != QG_OK) return (qg_status)st;
+  if (!x || !logits || !topk_ids || !topk_w || !route_ws || !out || !workspace) return QG_ERR_INVALID_ARG;
+  if (shared_gate && !layer->has_shared) return QG_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(shared_gate) % 4) return QG_ERR_MISALIGNED;
+  if (t > 4 && (layer->ffn % 128 != 0 || layer->hidden % 8 != 0)) return QG_ERR_UNSUPPORTED;
+  if (t * (int64_t)(topk + 1) >= ((int64_t)1 << 31)) return QG_ERR_UNSUPPORTED;
+  if (ldx < layer->hidden || ldo < layer->hidden) return QG_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(workspace) || !aligned16(route_ws) || !aligned16(topk_w) ||
+      !aligned16(topk_ids) || !aligned16(logits))
+    return QG_ERR_MISALIGNED;
+  if (ldx % 8 || ldo % 8) return QG_ERR_MISALIGNED;
+  if (route_ws_bytes < route_layout(t, layer->n_experts, topk).total) return QG_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo dev;
+  if (!current_device_info(&dev)) return QG_ERR_CUDA;
+  if (workspace_bytes < moe_layout(gu, dn, t, layer->n_experts, topk, dev.sms).total)
+    return QG_ERR_WORKSPACE_TOO_SMALL;
+  if (t > 4) {  // the router's own launches, then the prefill chain
+    st = launch_route(logits, t, layer->n_experts, topk, topk_ids, topk_w, route_ws, stream);
+    if (st != QG_OK) return (qg_status)st;
+    return (qg_status)launch_moe_prefill(layer, gu, dn, x, t, ldx, topk, topk_w, shared_gate, route_ws, out, ldo,
+                                         workspace, dev, stream, kMoeAll);
+  }
+  if (t * topk > kBlockRoutePairs) return QG_ERR_UNSUPPORTED;
+  return (qg_status)launch_moe_decode(layer, gu, dn, x, t, ldx, topk, topk_w, shared_gate, route_ws, out, ldo,
+                                      workspace, dev, stream, kMoeAll, logits, topk_ids, topk_w);
+}

@@ -26,6 +26,7 @@
 #include "qg_gemv_core.cuh"
 #include "qg_internal.h"
 #include "qg_route.h"
+#include "qg_route_dev.cuh"
 #include "qg_sync.cuh"
 
 namespace qg {
@@ -63,6 +64,13 @@ struct GroupedArgs {
   int64_t out_pstride;
   const int* meta;
   const int* groups;  // router's group table (kGroupInts ints per active expert)
+  // Routing inside the launch (decode gate/up from logits; null: the router's outputs above):
+  // every CTA routes the T tokens itself; CTA 0 also stores the router's outputs.
+  const float* logits;
+  int E;
+  int32_t* ids_out;
+  float* wts_out;
+  RouteView rv;
   int has_shared;
   int stages;
   int* status;
@@ -81,7 +89,7 @@ struct GroupInfo {
 constexpr int kGInfoCache = 8;
 
 struct GroupedSmem {
-  size_t bars, stages, xs, sums, red, lut, misc, ginfo, total;
+  size_t bars, stages, xs, sums, red, lut, misc, ginfo, route, total;
 };
 
 // Shared memory: mbarriers (full[S], empty[S], rfull[2], rempty[2]), the stage ring, the
@@ -108,14 +116,17 @@ __host__ __device__ inline GroupedSmem grouped_smem(int stage_bytes, int S, int 
   o += 64;
   L.ginfo = o;  // descriptors of the first kGInfoCache groups this CTA touches
   o += (size_t)kGInfoCache * sizeof(GroupInfo);
+  o = (o + 15) & ~(size_t)15;
+  L.route = o;  // routing scratch and group table when the launch routes its tokens
+  o += sizeof(BlockRouteSmem);
   L.total = o;
   return L;
 }
 
-__device__ __forceinline__ GroupInfo group_info(const GroupedArgs& a, int g, int n_active) {
+__device__ __forceinline__ GroupInfo group_info(const GroupedArgs& a, const int* groups, int g, int n_active) {
   GroupInfo gi;
   if (g < n_active) {  // one 32-byte entry of the router's group table
-    const int4* ge = reinterpret_cast<const int4*>(a.groups + (size_t)g * kGroupInts);
+    const int4* ge = reinterpret_cast<const int4*>(groups + (size_t)g * kGroupInts);
     const int4 h = ge[0], rows = ge[1];
     const int e = h.x, first = h.y;
     gi.codes = a.codes + (int64_t)e * a.cstride;
@@ -193,7 +204,16 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   // equal share of whole segments: no row tile is split across CTAs, so there are no
   // tickets or partials to combine here -- the P parts are summed by the consumer of the
   // outputs (the down GEMV's staging, the mid, the finish), in part order.
-  const int n_active = a.meta[0];
+  int n_active;
+  const int* groups;
+  if (a.logits) {  // route the T tokens here (every CTA the same table; CTA 0 stores it)
+    BlockRouteSmem& rs = *reinterpret_cast<BlockRouteSmem*>(smem + L.route);
+    n_active = route_decode_block(a.logits, a.T, a.E, a.topk, rs, blockIdx.x == 0, a.ids_out, a.wts_out, a.rv);
+    groups = rs.groups;
+  } else {
+    n_active = a.meta[0];
+    groups = a.groups;
+  }
   const int n_groups = n_active + (a.has_shared ? a.T : 0);
   const int spg = NT * P;
   const int64_t n_seg = (int64_t)n_groups * spg;
@@ -220,7 +240,7 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
         seg_units(sg, g, q, p, k0, k1);
         const uint8_t *bc, *bs, *ba;
         if (g < n_active) {
-          const int e = a.groups[(size_t)g * kGroupInts];
+          const int e = groups[(size_t)g * kGroupInts];
           bc = a.codes + (int64_t)e * a.cstride;
           bs = a.scales + (int64_t)e * a.sstride;
           ba = a.aux ? a.aux + (int64_t)e * a.astride : nullptr;
@@ -263,7 +283,7 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   // The groups this CTA touches: their descriptors are read once here.
   const int g_first = sg0 / spg;
   const int g_span = (sg1 - 1) / spg - g_first + 1;
-  if (tid < kGInfoCache && g_first + tid < n_groups) ginfo[tid] = group_info(a, g_first + tid, n_active);
+  if (tid < kGInfoCache && g_first + tid < n_groups) ginfo[tid] = group_info(a, groups, g_first + tid, n_active);
 
   if (warp == kGCW + 1) {  // reducer: each segment's 12 warp partials, summed in warp order
     __syncwarp();
@@ -275,7 +295,7 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
       if (ok) {
         int g, q, p, k0, k1;
         seg_units(sg, g, q, p, k0, k1);
-        const GroupInfo gi = (g - g_first < kGInfoCache) ? ginfo[g - g_first] : group_info(a, g, n_active);
+        const GroupInfo gi = (g - g_first < kGInfoCache) ? ginfo[g - g_first] : group_info(a, groups, g, n_active);
         const float* rb = red + (size_t)buf * kGCW * kGMaxRows * 128;
         float* outp = a.out + (int64_t)p * a.out_pstride;
         for (int e = lane; e < gi.m * 128; e += 32) {
@@ -349,7 +369,7 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   for (int sg = sg0; sg < sg1; ++sg) {
     int g, q, p, k0, k1;
     seg_units(sg, g, q, p, k0, k1);
-    const GroupInfo gi = (g - g_first < kGInfoCache) ? ginfo[g - g_first] : group_info(a, g, n_active);
+    const GroupInfo gi = (g - g_first < kGInfoCache) ? ginfo[g - g_first] : group_info(a, groups, g, n_active);
     float acc[4][kGMaxRows];
 #pragma unroll
     for (int rt = 0; rt < 4; ++rt)
@@ -582,7 +602,8 @@ static int launch_grouped(int fmt, const GroupedArgs& a0, int nrows, int KG, con
 
 int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
                       int64_t ldx, int topk, const float* topk_w, const float* shared_gate, const void* route_ws,
-                      void* out, int64_t ldo, void* ws, const DeviceInfo& dev, void* stream, int stage) {
+                      void* out, int64_t ldo, void* ws, const DeviceInfo& dev, void* stream, int stage,
+                      const float* logits, int32_t* topk_ids_out, float* topk_w_out) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const RouteView rv = route_view(const_cast<void*>(route_ws), T, m->n_experts, topk);
   const MoeLayout L = moe_layout(gu, dn, T, m->n_experts, topk, dev.sms);
@@ -617,6 +638,14 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
   a.out_pstride = L.pst_gu;
   a.meta = rv.meta;
   a.groups = rv.groups;
+  if (logits) {  // the gate/up launch routes the tokens and stores the router's outputs
+    a.logits = logits;
+    a.E = m->n_experts;
+    a.ids_out = topk_ids_out;
+    a.wts_out = topk_w_out;
+    a.rv = rv;
+    topk_w = topk_w_out;
+  }
   a.status = reinterpret_cast<int*>(w);
   const int rows = (int)(T * topk + (m->has_shared ? T : 0));
   int st = QG_OK;
@@ -635,6 +664,7 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
 
   qg_packed_sizes(m->fmt, dn.n, dn.k, &cb, &sb, &ab);
   GroupedArgs d = a;
+  d.logits = nullptr;  // the down launch reads the routing the gate/up launch stored
   d.codes = static_cast<const uint8_t*>(m->dn_codes);
   d.scales = static_cast<const uint8_t*>(m->dn_scales);
   d.aux = static_cast<const uint8_t*>(m->dn_aux);

@@ -75,9 +75,12 @@ MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, i
 // shared_gate: fp32 gate logits [T] of the shared expert (its output is weighed by their
 // sigmoid in the finish) or null (weight 1).
 enum MoeStage { kMoeAll = 0, kMoeGateUp = 1, kMoeDown = 2 };
+// logits non-null (decode, kMoeAll): the gate/up launch routes the tokens itself and stores
+// the router's outputs (topk_ids_out, topk_w_out, route_ws) on the way.
 int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
                       int64_t ldx, int topk, const float* topk_w, const float* shared_gate, const void* route_ws,
-                      void* out, int64_t ldo, void* ws, const DeviceInfo& dev, void* stream, int stage);
+                      void* out, int64_t ldo, void* ws, const DeviceInfo& dev, void* stream, int stage,
+                      const float* logits = nullptr, int32_t* topk_ids_out = nullptr, float* topk_w_out = nullptr);
 int launch_moe_prefill(const qg_moe_layer* m, const Geometry& gu, const Geometry& dn, const void* x, int64_t T,
                        int64_t ldx, int topk, const float* topk_w, const float* shared_gate, const void* route_ws,
                        void* out, int64_t ldo, void* ws, const DeviceInfo& dev, void* stream, int stage);

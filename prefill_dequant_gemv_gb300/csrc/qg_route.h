@@ -14,6 +14,8 @@ constexpr int kRouteTile = 192;  // pairs per grouped-prefill tile (the tensor-c
 // position, pair count, 0, then the tokens of its first kGroupRows pairs.
 constexpr int kGroupRows = 4;
 constexpr int kGroupInts = 8;
+// Pairs one CTA routes in the decode chain's gate/up launch (T <= 4 tokens, k <= 16).
+constexpr int kBlockRoutePairs = 64;
 
 struct RouteLayout {
   size_t meta, counts, offsets, active, pair_list, pair_pos, tiles, groups, zidx, block_counts, block_start, total;

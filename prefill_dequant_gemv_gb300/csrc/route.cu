@@ -13,92 +13,12 @@
 
 #include "qg_internal.h"
 #include "qg_route.h"
+#include "qg_route_dev.cuh"
 #include "qg_sync.cuh"
 
 namespace qg {
 
 constexpr int kRouteBlock = 1024;  // pairs per grouping block (one thread per pair)
-
-// Order-preserving 32-bit key of an fp32 logit: larger logit, larger key; -0 ties with +0
-// and NaN sorts below every number (a stable descending sort of the values puts NaN last)
-// but above key 0, which marks padding and experts already taken.
-__device__ __forceinline__ uint32_t order_key(float v) {
-  uint32_t u = __float_as_uint(v);
-  if (u == 0x80000000u) u = 0u;
-  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 1u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
-}
-
-// Largest key of a lane's 16 (ties to the lower slot, i.e. the lower expert index): a
-// 4-level tree over fixed register indices.
-__device__ __forceinline__ void lane_best(const uint32_t (&key)[16], uint32_t& bk, int& bi) {
-  uint32_t k8[8];
-  int i8[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const bool hi = key[2 * i + 1] > key[2 * i];
-    k8[i] = hi ? key[2 * i + 1] : key[2 * i];
-    i8[i] = hi ? 2 * i + 1 : 2 * i;
-  }
-#pragma unroll
-  for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      const bool hi = k8[i + w] > k8[i] || (k8[i + w] == k8[i] && i8[i + w] < i8[i]);
-      k8[i] = hi ? k8[i + w] : k8[i];
-      i8[i] = hi ? i8[i + w] : i8[i];
-    }
-  bk = k8[0];
-  bi = i8[0];
-}
-
-// Warp-level top-k of one token's logits (E <= 512): lane l holds the keys of logits l,
-// l+32, ... (16 registers; the expert of slot i is l + 32 i).  Each of k rounds takes the
-// warp maximum of the lanes' best keys and the warp minimum of the experts holding it (two
-// single-instruction warp reductions); the winner's lane clears that slot and finds its
-// next best.  Lane j keeps the j-th winner and the k lanes compute the softmax over the kept
-// logits in parallel.
-__device__ void warp_topk(const float* lg, int E, int k, int32_t* ids, float* wts, int* ids_copy = nullptr) {
-  const int lane = threadIdx.x & 31;
-  uint32_t key[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = e < E ? order_key(lg[e]) : 0u;
-  }
-  uint32_t bk;
-  int bi;
-  lane_best(key, bk, bi);
-  uint32_t mine = 0u, top = 0u;
-  int mine_id = 0;
-  for (int j = 0; j < k; ++j) {
-    const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, bk);
-    const int win = (int)__reduce_min_sync(0xFFFFFFFFu, bk == kmax ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
-    if (j == 0) top = kmax;
-    if (lane == j) {
-      mine = kmax;
-      mine_id = win;
-    }
-    if ((win & 31) == lane) {  // the winner's lane takes the slot out and finds its next best
-#pragma unroll
-      for (int i = 0; i < 16; ++i) key[i] = (i == (win >> 5)) ? 0u : key[i];
-      lane_best(key, bk, bi);
-    }
-  }
-  // softmax over the k kept logits (descending order), shifted by the largest
-  const float z = lane < k ? expf(key_value(mine) - key_value(top)) : 0.0f;
-  float sum = z;
-#pragma unroll
-  for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, off);
-  if (lane < k) {
-    ids[lane] = mine_id;
-    wts[lane] = z / sum;
-    if (ids_copy) ids_copy[lane] = mine_id;
-  }
-}
 
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* logits, int64_t T, int E, int k, int32_t* ids,
                                                          float* wts) {

@@ -167,3 +167,33 @@ def test_moe_decode_shared_gate(q, fmt, t):
     tol = moe_tolerance(oracle, layer, x, lg, k, ref)
     err = np.abs(to_f64(out) - ref)
     assert np.all(err <= tol), f"{np.sum(err > tol)} out of tolerance, worst {np.max(err - tol)}"
+
+
+@pytest.mark.parametrize("t,e,k,shared,fmt", [(1, 16, 4, True, wl.MXFP4), (2, 64, 10, True, wl.NVFP4),
+                                              (4, 512, 10, True, wl.MXFP4), (3, 32, 16, False, wl.MLX_AFFINE4_G64),
+                                              (4, 16, 16, True, wl.Q6K), (6, 16, 4, True, wl.MXFP4)])
+def test_moe_forward_routes_inside_the_chain(q, t, e, k, shared, fmt):
+    """qmoe_forward (router and FFN in one call; at 1-4 tokens the gate/up launch routes the
+    tokens itself) against qmoe_route + qmoe_ffn on fresh zeroed workspaces: the same output,
+    ids, weights and router workspace, byte for byte; and the output against the oracle."""
+    H, F = (512, 256) if fmt == wl.Q6K else (256, 128)
+    layer = wl.moe_layer(fmt, e, H, F, seed=340 + t, shared=shared)
+    x = wl.moe_tokens(t, H, seed=341)
+    lg = wl.router_logits(t, e, seed=342)
+    if t == 4 and e == 16:
+        lg[1] = lg[0]  # two tokens with the same experts: groups of several rows
+    pm = q.PackedMoE(layer)
+    xd, lt = dev_bf16(x), torch.from_numpy(np.ascontiguousarray(lg)).cuda()
+    gl = torch.from_numpy(wl.shared_gate_logits(t, seed=343)).cuda() if shared else None
+    rws_a = q.Workspace(q.qmoe_route_workspace_size(t, e, k))
+    ids_a, w_a, _ = q.route(lt, k, workspace=rws_a)
+    out_a = q.moe_ffn(pm, xd, w_a, rws_a, shared_gate=gl)
+    rws_b = q.Workspace(q.qmoe_route_workspace_size(t, e, k))
+    out_b, ids_b, w_b, _ = q.moe_forward(pm, xd, lt, k, route_ws=rws_b, shared_gate=gl)
+    torch.cuda.synchronize()
+    assert torch.equal(ids_a, ids_b) and torch.equal(w_a, w_b)
+    assert torch.equal(rws_a.buf, rws_b.buf)
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    ref = oracle.moe_forward(layer, x, lg, k, shared_gate=None if gl is None else gl.cpu().numpy())
+    err = np.abs(to_f64(out_b) - ref)
+    assert np.all(err <= moe_tolerance(oracle, layer, x, lg, k, ref))
