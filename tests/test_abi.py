@@ -179,3 +179,28 @@ def test_qgemm_grouped_host_validation(q):
                                            tensor_scale=1.0))
     assert call(layer=sh, gate=0xA002) == 3                     # misaligned gate logits
     assert L.qgemm_grouped_workspace_size(ctypes.byref(m), 4, 2, 3) == 0
+
+
+def test_qmoe_forward_host_validation(q):
+    """Argument errors of the router + FFN call come back before any device work."""
+    L = q.lib()
+    m = _moe_desc(q)
+    args = dict(x=0x3000, t=4, ldx=256, lg=0x4000, topk=2, gate=None, ids=0x5000, w=0x6000, rws=0x7000,
+                rwsb=1 << 20, out=0x8000, ldo=256, ws=0x9000, wsb=1 << 26)
+
+    def call(layer=m, **kw):
+        a = dict(args)
+        a.update(kw)
+        return L.qmoe_forward(ctypes.byref(layer), a["x"], a["t"], a["ldx"], a["lg"], a["topk"], a["gate"], a["ids"],
+                              a["w"], a["rws"], a["rwsb"], a["out"], a["ldo"], a["ws"], a["wsb"], None)
+
+    assert call(lg=None) == 1                      # logits required
+    assert call(ids=None) == 1
+    assert call(t=0) == 1
+    assert call(topk=9) == 1                       # more than the experts
+    assert call(gate=0xA000) == 1                  # gate logits without a shared expert
+    assert call(lg=0x4004) == 3                    # misaligned logits
+    assert call(ldo=128) == 1                      # output narrower than H
+    assert call(rwsb=16) == 4                      # router workspace too small
+    assert call(layer=_moe_desc(q, fmt=wl.Q6K)) == 1  # Q6_K layer without aux
+    assert call(layer=_moe_desc(q, fmt=wl.Q5_K)) == 2  # the 5-bit formats run on the dense paths only
