@@ -25,7 +25,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 template <int FMT>
 __device__ __forceinline__ void decode_word(const uint8_t* raw, int r, int wg, uint32_t w, uint32_t* o) {
   using F = Fmt<FMT>;
-  const int rt = r >> 5, lane = r & 31;
   const uint8_t* sp = raw + F::TB + r * F::SB;
   float v[8];
   if constexpr (FMT == FMT_NVFP4 || FMT == FMT_MXFP4) {
