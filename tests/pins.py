@@ -411,3 +411,24 @@ def check_operand_bf16(o, fmt, seed=31):
     else:
         ref = torch.from_numpy(w32.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
         assert np.array_equal(op, ref)
+
+
+def check_tolerance_output_ulp(o, seed=37):
+    """The output term of the tolerance, 2**-7 |ref|, is at least the gap between ref and
+    either bf16 neighbour (so two sides rounding one exact value to neighbouring bf16
+    numbers stay inside it), and is a strict bound: a flip of two ulps is outside it."""
+    rng = np.random.default_rng(seed)
+    v = o.round_to_bf16(rng.standard_normal(2000) * 10.0 ** rng.integers(-3, 4, 2000))
+    v = v[v != 0]
+    bits = o.bf16_bits_of(v).astype(np.int32)
+    up = o.bf16_value((bits + 1).astype(np.uint16))    # next bf16 away from zero (sign-magnitude)
+    down = o.bf16_value((bits - 1).astype(np.uint16))  # next bf16 toward zero
+    assert np.all(np.abs(up) > np.abs(v)) and np.all(np.abs(down) < np.abs(v))
+    assert np.all(np.abs(up - v) <= 2.0 ** -7 * np.abs(v))
+    assert np.all(np.abs(v - down) <= 2.0 ** -7 * np.abs(v))
+    w = wl.weight(wl.NVFP4, 4, 64, seed)
+    x = wl.activations(2, 64, seed)
+    ref, _ = o.gemv(w, x)
+    tol = o.tolerance(w, x, ref=ref)
+    base = o.tolerance(w, x)
+    assert np.allclose(tol - base, 2.0 ** -7 * np.abs(ref), rtol=1e-12, atol=0)

@@ -24,5 +24,5 @@ def test_bounded_wait_times_out_and_context_survives():
     y = q.gemv(pw, dev_bf16(x))
     torch.cuda.synchronize()
     ref, _ = oracle.gemv(w, x)
-    tol = oracle.tolerance(w, x, None)
+    tol = oracle.tolerance(w, x, None, ref=ref)
     assert np.all(np.abs(to_f64(y) - ref) <= tol)

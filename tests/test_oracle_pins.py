@@ -83,3 +83,7 @@ def test_moe_chain_composition():
 @pytest.mark.parametrize("fmt", ALL_FMTS)
 def test_bf16_operand(fmt):
     pins.check_operand_bf16(oracle, fmt)
+
+
+def test_tolerance_output_ulp():
+    pins.check_tolerance_output_ulp(oracle)
