@@ -180,11 +180,14 @@ qg_status qgemv(const qg_weight* w, const void* x, int m_rows, int64_t ldx,
 size_t qg_gemm_workspace_size(int fmt, int64_t n, int64_t k, int m);
 
 /* Quantized GEMM for any number of activation rows (tokens), dispatching by rows
- * (TurboEXL3 article §4.3, a path per row count): 1..4 rows run qgemv; more rows run the
- * prefill kernel, which decodes each 128 x 64 weight slice once into shared memory as
- * bf16 and multiplies it against up to 256 tokens on the tensor cores (tcgen05, fp32
- * accumulation in tensor memory) -- TurboEXL3 article §4.1, "decode once, multiply many
- * times"; no dequantised copy of the weights is written to device memory.
+ * (TurboEXL3 article §4.3, a path per row count): 1..4 rows run qgemv; 5..128 rows the
+ * small-token tensor-core GEMM (one token tile of 16 / 32 / 64 / 128); more rows the
+ * prefill GEMM with 256-token tiles.  Both tensor-core GEMMs decode each 128 x 64 weight
+ * slice once, on chip, into bf16 operands in tensor memory and multiply it against the
+ * tile's tokens (tcgen05, fp32 accumulation in tensor memory), splitting K over a cluster
+ * when the tiles fill less than half the GPU -- TurboEXL3 article §4.1: each weight
+ * decoded once and used for many tokens; no dequantised copy of the weights is written
+ * to device memory.
  *   y[t][n] = bf16( sum_k w[n,k] * x[t][k] (+ residual[t][n]) ),  t = 0..m_rows-1.
  * Same argument rules as qgemv; the workspace holds the device status word
  * (qg_workspace_status) and must be zero-filled before first use. */

@@ -4,7 +4,7 @@ Steps, in the order of the TurboEXL3 article §4.1 (prefill chain) and §4.2
 (decode chain):
 
 1. Route: each token keeps its top-k experts by router logit and weighs them by
-   a softmax over those k logits (§4.2: "the router's top-k and softmax").
+   a softmax over those k logits (§4.2 names the router's top-k and softmax).
    Reading: ties go to the lower expert index; the softmax is over the k kept
    logits (the same as a softmax over all experts renormalised over the k).
 2. Gate and up: one projection of 2F rows per expert; rows 0..F-1 are the gate,

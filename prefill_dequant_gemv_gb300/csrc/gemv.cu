@@ -6,19 +6,23 @@
 //
 // How (GB300 design, not the pages' Metal tile):
 //  * Work unit = one 128-row x 64-input tile of the packed layout (4.25-6.9 KB,
-//    contiguous).  The U = NT * KG units are cut into `gridDim.x` equal contiguous
-//    ranges (stream-K), one CTA per SM, so every SM streams the same byte count.
-//  * One producer lane issues 1-D bulk async copies of whole tiles into a deep
-//    ring of shared-memory stages (mbarrier completion, bounded waits); twelve
-//    consumer warps decode from shared memory.  Warp w takes the 16-input quarter
-//    (w % 4) of every 3rd unit; each lane owns 4 rows (one per 32-row tile), so
+//    contiguous).  Three ways to cut the U = NT * KG units over the SMs, all
+//    deterministic: one whole row tile per CTA when the row tiles nearly fill the GPU;
+//    each row tile split over a thread-block cluster (equal input ranges, partials
+//    summed in the first CTA's shared memory) when they fill less than half of it;
+//    otherwise equal contiguous unit ranges per SM (stream-K), where a row tile split
+//    across CTAs is finished by the last CTA to take its ticket -- the last arrival
+//    runs the finish, as in the TurboEXL3 article §4.3 -- summing the partials in CTA
+//    order.
+//  * One producer lane issues 1-D bulk async copies of whole tiles into a deep ring of
+//    shared-memory stages (mbarrier completion, bounded waits); 16 consumer warps (12 at
+//    four rows) decode from shared memory.  Warp w takes the 16-input quarter (w % 4)
+//    of every (w / 4)-th unit of a chunk; each lane owns 4 rows (one per 32-row tile), so
 //    every activation value read from shared memory feeds 4 rows.
-//  * Decode in registers to fp32 operands (qg_common.cuh), packed f32x2 FMAs into
-//    per-block partials, block scale applied once per block (Q6_K operand PR #19:
-//    the epilogue is one fma(dot, scale) per chain).
-//  * Row tiles split across CTAs are finished by the CTA that arrives last on the
-//    tile's ticket (TurboEXL3 article §4.3: "the threadgroup that arrives last runs
-//    the finish"); it sums the partials in CTA order, so results are deterministic.
+//  * Weights become exact f16 operands in registers (qg_common.cuh) multiplied into fp32
+//    with the mixed-precision FMA; the block scale (and the integer formats' operand
+//    constant) is applied once per 16 inputs and row (Q6_K operand PR #19: one
+//    fma(dot, scale) per chain).
 #include <cuda_runtime.h>
 
 #include <algorithm>

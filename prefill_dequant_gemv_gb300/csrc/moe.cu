@@ -1,11 +1,11 @@
 // Mixture-of-experts layer for 1..4 tokens (decode and speculative verify), in the five
 // dependent launches of the TurboEXL3 article §4.2: route (route.cu), gate/up, mid, down,
 // finish.  The shared expert runs as extra groups of the routed gate/up and down launches
-// (§4.2: "extra grid rows of the routed launches").
+// (as §4.2 runs it inside the routed launches).
 //
-//   gate/up  grouped GEMV: every active expert's 2F x H weights are read from HBM once
-//            for all the tokens that chose it (§4.2: "two tokens that chose the same
-//            expert share one decode of its weights"), fp32 results per (token, expert)
+//   gate/up  grouped GEMV: every active expert's 2F x H weights are read from HBM and
+//            decoded once for all the tokens that chose it (§4.2), fp32 results per
+//            (token, expert)
 //   down     grouped GEMV on h = bf16( silu(gate) * up ) (§4.1 "Mid": SwiGLU in 32-bit),
 //            which each CTA computes from the fp32 gate/up rows while staging its inputs
 //            (only the rows of the experts it works on), so the mid step needs no launch of
