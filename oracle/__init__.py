@@ -16,6 +16,8 @@ the source pages it follows:
 * "Q6_K operand PR" (perf: Q6_K's zero point in the operands of the Apple7/8
   register decode tile, #19), "What changed" and its commit messages (the 5-bit
   nibble operand of Q5_K, Q5_1 and Q5_0).
+* The same article, §2.2: the W4A4 mode, activations quantised to NVFP4 on the fly
+  (``act_quant``).
 
 Parity pins for every function live in ``tests/test_oracle_pins.py``.
 """
@@ -26,3 +28,4 @@ from .formats import (  # noqa: F401
 from .gemv import gemv, gemv_rows, row_norms, tolerance  # noqa: F401
 from .moe import route, sigmoid, silu, swiglu_bf16, moe_forward, expert_ffn  # noqa: F401
 from .layout import unpack, packed_sizes  # noqa: F401
+from .act_quant import e2m1_encode, e4m3_encode, quantize_act_nvfp4, gemm_w4a4  # noqa: F401

@@ -432,3 +432,153 @@ def check_tolerance_output_ulp(o, seed=37):
     tol = o.tolerance(w, x, ref=ref)
     base = o.tolerance(w, x)
     assert np.allclose(tol - base, 2.0 ** -7 * np.abs(ref), rtol=1e-12, atol=0)
+
+
+# ----------------------------------------------------------------- W4A4 (activations to NVFP4)
+def _e2m1_closed_form(v: np.ndarray) -> np.ndarray:
+    """Nearest-even E2M1 magnitude by a closed form: below 2 the grid has step 1/2, from
+    2 to 4 step 1, from 4 step 2 up to 6; np.round rounds half to even, and at each step
+    change the even neighbour is the power of two."""
+    a = np.abs(v.astype(np.float64))
+    return np.where(a < 2, np.round(2 * a) / 2, np.where(a < 4, np.round(a), np.minimum(6.0, 2 * np.round(a / 2))))
+
+
+def check_e2m1_encode(o, seed=41):
+    """E2M1 encoding: each code's own value maps back to it; midpoints, their fp32
+    neighbours and random values match the closed form; the sign bit follows the input's."""
+    codes = np.arange(16)
+    assert np.array_equal(o.e2m1_encode(o.e2m1_value(codes).astype(np.float32)), codes)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], dtype=np.float32)
+    mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)
+    rng = np.random.default_rng(seed)
+    v = np.concatenate([grid, mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(100)),
+                        rng.uniform(0, 9, 4000).astype(np.float32), np.float32([7.0, 1e30])])
+    v = np.concatenate([v, -v]).astype(np.float32)
+    got = o.e2m1_encode(v)
+    want = _e2m1_closed_form(v)
+    mag = np.abs(np.vectorize(lambda c: float(e2m1_from_page(int(c))))(got))
+    assert np.array_equal(mag, want), v[mag != want][:8]
+    assert np.array_equal((got >> 3) & 1, np.signbit(v).astype(np.uint8))
+    assert int(o.e2m1_encode(np.float32([-0.0]))[0]) == 8 and int(o.e2m1_encode(np.float32([0.1]))[0]) == 0
+
+
+def check_e4m3_encode(o, seed=43):
+    """E4M3 encoding: every finite code maps back to itself; values up to 448 (midpoints,
+    their fp32 neighbours, log-uniform draws) match torch's float8_e4m3fn conversion
+    (round to nearest even); larger values saturate at 448 (0x7E)."""
+    codes = np.arange(0x7F)
+    assert np.array_equal(o.e4m3_encode(o.e4m3fn_value(codes).astype(np.float32)), codes)
+    vals = o.e4m3fn_value(codes)
+    mids = ((vals[1:] + vals[:-1]) / 2).astype(np.float32)
+    rng = np.random.default_rng(seed)
+    v = np.concatenate([mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9)),
+                        np.exp2(rng.uniform(-12, np.log2(448.0), 4000)).astype(np.float32)])
+    v = v[v <= 448].astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = o.e4m3_encode(v)
+    assert np.array_equal(got, ref), v[got != ref][:8]
+    assert np.all(o.e4m3_encode(np.float32([448.0, 460.0, 464.0, 1e4, 3e38])) == 0x7E)
+    assert int(o.e4m3_encode(np.float32([0.0]))[0]) == 0
+
+
+def exact_nvfp4_activations(m: int, k: int, act_scale: float, seed: int):
+    """Activations that NVFP4 represents exactly: x = act_scale * E4M3(S) * E2M1(c) per
+    block of 16 with one magnitude-6 code per block, act_scale a power of two.  Built
+    with torch's E4M3 decoder and the page's E2M1 table; returns (x bf16 bits, c, S)."""
+    rng = np.random.default_rng(seed)
+    c = rng.integers(0, 16, (m, k)).astype(np.uint8)
+    c[c == 8] = 0  # -0 has no exact rational: keep zeros positive here (check_e2m1_encode pins -0)
+    blocks = c.reshape(m, k // 16, 16)
+    pos = rng.integers(0, 16, (m, k // 16))
+    sign = rng.integers(0, 2, (m, k // 16)).astype(np.uint8) << 3
+    np.put_along_axis(blocks, pos[..., None], (7 | sign)[..., None], axis=2)
+    s = rng.integers(0x10, 0x70, (m, k // 16)).astype(np.uint8)
+    sv = np.vectorize(lambda b: float(torch_e4m3(int(b))))(s)
+    ev = np.vectorize(lambda q: float(e2m1_from_page(int(q))))(c)
+    x = act_scale * np.repeat(sv, 16, axis=1) * ev
+    bits = (x.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    assert np.array_equal(bf16_value_np(bits), x), "the construction must be bf16-exact"
+    return bits, c, s
+
+
+def bf16_value_np(bits) -> np.ndarray:
+    return (np.asarray(bits).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def check_act_quant_round_trip(o, seed=47):
+    """Activations NVFP4 represents exactly (one magnitude-6 code per block) come back as
+    the same codes, the same E4M3 scales and the same values, for several power-of-two
+    tensor scales.  A wrong block size, divisor, scale order or sign rule breaks it."""
+    for i, a in enumerate((1.0, 0.125, 32.0)):
+        bits, c, s = exact_nvfp4_activations(3, 96, a, seed + i)
+        codes, scales, xe, xq = o.quantize_act_nvfp4(bits, a)
+        assert np.array_equal(scales, s), a
+        assert np.array_equal(codes, c), a
+        assert np.array_equal(xq, bf16_value_np(bits)), a
+        assert np.array_equal(xe, bf16_value_np(bits) / a), a
+
+
+def check_act_quant_nearest(o, seed=53):
+    """On arbitrary activations: each block's scale is a nearest E4M3 value to
+    amax / (6 act_scale), and each quantised value is a nearest point of its block's grid
+    act_scale * E4M3(S) * (+-E2M1) to x (up to the fp32 rounding of the division), with
+    x's sign; all-zero blocks give zero scales and codes."""
+    rng = np.random.default_rng(seed)
+    m, k = 4, 256
+    x = rng.standard_normal((m, k)) * np.exp2(rng.integers(-12, 12, (m, 1)))
+    x[1, :16] = 0.0
+    x[2, 16:32] *= 1e-30  # far below act_scale * 2**-9 * 6: the scale rounds to 0
+    bits = wl.bf16_bits_from_f32(x.astype(np.float32))
+    xv = bf16_value_np(bits)
+    grid_e4 = np.array([float(torch_e4m3(b)) for b in range(0x7F)])
+    grid_e2 = np.array([float(e2m1_from_page(c)) for c in range(8)])
+    for a in (1.0, 0.37, 3e-3):
+        codes, scales, xe, xq = o.quantize_act_nvfp4(bits, a)
+        for i in range(m):
+            for b in range(k // 16):
+                blk = xv[i, 16 * b:16 * b + 16]
+                r = np.abs(blk).max() / (6 * float(np.float32(a)))
+                sf = float(torch_e4m3(int(scales[i, b])))
+                assert abs(sf - r) <= np.min(np.abs(grid_e4 - r)) * (1 + 1e-6) + 1e-300, (a, i, b)
+                step = float(np.float32(a)) * sf
+                for j in range(16):
+                    xj, qj = blk[j], xq[i, 16 * b + j]
+                    best = np.min(np.abs(step * grid_e2 - abs(xj)))
+                    assert abs(abs(qj) - abs(xj)) <= best + 2.0 ** -20 * abs(xj) + 1e-300, (a, i, b, j)
+                    assert qj == 0 or np.sign(qj) == np.sign(xj)
+                    assert ((codes[i, 16 * b + j] >> 3) & 1) == int(np.signbit(xj))
+        assert np.all(scales[1, 0] == 0) and np.all(codes[1, :16] == 0)
+        assert scales[2, 1] == 0 and np.all(xq[2, 16:32] == 0)
+
+
+def check_w4a4_reduces_to_w4a16(o, seed=59):
+    """With activations NVFP4 represents exactly, the W4A4 GEMM is the W4A16 GEMM of the
+    same activations, bit for bit (a residual included)."""
+    w = wl.weight(wl.NVFP4, 48, 96, seed)
+    for a in (1.0, 0.25):
+        bits, _, _ = exact_nvfp4_activations(3, 96, a, seed + 1)
+        res = wl.activations(3, 48, seed=seed + 2, stream="residual")
+        y4, v4, _ = o.gemm_w4a4(w, bits, a, res)
+        y16, v16 = o.gemv(w, bits, res)
+        assert np.array_equal(y4, y16) and np.allclose(v4, v16, rtol=1e-15, atol=0)
+
+
+def check_w4a4_brute_force(o, seed=61):
+    """W4A4 outputs against exact rationals: sum_k fp32(w) * act_scale * E4M3(S) * E2M1(c)
+    with the scales and codes the oracle chose (those are pinned above), one bf16 rounding."""
+    w = wl.weight(wl.NVFP4, 6, 32, seed)
+    bits = wl.activations(2, 32, seed=seed + 1)
+    a = 0.37
+    y, v, _ = o.gemm_w4a4(w, bits, a)
+    codes, scales, _, _ = o.quantize_act_nvfp4(bits, a)
+    w32 = o.dequant(w)
+    af = Fraction(float(np.float32(a)))
+    for mi in range(2):
+        for ni in range(6):
+            terms = [Fraction(float(w32[ni, kk])) * af * torch_e4m3(int(scales[mi, kk // 16]))
+                     * e2m1_from_page(int(codes[mi, kk])) for kk in range(32)]
+            ex = sum(terms, Fraction(0))
+            bound = 34 * 2.0 ** -52 * float(sum(abs(t) for t in terms))
+            assert abs(Fraction(float(v[mi, ni])) - ex) <= Fraction(bound), (mi, ni)
+            lo, hi = frac_round_bf16(ex - Fraction(bound)), frac_round_bf16(ex + Fraction(bound))
+            assert Fraction(float(y[mi, ni])) in (lo, hi), (mi, ni)

@@ -223,3 +223,67 @@ def test_q5_operand_fifth_bit_at_bit_9(monkeypatch):
         return (np.uint16(0x3C00) | ((c & 0xF) << 4) | ((c >> 4) << 9)).astype(np.uint16)
     monkeypatch.setattr(oracle, "q5_half_operand_bits", bad)
     assert _fails(pins.check_q5_operand, oracle)
+
+
+A = sys.modules["oracle.act_quant"]
+
+
+def _both(monkeypatch, name, fn):
+    monkeypatch.setattr(oracle, name, fn)
+    monkeypatch.setattr(A, name, fn)
+
+
+def test_e2m1_encode_ties_down(monkeypatch):
+    def bad(q):
+        q = np.asarray(q, dtype=np.float32)
+        a = np.minimum(np.abs(q.astype(np.float64)), 6.0)
+        d = np.abs(a[..., None] - A._E2M1_GRID)
+        mag = np.argmax(d == d.min(axis=-1, keepdims=True), axis=-1).astype(np.uint8)  # lower of two
+        return mag | (np.signbit(q).astype(np.uint8) << 3)
+    _both(monkeypatch, "e2m1_encode", bad)
+    assert _fails(pins.check_e2m1_encode, oracle)
+
+
+def test_e4m3_encode_truncates(monkeypatch):
+    def bad(r):
+        r = np.asarray(r, dtype=np.float64)
+        return np.array([np.searchsorted(A._E4M3_GRID, v, side="right") - 1 for v in r.ravel()],
+                        dtype=np.uint8).reshape(r.shape)
+    _both(monkeypatch, "e4m3_encode", bad)
+    assert _fails(pins.check_e4m3_encode, oracle)
+
+
+def test_act_quant_divisor_four(monkeypatch):
+    orig = A.e4m3_encode
+    monkeypatch.setattr(A, "e4m3_encode", lambda r: orig(np.asarray(r, np.float32) * np.float32(1.5)))
+    assert _fails(pins.check_act_quant_round_trip, oracle)
+    assert _fails(pins.check_act_quant_nearest, oracle)
+
+
+def test_act_quant_sign_dropped(monkeypatch):
+    orig = A.quantize_act_nvfp4
+
+    def bad(x, a):
+        c, s, xe, xq = orig(x, a)
+        return c & 7, s, np.abs(xe), np.abs(xq)
+    _both(monkeypatch, "quantize_act_nvfp4", bad)
+    assert _fails(pins.check_act_quant_round_trip, oracle)
+
+
+def test_act_quant_tensor_scale_dropped(monkeypatch):
+    orig = A.quantize_act_nvfp4
+
+    def bad(x, a):
+        c, s, xe, xq = orig(x, a)
+        return c, s, xe, xe
+    _both(monkeypatch, "quantize_act_nvfp4", bad)
+    assert _fails(pins.check_act_quant_round_trip, oracle)
+    assert _fails(pins.check_w4a4_reduces_to_w4a16, oracle)
+
+
+def test_w4a4_skips_activation_quantisation(monkeypatch):
+    def bad(w, x, a, res=None, rows=None):
+        y, v = G.gemv(w, x, res)
+        return y, v, None
+    _both(monkeypatch, "gemm_w4a4", bad)
+    assert _fails(pins.check_w4a4_brute_force, oracle)

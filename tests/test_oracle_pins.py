@@ -87,3 +87,27 @@ def test_bf16_operand(fmt):
 
 def test_tolerance_output_ulp():
     pins.check_tolerance_output_ulp(oracle)
+
+
+def test_e2m1_encode_closed_form():
+    pins.check_e2m1_encode(oracle)
+
+
+def test_e4m3_encode_matches_library():
+    pins.check_e4m3_encode(oracle)
+
+
+def test_act_quant_round_trip():
+    pins.check_act_quant_round_trip(oracle)
+
+
+def test_act_quant_nearest_grid_points():
+    pins.check_act_quant_nearest(oracle)
+
+
+def test_w4a4_reduces_to_w4a16():
+    pins.check_w4a4_reduces_to_w4a16(oracle)
+
+
+def test_w4a4_brute_force_exact_rational():
+    pins.check_w4a4_brute_force(oracle)
