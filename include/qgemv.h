@@ -195,6 +195,49 @@ qg_status qgemm(const qg_weight* w, const void* x, int64_t m_rows, int64_t ldx,
                 const void* residual, int64_t ldr, void* y, int64_t ldy,
                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------ W4A4: NVFP4 activations
+ * TurboEXL3 article §2.2: besides W4A16, an NVFP4 checkpoint can run W4A4, quantising the
+ * activations to NVFP4 as well during the forward pass, with one scale per 16 values.
+ * The pages leave the activations' tensor scale open: here it is the caller's fp32
+ * act_scale (finite, > 0; a calibrated constant).  Per block of 16 consecutive values
+ * of a row along K, each step one fp32 operation rounded to nearest even:
+ *   S    = E4M3( amax / (6 * act_scale) )            nearest even, saturating at 448
+ *   den  = E4M3(S) * act_scale
+ *   code = E2M1( x / den )   (x * 0 when den == 0)    nearest even, saturating at 6,
+ *                                                     sign bit from x (-0 gives 8)
+ * Activations must be finite. */
+
+/* Quantise bf16 activations x [m][ldx] (k a multiple of 16; x 16-byte aligned, ldx a
+ * multiple of 8) to NVFP4.  Outputs, device memory, each optional (NULL: not written):
+ *   codes  : uint8 [m][ldc], two E2M1 codes per byte, value k in byte k/2, the even k in
+ *            the low nibble (ldc >= k/2, a multiple of 8; 16-byte aligned);
+ *   scales : uint8 [m][lds], the E4M3 byte of block k/16 (lds >= k/16);
+ *   xe     : bf16 [m][lde], E4M3(S) * E2M1(code) -- exact in bf16, act_scale left out --
+ *            the operand a bf16 GEMM multiplies (lde >= k, a multiple of 8; 16-byte aligned).
+ * Argument errors return before anything is launched. */
+qg_status qg_quant_act_nvfp4(const void* x, int64_t m_rows, int64_t k, int64_t ldx, float act_scale,
+                             uint8_t* codes, int64_t ldc, uint8_t* scales, int64_t lds,
+                             void* xe, int64_t lde, void* stream);
+
+/* Workspace bytes qgemm_w4a4 needs: the qgemm workspace of the same shape (first, so the
+ * status word stays at offset 0) plus m_rows x k bf16 quantised activations.  0 for a
+ * format other than NVFP4. */
+size_t qgemm_w4a4_workspace_size(int fmt, int64_t n, int64_t k, int64_t m_rows);
+
+/* W4A4 GEMM for an NVFP4 weight (other formats: QG_ERR_UNSUPPORTED):
+ *   y[t][n] = bf16( sum_k w[n,k] * xq[t][k] (+ residual[t][n]) ),
+ *   xq[t][k] = act_scale * E4M3(S) * E2M1(code)  (qg_quant_act_nvfp4 above).
+ * qg_quant_act_nvfp4 writes the expansion into the workspace, then qgemm multiplies it
+ * (the GEMV for 1..4 rows, the tensor-core GEMMs above that) with act_scale folded into
+ * the weight's tensor scale for the epilogue.  Both operands are exact in bf16, so each
+ * product is exactly that of the two FP4 values and their scales; the tensor cores run
+ * the bf16 kind, not a block-scaled FP4 one.  Same argument rules and workspace contract
+ * as qgemm (zero-filled before first use); act_scale * tensor_scale must be a finite
+ * positive fp32. */
+qg_status qgemm_w4a4(const qg_weight* w, const void* x, int64_t m_rows, int64_t ldx, float act_scale,
+                     const void* residual, int64_t ldr, void* y, int64_t ldy,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------------ mixture of experts
  * A layer of n_experts routed experts plus an optional shared expert, each an FFN with
  * gate/up (2F x H: rows 0..F-1 gate, F..2F-1 up) and down (H x F) quantized matrices.

@@ -68,6 +68,10 @@ _SIGNATURES = {
                           _P]),
     "qgemm_grouped": (_I, [ctypes.POINTER(qg_moe_layer), _I, _P, _I64, _I64, _I, _P, _P, _P, _P, _I64, _P, _SZ, _P]),
     "qg_selftest_wait_timeout": (_I, [_P, _SZ, _P]),
+    "qg_quant_act_nvfp4": (_I, [_P, _I64, _I64, _I64, ctypes.c_float, _P, _I64, _P, _I64, _P, _I64, _P]),
+    "qgemm_w4a4_workspace_size": (_SZ, [_I, _I64, _I64, _I64]),
+    "qgemm_w4a4": (_I, [ctypes.POINTER(qg_weight), _P, _I64, _I64, ctypes.c_float, _P, _I64, _P, _I64, _P, _SZ,
+                        _P]),
 }
 
 QG_MOE_GATE_UP_SWIGLU = 1
@@ -150,6 +154,22 @@ def qg_gemm_workspace_size(fmt: int, n: int, k: int, m: int) -> int:
 def qgemm(w: qg_weight, x_ptr: int, m: int, ldx: int, res_ptr: Optional[int], ldr: int, y_ptr: int, ldy: int,
           ws_ptr: int, ws_bytes: int, stream: int = 0):
     _check(lib().qgemm(ctypes.byref(w), x_ptr, m, ldx, res_ptr, ldr, y_ptr, ldy, ws_ptr, ws_bytes, stream), "qgemm")
+
+
+def qg_quant_act_nvfp4(x_ptr: int, m: int, k: int, ldx: int, act_scale: float, codes_ptr: Optional[int], ldc: int,
+                       scales_ptr: Optional[int], lds: int, xe_ptr: Optional[int], lde: int, stream: int = 0):
+    _check(lib().qg_quant_act_nvfp4(x_ptr, m, k, ldx, act_scale, codes_ptr, ldc, scales_ptr, lds, xe_ptr, lde, stream),
+           "qg_quant_act_nvfp4")
+
+
+def qgemm_w4a4_workspace_size(fmt: int, n: int, k: int, m: int) -> int:
+    return lib().qgemm_w4a4_workspace_size(fmt, n, k, m)
+
+
+def qgemm_w4a4(w: qg_weight, x_ptr: int, m: int, ldx: int, act_scale: float, res_ptr: Optional[int], ldr: int,
+               y_ptr: int, ldy: int, ws_ptr: int, ws_bytes: int, stream: int = 0):
+    _check(lib().qgemm_w4a4(ctypes.byref(w), x_ptr, m, ldx, act_scale, res_ptr, ldr, y_ptr, ldy, ws_ptr, ws_bytes,
+                            stream), "qgemm_w4a4")
 
 
 def qmoe_route_workspace_size(t: int, n_experts: int, topk: int) -> int:
@@ -284,6 +304,35 @@ def gemm(pw: PackedWeight, x, residual=None, out=None, workspace: Optional[Works
     qgemm(pw.desc, x.data_ptr(), m, x.stride(0), None if residual is None else residual.data_ptr(),
           0 if residual is None else residual.stride(0), out.data_ptr(), out.stride(0), workspace.ptr,
           workspace.nbytes, _stream_ptr())
+    return out
+
+
+def quant_act_nvfp4(x, act_scale: float):
+    """NVFP4-quantise bf16 activations x [m, k] on the device (W4A4).  Returns (codes uint8 [m, k/2], two
+    E2M1 codes a byte, the even k in the low nibble; scales uint8 [m, k/16] E4M3; xe bf16 [m, k], the exact
+    expansion E4M3(S) * E2M1(code) without act_scale)."""
+    import torch
+    m, k = x.shape
+    dev = x.device
+    codes = torch.empty((m, (k // 2 + 7) // 8 * 8), dtype=torch.uint8, device=dev)
+    scales = torch.empty((m, k // 16), dtype=torch.uint8, device=dev)
+    xe = torch.empty((m, (k + 7) // 8 * 8), dtype=torch.bfloat16, device=dev)
+    qg_quant_act_nvfp4(x.data_ptr(), m, k, x.stride(0), act_scale, codes.data_ptr(), codes.stride(0),
+                       scales.data_ptr(), scales.stride(0), xe.data_ptr(), xe.stride(0), _stream_ptr())
+    return codes[:, :k // 2], scales, xe[:, :k]
+
+
+def gemm_w4a4(pw: PackedWeight, x, act_scale: float, residual=None, out=None, workspace: Optional[Workspace] = None):
+    """y = bf16(W xq (+ residual)) with xq the NVFP4 quantisation of x (bf16 [m, k]) at tensor scale act_scale."""
+    import torch
+    m = x.shape[0]
+    if out is None:
+        out = torch.empty((m, (pw.n + 7) // 8 * 8), dtype=torch.bfloat16, device=x.device)[:, :pw.n]
+    if workspace is None:
+        workspace = Workspace(qgemm_w4a4_workspace_size(pw.fmt, pw.n, pw.k, m), x.device)
+    qgemm_w4a4(pw.desc, x.data_ptr(), m, x.stride(0), act_scale, None if residual is None else residual.data_ptr(),
+               0 if residual is None else residual.stride(0), out.data_ptr(), out.stride(0), workspace.ptr,
+               workspace.nbytes, _stream_ptr())
     return out
 
 

@@ -2,6 +2,8 @@
 // dispatch to the kernel launchers.  No entry point allocates memory.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "qg_internal.h"
@@ -150,6 +152,60 @@ extern "C" qg_status qgemm(const qg_weight* w, const void* x, int64_t m, int64_t
     return (qg_status)launch_gemm_small(g, w, x, m, ldx, residual, ldr, y, ldy, workspace, dev, stream);
   }
   return (qg_status)launch_prefill(g, w, x, m, ldx, residual, ldr, y, ldy, workspace, stream);
+}
+
+extern "C" qg_status qg_quant_act_nvfp4(const void* x, int64_t m, int64_t k, int64_t ldx, float act_scale,
+                                        uint8_t* codes, int64_t ldc, uint8_t* scales, int64_t lds, void* xe,
+                                        int64_t lde, void* stream) {
+  if (!x || m < 1 || k < 16 || k % 16 || !(act_scale > 0.0f) || !std::isfinite(act_scale)) return QG_ERR_INVALID_ARG;
+  if (ldx < k || (codes && ldc < k / 2) || (scales && lds < k / 16) || (xe && lde < k)) return QG_ERR_INVALID_ARG;
+  if (!aligned16(x) || ldx % 8 || (codes && (!aligned16(codes) || ldc % 8)) || (xe && (!aligned16(xe) || lde % 8)))
+    return QG_ERR_MISALIGNED;
+  return (qg_status)launch_quant_act_nvfp4(x, m, k, ldx, act_scale, codes, ldc, scales, lds, xe, lde, stream);
+}
+
+// W4A4 workspace: the qgemm workspace first (its status word at offset 0), then the
+// quantised activations' bf16 expansion, m rows of k rounded up to 8.
+static size_t w4a4_gemm_part(int fmt, int64_t n, int64_t k, int64_t m) {
+  const size_t g = qg_gemm_workspace_size(fmt, n, k, (int)std::min<int64_t>(m, 1 << 30));
+  return g ? (g + 255) / 256 * 256 : 0;
+}
+
+extern "C" size_t qgemm_w4a4_workspace_size(int fmt, int64_t n, int64_t k, int64_t m) {
+  if (fmt != QG_FMT_NVFP4 || m < 1) return 0;
+  const size_t g = w4a4_gemm_part(fmt, n, k, m);
+  return g ? g + (size_t)m * (size_t)((k + 7) / 8 * 8) * 2 : 0;
+}
+
+extern "C" qg_status qgemm_w4a4(const qg_weight* w, const void* x, int64_t m, int64_t ldx, float act_scale,
+                                const void* residual, int64_t ldr, void* y, int64_t ldy, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  // every check qgemm makes, before anything is launched
+  Geometry g;
+  int st = check_weight(w, &g);
+  if (st != QG_OK) return (qg_status)st;
+  if (w->fmt != QG_FMT_NVFP4 || m < 1) return QG_ERR_UNSUPPORTED;
+  if (!x || !y || !workspace || !(act_scale > 0.0f) || !std::isfinite(act_scale)) return QG_ERR_INVALID_ARG;
+  qg_weight ws = *w;  // the activation tensor scale joins the weight's in the GEMM's epilogue
+  ws.tensor_scale = w->tensor_scale * act_scale;
+  if (!(ws.tensor_scale > 0.0f) || !std::isfinite(ws.tensor_scale)) return QG_ERR_INVALID_ARG;
+  if (ldx < w->k || ldy < w->n || (residual && ldr < w->n)) return QG_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)) || !aligned16(workspace))
+    return QG_ERR_MISALIGNED;
+  if (ldx % 8 || ldy % 8 || (residual && ldr % 8)) return QG_ERR_MISALIGNED;
+  if ((m + 255) / 256 > 65535 || g.nt > 0x7FFFFFFF) return QG_ERR_UNSUPPORTED;
+  const size_t need = qgemm_w4a4_workspace_size(w->fmt, w->n, w->k, m);
+  if (!need) {  // 1..4 rows: the GEMV's plan needs the device; none, or no plan for this shape
+    DeviceInfo dev;
+    return current_device_info(&dev) ? QG_ERR_UNSUPPORTED : QG_ERR_CUDA;
+  }
+  if (workspace_bytes < need) return QG_ERR_WORKSPACE_TOO_SMALL;
+  const size_t off = w4a4_gemm_part(w->fmt, w->n, w->k, m);
+  void* xe = static_cast<char*>(workspace) + off;
+  const int64_t lde = (w->k + 7) / 8 * 8;
+  st = launch_quant_act_nvfp4(x, m, w->k, ldx, act_scale, nullptr, 0, nullptr, 0, xe, lde, stream);
+  if (st != QG_OK) return (qg_status)st;
+  return qgemm(&ws, xe, m, lde, residual, ldr, y, ldy, workspace, off, stream);
 }
 
 extern "C" size_t qmoe_route_workspace_size(int64_t t, int n_experts, int topk) {

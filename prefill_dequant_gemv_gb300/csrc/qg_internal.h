@@ -57,6 +57,10 @@ bool encode_token_rows(CUtensorMap* map, const void* x, int64_t rows, int64_t k,
 constexpr int64_t kSmallGemmMaxRows = 128;
 int launch_gemm_small(const Geometry& g, const qg_weight* w, const void* x, int64_t t, int64_t ldx, const void* res,
                       int64_t ldr, void* y, int64_t ldy, void* ws, const DeviceInfo& dev, void* stream);
+// NVFP4 activation quantisation (W4A4): codes / scales / exact bf16 expansion, each
+// output optional (NULL: not written).  Arguments validated by the caller.
+int launch_quant_act_nvfp4(const void* x, int64_t m, int64_t k, int64_t ldx, float act_scale, uint8_t* codes,
+                           int64_t ldc, uint8_t* scales, int64_t lds, void* xe, int64_t lde, void* stream);
 int launch_prefill(const Geometry& g, const qg_weight* w, const void* x, int64_t t, int64_t ldx, const void* res,
                    int64_t ldr, void* y, int64_t ldy, void* ws, void* stream);
 

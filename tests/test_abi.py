@@ -204,3 +204,38 @@ def test_qmoe_forward_host_validation(q):
     assert call(rwsb=16) == 4                      # router workspace too small
     assert call(layer=_moe_desc(q, fmt=wl.Q6K)) == 1  # Q6_K layer without aux
     assert call(layer=_moe_desc(q, fmt=wl.Q5_K)) == 2  # the 5-bit formats run on the dense paths only
+
+
+def test_quant_act_nvfp4_host_validation(q):
+    """Argument errors of the activation quantiser come back before anything is launched."""
+    L = q.lib()
+    args = dict(x=0x3000, m=4, k=256, ldx=256, a=1.0, c=0x4000, ldc=128, s=0x5000, lds=16, xe=0x6000, lde=256)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return L.qg_quant_act_nvfp4(a["x"], a["m"], a["k"], a["ldx"], a["a"], a["c"], a["ldc"], a["s"], a["lds"],
+                                    a["xe"], a["lde"], None)
+    assert call(x=None) == 1 and call(m=0) == 1 and call(k=250) == 1 and call(k=0) == 1
+    assert call(a=0.0) == 1 and call(a=-1.0) == 1 and call(a=float("inf")) == 1 and call(a=float("nan")) == 1
+    assert call(ldx=128) == 1 and call(ldc=64) == 1 and call(lds=8) == 1 and call(lde=128) == 1
+    assert call(x=0x3008) == 3 and call(ldx=260) == 3 and call(c=0x4008) == 3 and call(ldc=132) == 3
+    assert call(xe=0x6008) == 3 and call(lde=260) == 3
+
+
+def test_qgemm_w4a4_host_validation(q):
+    """The W4A4 GEMM makes every check qgemm makes (plus its own) before launching."""
+    L = q.lib()
+    w = _desc(q, tensor_scale=0.5)
+
+    def call(wd=w, x=0x3000, m=8, ldx=256, a=1.0, y=0x4000, ldy=256, ws=0x5000, wsb=1 << 20):
+        return L.qgemm_w4a4(ctypes.byref(wd), x, m, ldx, a, None, 0, y, ldy, ws, wsb, None)
+    assert call(wd=_desc(q, fmt=wl.MXFP4)) == 2 and call(m=0) == 2
+    assert call(x=None) == 1 and call(a=0.0) == 1 and call(a=float("nan")) == 1
+    assert call(wd=_desc(q, tensor_scale=1e30), a=1e30) == 1  # the product overflows fp32
+    assert call(ldx=128) == 1 and call(ldy=128) == 1
+    assert call(x=0x3008) == 3 and call(y=0x4008) == 3 and call(ldx=260) == 3
+    assert call(wsb=1000) == 4  # 8 rows: 256 + 8 x 256 x 2 bytes needed
+    assert q.qgemm_w4a4_workspace_size(wl.NVFP4, 256, 256, 8) == 256 + 8 * 256 * 2
+    assert q.qgemm_w4a4_workspace_size(wl.MXFP4, 256, 256, 8) == 0
+    assert q.qgemm_w4a4_workspace_size(wl.NVFP4, 256, 256, 0) == 0
