@@ -14,6 +14,16 @@
 // d6 = 6 * act_scale; r = amax / d6; S = E4M3(r) (nearest even, saturating at 448);
 // den = E4M3(S) * act_scale; q = x / den (x * 0 when den is 0); code = E2M1(q) (nearest
 // even, saturating at 6, with x's sign bit).
+//
+// The kernel is bound by instruction issue, so the sixteen divisions of a block are
+// replaced by one reciprocal and sixteen products, without changing a single code:
+// q' = RN(x * RN(1/den)) lies within 2 ulps of x/den (two roundings), and every value at
+// which E2M1's nearest-even rounding changes its code -- 0.25, 0.75, 1.25, 1.75, 2.5,
+// 3.5, 5 -- has at most 3 significant bits, so the low 21 mantissa bits of each are zero.
+// Unless q' lies within 8 ulps of such a value, q' and the correctly rounded quotient
+// are on the same side of every decision point and give the same code; the few that do
+// (exact ties and their neighbours among them) are divided exactly.  When den is a power
+// of two (or 0, where q' = x * 0 as q), q' is already the correctly rounded quotient.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
@@ -47,14 +57,23 @@ __device__ __forceinline__ float e4m3_pos_value(uint32_t b) {
 }
 
 // E2M1 code of q: the magnitude nearest |q| among 0, 0.5, 1, 1.5, 2, 3, 4, 6 with ties to
-// the even code -- at each midpoint the comparison is strict where the lower neighbour's
-// code is even (0.25, 1.25, 2.5, 5) and inclusive where the upper one's is (0.75, 1.75,
-// 3.5) -- and 7 (6) above 5; bit 3 is q's sign bit.
+// the even code, saturating at 6; bit 3 is q's sign bit.  Below 1 the grid has step 1/2:
+// 2^23 + 2|q| rounded once to fp32 is 2^23 + the nearest-even integer to 2|q| (0, 1 or 2
+// = codes 0, 0.5, 1.0).  From 1 up the grid keeps one mantissa bit: adding 2^21 - 1 plus
+// that bit to the fp32 bits rounds the mantissa to it, nearest even, and bits 22..30
+// (exponent, kept bit) then count codes from 252 up, clamped at 7.
 __device__ __forceinline__ uint32_t e2m1_code(float q) {
   const float a = fabsf(q);
-  const uint32_t c = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
-                     (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
-  return c | ((__float_as_uint(q) >> 31) << 3);
+  const uint32_t ua = __float_as_uint(a);
+  const uint32_t lo = __float_as_uint(__fmaf_rn(a, 2.0f, 0x1p23f)) & 3u;
+  const uint32_t hi = min(7u, ((ua + 0x1FFFFFu + ((ua >> 22) & 1u)) >> 22) - 252u);
+  return (a < 1.0f ? lo : hi) | ((__float_as_uint(q) >> 31) << 3);
+}
+
+// True when the fp32 value q lies within 8 ulps of a number whose low 21 mantissa bits are
+// zero -- among them every E2M1 decision point.
+__device__ __forceinline__ bool near_decision(float q) {
+  return ((__float_as_uint(q) + 8u) & 0x1FFFFFu) <= 16u;
 }
 
 // fp32 bits of the E2M1 magnitude of code c (0..7): 0, 0.5, then (1 + m/2) * 2^(e-1).
@@ -67,9 +86,9 @@ __global__ void __launch_bounds__(kQThreads) quant_act_nvfp4_kernel(QuantArgs a)
   // it waits for this grid to complete before it reads the expansion.
   if (threadIdx.x == 0) pdl_launch_dependents();
   const float d6 = __fmul_rn(6.0f, a.act_scale);
-  const int64_t total = a.m * a.kb;
-  for (int64_t i = (int64_t)blockIdx.x * kQThreads + threadIdx.x; i < total; i += (int64_t)gridDim.x * kQThreads) {
-    const int64_t row = i / a.kb, b = i - row * a.kb;
+  const uint32_t total = (uint32_t)(a.m * a.kb), kb = (uint32_t)a.kb;  // the host keeps it below 2^31
+  for (uint32_t i = blockIdx.x * kQThreads + threadIdx.x; i < total; i += gridDim.x * kQThreads) {
+    const int64_t row = i / kb, b = i - (uint32_t)row * kb;
     const uint4* src = reinterpret_cast<const uint4*>(a.x + row * a.ldx + b * 16);
     const uint4 v0 = __ldcs(src), v1 = __ldcs(src + 1);  // read once: do not keep in L2
     const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -84,11 +103,15 @@ __global__ void __launch_bounds__(kQThreads) quant_act_nvfp4_kernel(QuantArgs a)
     const uint32_t s = (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(amax, d6), __NV_SATFINITE, __NV_E4M3);
     const float sf = e4m3_pos_value(s);
     const float den = __fmul_rn(sf, a.act_scale);
+    const float rcp = den > 0.0f ? __frcp_rn(den) : 0.0f;  // den == 0: q' = x * 0, as q
+    // a normal power of two has an exact reciprocal: then q' is x / den rounded once
+    const bool exact = (__float_as_uint(den) & 0x7FFFFFu) == 0u;
     uint32_t cw[2] = {0u, 0u};
     uint32_t ew[8];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const float q = den > 0.0f ? __fdiv_rn(f[j], den) : f[j] * 0.0f;
+      float q = __fmul_rn(f[j], rcp);
+      if (!exact && near_decision(q)) q = __fdiv_rn(f[j], den);
       const uint32_t c = e2m1_code(q);
       cw[j >> 3] |= c << (4 * (j & 7));
       // sf * magnitude has at most 6 significant bits: exact in fp32, and its low 16 bits

@@ -161,6 +161,7 @@ extern "C" qg_status qg_quant_act_nvfp4(const void* x, int64_t m, int64_t k, int
   if (ldx < k || (codes && ldc < k / 2) || (scales && lds < k / 16) || (xe && lde < k)) return QG_ERR_INVALID_ARG;
   if (!aligned16(x) || ldx % 8 || (codes && (!aligned16(codes) || ldc % 8)) || (xe && (!aligned16(xe) || lde % 8)))
     return QG_ERR_MISALIGNED;
+  if (m > 0x7FFFFFFF / (k / 16)) return QG_ERR_UNSUPPORTED;  // 2^31 blocks of 16 at most
   return (qg_status)launch_quant_act_nvfp4(x, m, k, ldx, act_scale, codes, ldc, scales, lds, xe, lde, stream);
 }
 
@@ -193,7 +194,7 @@ extern "C" qg_status qgemm_w4a4(const qg_weight* w, const void* x, int64_t m, in
   if (!aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)) || !aligned16(workspace))
     return QG_ERR_MISALIGNED;
   if (ldx % 8 || ldy % 8 || (residual && ldr % 8)) return QG_ERR_MISALIGNED;
-  if ((m + 255) / 256 > 65535 || g.nt > 0x7FFFFFFF) return QG_ERR_UNSUPPORTED;
+  if ((m + 255) / 256 > 65535 || g.nt > 0x7FFFFFFF || m > 0x7FFFFFFF / (w->k / 16)) return QG_ERR_UNSUPPORTED;
   const size_t need = qgemm_w4a4_workspace_size(w->fmt, w->n, w->k, m);
   if (!need) {  // 1..4 rows: the GEMV's plan needs the device; none, or no plan for this shape
     DeviceInfo dev;

@@ -221,6 +221,7 @@ def test_quant_act_nvfp4_host_validation(q):
     assert call(ldx=128) == 1 and call(ldc=64) == 1 and call(lds=8) == 1 and call(lde=128) == 1
     assert call(x=0x3008) == 3 and call(ldx=260) == 3 and call(c=0x4008) == 3 and call(ldc=132) == 3
     assert call(xe=0x6008) == 3 and call(lde=260) == 3
+    assert call(m=1 << 27) == 2  # 2^31 blocks of 16: beyond the kernel's 32-bit block index
 
 
 def test_qgemm_w4a4_host_validation(q):
