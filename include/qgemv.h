@@ -214,7 +214,8 @@ qg_status qgemm(const qg_weight* w, const void* x, int64_t m_rows, int64_t ldx,
  *   scales : uint8 [m][lds], the E4M3 byte of block k/16 (lds >= k/16);
  *   xe     : bf16 [m][lde], E4M3(S) * E2M1(code) -- exact in bf16, act_scale left out --
  *            the operand a bf16 GEMM multiplies (lde >= k, a multiple of 8; 16-byte aligned).
- * Argument errors return before anything is launched. */
+ * m_rows * k/16 must stay below 2^31 (QG_ERR_UNSUPPORTED otherwise).  Argument errors
+ * return before anything is launched. */
 qg_status qg_quant_act_nvfp4(const void* x, int64_t m_rows, int64_t k, int64_t ldx, float act_scale,
                              uint8_t* codes, int64_t ldc, uint8_t* scales, int64_t lds,
                              void* xe, int64_t lde, void* stream);
