@@ -7,23 +7,24 @@
 // the scale byte, and the exact bf16 expansion E4M3(S) * E2M1(code) (two 16-byte stores)
 // that a bf16 tensor-core or CUDA-core GEMM multiplies; the activation tensor scale is
 // left for that GEMM's epilogue.  Consecutive threads take consecutive blocks of a row,
-// so every warp reads one contiguous 1 KB span.  HBM-bound: 32 bytes in and 32 + 8 + 1
-// bytes out per block.
+// so every warp reads one contiguous 1 KB span.  Memory traffic: 32 bytes in and
+// 32 + 8 + 1 bytes out per block; the arithmetic below, not HBM, sets the pace.
 //
 // Every rounding decision is one fp32 operation rounded to nearest even, in this order:
 // d6 = 6 * act_scale; r = amax / d6; S = E4M3(r) (nearest even, saturating at 448);
 // den = E4M3(S) * act_scale; q = x / den (x * 0 when den is 0); code = E2M1(q) (nearest
 // even, saturating at 6, with x's sign bit).
 //
-// The kernel is bound by instruction issue, so the sixteen divisions of a block are
+// The ALU pipe bounds the kernel, so the sixteen divisions of a block are
 // replaced by one reciprocal and sixteen products, without changing a single code:
 // q' = RN(x * RN(1/den)) lies within 2 ulps of x/den (two roundings), and every value at
 // which E2M1's nearest-even rounding changes its code -- 0.25, 0.75, 1.25, 1.75, 2.5,
 // 3.5, 5 -- has at most 3 significant bits, so the low 21 mantissa bits of each are zero.
 // Unless q' lies within 8 ulps of such a value, q' and the correctly rounded quotient
 // are on the same side of every decision point and give the same code; the few that do
-// (exact ties and their neighbours among them) are divided exactly.  When den is a power
-// of two (or 0, where q' = x * 0 as q), q' is already the correctly rounded quotient.
+// (exact ties and their neighbours among them) are divided exactly, as are an infinite or
+// NaN q' (a reciprocal that overflowed: low mantissa bits zero).  When den is a normal
+// power of two (or 0, where q' = x * 0 as q), q' is already the correctly rounded quotient.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
