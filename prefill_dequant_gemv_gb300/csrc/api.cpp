@@ -187,9 +187,9 @@ extern "C" qg_status qgemm_w4a4(const qg_weight* w, const void* x, int64_t m, in
   if (st != QG_OK) return (qg_status)st;
   if (w->fmt != QG_FMT_NVFP4 || m < 1) return QG_ERR_UNSUPPORTED;
   if (!x || !y || !workspace || !(act_scale > 0.0f) || !std::isfinite(act_scale)) return QG_ERR_INVALID_ARG;
-  qg_weight ws = *w;  // the activation tensor scale joins the weight's in the GEMM's epilogue
-  ws.tensor_scale = w->tensor_scale * act_scale;
-  if (!(ws.tensor_scale > 0.0f) || !std::isfinite(ws.tensor_scale)) return QG_ERR_INVALID_ARG;
+  qg_weight w_scaled = *w;  // the activation tensor scale joins the weight's in the GEMM's epilogue
+  w_scaled.tensor_scale = w->tensor_scale * act_scale;
+  if (!(w_scaled.tensor_scale > 0.0f) || !std::isfinite(w_scaled.tensor_scale)) return QG_ERR_INVALID_ARG;
   if (ldx < w->k || ldy < w->n || (residual && ldr < w->n)) return QG_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)) || !aligned16(workspace))
     return QG_ERR_MISALIGNED;
@@ -206,7 +206,7 @@ extern "C" qg_status qgemm_w4a4(const qg_weight* w, const void* x, int64_t m, in
   const int64_t lde = (w->k + 7) / 8 * 8;
   st = launch_quant_act_nvfp4(x, m, w->k, ldx, act_scale, nullptr, 0, nullptr, 0, xe, lde, stream);
   if (st != QG_OK) return (qg_status)st;
-  return qgemm(&ws, xe, m, lde, residual, ldr, y, ldy, workspace, off, stream);
+  return qgemm(&w_scaled, xe, m, lde, residual, ldr, y, ldy, workspace, off, stream);
 }
 
 extern "C" size_t qmoe_route_workspace_size(int64_t t, int n_experts, int topk) {
