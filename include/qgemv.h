@@ -345,13 +345,20 @@ qg_status qgemm_grouped(const qg_moe_layer* layer, int stage, const void* in, in
  * Same arguments and results as qgemv, minus the workspace.  The split-K scratch lives in
  * a fixed device array of QG_STATIC_WORKSPACE_BYTES inside the library, present on every
  * GPU that loads the library until the process exits.  The first call on a device looks
- * up that array's address (make it before any stream capture).  Every call clears the
- * array's status word and tickets; all calls share the array, so calls that overlap on
- * the GPU race -- serialise them (one stream).  Shapes needing more scratch than the
- * array holds return QG_ERR_WORKSPACE_TOO_SMALL; nothing is allocated. */
+ * up that array's address (make it before any stream capture; a failed lookup returns
+ * QG_ERR_CUDA and is tried again on the next call).  Every call clears the array's
+ * row-tile tickets; its status word is sticky, as a workspace's is, and a bounded wait
+ * that gave up (QG_ERR_TIMEOUT) is read with qgemv_static_ws_status.  All calls share the
+ * array, so calls that overlap on the GPU race -- serialise them (one stream).  Shapes
+ * needing more scratch than the array holds return QG_ERR_WORKSPACE_TOO_SMALL; nothing is
+ * allocated. */
 #define QG_STATIC_WORKSPACE_BYTES (4u << 20)
 qg_status qgemv_static_ws(const qg_weight* w, const void* x, int m_rows, int64_t ldx,
                           const void* residual, int64_t ldr, void* y, int64_t ldy, void* stream);
+/* Status word of the array qgemv_static_ws uses on the current device, as
+ * qg_workspace_status reads a workspace's: synchronises `stream`, stores the word in
+ * *status (QG_OK, or QG_ERR_TIMEOUT after a wait gave up) and clears it. */
+qg_status qgemv_static_ws_status(int* status, void* stream);
 
 /* Self-test of the shared failure path: launches one CTA whose mbarrier wait nothing will
  * complete; after the library's wait limit (2 s) the kernel records QG_ERR_TIMEOUT in the

@@ -60,16 +60,18 @@ def tolerance(w, x_bits, res_bits=None, rows=None, max_row_norm=None, ref=None) 
     Base bound (the stated contract): 2e-3 * ||x_m||_2 * max_n ||w_n||_2 on the value
     before the output's single bf16 rounding.  After that rounding the two sides may
     land on neighbouring bf16 numbers when the exact value is near a rounding boundary,
-    so one bf16 ulp of the output is added: 2**-7 * |ref| (an upper bound on the spacing
-    next to ref) when the reference outputs `ref` are given.  Without `ref`, with a
-    residual, 2**-7 * |res| stands in for it (the residual dominates the magnitude)."""
+    so one bf16 ulp of the output is added: max(2**-7 * |ref|, 2**-133) (an upper bound on
+    the spacing next to ref; below bf16's smallest normal number, 2**-126, the spacing is
+    the subnormal quantum 2**-133) when the reference outputs `ref` are given.  Without
+    `ref`, with a residual, 2**-7 * |res| stands in for it (the residual dominates the
+    magnitude)."""
     x64 = bf16_value(x_bits)
     xn = np.linalg.norm(x64, axis=1)
     wmax = float(np.max(row_norms(w))) if max_row_norm is None else float(max_row_norm)
     ncols = w.n if rows is None else len(rows)
     tol = np.repeat((2e-3 * xn * wmax)[:, None], ncols, axis=1)
     if ref is not None:
-        tol = tol + 2.0 ** -7 * np.abs(np.asarray(ref, dtype=np.float64))
+        tol = tol + np.maximum(2.0 ** -7 * np.abs(np.asarray(ref, dtype=np.float64)), 2.0 ** -133)
     elif res_bits is not None:
         r = bf16_value(res_bits) if rows is None else bf16_value(np.asarray(res_bits)[:, rows])
         tol = tol + 2.0 ** -7 * np.abs(r)

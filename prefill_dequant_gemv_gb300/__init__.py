@@ -57,6 +57,7 @@ _SIGNATURES = {
     "qg_workspace_status": (_I, [_P, ctypes.POINTER(_I), _P]),
     "qgemv": (_I, [ctypes.POINTER(qg_weight), _P, _I, _I64, _P, _I64, _P, _I64, _P, _SZ, _P]),
     "qgemv_static_ws": (_I, [ctypes.POINTER(qg_weight), _P, _I, _I64, _P, _I64, _P, _I64, _P]),
+    "qgemv_static_ws_status": (_I, [ctypes.POINTER(_I), _P]),
     "qg_gemm_workspace_size": (_SZ, [_I, _I64, _I64, _I]),
     "qgemm": (_I, [ctypes.POINTER(qg_weight), _P, _I64, _I64, _P, _I64, _P, _I64, _P, _SZ, _P]),
     "qmoe_route_workspace_size": (_SZ, [_I64, _I, _I]),
@@ -214,6 +215,14 @@ def qgemv_static_ws(w: qg_weight, x_ptr: int, m: int, ldx: int, res_ptr: Optiona
     """qgemv without a workspace argument, for callers that cannot allocate device memory
     (its scratch is a fixed array inside the library, shared by all calls)."""
     _check(lib().qgemv_static_ws(ctypes.byref(w), x_ptr, m, ldx, res_ptr, ldr, y_ptr, ldy, stream), "qgemv_static_ws")
+
+
+def qgemv_static_ws_status(stream: int = 0) -> int:
+    """Read and clear the status word of qgemv_static_ws's array on the current device
+    (synchronises `stream`): QG_OK, or QG_ERR_TIMEOUT after a bounded wait gave up."""
+    v = _I(0)
+    _check(lib().qgemv_static_ws_status(ctypes.byref(v), stream), "qgemv_static_ws_status")
+    return v.value
 
 
 def qg_selftest_wait_timeout(ws_ptr: int, ws_bytes: int, stream: int = 0):

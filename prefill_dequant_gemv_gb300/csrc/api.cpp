@@ -51,6 +51,18 @@ static int check_weight(const qg_weight* w, Geometry* g) {
   return QG_OK;
 }
 
+int check_gemv_call(const qg_weight* w, const void* x, int m, int64_t ldx, const void* residual, int64_t ldr,
+                    const void* y, int64_t ldy, Geometry* g) {
+  int st = check_weight(w, g);
+  if (st != QG_OK) return st;
+  if (m < 1 || m > 4) return QG_ERR_UNSUPPORTED;
+  if (!x || !y) return QG_ERR_INVALID_ARG;
+  if (ldx < w->k || ldy < w->n || (residual && ldr < w->n)) return QG_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || (residual && !aligned16(residual))) return QG_ERR_MISALIGNED;
+  if (ldx % 8 || ldy % 8 || (residual && ldr % 8)) return QG_ERR_MISALIGNED;
+  return QG_OK;
+}
+
 }  // namespace qg
 
 using namespace qg;
@@ -97,14 +109,10 @@ extern "C" qg_status qg_workspace_init(void* workspace, size_t bytes, void* stre
 extern "C" qg_status qgemv(const qg_weight* w, const void* x, int m, int64_t ldx, const void* residual, int64_t ldr,
                            void* y, int64_t ldy, void* workspace, size_t workspace_bytes, void* stream) {
   Geometry g;
-  int st = check_weight(w, &g);
+  int st = check_gemv_call(w, x, m, ldx, residual, ldr, y, ldy, &g);
   if (st != QG_OK) return (qg_status)st;
-  if (m < 1 || m > 4) return QG_ERR_UNSUPPORTED;
-  if (!x || !y || !workspace) return QG_ERR_INVALID_ARG;
-  if (ldx < w->k || ldy < w->n || (residual && ldr < w->n)) return QG_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(y) || (residual && !aligned16(residual)) || !aligned16(workspace))
-    return QG_ERR_MISALIGNED;
-  if (ldx % 8 || ldy % 8 || (residual && ldr % 8)) return QG_ERR_MISALIGNED;
+  if (!workspace) return QG_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return QG_ERR_MISALIGNED;
   DeviceInfo dev;
   if (!current_device_info(&dev)) return QG_ERR_CUDA;
   GemvPlan p;

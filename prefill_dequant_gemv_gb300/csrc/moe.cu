@@ -411,10 +411,12 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
     const int i = sg - sg0, buf = i & 1;
     if (i >= 2 && ok && !mbar_wait_bounded(&rempty[buf], (uint32_t)((i >> 1) - 1) & 1u, a.status)) ok = false;
     float* rb = red + ((size_t)buf * kGCW + warp) * kGMaxRows * 128;
+    if (ok) {  // after a timed-out wait the reducer may still read this buffer: leave it
 #pragma unroll
-    for (int rt = 0; rt < 4; ++rt)
+      for (int rt = 0; rt < 4; ++rt)
 #pragma unroll
-      for (int m = 0; m < kGMaxRows; ++m) rb[m * 128 + rt * 32 + lane] = acc[rt][m];
+        for (int m = 0; m < kGMaxRows; ++m) rb[m * 128 + rt * 32 + lane] = acc[rt][m];
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&rfull[buf]);
   }

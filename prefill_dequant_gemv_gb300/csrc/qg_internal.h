@@ -43,6 +43,10 @@ struct GemvPlan {
   int csplit;        // > 1: each row tile split across a cluster of csplit CTAs
 };
 bool plan_gemv(const Geometry& g, int m, const DeviceInfo& dev, GemvPlan* p);
+// Host-side checks of a GEMV call's weight, rows, activations, residual and output (every
+// rule of qgemv but the workspace's); fills g.  Returns a qg_status.
+int check_gemv_call(const qg_weight* w, const void* x, int m, int64_t ldx, const void* residual, int64_t ldr,
+                    const void* y, int64_t ldy, Geometry* g);
 
 // Launchers (return a qg_status).
 int launch_gemv(const Geometry& g, const qg_weight* w, const void* x, int m, int64_t ldx,

@@ -414,24 +414,85 @@ def check_operand_bf16(o, fmt, seed=31):
 
 
 def check_tolerance_output_ulp(o, seed=37):
-    """The output term of the tolerance, 2**-7 |ref|, is at least the gap between ref and
-    either bf16 neighbour (so two sides rounding one exact value to neighbouring bf16
-    numbers stay inside it), and is a strict bound: a flip of two ulps is outside it."""
+    """The output term of the tolerance, max(2**-7 |ref|, 2**-133), is at least the gap
+    between ref and either bf16 neighbour (so two sides rounding one exact value to
+    neighbouring bf16 numbers stay inside it) -- for normal outputs and for bf16's
+    subnormals, whose spacing is 2**-133 -- and is a strict bound: a flip of two ulps is
+    outside it."""
     rng = np.random.default_rng(seed)
-    v = o.round_to_bf16(rng.standard_normal(2000) * 10.0 ** rng.integers(-3, 4, 2000))
+    v = o.round_to_bf16(np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-3, 4, 2000),
+                                        rng.standard_normal(500) * 2.0 ** -128,  # subnormal bf16
+                                        rng.standard_normal(100) * 2.0 ** -125]))
     v = v[v != 0]
     bits = o.bf16_bits_of(v).astype(np.int32)
     up = o.bf16_value((bits + 1).astype(np.uint16))    # next bf16 away from zero (sign-magnitude)
     down = o.bf16_value((bits - 1).astype(np.uint16))  # next bf16 toward zero
+    gap = np.maximum(2.0 ** -7 * np.abs(v), 2.0 ** -133)
     assert np.all(np.abs(up) > np.abs(v)) and np.all(np.abs(down) < np.abs(v))
-    assert np.all(np.abs(up - v) <= 2.0 ** -7 * np.abs(v))
-    assert np.all(np.abs(v - down) <= 2.0 ** -7 * np.abs(v))
+    assert np.all(np.abs(up - v) <= gap)
+    assert np.all(np.abs(v - down) <= gap)
+    assert np.all(np.abs(up - down) > gap)  # two ulps apart: outside the term
+    sub = np.abs(v) < 2.0 ** -126
+    assert sub.sum() > 100 and np.all(np.abs(up - v)[sub] == 2.0 ** -133)
     w = wl.weight(wl.NVFP4, 4, 64, seed)
     x = wl.activations(2, 64, seed)
     ref, _ = o.gemv(w, x)
     tol = o.tolerance(w, x, ref=ref)
     base = o.tolerance(w, x)
-    assert np.allclose(tol - base, 2.0 ** -7 * np.abs(ref), rtol=1e-12, atol=0)
+    assert np.allclose(tol - base, np.maximum(2.0 ** -7 * np.abs(ref), 2.0 ** -133), rtol=1e-12, atol=0)
+
+
+def _exact_norm(values) -> float:
+    """sqrt of an exact rational sum of squares, correctly rounded to fp64 (the integer
+    square root of the scaled sum fixes 60 bits before the one rounding)."""
+    s = sum((Fraction(v) * Fraction(v) for v in values), Fraction(0))
+    if s == 0:
+        return 0.0
+    e = (s.numerator.bit_length() - s.denominator.bit_length()) // 2 - 62
+    scaled = s / (Fraction(4) ** e)  # s = scaled * 2^(2e), scaled ~ 2^124
+    r = math.isqrt(scaled.numerator // scaled.denominator)
+    return math.ldexp(float(r), e)
+
+
+def check_tolerance_base(o, seed=67):
+    """The stated bound 2e-3 * ||x_m||_2 * max_n ||w_n||_2, pinned with norms taken here in
+    exact rational arithmetic from the format definitions (``exact_weight``) and the bf16
+    activation values:
+      - ``row_norms`` returns one norm per output row n of the N x K weight, in row order;
+      - the base term (no residual, no ``ref``) is that product for every output of row m;
+      - with ``rows=`` the max still runs over every row of w (the bound is the weight's,
+        not the sample's), and the residual term 2**-7 |res| follows the selected columns.
+    A norm over the wrong axis, a mean for the max, a sample-only max or a dropped residual
+    term each fail one of these."""
+    for fmt in (wl.NVFP4, wl.Q6K, wl.MLX_AFFINE4_G64):
+        n, k = shape_for(fmt, 12, 64)
+        m = 3
+        w, x, res = wl.gemv_case(fmt, n, k, m, seed=seed, residual=True)
+        # row 5 made clearly the largest (its scales raised), so a max over a sample that
+        # skips it differs from the max over the weight
+        if fmt == wl.NVFP4:  # every block of row 5 at twice the largest scale (E4M3 byte + 8)
+            w.scales[5] = int(w.scales.max()) + 8
+        elif fmt == wl.Q6K:
+            w.aux[5] = (2.0 * w.aux.astype(np.float32).max()).astype(w.aux.dtype)
+        else:
+            w.scales[5] = (w.scales[5].astype(np.float32) * 4).astype(w.scales.dtype)
+            w.aux[5] = (w.aux[5].astype(np.float32) * 4).astype(w.aux.dtype)
+        wn = np.array([_exact_norm(exact_weight(w, i, j) for j in range(k)) for i in range(n)])
+        xn = np.array([_exact_norm(bf16_frac(x[mi, j]) for j in range(k)) for mi in range(m)])
+        assert int(np.argmax(wn)) == 5, wn
+        got = np.asarray(o.row_norms(w), dtype=np.float64)
+        assert got.shape == (n,), got.shape
+        assert np.allclose(got, wn, rtol=1e-6, atol=0), (fmt, got, wn)
+        sub = np.array([0, 2, 9])  # excludes the largest row
+        assert np.allclose(np.asarray(o.row_norms(w, sub)), wn[sub], rtol=1e-6, atol=0)
+        want = 2e-3 * xn[:, None] * wn.max()
+        base = np.asarray(o.tolerance(w, x), dtype=np.float64)
+        assert base.shape == (m, n), base.shape
+        assert np.allclose(base, np.repeat(want, n, axis=1), rtol=1e-6, atol=0), fmt
+        tr = np.asarray(o.tolerance(w, x, res_bits=res, rows=sub), dtype=np.float64)
+        rv = np.array([[float(bf16_frac(res[mi, c])) for c in sub] for mi in range(m)])
+        assert tr.shape == (m, sub.size), tr.shape
+        assert np.allclose(tr, want + 2.0 ** -7 * np.abs(rv), rtol=1e-6, atol=0), fmt
 
 
 # ----------------------------------------------------------------- W4A4 (activations to NVFP4)

@@ -287,3 +287,62 @@ def test_w4a4_skips_activation_quantisation(monkeypatch):
         return y, v, None
     _both(monkeypatch, "gemm_w4a4", bad)
     assert _fails(pins.check_w4a4_brute_force, oracle)
+
+
+# ----------------------------------------------------------------- the parity bound itself
+def _bad_tolerance(xnorm_axis=1, reduce=np.max, sample_max=False, keep_res=True):
+    """A copy of the oracle's tolerance with one planted change (the same steps otherwise)."""
+    def tol(w, x_bits, res_bits=None, rows=None, max_row_norm=None, ref=None):
+        x64 = oracle.bf16_value(x_bits)
+        xn = np.linalg.norm(x64, axis=xnorm_axis)
+        norms = G.row_norms(w, rows if sample_max else None)
+        wmax = float(reduce(norms)) if max_row_norm is None else float(max_row_norm)
+        ncols = w.n if rows is None else len(rows)
+        t = np.repeat((2e-3 * xn * wmax)[:, None], ncols, axis=1) if xn.shape[0] == x64.shape[0] \
+            else np.repeat((2e-3 * xn[: x64.shape[0]] * wmax)[:, None], ncols, axis=1)
+        if ref is not None:
+            t = t + 2.0 ** -7 * np.abs(np.asarray(ref, dtype=np.float64))
+        elif res_bits is not None and keep_res:
+            r = oracle.bf16_value(res_bits) if rows is None else oracle.bf16_value(np.asarray(res_bits)[:, rows])
+            t = t + 2.0 ** -7 * np.abs(r)
+        return t
+    return tol
+
+
+def test_row_norms_over_columns(monkeypatch):
+    def cols(w, rows=None):
+        return np.linalg.norm(oracle.dequant(w).astype(np.float64), axis=0)
+    monkeypatch.setattr(G, "row_norms", cols)
+    monkeypatch.setattr(oracle, "row_norms", cols)
+    assert _fails(pins.check_tolerance_base, oracle)
+
+
+def test_tolerance_mean_row_norm(monkeypatch):
+    monkeypatch.setattr(oracle, "tolerance", _bad_tolerance(reduce=np.mean))
+    assert _fails(pins.check_tolerance_base, oracle)
+
+
+def test_tolerance_activation_norm_over_inputs(monkeypatch):
+    monkeypatch.setattr(oracle, "tolerance", _bad_tolerance(xnorm_axis=0))
+    assert _fails(pins.check_tolerance_base, oracle)
+
+
+def test_tolerance_max_over_sampled_rows_only(monkeypatch):
+    monkeypatch.setattr(oracle, "tolerance", _bad_tolerance(sample_max=True))
+    assert _fails(pins.check_tolerance_base, oracle)
+
+
+def test_tolerance_residual_term_dropped(monkeypatch):
+    monkeypatch.setattr(oracle, "tolerance", _bad_tolerance(keep_res=False))
+    assert _fails(pins.check_tolerance_base, oracle)
+
+
+def test_tolerance_copy_is_faithful():
+    """The unmutated copy above passes the pin, so each mutation's failure is its own."""
+    import pytest
+    mp = pytest.MonkeyPatch()
+    try:
+        mp.setattr(oracle, "tolerance", _bad_tolerance())
+        pins.check_tolerance_base(oracle)
+    finally:
+        mp.undo()

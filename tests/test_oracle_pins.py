@@ -111,3 +111,7 @@ def test_w4a4_reduces_to_w4a16():
 
 def test_w4a4_brute_force_exact_rational():
     pins.check_w4a4_brute_force(oracle)
+
+
+def test_tolerance_base_term_and_row_norms():
+    pins.check_tolerance_base(oracle)

@@ -143,6 +143,52 @@ def activations(m: int, k: int, seed: int = 0, stream: str = "x") -> np.ndarray:
     return bf16_bits_from_f32(rs.standard_normal(size=(m, k), dtype=np.float32))
 
 
+EDGE_KINDS = ("spread", "zero_next_to_huge", "subnormal", "near_max", "nonfinite")
+
+
+def activations_edge(m: int, k: int, kind: str, seed: int = 0) -> np.ndarray:
+    """bf16 bit patterns [m, k] of activations with the magnitude structure ``kind``, drawn
+    as fp32 N(0,1) values times powers of two (exact in fp32), rounded to bf16 once:
+
+    * "spread": inside every 16-input quarter the values take magnitudes 2^0, 2^-20, 2^-27
+      and 2^-30 (a quarter's largest and smallest value are up to 2^30 apart); every fourth
+      quarter also holds one value 2^20 times larger.
+    * "zero_next_to_huge": quarters cycle through all zero, values near 2^100, and N(0,1).
+    * "subnormal": row 0 only bf16 subnormals (|x| < 2^-126); the other rows subnormal
+      quarters next to N(0,1) ones.
+    * "near_max": N(0,1) values plus, per row, one value of magnitude 1.5 * 2^127 (bf16's
+      largest finite numbers are just below 2^128).
+    * "nonfinite": N(0,1) rows; row 1 (when present) holds one +inf, row 2 one NaN and row 3
+      one -inf.
+    """
+    rs = streams(seed)["x"]
+    v = rs.standard_normal(size=(m, k), dtype=np.float32)
+    q = np.arange(k) // 16  # quarter index of each input
+    if kind == "spread":
+        e = rs.choice(np.array([0, -20, -27, -30]), size=(m, k))
+        e[:, ::16] = 0  # every quarter keeps values at full magnitude
+        v = v * np.exp2(e).astype(np.float32)
+        big = (q % 4 == 1) & (np.arange(k) % 16 == 5)
+        v[:, big] = v[:, big] * np.float32(2.0 ** 20)
+    elif kind == "zero_next_to_huge":
+        v[:, q % 3 == 0] = 0.0
+        v[:, q % 3 == 1] *= np.float32(2.0 ** 100)
+    elif kind == "subnormal":
+        sub = np.full((m, k), True) if m == 1 else np.broadcast_to(q % 2 == 0, (m, k)).copy()
+        sub[0] = True
+        v = np.where(sub, v * np.float32(2.0 ** -130), v).astype(np.float32)
+    elif kind == "near_max":
+        j = rs.integers(0, k, size=m)
+        v[np.arange(m), j] = np.sign(v[np.arange(m), j]) * np.float32(1.5 * 2.0 ** 127)
+    elif kind == "nonfinite":
+        for row, val in ((1, np.inf), (2, np.nan), (3, -np.inf)):
+            if row < m:
+                v[row, rs.integers(0, k)] = val
+    else:
+        raise ValueError(kind)
+    return bf16_bits_from_f32(v)
+
+
 def gemv_case(fmt: int, n: int, k: int, m: int, seed: int = 0, residual: bool = False):
     """(weight, x bits [m,k], residual bits [m,n] or None) for one GEMV workload."""
     rs = streams(seed)
