@@ -62,9 +62,9 @@ struct SmemLayout {
   size_t bars, stages, xs, sums, red, cbuf, lut, misc, total;
 };
 
-__host__ __device__ inline SmemLayout gemv_smem_layout(int stage_bytes, int S, int M, int nslots, int csplit) {
-  // stage_bytes: bytes of one chunk stage
-  const int kCW = consumer_warps(M);
+__host__ __device__ inline SmemLayout gemv_smem_layout(int stage_bytes, int S, int M, int nslots, int csplit,
+                                                       int kCW) {
+  // stage_bytes: bytes of one chunk stage; kCW: consumer warps
   SmemLayout L;
   size_t o = 0;
   L.bars = o;
@@ -112,25 +112,132 @@ __device__ void stage_x(const GemvArgs& a, uint32_t* xs, float* sums, int sbase,
   }
 }
 
+// Stage the activation rows for the tensor-core consumer: f16 with ONE power-of-two scale
+// per token over this CTA's input groups, 2^p with p = tok_exp(the token's largest |x|),
+// so B of every MMA shares it and the partial sums need no per-quarter rescaling.  The
+// largest value lands in [2^14, 2^15); bf16 values more than 2^32 below it round onto f16's
+// subnormal grid (absolute error under 2^-40 of the token's max: far inside the stated
+// bound).  Two passes: the token maxima (each thread keeps its first R items in
+// registers), a block-wide max in pmax[m] (zeroed before the kernel's first barrier), then
+// the conversion.  Row m, slot s, quarter kq -> 8 staging words, natural pair order.
 template <int M>
-__device__ __forceinline__ void finish_out(const GemvArgs& a, uint32_t q, int e, float v) {
+__device__ __forceinline__ void load_quarter(const GemvArgs& a, int it, int sbase, int nslots, uint32_t (&u)[8]) {
+  const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
+  const int64_t k0 = (int64_t)((sbase + s) % a.KG) * 64 + kq * 16;
+  if (k0 < a.k) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + m * a.ldx + k0);
+    const uint4 r0 = src[0], r1 = src[1];
+    u[0] = r0.x; u[1] = r0.y; u[2] = r0.z; u[3] = r0.w;
+    u[4] = r1.x; u[5] = r1.y; u[6] = r1.z; u[7] = r1.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u[i] = 0;
+  }
+}
+
+// Largest bf16 magnitude bits of a quarter, folded into the token's running maximum.
+template <int M>
+__device__ __forceinline__ void fold_max(const uint32_t (&u)[8], int m, uint32_t (&mx)[M]) {
+  uint32_t mb = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mb = max(mb, max(u[i] & 0x7FFFu, (u[i] >> 16) & 0x7FFFu));
+#pragma unroll
+  for (int mm = 0; mm < M; ++mm)
+    if (mm == m) mx[mm] = max(mx[mm], mb);
+}
+
+template <int M>
+__device__ __forceinline__ void store_quarter_tok(uint32_t* xs, int it, int nslots, const int (&p)[M],
+                                                  const uint32_t (&u)[8]) {
+  const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
+  int pm = 0;
+#pragma unroll
+  for (int mm = 0; mm < M; ++mm)
+    if (mm == m) pm = p[mm];
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float lo, hi;
+    bf16x2_to_f32(u[i], lo, hi);
+    __half2 h = __floats2half2_rn(mul_pow2(lo, pm), mul_pow2(hi, pm));
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)(m * nslots + s) * 32 + kq * 8);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// Stage the activation rows for the tensor-core consumer: f16 with ONE power-of-two scale
+// per token over this CTA's input groups, 2^p with p = tok_exp(the token's largest |x|),
+// so B of every MMA shares it and the partial sums need no per-quarter rescaling.  The
+// largest value lands in [2^14, 2^15); bf16 values more than 2^32 below it round onto f16's
+// subnormal grid (absolute error under 2^-40 of the token's max: far inside the stated
+// bound).  Two passes: the token maxima (each thread keeps its first R items in
+// registers), a block-wide max in pmax[m] (zeroed before the kernel's first barrier), then
+// the conversion.  Row m, slot s, quarter kq -> 8 staging words, natural pair order.
+template <int M, int kCT>
+__device__ void stage_x_tok(const GemvArgs& a, uint32_t* xs, uint32_t* pmax, int sbase, int nslots, int tid) {
+  constexpr int R = 4;
+  const int items = M * nslots * 4;
+  uint32_t mx[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) mx[m] = 0;
+  uint32_t held[R][8];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int it = tid + r * kCT;
+    if (it < items) {
+      load_quarter<M>(a, it, sbase, nslots, held[r]);
+      fold_max<M>(held[r], (it >> 2) / nslots, mx);
+    }
+  }
+  for (int it = tid + R * kCT; it < items; it += kCT) {
+    uint32_t u[8];
+    load_quarter<M>(a, it, sbase, nslots, u);
+    fold_max<M>(u, (it >> 2) / nslots, mx);
+  }
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const uint32_t v = __reduce_max_sync(0xFFFFFFFFu, mx[m]);
+    if ((tid & 31) == 0 && v) atomicMax(&pmax[m], v);
+  }
+  named_sync(1, kCT);
+  int p[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) p[m] = tok_exp(pmax[m]);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int it = tid + r * kCT;
+    if (it < items) store_quarter_tok<M>(xs, it, nslots, p, held[r]);
+  }
+  for (int it = tid + R * kCT; it < items; it += kCT) {
+    uint32_t u[8];
+    load_quarter<M>(a, it, sbase, nslots, u);
+    store_quarter_tok<M>(xs, it, nslots, p, u);
+  }
+}
+
+// Output e = m * 128 + row of row tile q: ts * v (+ residual), rounded to bf16 once.
+template <int M>
+__device__ __forceinline__ void finish_out(const GemvArgs& a, uint32_t q, int e, float v, float ts) {
   const int m = e / 128, row = e % 128;
   const int64_t n = (int64_t)q * 128 + row;
   if (n >= a.n) return;
-  float r = a.ts * v;
+  float r = ts * v;
   if (a.res) r += __bfloat162float(a.res[m * a.ldr + n]);
   a.y[m * a.ldy + n] = __float2bfloat16_rn(r);
 }
 
 template <int FMT, int M>
-__global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(const GemvArgs a) {
-  constexpr int kCW = consumer_warps(M);  // consumer warps
+__global__ void __launch_bounds__(gemv_warps(FMT, M) * 32 + 32, 1) gemv_kernel(const GemvArgs a) {
+  constexpr bool kMma = gemv_mma(FMT, M);  // tensor-core consumer (E2M1 formats)
+  constexpr int kCW = gemv_warps(FMT, M);  // consumer warps
   constexpr int kCT = kCW * 32;           // consumer threads (one producer warp follows)
   constexpr int kGroups = kCW / 4;        // unit groups (4 warps: one per 16-input quarter)
   extern __shared__ __align__(128) uint8_t smem[];
   using SG = Stage<FMT>;
   const int S = a.stages, nslots = a.nslots;
-  const SmemLayout L = gemv_smem_layout(Stage<FMT>::bytes(consumer_warps(M) / 4), S, M, nslots, a.csplit);
+  const SmemLayout L = gemv_smem_layout(Stage<FMT>::bytes(kCW / 4), S, M, nslots, a.csplit, kCW);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + S;
   uint8_t* stages = smem + L.stages;
@@ -161,6 +268,8 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
   }
   if (M > 1 && tid == 0) mbar_init(xready, 1);
   if (tid < S + (M > 1 ? 1 : 0)) fence_mbar_init();
+  uint32_t* pmax = reinterpret_cast<uint32_t*>(sums);  // tensor-core staging: token maxima
+  if (kMma && tid < M) pmax[tid] = 0;
   __syncthreads();
   // The next kernel may start streaming its weights while this one runs; it reads
   // activations and the workspace only after this grid has completed (pdl_wait).
@@ -209,13 +318,18 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
     return;
   }
 
-  if (FMT == FMT_NVFP4 && tid < 128) {  // E4M3 -> fp32 table (exact), two entries per thread
+  // E4M3 -> fp32 table, two entries per thread: the block scale times the tensor scale
+  // (one rounding), so that no partial sum carries the factor 1 / ts.
+  if (FMT == FMT_NVFP4 && tid < 128) {
     const float2 v = e4m3x2_f32<0>((uint32_t)(2 * tid) | ((uint32_t)(2 * tid + 1) << 8));
-    lut[2 * tid] = v.x;
-    lut[2 * tid + 1] = v.y;
+    lut[2 * tid] = v.x * a.ts;
+    lut[2 * tid + 1] = v.y * a.ts;
   }
   pdl_wait();  // activations, residual and workspace may come from the preceding kernel
-  stage_x<FMT, M, kCT>(a, xs, sums, sbase, nslots, tid);
+  if constexpr (kMma)
+    stage_x_tok<M, kCT>(a, xs, pmax, sbase, nslots, tid);
+  else
+    stage_x<FMT, M, kCT>(a, xs, sums, sbase, nslots, tid);
   named_sync(1, kCT);
   if (M > 1 && tid == 0) mbar_arrive(xready);
 
@@ -234,6 +348,7 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
   const uint32_t crank = clustered ? cluster_rank() : 0;
   uint32_t part_q0 = 0, part_q1 = 0;  // row tiles this CTA holds only part of
   int nparts = 0;
+  const float ts_out = FMT == FMT_NVFP4 ? 1.0f : a.ts;  // the E4M3 table carries ts
   while (u < uu1) {
     const uint32_t q = u / (uint32_t)KG;
     const uint32_t seg_end = min(uu1, (q + 1) * (uint32_t)KG);
@@ -242,6 +357,11 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
     for (int rt = 0; rt < 4; ++rt)
 #pragma unroll
       for (int m = 0; m < M; ++m) acc[rt][m] = 0.0f;
+    float acc2[2][4];  // tensor-core consumer (consume_mma)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc2[j][i] = 0.0f;
     for (; ok && uu0 + i < seg_end; i += C) {
       if (!mbar_wait_bounded(&full[s], ph, a.status)) {
         ok = false;
@@ -249,15 +369,21 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
       }
       const uint8_t* st = stages + (size_t)s * SB;
       const uint32_t uu = uu0 + i;
-      const uint8_t* aux = st + C * (SG::CODE + SG::SCALE) + ((uu >> 2) - ((uu - ug) >> 2)) * SG::AUX;
-      const uint32_t* xr[M];
-      const float* zr[M];
+      if constexpr (kMma) {
+        consume_mma<FMT, M>(st + ug * SG::CODE, st + C * SG::CODE + ug * SG::SCALE,
+                            reinterpret_cast<const uint8_t*>(xs) + (size_t)slot * 128, (uint32_t)nslots * 128, lut,
+                            kq, lane, acc2);
+      } else {
+        const uint8_t* aux = st + C * (SG::CODE + SG::SCALE) + ((uu >> 2) - ((uu - ug) >> 2)) * SG::AUX;
+        const uint32_t* xr[M];
+        const float* zr[M];
 #pragma unroll
-      for (int m = 0; m < M; ++m) {
-        xr[m] = reinterpret_cast<const uint32_t*>(xq_base + (size_t)slot * 128) + (size_t)m * nslots * 32;
-        zr[m] = sq_base + (size_t)slot * 16 + (size_t)m * nslots * 16;
+        for (int m = 0; m < M; ++m) {
+          xr[m] = reinterpret_cast<const uint32_t*>(xq_base + (size_t)slot * 128) + (size_t)m * nslots * 32;
+          zr[m] = sq_base + (size_t)slot * 16 + (size_t)m * nslots * 16;
+        }
+        consume<FMT, M>(st + ug * SG::CODE, st + C * SG::CODE + ug * SG::SCALE, aux, xr, zr, lut, kq, lane, acc);
       }
-      consume<FMT, M>(st + ug * SG::CODE, st + C * SG::CODE + ug * SG::SCALE, aux, xr, zr, lut, kq, lane, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       if (++s == S) {
@@ -267,20 +393,41 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
       slot += C;
       while (slot >= KG) slot -= KG;
     }
+    // Partials in shared memory: per warp (CUDA-core consumer) or per unit group (tensor-core
+    // consumer: the four warps of a group own disjoint rows), summed below in fixed order.
+    if constexpr (kMma) {
+      const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int rt = 0; rt < 4; ++rt)
+      for (int j = 0; j < 2; ++j)
 #pragma unroll
-      for (int m = 0; m < M; ++m) red[(warp * M + m) * 128 + rt * 32 + lane] = acc[rt][m];
+        for (int i = 0; i < 4; ++i) acc2[j][i] += __shfl_xor_sync(0xFFFFFFFFu, acc2[j][i], 2);  // parities
+      if (t < 2) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int m = 2 * t + (i & 1), row = 32 * kq + 16 * j + g + 8 * (i >> 1);
+            if (m < M) red[(ug * M + m) * 128 + row] = acc2[j][i];
+          }
+      }
+    } else {
+#pragma unroll
+      for (int rt = 0; rt < 4; ++rt)
+#pragma unroll
+        for (int m = 0; m < M; ++m) red[(warp * M + m) * 128 + rt * 32 + lane] = acc[rt][m];
+    }
     named_sync(1, kCT);
 
     const bool whole = (u == q * (uint32_t)KG) && (seg_end == (q + 1) * (uint32_t)KG);
     const int slot_ws = (u == uu0) ? 0 : 1;
+    constexpr int kParts = kMma ? kGroups : kCW;
     for (int e = tid; e < M * 128; e += kCT) {
       float v = 0.0f;
 #pragma unroll 4
-      for (int w2 = 0; w2 < kCW; ++w2) v += red[w2 * M * 128 + e];
+      for (int w2 = 0; w2 < kParts; ++w2) v += red[w2 * M * 128 + e];
+      if (kMma) v = mul_pow2(v, -tok_exp(pmax[e / 128]));  // back from the token's staging scale
       if (whole)
-        finish_out<M>(a, q, e, v);
+        finish_out<M>(a, q, e, v, ts_out);
       else if (clustered)  // into rank 0's buffer, slot = this CTA's rank
         st_cluster_f32(cluster_map(cbuf + (size_t)crank * M * 128 + e, 0), v);
       else
@@ -338,7 +485,7 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
           v += v3;
         }
         for (; c < nc; ++c) v += __ldcg(part + (size_t)(2 * c) * M * 128 + e);
-        finish_out<M>(a, q, e, v);
+        finish_out<M>(a, q, e, v, ts_out);
       }
       if (tid == 0) a.ws_cnt[q] = 0;
     }
@@ -352,7 +499,7 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
       for (int e = tid; e < M * 128; e += kCT) {
         float v = cbuf[e];
         for (int r = 1; r < a.csplit; ++r) v += cbuf[(size_t)r * M * 128 + e];
-        finish_out<M>(a, q, e, v);
+        finish_out<M>(a, q, e, v, ts_out);
       }
     }
   }
@@ -360,7 +507,7 @@ __global__ void __launch_bounds__(consumer_warps(M) * 32 + 32, 1) gemv_kernel(co
 
 // ---------------------------------------------------------------- host side
 static int stage_bytes_of(int fmt, int m) {
-  const int C = consumer_warps(m) / 4;
+  const int C = gemv_warps(fmt, m) / 4;
   switch (fmt) {
     case FMT_MLX: return Stage<FMT_MLX>::bytes(C);
     case FMT_MXFP4: return Stage<FMT_MXFP4>::bytes(C);
@@ -374,7 +521,8 @@ static int stage_bytes_of(int fmt, int m) {
 
 bool plan_gemv(const Geometry& g, int m, const DeviceInfo& dev, GemvPlan* p) {
   const int sbytes = stage_bytes_of(g.fmt, m);
-  const int C = consumer_warps(m) / 4;
+  const int kcw = gemv_warps(g.fmt, m);
+  const int C = kcw / 4;
   const int64_t U = g.nt * g.kg;
   if (U >= (int64_t(1) << 31)) return false;
   const size_t budget = (size_t)dev.max_smem_optin;
@@ -393,16 +541,16 @@ bool plan_gemv(const Geometry& g, int m, const DeviceInfo& dev, GemvPlan* p) {
   for (;;) {
     const int64_t len = (U + G - 1) / G;
     const int nslots = (int)std::min<int64_t>(len, g.kg);
-    const SmemLayout L0 = gemv_smem_layout(sbytes, 2, m, nslots, csplit);
+    const SmemLayout L0 = gemv_smem_layout(sbytes, 2, m, nslots, csplit, kcw);
     if (L0.total <= budget || G >= U) {
       if (L0.total > budget) return false;
       int S = (int)std::min<int64_t>((len + C - 1) / C, (int64_t)kMaxStages);
       S = std::max(S, 2);
-      while (S > 2 && gemv_smem_layout(sbytes, S, m, nslots, csplit).total > budget) --S;
+      while (S > 2 && gemv_smem_layout(sbytes, S, m, nslots, csplit, kcw).total > budget) --S;
       p->grid = (int)G;
       p->nslots = nslots;
       p->stages = S;
-      p->smem = gemv_smem_layout(sbytes, S, m, nslots, csplit).total;
+      p->smem = gemv_smem_layout(sbytes, S, m, nslots, csplit, kcw).total;
       p->csplit = csplit;
       p->units = U;
       p->off_cnt = kWsHeader;
@@ -432,7 +580,7 @@ static int launch_t(const GemvArgs& a, const GemvPlan& p, cudaStream_t s) {
   // stream finishes (the kernel waits for it before reading anything that kernel writes).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.grid);
-  cfg.blockDim = dim3((unsigned)(consumer_warps(M) * 32 + 32));
+  cfg.blockDim = dim3((unsigned)(gemv_warps(FMT, M) * 32 + 32));
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];

@@ -105,12 +105,26 @@ __device__ __forceinline__ float hfma_hi(uint32_t a, uint32_t b, float c) {
   return d;
 }
 
-// Two E2M1 codes (byte b of wd) -> f16x2 (low nibble in the low half); exact.
+// Two E2M1 codes (byte b of wd) -> f16x2 (low nibble in the low half); exact.  The word is
+// split into its four bytes with one vector move, which the conversion reads in place
+// (measured on this GPU: 85 against 57 weights per clock per SM for shifting each byte
+// down to bit 0 first, the same results bit for bit).
 template <int b>
 __device__ __forceinline__ uint32_t e2m1x2_h2(uint32_t wd) {
+  static_assert(b >= 0 && b < 4, "byte index");
   uint32_t h2;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(h2) : "r"(wd >> (8 * b)));
+  if (b == 0)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b0;\n\t}"
+        : "=r"(h2) : "r"(wd));
+  else if (b == 1)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b1;\n\t}"
+        : "=r"(h2) : "r"(wd));
+  else if (b == 2)
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b2;\n\t}"
+        : "=r"(h2) : "r"(wd));
+  else
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b3;\n\t}"
+        : "=r"(h2) : "r"(wd));
   return h2;
 }
 

@@ -15,6 +15,13 @@ namespace qg {
 // accumulators and activations need the 128 registers a 13-warp CTA allows (warps are
 // allocated in groups of four).
 __host__ __device__ constexpr int consumer_warps(int m) { return m >= 4 ? 12 : 16; }
+// The dense GEMV multiplies the E2M1 formats on the tensor cores (consume_mma) from
+// kMmaMinRows activation rows on; its few accumulators leave room for 16 consumer warps.
+constexpr int kMmaMinRows = 2;
+__host__ __device__ constexpr bool gemv_mma(int fmt, int m) {
+  return (fmt == FMT_NVFP4 || fmt == FMT_MXFP4) && m >= kMmaMinRows;
+}
+__host__ __device__ constexpr int gemv_warps(int fmt, int m) { return gemv_mma(fmt, m) ? 16 : consumer_warps(m); }
 constexpr int kMaxStages = 48;
 
 // One pipeline stage holds a chunk of C consecutive units (tile index = unit index,
@@ -43,8 +50,12 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t v, float& lo, float& hi) 
 // (8 significant bits) lands inside f16's range; a value more than 2^27 below the
 // quarter's maximum would round, far below the stated tolerance.  Writes the two 16-byte
 // staging words to `dst` and returns the quarter's record {2^-p (E2M1) or 64 * 2^-p
-// (integer formats), Z, X, 0}; Z and X, in unscaled units, remove the integer operands'
-// constant and the Q6_K zero point in the fold.
+// (integer formats), Z, X, 0}: Z, in scaled units, is the integer operands' constant part
+// (for Q6_K also half the quarter's scaled sum, the zero point 32 / 64), so the fold
+// subtracts it before anything leaves the scaled range; X is the quarter's sum in
+// unscaled units (the affine formats' bias term).  Every product the fold forms is then
+// within fp32's range whenever the true partial sum is, even for activations near bf16's
+// largest values.
 // Layout per 8 inputs (one code word): four f16x2 words in the order the decoder
 // produces operand pairs -- E2M1: (x0,x1) (x2,x3) (x4,x5) (x6,x7); integer formats:
 // (16x0,16x4) (x1,x5) (16x2,16x6) (x3,x7).
@@ -86,11 +97,11 @@ __device__ __forceinline__ float4 stage_quarter(const uint32_t (&u)[8], uint32_t
     for (int i = 0; i < 12; ++i) x4 += q[i];
 #pragma unroll
     for (int i = 12; i < 16; ++i) x16 += q[i];
-    const float xsum = (x4 + x16) * inv;              // X, unscaled
-    const float xop = fmaf(4.0f, x4, 16.0f * x16) * inv;  // the operands' constant part, unscaled
+    const float xs = x4 + x16;                         // the quarter's scaled sum
+    const float xop = fmaf(4.0f, x4, 16.0f * x16);     // the operands' constant part, scaled
     z.x = 64.0f * inv;
-    z.y = fmaf(64.0f, xop, 32.0f * xsum);  // and the zero point 32
-    z.z = xsum;
+    z.y = fmaf(0.5f, xs, xop);  // and the zero point: 32 * sum / 64
+    z.z = xs * inv;
   } else if (kInt) {
     float x16 = 0.0f, x1 = 0.0f;
 #pragma unroll
@@ -101,11 +112,9 @@ __device__ __forceinline__ float4 stage_quarter(const uint32_t (&u)[8], uint32_t
       x16 += (q[0] + q[4]) + (q[2] + q[6]);
       x1 += (q[1] + q[5]) + (q[3] + q[7]);
     }
-    const float xsum = (x16 + x1) * inv;           // X, unscaled
-    const float xop = fmaf(16.0f, x16, x1) * inv;  // the operands' constant part, unscaled
     z.x = 64.0f * inv;
-    z.y = 64.0f * xop;
-    z.z = xsum;
+    z.y = fmaf(16.0f, x16, x1);  // the operands' constant part, scaled
+    z.z = (x16 + x1) * inv;      // X, unscaled
   } else {
 #pragma unroll
     for (int i = 0; i < 2; ++i)
@@ -198,25 +207,27 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
         P[m][1] = p1;
       }
     }
-    // Fold the quarter's partial with the block scale (once per block and row).
+    // Fold the quarter's partial with the block scale (once per block and row): the block
+    // scale meets the scaled partial first and the power of two 2^-p last, so no product
+    // leaves fp32's range unless the true partial sum does.
     const int row = rt * 32 + lane;
     const uint8_t* sp = scl + row * F::SB;
-    if (FMT == FMT_NVFP4) {
+    if (FMT == FMT_NVFP4) {  // the table holds E4M3 x the tensor scale
       const float S = e4m3_lut[sp[kq]];
 #pragma unroll
-      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * zq[m].x, P[m][0] + P[m][1], acc[rt][m]);
+      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * (P[m][0] + P[m][1]), zq[m].x, acc[rt][m]);
     } else if (FMT == FMT_MXFP4) {
       const float S = e8m0_f32(sp[kq >> 1]);
 #pragma unroll
-      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * zq[m].x, P[m][0] + P[m][1], acc[rt][m]);
+      for (int m = 0; m < M; ++m) acc[rt][m] = fmaf(S * (P[m][0] + P[m][1]), zq[m].x, acc[rt][m]);
     } else if (FMT == FMT_MLX) {
       const uint32_t sw = *reinterpret_cast<const uint32_t*>(sp);
       const float s = __half2float(__ushort_as_half((unsigned short)(sw & 0xFFFFu)));
       const float bias = __half2float(__ushort_as_half((unsigned short)(sw >> 16)));
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        const float dot = fmaf(zq[m].x, P[m][0] + P[m][1], -zq[m].y);
-        acc[rt][m] = fmaf(s, dot, fmaf(bias, zq[m].z, acc[rt][m]));
+        const float dot = (P[m][0] + P[m][1]) - zq[m].y;  // sum code * x / 64, scaled
+        acc[rt][m] = fmaf(s * dot, zq[m].x, fmaf(bias, zq[m].z, acc[rt][m]));
       }
     } else if (FMT == FMT_Q6K) {
       const float sc = (float)(int8_t)sp[kq];
@@ -224,15 +235,106 @@ __device__ __forceinline__ void consume(const uint8_t* st, const uint8_t* scl, c
       const float ds = d * sc;
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        const float dot = fmaf(zq[m].x, P[m][0] + P[m][1], -zq[m].y);
-        acc[rt][m] = fmaf(ds, dot, acc[rt][m]);
+        const float dot = (P[m][0] + P[m][1]) - zq[m].y;  // sum (code - 32) * x / 64, scaled
+        acc[rt][m] = fmaf(ds * dot, zq[m].x, acc[rt][m]);
       }
     } else {  // 5-bit: w = s * code + bias over the quarter's 32-input block
       const float2 sb = q5_affine<FMT>(sp, aux + row * fmt_aux_row(FMT), kq >> 1);
 #pragma unroll
       for (int m = 0; m < M; ++m) {
-        const float dot = fmaf(zq[m].x, P[m][0] + P[m][1], -zq[m].y);
-        acc[rt][m] = fmaf(sb.x, dot, fmaf(sb.y, zq[m].z, acc[rt][m]));
+        const float dot = (P[m][0] + P[m][1]) - zq[m].y;
+        acc[rt][m] = fmaf(sb.x * dot, zq[m].x, fmaf(sb.y, zq[m].z, acc[rt][m]));
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- tensor-core consumer
+// Exponent p of the power of two 2^p that puts a token's largest |x| (bf16 magnitude bits
+// `mb`, subnormals included) in [2^14, 2^15): the f16 staging scale of the tensor-core
+// GEMV.  0 for an all-zero token or one holding inf or NaN (those propagate unscaled).
+__device__ __forceinline__ int tok_exp(uint32_t mb) {
+  if (mb == 0 || mb >= 0x7F80u) return 0;
+  const int e = mb >= 0x80u ? (int)(mb >> 7) - 127 : (31 - __clz((int)mb)) - 133;
+  return 14 - e;
+}
+// v * 2^p for |p| <= 150, as two multiplies by normal powers of two (each exact unless the
+// result leaves fp32's range or turns subnormal, where it rounds once).
+__device__ __forceinline__ float mul_pow2(float v, int p) {
+  const int p1 = p / 2, p2 = p - p1;
+  return v * __uint_as_float((uint32_t)(p1 + 127) << 23) * __uint_as_float((uint32_t)(p2 + 127) << 23);
+}
+
+// mma.sync m16n8k16 (row.col), f16 x f16 products accumulated in fp32: d += a * b.
+// Fragments (g = lane / 4, t = lane % 4): a0 = A(g, 2t..2t+1), a1 = A(g+8, 2t..2t+1),
+// a2 = A(g, 2t+8..2t+9), a3 = A(g+8, 2t+8..2t+9); b0 = B(2t..2t+1, g), b1 = B(2t+8..2t+9, g);
+// d0, d1 = D(g, 2t..2t+1), d2, d3 = D(g+8, 2t..2t+1).
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One consumer warp, one unit (128 x 64 tile), the 32 rows 32 rq .. 32 rq + 31 (two groups of
+// 16), all 64 inputs, on the tensor cores: the 1-4 activation rows are a dense contraction
+// once each weight is an exact f16 operand, and the mixed-precision FMA's issue rate -- one
+// product per lane and clock -- is what bounds a 2-4 row GEMV on CUDA cores.
+//
+// A = the decoded E2M1 values of 16 rows (lane (g, t) holds code word t of rows g and g + 8
+// of each 32-input chunk: no re-arrangement of the packed layout), B = the staged f16
+// activations (one power-of-two scale per token, stage_x_tok).  The MMA's eight columns
+// are (token, quarter parity): column n takes token n % 4 from the inputs of quarter
+// 2c + n / 4 only (the lanes whose code word lies in the other quarter supply zeros), so
+// every output of the MMA is the sum over ONE 16-input quarter of one row for one token,
+// which then takes its block scale with one FMA into the accumulator.  acc[j][i]: row
+// 32 rq + 16 j + g (+ 8 for i >= 2), token 2 (t % 2) + i % 2, parity t / 2 (the two
+// parities are summed once per segment).
+// xslot: token 0's 64 staged activations (bytes) of this unit's input group, xtok the bytes
+// between tokens.  The E4M3 table holds the block scale times the tensor scale.
+template <int FMT, int M>
+__device__ __forceinline__ void consume_mma(const uint8_t* st, const uint8_t* scl, const uint8_t* xslot,
+                                            uint32_t xtok, const float* e4m3_lut, int rq, int lane,
+                                            float (&acc)[2][4]) {
+  static_assert(FMT == FMT_NVFP4 || FMT == FMT_MXFP4, "E2M1 formats only");
+  const int g = lane >> 2, t = lane & 3, par = t >> 1;
+  const int btok = g & 3;
+  const bool bon = btok < M && par == (g >> 2);
+  uint32_t sw[4];  // scale bytes of rows 32 rq + g + 8 i
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = 32 * rq + g + 8 * i;
+    if (FMT == FMT_NVFP4)
+      sw[i] = *reinterpret_cast<const uint32_t*>(scl + row * 4);
+    else
+      sw[i] = *reinterpret_cast<const uint16_t*>(scl + row * 2);
+  }
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint4 bx = make_uint4(0u, 0u, 0u, 0u);
+    if (bon) bx = *reinterpret_cast<const uint4*>(xslot + btok * xtok + 64 * c + 16 * t);
+    const int q = 2 * c + par;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint8_t* base = st + (rq * 2 + c) * 512 + 256 * j + 4 * lane;
+      const uint32_t wl = *reinterpret_cast<const uint32_t*>(base);
+      const uint32_t wh = *reinterpret_cast<const uint32_t*>(base + 128);
+      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      mma_f16(d, e2m1x2_h2<0>(wl), e2m1x2_h2<0>(wh), e2m1x2_h2<1>(wl), e2m1x2_h2<1>(wh), bx.x, bx.y);
+      mma_f16(d, e2m1x2_h2<2>(wl), e2m1x2_h2<2>(wh), e2m1x2_h2<3>(wl), e2m1x2_h2<3>(wh), bx.z, bx.w);
+      float sl, sh;
+      if (FMT == FMT_NVFP4) {
+        sl = e4m3_lut[(sw[2 * j] >> (8 * q)) & 0xFFu];
+        sh = e4m3_lut[(sw[2 * j + 1] >> (8 * q)) & 0xFFu];
+      } else {
+        sl = e8m0_f32(sw[2 * j] >> (8 * c));
+        sh = e8m0_f32(sw[2 * j + 1] >> (8 * c));
+      }
+      acc[j][0] = fmaf(sl, d[0], acc[j][0]);
+      acc[j][2] = fmaf(sh, d[2], acc[j][2]);
+      if (M > 1) {
+        acc[j][1] = fmaf(sl, d[1], acc[j][1]);
+        acc[j][3] = fmaf(sh, d[3], acc[j][3]);
       }
     }
   }
