@@ -91,24 +91,25 @@ __host__ __device__ inline SmemLayout gemv_smem_layout(int stage_bytes, int S, i
 
 // Stage the activation rows of a CTA's input groups into shared memory (see
 // stage_quarter): row m, slot s, quarter kq -> 8 staging words and one record.
+template <int M>
+__device__ __forceinline__ void load_quarter(const GemvArgs& a, int it, int sbase, int nslots, uint32_t (&u)[8]);
+
 template <int FMT, int M, int kCT>
 __device__ void stage_x(const GemvArgs& a, uint32_t* xs, float* sums, int sbase, int nslots, int tid) {
+  constexpr int R = 2;  // items whose loads go out together
   const int items = M * nslots * 4;
-  for (int it = tid; it < items; it += kCT) {
-    const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
-    const int64_t k0 = (int64_t)((sbase + s) % a.KG) * 64 + kq * 16;
-    uint32_t u[8];
-    if (k0 < a.k) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.x + m * a.ldx + k0);
-      const uint4 r0 = src[0], r1 = src[1];
-      u[0] = r0.x; u[1] = r0.y; u[2] = r0.z; u[3] = r0.w;
-      u[4] = r1.x; u[5] = r1.y; u[6] = r1.z; u[7] = r1.w;
-    } else {
+  for (int it0 = tid; it0 < items; it0 += R * kCT) {
+    uint32_t u[R][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) u[i] = 0;
+    for (int r = 0; r < R; ++r) load_quarter<M>(a, min(it0 + r * kCT, items - 1), sbase, nslots, u[r]);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int it = it0 + r * kCT;
+      if (it >= items) break;
+      const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
+      const float4 z = stage_quarter<FMT>(u[r], xs + (size_t)(m * nslots + s) * 32 + kq * 8);
+      reinterpret_cast<float4*>(sums)[(size_t)(m * nslots + s) * 4 + kq] = z;
     }
-    const float4 z = stage_quarter<FMT>(u, xs + (size_t)(m * nslots + s) * 32 + kq * 8);
-    reinterpret_cast<float4*>(sums)[(size_t)(m * nslots + s) * 4 + kq] = z;
   }
 }
 
@@ -120,16 +121,20 @@ __device__ void stage_x(const GemvArgs& a, uint32_t* xs, float* sums, int sbase,
 // bound).  Two passes: the token maxima (each thread keeps its first R items in
 // registers), a block-wide max in pmax[m] (zeroed before the kernel's first barrier), then
 // the conversion.  Row m, slot s, quarter kq -> 8 staging words, natural pair order.
+// The 16 activations of item `it` (row m, slot s, quarter kq) as eight bf16 pairs; inputs
+// past K read as zero.  The loads are unconditional (from row 0's first quarter when the
+// item lies past K) so that a thread's loads of several items all go out before any result
+// is used.
 template <int M>
 __device__ __forceinline__ void load_quarter(const GemvArgs& a, int it, int sbase, int nslots, uint32_t (&u)[8]) {
   const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
   const int64_t k0 = (int64_t)((sbase + s) % a.KG) * 64 + kq * 16;
-  if (k0 < a.k) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + m * a.ldx + k0);
-    const uint4 r0 = src[0], r1 = src[1];
-    u[0] = r0.x; u[1] = r0.y; u[2] = r0.z; u[3] = r0.w;
-    u[4] = r1.x; u[5] = r1.y; u[6] = r1.z; u[7] = r1.w;
-  } else {
+  const bool in = k0 < a.k;
+  const uint4* src = reinterpret_cast<const uint4*>(in ? a.x + m * a.ldx + k0 : a.x);
+  const uint4 r0 = src[0], r1 = src[1];
+  u[0] = r0.x; u[1] = r0.y; u[2] = r0.z; u[3] = r0.w;
+  u[4] = r1.x; u[5] = r1.y; u[6] = r1.z; u[7] = r1.w;
+  if (!in) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) u[i] = 0;
   }
@@ -146,20 +151,24 @@ __device__ __forceinline__ void fold_max(const uint32_t (&u)[8], int m, uint32_t
     if (mm == m) mx[mm] = max(mx[mm], mb);
 }
 
+// f1[m] * f2[m] = 2^p of token m, each factor a normal power of two.
 template <int M>
-__device__ __forceinline__ void store_quarter_tok(uint32_t* xs, int it, int nslots, const int (&p)[M],
-                                                  const uint32_t (&u)[8]) {
+__device__ __forceinline__ void store_quarter_tok(uint32_t* xs, int it, int nslots, const float (&f1)[M],
+                                                  const float (&f2)[M], const uint32_t (&u)[8]) {
   const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
-  int pm = 0;
+  float a1 = 1.0f, a2 = 1.0f;
 #pragma unroll
   for (int mm = 0; mm < M; ++mm)
-    if (mm == m) pm = p[mm];
+    if (mm == m) {
+      a1 = f1[mm];
+      a2 = f2[mm];
+    }
   uint32_t w[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     float lo, hi;
     bf16x2_to_f32(u[i], lo, hi);
-    __half2 h = __floats2half2_rn(mul_pow2(lo, pm), mul_pow2(hi, pm));
+    __half2 h = __floats2half2_rn(lo * a1 * a2, hi * a1 * a2);
     w[i] = *reinterpret_cast<uint32_t*>(&h);
   }
   uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)(m * nslots + s) * 32 + kq * 8);
@@ -183,13 +192,13 @@ __device__ void stage_x_tok(const GemvArgs& a, uint32_t* xs, uint32_t* pmax, int
 #pragma unroll
   for (int m = 0; m < M; ++m) mx[m] = 0;
   uint32_t held[R][8];
+  // every held item's loads first (one round trip to memory), then their maxima
+#pragma unroll
+  for (int r = 0; r < R; ++r) load_quarter<M>(a, min(tid + r * kCT, items - 1), sbase, nslots, held[r]);
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int it = tid + r * kCT;
-    if (it < items) {
-      load_quarter<M>(a, it, sbase, nslots, held[r]);
-      fold_max<M>(held[r], (it >> 2) / nslots, mx);
-    }
+    if (it < items) fold_max<M>(held[r], (it >> 2) / nslots, mx);
   }
   for (int it = tid + R * kCT; it < items; it += kCT) {
     uint32_t u[8];
@@ -202,18 +211,22 @@ __device__ void stage_x_tok(const GemvArgs& a, uint32_t* xs, uint32_t* pmax, int
     if ((tid & 31) == 0 && v) atomicMax(&pmax[m], v);
   }
   named_sync(1, kCT);
-  int p[M];
+  float f1[M], f2[M];
 #pragma unroll
-  for (int m = 0; m < M; ++m) p[m] = tok_exp(pmax[m]);
+  for (int m = 0; m < M; ++m) {
+    const int p = tok_exp(pmax[m]), p1 = p / 2;
+    f1[m] = __uint_as_float((uint32_t)(p1 + 127) << 23);
+    f2[m] = __uint_as_float((uint32_t)(p - p1 + 127) << 23);
+  }
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int it = tid + r * kCT;
-    if (it < items) store_quarter_tok<M>(xs, it, nslots, p, held[r]);
+    if (it < items) store_quarter_tok<M>(xs, it, nslots, f1, f2, held[r]);
   }
   for (int it = tid + R * kCT; it < items; it += kCT) {
     uint32_t u[8];
     load_quarter<M>(a, it, sbase, nslots, u);
-    store_quarter_tok<M>(xs, it, nslots, p, u);
+    store_quarter_tok<M>(xs, it, nslots, f1, f2, u);
   }
 }
 
@@ -233,11 +246,13 @@ __global__ void __launch_bounds__(gemv_warps(FMT, M) * 32 + 32, 1) gemv_kernel(c
   constexpr bool kMma = gemv_mma(FMT, M);  // tensor-core consumer (E2M1 formats)
   constexpr int kCW = gemv_warps(FMT, M);  // consumer warps
   constexpr int kCT = kCW * 32;           // consumer threads (one producer warp follows)
-  constexpr int kGroups = kCW / 4;        // unit groups (4 warps: one per 16-input quarter)
+  constexpr int kWPU = 2;                 // warps per unit: two 16-input quarters (CUDA cores) or
+                                          // 64 rows (tensor cores) each, per chunk
+  constexpr int kGroups = kCW / kWPU;     // unit groups
   extern __shared__ __align__(128) uint8_t smem[];
   using SG = Stage<FMT>;
   const int S = a.stages, nslots = a.nslots;
-  const SmemLayout L = gemv_smem_layout(Stage<FMT>::bytes(kCW / 4), S, M, nslots, a.csplit, kCW);
+  const SmemLayout L = gemv_smem_layout(Stage<FMT>::bytes(kCW / 2), S, M, nslots, a.csplit, kCW);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + S;
   uint8_t* stages = smem + L.stages;
@@ -334,16 +349,16 @@ __global__ void __launch_bounds__(gemv_warps(FMT, M) * 32 + 32, 1) gemv_kernel(c
   if (M > 1 && tid == 0) mbar_arrive(xready);
 
   // This warp's units: relative index i = C * chunk + ug, one per chunk, processed
-  // in order; (stage, parity, activation slot) advance incrementally.
-  const int ug = warp >> 2, kq = warp & 3;
+  // in order; (stage, parity, activation slot) advance incrementally.  Within a unit the
+  // warp takes half kh: quarters 2 kh, 2 kh + 1 (CUDA cores) or rows 64 kh .. 64 kh + 63
+  // (tensor cores).
+  const int ug = warp / kWPU, kh = warp % kWPU;
   bool ok = true;
   uint32_t i = (uint32_t)ug;
   int s = 0;
   uint32_t ph = 0;
   int slot = (int)((uu0 + i) % (uint32_t)KG) - sbase;
   if (slot < 0) slot += KG;
-  const uint8_t* xq_base = reinterpret_cast<const uint8_t*>(xs) + kq * 32;
-  const float* sq_base = sums + kq * 4;
   uint32_t u = uu0;
   const uint32_t crank = clustered ? cluster_rank() : 0;
   uint32_t part_q0 = 0, part_q1 = 0;  // row tiles this CTA holds only part of
@@ -357,32 +372,40 @@ __global__ void __launch_bounds__(gemv_warps(FMT, M) * 32 + 32, 1) gemv_kernel(c
     for (int rt = 0; rt < 4; ++rt)
 #pragma unroll
       for (int m = 0; m < M; ++m) acc[rt][m] = 0.0f;
-    float acc2[2][4];  // tensor-core consumer (consume_mma)
+    float acc2[2][2][4];  // tensor-core consumer (consume_mma), one set per 32-row quarter
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc2[j][i] = 0.0f;
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc2[h][j][i] = 0.0f;
     for (; ok && uu0 + i < seg_end; i += C) {
-      if (!mbar_wait_bounded(&full[s], ph, a.status)) {
+      if (!mbar_try_wait(&full[s], ph) && !mbar_wait_bounded(&full[s], ph, a.status)) {
         ok = false;
         break;
       }
       const uint8_t* st = stages + (size_t)s * SB;
       const uint32_t uu = uu0 + i;
       if constexpr (kMma) {
-        consume_mma<FMT, M>(st + ug * SG::CODE, st + C * SG::CODE + ug * SG::SCALE,
-                            reinterpret_cast<const uint8_t*>(xs) + (size_t)slot * 128, (uint32_t)nslots * 128, lut,
-                            kq, lane, acc2);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          consume_mma<FMT, M>(st + ug * SG::CODE, st + C * SG::CODE + ug * SG::SCALE,
+                              reinterpret_cast<const uint8_t*>(xs) + (size_t)slot * 128, (uint32_t)nslots * 128, lut,
+                              2 * kh + h, lane, acc2[h]);
       } else {
         const uint8_t* aux = st + C * (SG::CODE + SG::SCALE) + ((uu >> 2) - ((uu - ug) >> 2)) * SG::AUX;
-        const uint32_t* xr[M];
-        const float* zr[M];
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-          xr[m] = reinterpret_cast<const uint32_t*>(xq_base + (size_t)slot * 128) + (size_t)m * nslots * 32;
-          zr[m] = sq_base + (size_t)slot * 16 + (size_t)m * nslots * 16;
+        for (int h = 0; h < 2; ++h) {
+          const int kq = 2 * kh + h;
+          const uint32_t* xr[M];
+          const float* zr[M];
+#pragma unroll
+          for (int m = 0; m < M; ++m) {
+            xr[m] = xs + (size_t)(m * nslots + slot) * 32 + kq * 8;
+            zr[m] = sums + (size_t)(m * nslots + slot) * 16 + kq * 4;
+          }
+          consume<FMT, M>(st + ug * SG::CODE, st + C * SG::CODE + ug * SG::SCALE, aux, xr, zr, lut, kq, lane, acc);
         }
-        consume<FMT, M>(st + ug * SG::CODE, st + C * SG::CODE + ug * SG::SCALE, aux, xr, zr, lut, kq, lane, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -398,17 +421,21 @@ __global__ void __launch_bounds__(gemv_warps(FMT, M) * 32 + 32, 1) gemv_kernel(c
     if constexpr (kMma) {
       const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc2[j][i] += __shfl_xor_sync(0xFFFFFFFFu, acc2[j][i], 2);  // parities
-      if (t < 2) {
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int m = 2 * t + (i & 1), row = 32 * kq + 16 * j + g + 8 * (i >> 1);
-            if (m < M) red[(ug * M + m) * 128 + row] = acc2[j][i];
-          }
+          for (int i = 0; i < 4; ++i) acc2[h][j][i] += __shfl_xor_sync(0xFFFFFFFFu, acc2[h][j][i], 2);  // parities
+      if (t < 2) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int m = 2 * t + (i & 1), row = 32 * (2 * kh + h) + 16 * j + g + 8 * (i >> 1);
+              if (m < M) red[(ug * M + m) * 128 + row] = acc2[h][j][i];
+            }
       }
     } else {
 #pragma unroll
@@ -507,7 +534,7 @@ __global__ void __launch_bounds__(gemv_warps(FMT, M) * 32 + 32, 1) gemv_kernel(c
 
 // ---------------------------------------------------------------- host side
 static int stage_bytes_of(int fmt, int m) {
-  const int C = gemv_warps(fmt, m) / 4;
+  const int C = gemv_warps(fmt, m) / 2;  // units per chunk: one per two consumer warps
   switch (fmt) {
     case FMT_MLX: return Stage<FMT_MLX>::bytes(C);
     case FMT_MXFP4: return Stage<FMT_MXFP4>::bytes(C);
@@ -522,7 +549,7 @@ static int stage_bytes_of(int fmt, int m) {
 bool plan_gemv(const Geometry& g, int m, const DeviceInfo& dev, GemvPlan* p) {
   const int sbytes = stage_bytes_of(g.fmt, m);
   const int kcw = gemv_warps(g.fmt, m);
-  const int C = kcw / 4;
+  const int C = kcw / 2;
   const int64_t U = g.nt * g.kg;
   if (U >= (int64_t(1) << 31)) return false;
   const size_t budget = (size_t)dev.max_smem_optin;

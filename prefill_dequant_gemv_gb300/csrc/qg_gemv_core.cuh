@@ -32,7 +32,8 @@ template <int FMT> struct Stage {
   static constexpr int CODE = Fmt<FMT>::TB;            // per unit
   static constexpr int SCALE = 128 * Fmt<FMT>::SB;     // per unit
   static constexpr int AUX = fmt_aux(FMT);             // per 4 units (Q6_K d, Q5_K d and dmin)
-  __host__ __device__ static constexpr int bytes(int C) { return C * (CODE + SCALE) + 2 * AUX; }
+  // C consecutive units touch at most (C + 3) / 4 + 1 groups of four units' aux records
+  __host__ __device__ static constexpr int bytes(int C) { return C * (CODE + SCALE) + ((C + 3) / 4 + 1) * AUX; }
 };
 
 __host__ __device__ inline int64_t owner_cta(int64_t u, int64_t U, int64_t G) {
