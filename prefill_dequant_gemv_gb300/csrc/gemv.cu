@@ -56,7 +56,10 @@ struct GemvArgs {
 };
 
 constexpr int kMaxCsplit = 8;  // portable cluster size
-constexpr int kEarlyChunks = 2;  // weight chunks a CTA requests before its activations are staged
+// Weight chunks a CTA requests before its activation loads are out: the rest wait, so the
+// activations -- on the critical path, since nothing is consumed before they are staged --
+// do not queue behind this CTA's whole weight burst.
+constexpr int kEarlyChunks = 1;
 
 struct SmemLayout {
   size_t bars, stages, xs, sums, red, cbuf, lut, misc, total;
@@ -89,54 +92,83 @@ __host__ __device__ inline SmemLayout gemv_smem_layout(int stage_bytes, int S, i
   return L;
 }
 
-// Stage the activation rows of a CTA's input groups into shared memory (see
-// stage_quarter): row m, slot s, quarter kq -> 8 staging words and one record.
-template <int M>
-__device__ __forceinline__ void load_quarter(const GemvArgs& a, int it, int sbase, int nslots, uint32_t (&u)[8]);
-
-template <int FMT, int M, int kCT>
-__device__ void stage_x(const GemvArgs& a, uint32_t* xs, float* sums, int sbase, int nslots, int tid) {
-  constexpr int R = 2;  // items whose loads go out together
-  const int items = M * nslots * 4;
-  for (int it0 = tid; it0 < items; it0 += R * kCT) {
-    uint32_t u[R][8];
-#pragma unroll
-    for (int r = 0; r < R; ++r) load_quarter<M>(a, min(it0 + r * kCT, items - 1), sbase, nslots, u[r]);
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int it = it0 + r * kCT;
-      if (it >= items) break;
-      const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
-      const float4 z = stage_quarter<FMT>(u[r], xs + (size_t)(m * nslots + s) * 32 + kq * 8);
-      reinterpret_cast<float4*>(sums)[(size_t)(m * nslots + s) * 4 + kq] = z;
-    }
+// A thread's activation staging items -- (row m, slot s, quarter kq) of the CTA's
+// M x nslots x 4 -- are every kCT-th item from item tid: kq is the thread's own (kCT is a
+// multiple of 4) and (m, s) advances by kCT / 4 slots at a time, without a division.
+struct XItem {
+  int m, s, kq;
+};
+struct XStep {
+  int dm, ds;  // kCT / 4 slots as whole rows and remaining slots
+};
+__device__ __forceinline__ XItem item_first(int tid, int nslots) {
+  const int j = tid >> 2, m = j / nslots;
+  return XItem{m, j - m * nslots, tid & 3};
+}
+__device__ __forceinline__ XStep item_step(int kCT, int nslots) {
+  const int q = (kCT >> 2) / nslots;
+  return XStep{q, (kCT >> 2) - q * nslots};
+}
+__device__ __forceinline__ void item_next(XItem& x, const XStep& st, int nslots) {
+  x.m += st.dm;
+  x.s += st.ds;
+  if (x.s >= nslots) {
+    x.s -= nslots;
+    ++x.m;
   }
 }
 
-// Stage the activation rows for the tensor-core consumer: f16 with ONE power-of-two scale
-// per token over this CTA's input groups, 2^p with p = tok_exp(the token's largest |x|),
-// so B of every MMA shares it and the partial sums need no per-quarter rescaling.  The
-// largest value lands in [2^14, 2^15); bf16 values more than 2^32 below it round onto f16's
-// subnormal grid (absolute error under 2^-40 of the token's max: far inside the stated
-// bound).  Two passes: the token maxima (each thread keeps its first R items in
-// registers), a block-wide max in pmax[m] (zeroed before the kernel's first barrier), then
-// the conversion.  Row m, slot s, quarter kq -> 8 staging words, natural pair order.
-// The 16 activations of item `it` (row m, slot s, quarter kq) as eight bf16 pairs; inputs
-// past K read as zero.  The loads are unconditional (from row 0's first quarter when the
-// item lies past K) so that a thread's loads of several items all go out before any result
-// is used.
+// The 16 activations of item x as eight bf16 pairs; inputs past K, and items past the last
+// row (x.m >= M), read as zero.  The loads are unconditional (from x's first element when
+// the item is outside) so that a thread's loads of several items all go out before any
+// result is used, and volatile so that each is made exactly once where it stands.
 template <int M>
-__device__ __forceinline__ void load_quarter(const GemvArgs& a, int it, int sbase, int nslots, uint32_t (&u)[8]) {
-  const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
-  const int64_t k0 = (int64_t)((sbase + s) % a.KG) * 64 + kq * 16;
-  const bool in = k0 < a.k;
-  const uint4* src = reinterpret_cast<const uint4*>(in ? a.x + m * a.ldx + k0 : a.x);
-  const uint4 r0 = src[0], r1 = src[1];
-  u[0] = r0.x; u[1] = r0.y; u[2] = r0.z; u[3] = r0.w;
-  u[4] = r1.x; u[5] = r1.y; u[6] = r1.z; u[7] = r1.w;
+__device__ __forceinline__ void load_quarter(const GemvArgs& a, const XItem& x, int sbase, uint32_t (&u)[8]) {
+  int g = sbase + x.s;  // input group: sbase + s < 2 KG
+  if (g >= a.KG) g -= a.KG;
+  const int64_t k0 = (int64_t)g * 64 + x.kq * 16;
+  const bool in = x.m < M && k0 < a.k;
+  const __nv_bfloat16* src = in ? a.x + x.m * a.ldx + k0 : a.x;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]) : "l"(src));
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]) : "l"(src + 8));
   if (!in) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) u[i] = 0;
+  }
+}
+
+// Stage the activation rows of a CTA's input groups into shared memory for the CUDA-core
+// consumer (see stage_quarter): row m, slot s, quarter kq -> 8 staging words and one
+// record.  xissued: every consumer warp arrives once its first loads are out (the producer
+// holds the weight stream back until then).
+template <int FMT, int M, int kCT>
+__device__ void stage_x(const GemvArgs& a, uint32_t* xs, float* sums, int sbase, int nslots, int tid,
+                        uint64_t* xissued) {
+  constexpr int R = 2;  // items whose loads go out together
+  const XStep st = item_step(kCT, nslots);
+  XItem it = item_first(tid, nslots);
+  XItem its[R];
+  uint32_t u[R][8];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    its[r] = it;
+    load_quarter<M>(a, it, sbase, u[r]);
+    item_next(it, st, nslots);
+  }
+  __syncwarp();
+  if ((tid & 31) == 0) mbar_arrive(xissued);
+  auto stage = [&](const XItem& x, const uint32_t (&v)[8]) {
+    const int j = x.m * nslots + x.s;
+    const float4 z = stage_quarter<FMT>(v, xs + (size_t)j * 32 + x.kq * 8);
+    reinterpret_cast<float4*>(sums)[(size_t)j * 4 + x.kq] = z;
+  };
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    if (its[r].m < M) stage(its[r], u[r]);
+  for (; it.m < M; item_next(it, st, nslots)) {
+    uint32_t v[8];
+    load_quarter<M>(a, it, sbase, v);
+    stage(it, v);
   }
 }
 
@@ -151,18 +183,13 @@ __device__ __forceinline__ void fold_max(const uint32_t (&u)[8], int m, uint32_t
     if (mm == m) mx[mm] = max(mx[mm], mb);
 }
 
-// f1[m] * f2[m] = 2^p of token m, each factor a normal power of two.
-template <int M>
-__device__ __forceinline__ void store_quarter_tok(uint32_t* xs, int it, int nslots, const float (&f1)[M],
-                                                  const float (&f2)[M], const uint32_t (&u)[8]) {
-  const int kq = it & 3, s = (it >> 2) % nslots, m = (it >> 2) / nslots;
-  float a1 = 1.0f, a2 = 1.0f;
-#pragma unroll
-  for (int mm = 0; mm < M; ++mm)
-    if (mm == m) {
-      a1 = f1[mm];
-      a2 = f2[mm];
-    }
+// Item x as f16 times its token's 2^p (p = tok_exp of the token's maximum in pmax), applied
+// as two normal powers of two.
+__device__ __forceinline__ void store_quarter_tok(uint32_t* xs, const XItem& x, int nslots, const uint32_t* pmax,
+                                                  const uint32_t (&u)[8]) {
+  const int p = tok_exp(pmax[x.m]), p1 = p / 2;
+  const float a1 = __uint_as_float((uint32_t)(p1 + 127) << 23);
+  const float a2 = __uint_as_float((uint32_t)(p - p1 + 127) << 23);
   uint32_t w[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -171,7 +198,7 @@ __device__ __forceinline__ void store_quarter_tok(uint32_t* xs, int it, int nslo
     __half2 h = __floats2half2_rn(lo * a1 * a2, hi * a1 * a2);
     w[i] = *reinterpret_cast<uint32_t*>(&h);
   }
-  uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)(m * nslots + s) * 32 + kq * 8);
+  uint4* dst = reinterpret_cast<uint4*>(xs + (size_t)(x.m * nslots + x.s) * 32 + x.kq * 8);
   dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
   dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
@@ -185,25 +212,32 @@ __device__ __forceinline__ void store_quarter_tok(uint32_t* xs, int it, int nslo
 // registers), a block-wide max in pmax[m] (zeroed before the kernel's first barrier), then
 // the conversion.  Row m, slot s, quarter kq -> 8 staging words, natural pair order.
 template <int M, int kCT>
-__device__ void stage_x_tok(const GemvArgs& a, uint32_t* xs, uint32_t* pmax, int sbase, int nslots, int tid) {
+__device__ void stage_x_tok(const GemvArgs& a, uint32_t* xs, uint32_t* pmax, int sbase, int nslots, int tid,
+                            uint64_t* xissued) {
   constexpr int R = 4;
-  const int items = M * nslots * 4;
+  const XStep st = item_step(kCT, nslots);
   uint32_t mx[M];
 #pragma unroll
   for (int m = 0; m < M; ++m) mx[m] = 0;
+  XItem it = item_first(tid, nslots);
+  XItem its[R];
   uint32_t held[R][8];
   // every held item's loads first (one round trip to memory), then their maxima
 #pragma unroll
-  for (int r = 0; r < R; ++r) load_quarter<M>(a, min(tid + r * kCT, items - 1), sbase, nslots, held[r]);
-#pragma unroll
   for (int r = 0; r < R; ++r) {
-    const int it = tid + r * kCT;
-    if (it < items) fold_max<M>(held[r], (it >> 2) / nslots, mx);
+    its[r] = it;
+    load_quarter<M>(a, it, sbase, held[r]);
+    item_next(it, st, nslots);
   }
-  for (int it = tid + R * kCT; it < items; it += kCT) {
-    uint32_t u[8];
-    load_quarter<M>(a, it, sbase, nslots, u);
-    fold_max<M>(u, (it >> 2) / nslots, mx);
+  __syncwarp();
+  if ((tid & 31) == 0) mbar_arrive(xissued);
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    if (its[r].m < M) fold_max<M>(held[r], its[r].m, mx);
+  for (XItem x = it; x.m < M; item_next(x, st, nslots)) {
+    uint32_t v[8];
+    load_quarter<M>(a, x, sbase, v);
+    fold_max<M>(v, x.m, mx);
   }
 #pragma unroll
   for (int m = 0; m < M; ++m) {
@@ -211,22 +245,13 @@ __device__ void stage_x_tok(const GemvArgs& a, uint32_t* xs, uint32_t* pmax, int
     if ((tid & 31) == 0 && v) atomicMax(&pmax[m], v);
   }
   named_sync(1, kCT);
-  float f1[M], f2[M];
 #pragma unroll
-  for (int m = 0; m < M; ++m) {
-    const int p = tok_exp(pmax[m]), p1 = p / 2;
-    f1[m] = __uint_as_float((uint32_t)(p1 + 127) << 23);
-    f2[m] = __uint_as_float((uint32_t)(p - p1 + 127) << 23);
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int it = tid + r * kCT;
-    if (it < items) store_quarter_tok<M>(xs, it, nslots, f1, f2, held[r]);
-  }
-  for (int it = tid + R * kCT; it < items; it += kCT) {
-    uint32_t u[8];
-    load_quarter<M>(a, it, sbase, nslots, u);
-    store_quarter_tok<M>(xs, it, nslots, f1, f2, u);
+  for (int r = 0; r < R; ++r)
+    if (its[r].m < M) store_quarter_tok(xs, its[r], nslots, pmax, held[r]);
+  for (; it.m < M; item_next(it, st, nslots)) {
+    uint32_t v[8];
+    load_quarter<M>(a, it, sbase, v);
+    store_quarter_tok(xs, it, nslots, pmax, v);
   }
 }
 
@@ -262,7 +287,7 @@ __global__ void __launch_bounds__(gemv_warps(FMT, M) * 32 + 32, 1) gemv_kernel(c
   float* cbuf = reinterpret_cast<float*>(smem + L.cbuf);
   float* lut = reinterpret_cast<float*>(smem + L.lut);
   int* flag = reinterpret_cast<int*>(smem + L.misc);
-  uint64_t* xready = reinterpret_cast<uint64_t*>(smem + L.misc + 16);  // the activations are staged
+  uint64_t* xissued = reinterpret_cast<uint64_t*>(smem + L.misc + 16);  // the activation loads are out
   const bool clustered = a.csplit > 1;
 
   const int64_t U = a.U;
@@ -281,8 +306,8 @@ __global__ void __launch_bounds__(gemv_warps(FMT, M) * 32 + 32, 1) gemv_kernel(c
     mbar_init(&full[s], 1);
     mbar_init(&empty[s], kCW);  // every consumer warp releases each chunk once
   }
-  if (M > 1 && tid == 0) mbar_init(xready, 1);
-  if (tid < S + (M > 1 ? 1 : 0)) fence_mbar_init();
+  if (tid == 0) mbar_init(xissued, kCW);
+  if (tid < S + 1) fence_mbar_init();
   uint32_t* pmax = reinterpret_cast<uint32_t*>(sums);  // tensor-core staging: token maxima
   if (kMma && tid < M) pmax[tid] = 0;
   __syncthreads();
@@ -305,7 +330,7 @@ __global__ void __launch_bounds__(gemv_warps(FMT, M) * 32 + 32, 1) gemv_kernel(c
         // With several activation rows, two chunks go out at once and the rest wait until the
         // activations are staged, so their loads do not queue behind this CTA's whole weight
         // burst (17408 x 5120 at four rows: 27.7 -> 26.4 us; one row stages too little to gain).
-        if (M > 1 && j == kEarlyChunks && !mbar_wait_bounded(xready, 0, a.status)) break;
+        if (j == kEarlyChunks && !mbar_wait_bounded(xissued, 0, a.status)) break;
         const uint32_t ub = min(uu1, ua + C);
         const uint32_t nu = ub - ua;
         uint8_t* dst = stages + (size_t)s * SB;
@@ -342,11 +367,10 @@ __global__ void __launch_bounds__(gemv_warps(FMT, M) * 32 + 32, 1) gemv_kernel(c
   }
   pdl_wait();  // activations, residual and workspace may come from the preceding kernel
   if constexpr (kMma)
-    stage_x_tok<M, kCT>(a, xs, pmax, sbase, nslots, tid);
+    stage_x_tok<M, kCT>(a, xs, pmax, sbase, nslots, tid, xissued);
   else
-    stage_x<FMT, M, kCT>(a, xs, sums, sbase, nslots, tid);
+    stage_x<FMT, M, kCT>(a, xs, sums, sbase, nslots, tid, xissued);
   named_sync(1, kCT);
-  if (M > 1 && tid == 0) mbar_arrive(xready);
 
   // This warp's units: relative index i = C * chunk + ug, one per chunk, processed
   // in order; (stage, parity, activation slot) advance incrementally.  Within a unit the
