@@ -180,10 +180,22 @@ static size_t w4a4_gemm_part(int fmt, int64_t n, int64_t k, int64_t m) {
   return g ? (g + 255) / 256 * 256 : 0;
 }
 
+// 5 or more rows: the block-scaled FP4 GEMM, its workspace the status header, then the
+// quantised activations' codes [m][w4a4_ldc] and E4M3 scales [m][w4a4_lds].
+static int64_t w4a4_ldc(int64_t k) { return (k / 2 + 15) / 16 * 16; }
+static int64_t w4a4_lds(int64_t k) { return (k / 16 + 15) / 16 * 16; }
+static size_t w4a4_fp4_codes_off() { return kWsHeader; }
+static size_t w4a4_fp4_scales_off(int64_t k, int64_t m) {
+  return (w4a4_fp4_codes_off() + (size_t)m * (size_t)w4a4_ldc(k) + 255) / 256 * 256;
+}
+
 extern "C" size_t qgemm_w4a4_workspace_size(int fmt, int64_t n, int64_t k, int64_t m) {
   if (fmt != QG_FMT_NVFP4 || m < 1) return 0;
-  const size_t g = w4a4_gemm_part(fmt, n, k, m);
-  return g ? g + (size_t)m * (size_t)((k + 7) / 8 * 8) * 2 : 0;
+  Geometry g;
+  if (!geometry(fmt, n, k, &g)) return 0;
+  if (m >= 5) return w4a4_fp4_scales_off(k, m) + (size_t)m * (size_t)w4a4_lds(k);
+  const size_t gp = w4a4_gemm_part(fmt, n, k, m);
+  return gp ? gp + (size_t)m * (size_t)((k + 7) / 8 * 8) * 2 : 0;
 }
 
 extern "C" qg_status qgemm_w4a4(const qg_weight* w, const void* x, int64_t m, int64_t ldx, float act_scale,
@@ -209,6 +221,15 @@ extern "C" qg_status qgemm_w4a4(const qg_weight* w, const void* x, int64_t m, in
     return current_device_info(&dev) ? QG_ERR_UNSUPPORTED : QG_ERR_CUDA;
   }
   if (workspace_bytes < need) return QG_ERR_WORKSPACE_TOO_SMALL;
+  if (m >= 5) {  // quantise to codes and scales, then the block-scaled FP4 GEMM multiplies them
+    uint8_t* codes = static_cast<uint8_t*>(workspace) + w4a4_fp4_codes_off();
+    uint8_t* scales = static_cast<uint8_t*>(workspace) + w4a4_fp4_scales_off(w->k, m);
+    st = launch_quant_act_nvfp4(x, m, w->k, ldx, act_scale, codes, w4a4_ldc(w->k), scales, w4a4_lds(w->k), nullptr, 0,
+                                stream);
+    if (st != QG_OK) return (qg_status)st;
+    return (qg_status)launch_gemm_fp4(g, w, act_scale, codes, w4a4_ldc(w->k), scales, w4a4_lds(w->k), m, residual,
+                                      ldr, y, ldy, workspace, stream);
+  }
   const size_t off = w4a4_gemm_part(w->fmt, w->n, w->k, m);
   void* xe = static_cast<char*>(workspace) + off;
   const int64_t lde = (w->k + 7) / 8 * 8;

@@ -67,6 +67,12 @@ int launch_quant_act_nvfp4(const void* x, int64_t m, int64_t k, int64_t ldx, flo
                            int64_t ldc, uint8_t* scales, int64_t lds, void* xe, int64_t lde, void* stream);
 int launch_prefill(const Geometry& g, const qg_weight* w, const void* x, int64_t t, int64_t ldx, const void* res,
                    int64_t ldr, void* y, int64_t ldy, void* ws, void* stream);
+// W4A4 GEMM on the block-scaled FP4 tensor cores: NVFP4 weight w, activations already
+// quantised to NVFP4 (codes [t][ldc] bytes, two per byte; E4M3 scales [t][lds]; ldc and lds
+// multiples of 16, both arrays 16-byte aligned), y = bf16(ts_w * act_scale * sum (+ res)).
+int launch_gemm_fp4(const Geometry& g, const qg_weight* w, float act_scale, const uint8_t* xcodes, int64_t ldc,
+                    const uint8_t* xscales, int64_t lds, int64_t t, const void* res, int64_t ldr, void* y, int64_t ldy,
+                    void* ws, void* stream);
 
 constexpr size_t kWsHeader = 256;  // status word + reserved
 

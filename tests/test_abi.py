@@ -236,7 +236,10 @@ def test_qgemm_w4a4_host_validation(q):
     assert call(wd=_desc(q, tensor_scale=1e30), a=1e30) == 1  # the product overflows fp32
     assert call(ldx=128) == 1 and call(ldy=128) == 1
     assert call(x=0x3008) == 3 and call(y=0x4008) == 3 and call(ldx=260) == 3
-    assert call(wsb=1000) == 4  # 8 rows: 256 + 8 x 256 x 2 bytes needed
-    assert q.qgemm_w4a4_workspace_size(wl.NVFP4, 256, 256, 8) == 256 + 8 * 256 * 2
+    # 8 rows (the FP4 GEMM): status header, then codes 8 x 128 bytes from offset 256, then
+    # E4M3 scales 8 x 16 bytes from the next 256-byte boundary (1280)
+    assert q.qgemm_w4a4_workspace_size(wl.NVFP4, 256, 256, 8) == 1280 + 8 * 16
+    assert call(wsb=1000) == 4
+    assert q.qgemm_w4a4_workspace_size(wl.NVFP4, 256, 1000, 8) == 0  # K not a multiple of 16
     assert q.qgemm_w4a4_workspace_size(wl.MXFP4, 256, 256, 8) == 0
     assert q.qgemm_w4a4_workspace_size(wl.NVFP4, 256, 256, 0) == 0

@@ -140,9 +140,11 @@ def test_w4a4_full_size_sampled(q, m):
 
 @pytest.mark.parametrize("m", [3, 40, 300])
 def test_w4a4_on_exact_activations_equals_w4a16(q, m):
-    """Activations NVFP4 represents exactly, at a power-of-two tensor scale: the W4A4 call
-    returns the W4A16 call's outputs bit for bit (the quantiser reproduces them and the
-    power-of-two scale moves exactly between the operand and the epilogue)."""
+    """Activations NVFP4 represents exactly, at a power-of-two tensor scale: both calls form
+    the same exact products.  At 1..4 rows W4A4 runs the W4A16 GEMV on the exact expansion
+    and returns its outputs bit for bit; from 5 rows it multiplies the FP4 codes on the
+    block-scaled tensor cores, whose fp32 sums may round in another order, so both sides
+    are held to the oracle's bound."""
     w = wl.weight(wl.NVFP4, 384, 1024, seed=m)
     bits, _, _ = pins.exact_nvfp4_activations(m, 1024, 0.25, seed=m)
     pw = q.PackedWeight.from_logical(w)
@@ -150,4 +152,33 @@ def test_w4a4_on_exact_activations_equals_w4a16(q, m):
     y4 = q.gemm_w4a4(pw, xt, 0.25)
     y16 = q.gemm(pw, xt)
     torch.cuda.synchronize()
-    assert torch.equal(y4.contiguous().view(torch.int16), y16.contiguous().view(torch.int16))
+    if m <= 4:
+        assert torch.equal(y4.contiguous().view(torch.int16), y16.contiguous().view(torch.int16))
+    else:
+        ref, _ = oracle.gemv(w, bits)
+        tol = oracle.tolerance(w, bits, ref=ref)
+        assert np.all(np.abs(to_f64(y4) - ref) <= tol)
+        assert np.all(np.abs(to_f64(y16) - ref) <= tol)
+
+
+@pytest.mark.parametrize("n,k,m", [(257, 208, 300), (640, 1280, 513), (128, 64, 5), (1000, 4096, 260)])
+def test_w4a4_fp4_tensor_core_shapes(q, n, k, m):
+    """The block-scaled FP4 GEMM (5 or more rows): K tails inside a 256-deep stage and inside a
+    64-deep tile (K = 208, 64), several token tiles with a ragged last one, ragged row tiles, a
+    residual; every output against the oracle, and two calls bit for bit."""
+    w, _, res = wl.gemv_case(wl.NVFP4, n, k, m, seed=n + k, residual=True)
+    bits = _activations(m, k, seed=m + k)
+    pw = q.PackedWeight.from_logical(w)
+    xt, rt = dev_bf16(bits), dev_bf16(res)
+    ws = q.Workspace(q.qgemm_w4a4_workspace_size(wl.NVFP4, n, k, m))
+    y1 = q.gemm_w4a4(pw, xt, 0.3, rt, workspace=ws).clone()
+    y2 = q.gemm_w4a4(pw, xt, 0.3, rt, workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert torch.equal(y1.contiguous().view(torch.int16), y2.contiguous().view(torch.int16))
+    got = to_f64(y1)
+    ref, _, xq = oracle.gemm_w4a4(w, bits, 0.3, res)
+    tol = _w4a4_tol(w, xq, ref) + 2.0 ** -7 * np.abs(oracle.bf16_value(res))
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got))
+    assert np.all(err <= tol), (float(np.max(err / tol)), np.unravel_index(np.argmax(err / tol), err.shape))
