@@ -8,11 +8,11 @@
 //
 // One CTA computes a 128-row x 256-token output tile over the whole K, in stages of four
 // 64-deep K steps:
-//   warp 0      producer: per stage, the four packed weight tiles (4 x 4 KB) by one 5-D TMA
+//   warp 0      producer: per stage, the four packed weight tiles (4 x 4 KB) by one 4-D TMA
 //               that lays them out as the tensor cores' no-swizzle K-major operand (the packed
 //               tile keeps 8-row x 16-byte core matrices contiguous, 32-row groups apart:
-//               the TMA's dimensions (16 B, 8 rows, 2 K-halves, 4 row blocks, group) make the
-//               row-block stride uniform), the tiles' E4M3 scales (bulk copy), the 256 x 256
+//               the TMA's dimensions (128-byte core matrix, 2 K-halves, 4 row blocks, group)
+//               make the row-block stride uniform), the tiles' E4M3 scales (bulk copy), the 256 x 256
 //               activation codes (2-D TMA, 128-byte swizzle) and their E4M3 scales (2-D TMA)
 //   warps 2..5  write the stage's scale factors into tensor memory (tcgen05.st; each warp its
 //               lane quarter, every quarter the same copy: row r's four scales of a K step in
@@ -88,11 +88,11 @@ __device__ __forceinline__ void mma_fp4(uint32_t d_tmem, uint64_t adesc, uint64_
       : "memory");
 }
 
-__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, int c4, uint64_t* bar) {
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c3, uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, "
-      "%6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(0), "r"(0), "r"(c4), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(0), "r"(c3), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kF4Threads, 1)
         const int kt = j * kF4KS, nk = min(kF4KS, KG - kt);
         const int64_t tile = (int64_t)tile_n * KG + kt;
         mbar_arrive_expect_tx(&full[s], kF4A + nk * 512 + kF4B + kF4SB);
-        tma_load_5d(st + kF4B, &tmw, (int)(tile * 4), &full[s]);
+        tma_load_4d(st + kF4B, &tmw, (int)(tile * 4), &full[s]);
         bulk_g2s(st + kF4B + kF4A, a.scales + tile * 512, nk * 512, &full[s]);
         if (j == 0) pdl_wait();  // the quantised activations come from the preceding kernel
         tma_load_2d(st, &tmx, kt * 32, t0, &full[s]);
@@ -318,13 +318,14 @@ int launch_gemm_fp4(const Geometry& g, const qg_weight* w, float act_scale, cons
     return QG_ERR_CUDA;
   EncodeFn enc = reinterpret_cast<EncodeFn>(fn);
   const cuuint32_t e1[5] = {1, 1, 1, 1, 1};
-  // weight codes: (16 bytes, 8 rows, 2 K halves, 4 row blocks, 32-row group over all tiles)
+  // weight codes: (one 8-row x 16-byte core matrix = 128 contiguous bytes, 2 K halves, 4 row
+  // blocks, 32-row group over all tiles)
   CUtensorMap tmw, tmx, tms;
   {
-    const cuuint64_t dims[5] = {16, 8, 2, 4, (cuuint64_t)(g.nt * g.kg * 4)};
-    const cuuint64_t strides[4] = {16, 512, 128, 1024};
-    const cuuint32_t box[5] = {16, 8, 2, 4, (cuuint32_t)(kF4KS * 4)};
-    if (enc(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(w->codes), dims, strides, box, e1,
+    const cuuint64_t dims[4] = {128, 2, 4, (cuuint64_t)(g.nt * g.kg * 4)};
+    const cuuint64_t strides[3] = {512, 128, 1024};
+    const cuuint32_t box[4] = {128, 2, 4, (cuuint32_t)(kF4KS * 4)};
+    if (enc(&tmw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(w->codes), dims, strides, box, e1,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return QG_ERR_CUDA;
