@@ -15,14 +15,19 @@
 //    runs the finish, as in the TurboEXL3 article §4.3 -- summing the partials in CTA
 //    order.
 //  * One producer lane issues 1-D bulk async copies of whole tiles into a deep ring of
-//    shared-memory stages (mbarrier completion, bounded waits); 16 consumer warps (12 at
-//    four rows) decode from shared memory.  Warp w takes the 16-input quarter (w % 4)
-//    of every (w / 4)-th unit of a chunk; each lane owns 4 rows (one per 32-row tile), so
-//    every activation value read from shared memory feeds 4 rows.
-//  * Weights become exact f16 operands in registers (qg_common.cuh) multiplied into fp32
-//    with the mixed-precision FMA; the block scale (and the integer formats' operand
-//    constant) is applied once per 16 inputs and row (Q6_K operand PR #19: one
-//    fma(dot, scale) per chain).
+//    shared-memory stages (mbarrier completion, bounded waits); it requests one chunk, then
+//    waits until the consumers' activation loads are out.  16 consumer warps (12 at four
+//    rows on CUDA cores) decode from shared memory; warp w takes half of unit w / 2 of
+//    every chunk.
+//  * CUDA-core consumer (every format at one row; the integer formats at 2-4): the warp's
+//    half is two 16-input quarters; each lane owns 4 rows (one per 32-row tile), so every
+//    activation value read from shared memory feeds 4 rows.  Weights become exact f16
+//    operands in registers (qg_common.cuh) multiplied into fp32 with the mixed-precision
+//    FMA; the block scale (and the integer formats' operand constant) is applied once per 16
+//    inputs and row (Q6_K operand PR #19: one fma(dot, scale) per chain).
+//  * Tensor-core consumer (E2M1 formats at 2-4 rows, consume_mma): the warp's half is 64
+//    rows; the decoded weights are A of mma.sync m16n8k16, the 1-4 activation rows B (the
+//    FMA's one product per lane and clock, not the bytes, bounds 2-4 rows on CUDA cores).
 #include <cuda_runtime.h>
 
 #include <algorithm>
