@@ -12,15 +12,18 @@
 //            its own; fp32 results per (token, expert)
 //   finish   out[t] = bf16( sum_j p[t, j] * down_{e_j}[t] + shared[t] ) (§4.1 "Finish")
 //
-// The grouped GEMV runs the dense GEMV's decode (qg_gemv_core.cuh) over segments (group,
-// 128-row tile, 1/P of the inputs) with groups = active experts (ascending) then the shared
-// expert once per token; each CTA takes an equal share of whole segments, its 12 consumer
-// warps hand each segment's partials to a reducer warp (two buffers, so they run on), and
-// the P parts of an output are summed by whoever reads it next, in part order.
+// The grouped GEMV runs the dense GEMV's decode (qg_gemv_core.cuh) over the units (group,
+// 128-row tile, 64 inputs) of groups = active experts (ascending), then the shared expert as
+// one group of all the tokens.  Each CTA takes an equal contiguous share of the units
+// (stream-K, so the CTAs finish together whatever the routing); its 12 consumer warps hand
+// each row tile's partials to a reducer warp (two buffers, so they run on).  A row tile cut
+// by a share boundary is written as one output part per CTA (parts past the last piece are
+// zero), and the parts are summed by whoever reads the output next, in part order.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
 #include "qg_common.cuh"
 #include "qg_gemv_core.cuh"
@@ -31,10 +34,11 @@
 
 namespace qg {
 
-constexpr int kGCW = 12;              // consumer warps (3 units per chunk, 128 registers a thread: no spills)
+constexpr int kGCW = 12;              // consumer warps (128 registers a thread: no spills)
 constexpr int kGCT = kGCW * 32;
-constexpr int kGC = kGCW / 4;         // units per chunk
-constexpr int kGThreads = kGCT + 64;  // + the producer warp and the reducer warp
+constexpr int kGC = kGCW / 2;         // units per chunk: two warps per unit, two quarters each
+constexpr int kGRW = 2;               // reducer warps
+constexpr int kGThreads = kGCT + 32 + 32 * kGRW;  // + the producer warp and the reducer warps
 constexpr int kGMaxRows = 4;
 
 struct GroupedArgs {
@@ -48,7 +52,7 @@ struct GroupedArgs {
   float ts, sh_ts;
   int64_t n, k;
   int NT, KG;
-  int P;  // input parts: a segment is (group, 128-row tile, 1/P of the inputs)
+  int P;  // output parts: a row tile split over CTAs writes one part per CTA, the rest zero
   int T, topk;
   int mode;  // 0: input rows are tokens (x); 1: input rows are grouped pairs, shared rows
              // after: bf16 rows of x, or (gu non-null) the SwiGLU of the fp32 gate/up rows gu
@@ -58,6 +62,7 @@ struct GroupedArgs {
   int64_t ldg;
   int gu_parts;
   int64_t gu_pstride;
+  int gu_nt, gu_kg;     // the gate/up launch's row tiles and 64-input groups (its pieces per tile)
   int nrows;  // input rows (staging slots)
   float* out;  // P partial outputs, out_pstride floats apart
   int64_t ldo;
@@ -85,12 +90,21 @@ struct GroupInfo {
   int m;
   int in_row[kGMaxRows];
   int out_row[kGMaxRows];
+  int w;          // cost of one unit (unit_cost(m))
+  int cu;         // cost of the groups before this one, per unit of a group
+  uint32_t cbase;  // cost of all the units of the groups before this one (units a group x cu)
 };
 constexpr int kGInfoCache = 8;
 
+// Relative cost of one unit of a group of m rows on the CUDA-core consumer: the decode is
+// paid once, the multiply-adds and folds once per row (measured 1 : 1.44 : 1.88 : 2.34 for
+// 1..4 rows in the dense GEMV's consume loop).
+__host__ __device__ constexpr int unit_cost(int m) { return 2 * m + 3; }
+
 struct GroupedSmem {
-  size_t bars, stages, xs, sums, red, lut, misc, ginfo, route, total;
+  size_t bars, stages, xs, sums, red, lut, misc, ginfo, gpc, route, total;
 };
+constexpr int kGPcTiles = 64;  // gate/up row tiles a pieces table covers
 
 // Shared memory: mbarriers (full[S], empty[S], rfull[2], rempty[2]), the stage ring, the
 // staged activations, two reduction buffers (one per segment in flight), the E4M3 table
@@ -116,6 +130,8 @@ __host__ __device__ inline GroupedSmem grouped_smem(int stage_bytes, int S, int 
   o += 64;
   L.ginfo = o;  // descriptors of the first kGInfoCache groups this CTA touches
   o += (size_t)kGInfoCache * sizeof(GroupInfo);
+  L.gpc = o;  // down launch: pieces of each gate/up row tile of the cached groups
+  o += (size_t)kGInfoCache * kGPcTiles;
   o = (o + 15) & ~(size_t)15;
   L.route = o;  // routing scratch and group table when the launch routes its tokens
   o += sizeof(BlockRouteSmem);
@@ -123,7 +139,10 @@ __host__ __device__ inline GroupedSmem grouped_smem(int stage_bytes, int S, int 
   return L;
 }
 
-__device__ __forceinline__ GroupInfo group_info(const GroupedArgs& a, const int* groups, int g, int n_active) {
+// Descriptor of group g (UG units a group).  The cost before group g in closed form: the
+// groups before it hold `first` pairs (rows) between them, so their units cost
+// UG * (2 first + 3 g); the shared group follows all T * topk pairs.
+__device__ __forceinline__ GroupInfo group_info(const GroupedArgs& a, const int* groups, int g, int n_active, int UG) {
   GroupInfo gi;
   if (g < n_active) {  // one 32-byte entry of the router's group table
     const int4* ge = reinterpret_cast<const int4*>(groups + (size_t)g * kGroupInts);
@@ -134,6 +153,9 @@ __device__ __forceinline__ GroupInfo group_info(const GroupedArgs& a, const int*
     gi.aux = a.aux ? a.aux + (int64_t)e * a.astride : nullptr;
     gi.ts = a.ts;
     gi.m = min(kGMaxRows, h.z);
+    gi.w = unit_cost(gi.m);
+    gi.cu = 2 * first + 3 * g;
+    gi.cbase = (uint32_t)UG * (uint32_t)gi.cu;
     const int tok[kGroupRows] = {rows.x, rows.y, rows.z, rows.w};
 #pragma unroll
     for (int i = 0; i < kGMaxRows; ++i) {
@@ -141,15 +163,18 @@ __device__ __forceinline__ GroupInfo group_info(const GroupedArgs& a, const int*
       gi.out_row[i] = first + j;
       gi.in_row[i] = a.mode == 0 ? tok[j] : first + j;
     }
-  } else {  // shared expert, token t = g - n_active
-    const int t = g - n_active;
+  } else {  // the shared expert: one group of all T tokens
     gi.codes = a.sh_codes;
     gi.scales = a.sh_scales;
     gi.aux = a.sh_aux;
     gi.ts = a.sh_ts;
-    gi.m = 1;
+    gi.m = a.T;
+    gi.w = unit_cost(a.T);
+    gi.cu = 2 * a.T * a.topk + 3 * n_active;
+    gi.cbase = (uint32_t)UG * (uint32_t)gi.cu;
 #pragma unroll
     for (int i = 0; i < kGMaxRows; ++i) {
+      const int t = min(i, a.T - 1);
       gi.out_row[i] = a.T * a.topk + t;
       gi.in_row[i] = a.mode == 0 ? t : a.T * a.topk + t;
     }
@@ -165,17 +190,39 @@ __device__ __forceinline__ uint32_t swiglu_bf16x2(float g0, float u0, float g1, 
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// The CTA's chunks, in order: at most kGC consecutive units of one group (a chunk may span
+// row tiles of its group, never two groups, whose weights lie apart).
+struct ChunkIter {
+  int c0, c1;  // units [c0, c1)
+  int g;       // their group
+  int gend;    // end of the group's units within the CTA's range
+};
+__device__ __forceinline__ void chunk_first(ChunkIter& it, int u0, int u1, int UG) {
+  it.g = u0 / UG;
+  it.gend = min(u1, (it.g + 1) * UG);
+  it.c0 = u0;
+  it.c1 = min(u0 + kGC, it.gend);
+}
+__device__ __forceinline__ void chunk_next(ChunkIter& it, int u1, int UG) {
+  it.c0 = it.c1;
+  if (it.c0 == it.gend) {
+    ++it.g;
+    it.gend = min(u1, (it.g + 1) * UG);
+  }
+  it.c1 = min(it.c0 + kGC, it.gend);
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const GroupedArgs a) {
   using SG = Stage<FMT>;
   extern __shared__ __align__(128) uint8_t smem[];
-  const int S = a.stages, KG = a.KG, NT = a.NT, P = a.P;
+  const int S = a.stages, KG = a.KG, NT = a.NT;
   const int SBY = SG::bytes(kGC);
   const GroupedSmem L = grouped_smem(SBY, S, a.nrows, KG);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + S;
-  uint64_t* rfull = empty + S;  // [2]: a segment's 12 partials are in red[buf]
-  uint64_t* rempty = rfull + 2;  // [2]: the reducer has consumed red[buf]
+  uint64_t* rfull = empty + S;  // [2]: every consumer warp's partial of a tile piece is in red[buf]
+  uint64_t* rempty = rfull + 2;  // [2]: the reducers have consumed red[buf]
   uint8_t* stages = smem + L.stages;
   uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L.xs);
   float* sums = reinterpret_cast<float*>(smem + L.sums);
@@ -190,7 +237,7 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   }
   if (tid < 2) {
     mbar_init(&rfull[tid], kGCW);
-    mbar_init(&rempty[tid], 1);
+    mbar_init(&rempty[tid], kGRW);
   }
   if (tid < S + 2) fence_mbar_init();
   __syncthreads();
@@ -199,81 +246,181 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   if (tid == 0) pdl_launch_dependents();
   pdl_wait();
 
-  // Segments: (group, row tile q, input part p), p-major inside a row tile; groups are the
-  // active experts, then the shared expert once per token.  Each CTA takes a contiguous,
-  // equal share of whole segments: no row tile is split across CTAs, so there are no
-  // tickets or partials to combine here -- the P parts are summed by the consumer of the
-  // outputs (the down GEMV's staging, the mid, the finish), in part order.
+  // Stage input row `row`, 64-input group sl, quarter kq into xs / sums: bf16 rows of x
+  // (mode 0: tokens; mode 1 from the caller: h), or h = bf16( silu(g) * u ) from the fp32
+  // gate/up rows, their first npg (gate) and npu (up) parts summed in part order -- every
+  // load of a part issued before the first add.
+  auto stage_item = [&](int row, int sl, int kq, int npg, int npu) {
+    const int64_t k0 = (int64_t)sl * 64 + kq * 16;
+    uint32_t u[8];
+    if (k0 >= a.k) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) u[i] = 0;
+    } else if (a.gu == nullptr) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + (int64_t)row * a.ldx + k0);
+      const uint4 r0 = src[0], r1 = src[1];
+      u[0] = r0.x; u[1] = r0.y; u[2] = r0.z; u[3] = r0.w;
+      u[4] = r1.x; u[5] = r1.y; u[6] = r1.z; u[7] = r1.w;
+    } else {
+      const float4* gp = reinterpret_cast<const float4*>(a.gu + (int64_t)row * a.ldg + k0);
+      const float4* up = reinterpret_cast<const float4*>(a.gu + (int64_t)row * a.ldg + a.k + k0);
+      const int64_t ps = a.gu_pstride / 4;
+      float4 g4[4], u4[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        g4[q4] = __ldcg(gp + q4);
+        u4[q4] = __ldcg(up + q4);
+      }
+      for (int pp = 1; pp < max(npg, npu); ++pp) {
+        float4 gx[4], ux[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          gx[q4] = pp < npg ? __ldcg(gp + pp * ps + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+          ux[q4] = pp < npu ? __ldcg(up + pp * ps + q4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          if (pp < npg) {
+            g4[q4].x += gx[q4].x; g4[q4].y += gx[q4].y; g4[q4].z += gx[q4].z; g4[q4].w += gx[q4].w;
+          }
+          if (pp < npu) {
+            u4[q4].x += ux[q4].x; u4[q4].y += ux[q4].y; u4[q4].z += ux[q4].z; u4[q4].w += ux[q4].w;
+          }
+        }
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        u[2 * q4] = swiglu_bf16x2(g4[q4].x, u4[q4].x, g4[q4].y, u4[q4].y);
+        u[2 * q4 + 1] = swiglu_bf16x2(g4[q4].z, u4[q4].z, g4[q4].w, u4[q4].w);
+      }
+    }
+    const float4 z = stage_quarter<FMT>(u, xs + (size_t)(row * KG + sl) * 32 + kq * 8);
+    reinterpret_cast<float4*>(sums)[(size_t)(row * KG + sl) * 4 + kq] = z;
+  };
+  // Mode 0: every token row, items it0, it0 + step, ...
+  auto stage_tokens = [&](int it0, int step) {
+    for (int it = it0; it < a.nrows * KG * 4; it += step) {
+      const int j = it >> 2, row = j / KG;
+      stage_item(row, j - row * KG, it & 3, 1, 1);
+    }
+  };
+
+  // Groups: the active experts (ascending), then the shared expert as one group of all T
+  // tokens.  Routing inside the launch: every CTA routes the T tokens itself (CTA 0 also
+  // stores the router's outputs) while its other consumer warps stage the tokens, which do
+  // not depend on the routing.
   int n_active;
   const int* groups;
-  if (a.logits) {  // route the T tokens here (every CTA the same table; CTA 0 stores it)
+  const bool routed = a.logits != nullptr;
+  if (routed) {
     BlockRouteSmem& rs = *reinterpret_cast<BlockRouteSmem*>(smem + L.route);
-    n_active = route_decode_block(a.logits, a.T, a.E, a.topk, rs, blockIdx.x == 0, a.ids_out, a.wts_out, a.rv);
+    n_active = route_decode_block(a.logits, a.T, a.E, a.topk, rs, blockIdx.x == 0, a.ids_out, a.wts_out, a.rv,
+                                  [&]() {
+                                    if (warp < kGCW) stage_tokens(tid - 32 * a.T, kGCT - 32 * a.T);
+                                  });
     groups = rs.groups;
   } else {
     n_active = a.meta[0];
     groups = a.groups;
   }
-  const int n_groups = n_active + (a.has_shared ? a.T : 0);
-  const int spg = NT * P;
-  const int64_t n_seg = (int64_t)n_groups * spg;
-  const int64_t G = min((int64_t)gridDim.x, n_seg), b = blockIdx.x;
-  if (b >= G) return;
-  const int sg0 = (int)(b * n_seg / G), sg1 = (int)((b + 1) * n_seg / G);
-  const int nck = (KG + kGC - 1) / kGC;  // chunks per row tile; part p takes chunks [p*nck/P, (p+1)*nck/P)
-  auto seg_units = [&](int sg, int& g, int& q, int& p, int& k0, int& k1) {
-    g = sg / spg;
-    const int r = sg - g * spg;
-    q = r / P;
-    p = r - q * P;
-    k0 = kGC * (p * nck / P);
-    k1 = min(KG, kGC * ((p + 1) * nck / P));
-  };
 
-  if (warp == kGCW) {  // producer: the segments' units, chunks never span two segments
+  // The unit range of this CTA: units (group, row tile, 64-input group) in that order, an
+  // equal contiguous share of their cost per CTA (stream-K weighted by unit_cost: unit u
+  // belongs to CTA floor(C(u) G / Ctot), C(u) the cost of the units before it).  G CTAs take
+  // part, few enough that every share holds at least the costliest unit, so none is empty.
+  // A row tile cut by a share boundary leaves one piece per CTA, written to output part
+  // (CTA - the tile's first CTA).  Costs times G stay below 2^32 (checked on the host), so
+  // this is 32-bit arithmetic.
+  const int n_groups = n_active + (a.has_shared ? 1 : 0);
+  const int UG = NT * KG;  // units per group
+  const int wmax = unit_cost(a.T);  // no group has more than T rows
+  const uint32_t Csh = (uint32_t)UG * (uint32_t)(2 * a.T * a.topk + 3 * n_active);  // the routed groups
+  const uint32_t Ctot = Csh + (a.has_shared ? (uint32_t)(UG * wmax) : 0u);
+  const uint32_t G = max(1u, min(gridDim.x, Ctot / (uint32_t)wmax)), b = blockIdx.x;
+  if (b >= G) return;
+  int u0, u1;
+  {  // this warp's lanes hold the cost before groups lane, lane + 32, lane + 64 (<= 65 groups)
+    uint32_t cg[3];
+    int wg[3];
+    bool has[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int g = lane + 32 * k;
+      cg[k] = 0u;
+      wg[k] = 1;
+      has[k] = g < n_groups;
+      if (g < n_active) {
+        const int4 h = reinterpret_cast<const int4*>(groups + (size_t)g * kGroupInts)[0];
+        cg[k] = (uint32_t)UG * (uint32_t)(2 * h.y + 3 * g);
+        wg[k] = unit_cost(min(kGMaxRows, h.z));
+      } else if (g == n_active && a.has_shared) {
+        cg[k] = Csh;
+        wg[k] = wmax;
+      }
+    }
+    // first unit of share bb: the smallest u with C(u) G >= bb Ctot
+    auto share_start = [&](uint32_t bb) -> int {
+      if (bb >= G) return n_groups * UG;
+      const uint32_t tgt = bb * Ctot;
+      int n = 0;  // groups starting at or before the target (C is increasing in g)
+#pragma unroll
+      for (int k = 0; k < 3; ++k) n += __popc(__ballot_sync(0xFFFFFFFFu, has[k] && cg[k] * G <= tgt));
+      const int gs = n - 1, ks = gs >> 5;
+      const uint32_t c = __shfl_sync(0xFFFFFFFFu, ks == 0 ? cg[0] : ks == 1 ? cg[1] : cg[2], gs & 31);
+      const uint32_t wG = (uint32_t)__shfl_sync(0xFFFFFFFFu, ks == 0 ? wg[0] : ks == 1 ? wg[1] : wg[2], gs & 31) * G;
+      const uint32_t j = (tgt - c * G + wG - 1) / wG;
+      return (int)min((uint32_t)(gs * UG) + j, (uint32_t)((gs + 1) * UG));
+    };
+    u0 = share_start(b);
+    u1 = share_start(b + 1);
+  }
+  const int t0 = u0 / KG;                     // first row tile (g * NT + q) of the range
+  const int npieces = (u1 - 1) / KG - t0 + 1;  // row tiles it touches
+  const int g_first = u0 / UG;
+  const int g_span = (u1 - 1) / UG - g_first + 1;
+
+  if (warp == kGCW) {  // producer: the range's chunks
     if (lane == 0) {
-      int s = 0, j = 0;
+      const uint64_t pol = l2_evict_first();  // every weight is read once per call
+      int s = 0;
       uint32_t ph = 0;
-      bool ok = true;
-      for (int sg = sg0; ok && sg < sg1; ++sg) {
-        int g, q, p, k0, k1;
-        seg_units(sg, g, q, p, k0, k1);
-        const uint8_t *bc, *bs, *ba;
-        if (g < n_active) {
-          const int e = groups[(size_t)g * kGroupInts];
-          bc = a.codes + (int64_t)e * a.cstride;
-          bs = a.scales + (int64_t)e * a.sstride;
-          ba = a.aux ? a.aux + (int64_t)e * a.astride : nullptr;
-        } else {
-          bc = a.sh_codes;
-          bs = a.sh_scales;
-          ba = a.sh_aux;
+      int j = 0, pg = -1;
+      const uint8_t *bc = nullptr, *bs = nullptr, *ba = nullptr;
+      ChunkIter it;
+      for (chunk_first(it, u0, u1, UG); it.c0 < u1; chunk_next(it, u1, UG), ++j) {
+        if (it.g != pg) {
+          pg = it.g;
+          if (it.g < n_active) {
+            const int e = groups[(size_t)it.g * kGroupInts];
+            bc = a.codes + (int64_t)e * a.cstride;
+            bs = a.scales + (int64_t)e * a.sstride;
+            ba = a.aux ? a.aux + (int64_t)e * a.astride : nullptr;
+          } else {
+            bc = a.sh_codes;
+            bs = a.sh_scales;
+            ba = a.sh_aux;
+          }
         }
-        for (int kc = k0; kc < k1; kc += kGC, ++j) {
-          if (j >= S && !mbar_wait_bounded(&empty[s], ph ^ 1u, a.status)) {
-            ok = false;
-            break;
-          }
-          const int l0 = q * KG + kc;  // unit index within the group
-          const int nu = min(kGC, k1 - kc);
-          uint8_t* dst = stages + (size_t)s * SBY;
-          uint32_t bytes = (uint32_t)nu * (SG::CODE + SG::SCALE);
-          int aux_a = 0, aux_n = 0;
-          if (SG::AUX) {
-            aux_a = l0 >> 2;
-            aux_n = ((l0 + nu - 1) >> 2) - aux_a + 1;
-            bytes += (uint32_t)aux_n * SG::AUX;
-          }
-          mbar_arrive_expect_tx(&full[s], bytes);
-          bulk_g2s(dst, bc + (size_t)l0 * SG::CODE, (uint32_t)nu * SG::CODE, &full[s]);
-          bulk_g2s(dst + kGC * SG::CODE, bs + (size_t)l0 * SG::SCALE, (uint32_t)nu * SG::SCALE, &full[s]);
-          if (SG::AUX)
-            bulk_g2s(dst + kGC * (SG::CODE + SG::SCALE), ba + (size_t)aux_a * SG::AUX, (uint32_t)aux_n * SG::AUX,
-                     &full[s]);
-          if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-          }
+        if (j >= S && !mbar_wait_bounded(&empty[s], ph ^ 1u, a.status)) break;
+        const int l0 = it.c0 - it.g * UG;  // unit index within the group
+        const int nu = it.c1 - it.c0;
+        uint8_t* dst = stages + (size_t)s * SBY;
+        uint32_t bytes = (uint32_t)nu * (SG::CODE + SG::SCALE);
+        int aux_a = 0, aux_n = 0;
+        if (SG::AUX) {
+          aux_a = l0 >> 2;
+          aux_n = ((l0 + nu - 1) >> 2) - aux_a + 1;
+          bytes += (uint32_t)aux_n * SG::AUX;
+        }
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_g2s_hint(dst, bc + (size_t)l0 * SG::CODE, (uint32_t)nu * SG::CODE, &full[s], pol);
+        bulk_g2s_hint(dst + kGC * SG::CODE, bs + (size_t)l0 * SG::SCALE, (uint32_t)nu * SG::SCALE, &full[s], pol);
+        if (SG::AUX)
+          bulk_g2s_hint(dst + kGC * (SG::CODE + SG::SCALE), ba + (size_t)aux_a * SG::AUX,
+                        (uint32_t)aux_n * SG::AUX, &full[s], pol);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
         }
       }
     }
@@ -281,29 +428,65 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   }
 
   // The groups this CTA touches: their descriptors are read once here.
-  const int g_first = sg0 / spg;
-  const int g_span = (sg1 - 1) / spg - g_first + 1;
-  if (tid < kGInfoCache && g_first + tid < n_groups) ginfo[tid] = group_info(a, groups, g_first + tid, n_active);
+  if (tid < kGInfoCache && tid < g_span) ginfo[tid] = group_info(a, groups, g_first + tid, n_active, UG);
+  // Down launch: how many parts each gate/up row tile of those groups was written in -- the
+  // gate/up launch's weighted split over the same groups (same routing, same grid), redone.
+  uint8_t* gpc = smem + L.gpc;
+  const bool use_gpc = a.mode == 1 && a.gu != nullptr && g_span <= kGInfoCache && a.gu_nt <= kGPcTiles;
+  for (int i = tid; use_gpc && tid < kGCT && i < g_span * a.gu_nt; i += kGCT) {  // consumer threads
+    const int gs = i / a.gu_nt, tg = i - gs * a.gu_nt;
+    const GroupInfo gg = group_info(a, groups, g_first + gs, n_active, 1);
+    const uint32_t ug = (uint32_t)(a.gu_nt * a.gu_kg);
+    const uint32_t ctot = ug * (uint32_t)(2 * a.T * a.topk + 3 * n_active + (a.has_shared ? wmax : 0));
+    const uint32_t gn = max(1u, min(gridDim.x, ctot / (uint32_t)wmax));
+    const uint32_t ct = ug * (uint32_t)gg.cu + (uint32_t)(tg * a.gu_kg * gg.w);
+    const uint32_t f = ct * gn / ctot, l = (ct + (uint32_t)((a.gu_kg - 1) * gg.w)) * gn / ctot;
+    gpc[gs * kGPcTiles + tg] = (uint8_t)min((uint32_t)a.gu_parts, l - f + 1u);
+  }
 
-  if (warp == kGCW + 1) {  // reducer: each segment's 12 warp partials, summed in warp order
+  if (warp > kGCW) {  // reducers: each tile piece's 12 warp partials, summed in warp order
+    const int rl = (warp - kGCW - 1) * 32 + lane;  // float4 column of the piece's rows
     __syncwarp();
-    named_sync(2, kGCT + 32);  // descriptors ready
+    named_sync(2, kGCT + 32 * kGRW);  // descriptors ready
     bool ok = true;
-    for (int sg = sg0; sg < sg1; ++sg) {
-      const int i = sg - sg0, buf = i & 1;
-      if (ok && !mbar_wait_bounded(&rfull[buf], (uint32_t)(i >> 1) & 1u, a.status)) ok = false;
+    for (int i = 0; i < npieces; ++i) {
+      const int buf = i & 1;
+      if (ok && !mbar_try_wait(&rfull[buf], (uint32_t)(i >> 1) & 1u) &&
+          !mbar_wait_bounded(&rfull[buf], (uint32_t)(i >> 1) & 1u, a.status))
+        ok = false;
       if (ok) {
-        int g, q, p, k0, k1;
-        seg_units(sg, g, q, p, k0, k1);
-        const GroupInfo gi = (g - g_first < kGInfoCache) ? ginfo[g - g_first] : group_info(a, groups, g, n_active);
-        const float* rb = red + (size_t)buf * kGCW * kGMaxRows * 128;
-        float* outp = a.out + (int64_t)p * a.out_pstride;
-        for (int e = lane; e < gi.m * 128; e += 32) {
-          float v = 0.0f;
+        const int tile = t0 + i, g = tile / NT, q = tile - g * NT;
+        const GroupInfo gi = (g - g_first < kGInfoCache) ? ginfo[g - g_first] : group_info(a, groups, g, n_active, UG);
+        const uint32_t ct = gi.cbase + (uint32_t)((tile - g * NT) * KG * gi.w);  // cost before the tile
+        const int part = (int)(b - ct * G / Ctot);
+        const bool last = (ct + (uint32_t)((KG - 1) * gi.w)) * G / Ctot == b;
+        const int pend = last ? a.P : part + 1;  // the tile's last piece zeroes the parts after it
+        if (part >= a.P && lane == 0) atomicExch(a.status, kStatusUnsupported);  // more pieces than parts
+        const float4* rb = reinterpret_cast<const float4*>(red + (size_t)buf * kGCW * kGMaxRows * 128);
+        for (int e4 = rl; part < a.P && e4 < gi.m * 32; e4 += 32 * kGRW) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int w2 = 0; w2 < kGCW; ++w2) v += rb[w2 * kGMaxRows * 128 + e];
-          const int64_t n = (int64_t)q * 128 + (e & 127);
-          if (n < a.n) outp[(int64_t)gi.out_row[e >> 7] * a.ldo + n] = v * gi.ts;
+          for (int w2 = 0; w2 < kGCW; ++w2) {
+            const float4 x = rb[w2 * kGMaxRows * 32 + e4];
+            v.x += x.x;
+            v.y += x.y;
+            v.z += x.z;
+            v.w += x.w;
+          }
+          v = make_float4(v.x * gi.ts, v.y * gi.ts, v.z * gi.ts, v.w * gi.ts);
+          const int64_t n = (int64_t)q * 128 + (e4 & 31) * 4;
+          float* o = a.out + (int64_t)gi.out_row[e4 >> 5] * a.ldo + n;
+          for (int p = part; p < pend; ++p) {
+            const float4 x = p == part ? v : make_float4(0.f, 0.f, 0.f, 0.f);
+            float* op = o + (int64_t)p * a.out_pstride;
+            if (n + 3 < a.n) {
+              *reinterpret_cast<float4*>(op) = x;
+            } else {
+              if (n < a.n) op[0] = x.x;
+              if (n + 1 < a.n) op[1] = x.y;
+              if (n + 2 < a.n) op[2] = x.z;
+            }
+          }
         }
       }
       __syncwarp();
@@ -317,109 +500,115 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
     lut[2 * tid] = v.x;
     lut[2 * tid + 1] = v.y;
   }
-  named_sync(2, kGCT + 32);  // descriptors ready (consumers and reducer)
-  // Stage the input rows over all of K.  Mode 0: every token row of x.  Mode 1: the rows of
-  // the groups this CTA touches (all rows if it touches more than kGInfoCache groups), each
-  // computed as h = bf16( silu(g) * u ) from the fp32 gate/up outputs (their parts summed).
-  const bool by_group = a.mode == 1 && g_span <= kGInfoCache;
-  const int nslot = by_group ? g_span * kGMaxRows : a.nrows;
-  for (int it = tid; it < nslot * KG * 4; it += kGCT) {
-    const int kq = it & 3, sl = (it >> 2) % KG, slot = (it >> 2) / KG;
-    int row = slot;
-    if (by_group) {
+  named_sync(2, kGCT + 32 * kGRW);  // descriptors ready (consumers and reducers)
+  // Stage the input rows over all of K (mode 0 routed here: staged during the routing).
+  // Mode 1: the rows of the groups this CTA touches (all rows if it touches more than
+  // kGInfoCache groups).
+  if (a.mode == 0) {
+    if (!routed) stage_tokens(tid, kGCT);
+  } else if (g_span <= kGInfoCache) {
+    for (int it = tid; it < g_span * kGMaxRows * KG * 4; it += kGCT) {
+      const int kq = it & 3, sl = (it >> 2) % KG, slot = (it >> 2) / KG;
       const GroupInfo& gs = ginfo[slot / kGMaxRows];
       if (slot % kGMaxRows >= gs.m) continue;
-      row = gs.in_row[slot % kGMaxRows];
-    }
-    const int64_t k0 = (int64_t)sl * 64 + kq * 16;
-    uint32_t u[8];
-    if (k0 >= a.k) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) u[i] = 0;
-    } else if (a.gu == nullptr) {  // bf16 rows of x (mode 0) or of h (mode 1, staged calls)
-      const uint4* src = reinterpret_cast<const uint4*>(a.x + (int64_t)row * a.ldx + k0);
-      const uint4 r0 = src[0], r1 = src[1];
-      u[0] = r0.x; u[1] = r0.y; u[2] = r0.z; u[3] = r0.w;
-      u[4] = r1.x; u[5] = r1.y; u[6] = r1.z; u[7] = r1.w;
-    } else {
-      const float* gp = a.gu + (int64_t)row * a.ldg + k0;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        float4 g4 = __ldcg(reinterpret_cast<const float4*>(gp) + q4);
-        float4 u4 = __ldcg(reinterpret_cast<const float4*>(gp + a.k) + q4);
-        for (int pp = 1; pp < a.gu_parts; ++pp) {
-          const float4 gx = __ldcg(reinterpret_cast<const float4*>(gp + pp * a.gu_pstride) + q4);
-          const float4 ux = __ldcg(reinterpret_cast<const float4*>(gp + pp * a.gu_pstride + a.k) + q4);
-          g4.x += gx.x; g4.y += gx.y; g4.z += gx.z; g4.w += gx.w;
-          u4.x += ux.x; u4.y += ux.y; u4.z += ux.z; u4.w += ux.w;
-        }
-        u[2 * q4] = swiglu_bf16x2(g4.x, u4.x, g4.y, u4.y);
-        u[2 * q4 + 1] = swiglu_bf16x2(g4.z, u4.z, g4.w, u4.w);
+      int npg = a.gu_parts, npu = a.gu_parts;
+      if (use_gpc) {
+        const int k0 = sl * 64 + kq * 16;
+        const uint8_t* pc = gpc + (slot / kGMaxRows) * kGPcTiles;
+        npg = k0 < a.k ? pc[k0 / 128] : 1;
+        npu = k0 < a.k ? pc[(a.k + k0) / 128] : 1;
       }
+      stage_item(gs.in_row[slot % kGMaxRows], sl, kq, npg, npu);
     }
-    const float4 z = stage_quarter<FMT>(u, xs + (size_t)(row * KG + sl) * 32 + kq * 8);
-    reinterpret_cast<float4*>(sums)[(size_t)(row * KG + sl) * 4 + kq] = z;
+  } else {
+    for (int it = tid; it < a.nrows * KG * 4; it += kGCT) {
+      const int j = it >> 2, row = j / KG;
+      stage_item(row, j - row * KG, it & 3, a.gu_parts, a.gu_parts);
+    }
   }
   named_sync(1, kGCT);
 
-  const int ug = warp >> 2, kq = warp & 3;
+  // Warp w takes unit w / 2 of every chunk, quarters 2 (w % 2) and 2 (w % 2) + 1 of it,
+  // accumulating one tile piece at a time; a piece's partial goes to the reducer once the
+  // warp's chunks have moved past it (zeros for a piece it had no unit of).
+  const int ug = warp >> 1, kh = warp & 1;
   bool ok = true;
   int s = 0;
   uint32_t ph = 0;
-  for (int sg = sg0; sg < sg1; ++sg) {
-    int g, q, p, k0, k1;
-    seg_units(sg, g, q, p, k0, k1);
-    const GroupInfo gi = (g - g_first < kGInfoCache) ? ginfo[g - g_first] : group_info(a, groups, g, n_active);
-    float acc[4][kGMaxRows];
+  int cur = 0;  // the piece being accumulated
+  float acc[4][kGMaxRows];
+#pragma unroll
+  for (int rt = 0; rt < 4; ++rt)
+#pragma unroll
+    for (int m = 0; m < kGMaxRows; ++m) acc[rt][m] = 0.0f;
+  auto flush = [&](int i) {
+    const int buf = i & 1;
+    if (i >= 2 && ok && !mbar_wait_bounded(&rempty[buf], (uint32_t)((i >> 1) - 1) & 1u, a.status)) ok = false;
+    float* rb = red + ((size_t)buf * kGCW + warp) * kGMaxRows * 128;
 #pragma unroll
     for (int rt = 0; rt < 4; ++rt)
 #pragma unroll
-      for (int m = 0; m < kGMaxRows; ++m) acc[rt][m] = 0.0f;
-    const uint32_t* xr[kGMaxRows];
-    const float* zr[kGMaxRows];
-    for (int kc = k0; kc < k1; kc += kGC) {
-      if (ok && !mbar_wait_bounded(&full[s], ph, a.status)) ok = false;
-      const int kg = kc + ug;
-      if (ok && kg < k1) {
-        const int ul = q * KG + kg;  // unit within the group
-        const uint8_t* st = stages + (size_t)s * SBY;
-        const int l0 = q * KG + kc;  // first unit of this chunk
-        const uint8_t* aux = st + kGC * (SG::CODE + SG::SCALE) + ((ul >> 2) - (l0 >> 2)) * SG::AUX;
-#pragma unroll
-        for (int m = 0; m < kGMaxRows; ++m) {
-          xr[m] = xs + (size_t)(gi.in_row[m] * KG + kg) * 32 + kq * 8;
-          zr[m] = sums + ((size_t)(gi.in_row[m] * KG + kg) * 4 + kq) * 4;
-        }
-        const uint8_t* cst = st + ug * SG::CODE;
-        const uint8_t* sst = st + kGC * SG::CODE + ug * SG::SCALE;
-        switch (gi.m) {
-          case 1: consume<FMT, 1, kGMaxRows>(cst, sst, aux, xr, zr, lut, kq, lane, acc); break;
-          case 2: consume<FMT, 2, kGMaxRows>(cst, sst, aux, xr, zr, lut, kq, lane, acc); break;
-          case 3: consume<FMT, 3, kGMaxRows>(cst, sst, aux, xr, zr, lut, kq, lane, acc); break;
-          default: consume<FMT, 4, kGMaxRows>(cst, sst, aux, xr, zr, lut, kq, lane, acc); break;
-        }
+      for (int m = 0; m < kGMaxRows; ++m) {
+        if (ok) rb[m * 128 + rt * 32 + lane] = acc[rt][m];  // after a timed-out wait: leave it
+        acc[rt][m] = 0.0f;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-      if (++s == S) {
-        s = 0;
-        ph ^= 1u;
-      }
-    }
-    // Hand the warp's partial to the reducer (two buffers: the warps run on into the next
-    // segment while the reducer sums this one).
-    const int i = sg - sg0, buf = i & 1;
-    if (i >= 2 && ok && !mbar_wait_bounded(&rempty[buf], (uint32_t)((i >> 1) - 1) & 1u, a.status)) ok = false;
-    float* rb = red + ((size_t)buf * kGCW + warp) * kGMaxRows * 128;
-    if (ok) {  // after a timed-out wait the reducer may still read this buffer: leave it
-#pragma unroll
-      for (int rt = 0; rt < 4; ++rt)
-#pragma unroll
-        for (int m = 0; m < kGMaxRows; ++m) rb[m * 128 + rt * 32 + lane] = acc[rt][m];
-    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&rfull[buf]);
+  };
+  // One loop per run of chunks of a group, compiled for the group's row count: the loop the
+  // warps spin in holds one consume variant, so it stays in the instruction cache.
+  ChunkIter it;
+  chunk_first(it, u0, u1, UG);
+  while (it.c0 < u1) {
+    const int g = it.g;
+    const GroupInfo gi = (g - g_first < kGInfoCache) ? ginfo[g - g_first] : group_info(a, groups, g, n_active, UG);
+    auto run = [&](auto rows) {
+      constexpr int M = decltype(rows)::value;
+      for (; it.c0 < u1 && it.g == g; chunk_next(it, u1, UG)) {
+        // Hand over every piece before this warp's unit (or before the chunk, without one)
+        // before waiting for the chunk: a warp with no unit for a while must not hold back
+        // the reducers, which the other warps wait for.
+        const int uw = it.c0 + ug;
+        const int tile = (uw < it.c1 ? uw : it.c0) / KG;
+        while (cur < tile - t0) flush(cur++);
+        if (ok && !mbar_try_wait(&full[s], ph) && !mbar_wait_bounded(&full[s], ph, a.status)) ok = false;
+        if (ok && uw < it.c1) {
+          const int l = uw - g * UG, l0 = it.c0 - g * UG;  // units within the group
+          const int kg = uw - tile * KG;
+          const uint8_t* st = stages + (size_t)s * SBY;
+          const uint8_t* cst = st + ug * SG::CODE;
+          const uint8_t* sst = st + kGC * SG::CODE + ug * SG::SCALE;
+          const uint8_t* aux = st + kGC * (SG::CODE + SG::SCALE) + ((l >> 2) - (l0 >> 2)) * SG::AUX;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int kq = 2 * kh + h;
+            const uint32_t* xr[kGMaxRows];
+            const float* zr[kGMaxRows];
+#pragma unroll
+            for (int m = 0; m < kGMaxRows; ++m) {
+              const int r = gi.in_row[m < M ? m : 0];
+              xr[m] = xs + (size_t)(r * KG + kg) * 32 + kq * 8;
+              zr[m] = sums + ((size_t)(r * KG + kg) * 4 + kq) * 4;
+            }
+            consume<FMT, M, kGMaxRows>(cst, sst, aux, xr, zr, lut, kq, lane, acc);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    };
+    switch (gi.m) {
+      case 1: run(std::integral_constant<int, 1>{}); break;
+      case 2: run(std::integral_constant<int, 2>{}); break;
+      case 3: run(std::integral_constant<int, 3>{}); break;
+      default: run(std::integral_constant<int, 4>{}); break;
+    }
   }
+  while (cur < npieces) flush(cur++);
   // the reducer still reads red: it returns on its own; nothing here waits for it
 }
 
@@ -528,14 +717,14 @@ int grouped_stage_bytes(int fmt) {
 }
 }  // namespace
 
-// Input parts of a decode GEMV: the fewest that give every CTA about four whole segments
-// (group, row tile, part) at the most groups the routing can produce, so equal shares of
-// whole segments stay balanced; parts are whole chunks of kGC units, so at most one part
-// per row tile -- the last -- leaves warps idle in its last chunk.
-static int grouped_parts(int64_t max_groups, int64_t nt, int64_t kg, int sms) {
-  const int64_t nck = (kg + kGC - 1) / kGC;
-  int64_t p = (4 * (int64_t)sms + max_groups * nt - 1) / (max_groups * nt);
-  return (int)std::max<int64_t>(1, std::min<int64_t>(p, nck));
+// Output parts of a decode GEMV: the most CTA shares one row tile of kg units can meet.  A
+// share spans at least Ctot / grid of cost, a tile at most kg * unit_cost(T); the least total
+// cost the routing can produce is that of topk groups (a token's experts are distinct) holding
+// all T * topk rows: nt * kg * (2 T topk + 3 topk).
+static int grouped_parts(int64_t T, int64_t topk, int64_t nt, int64_t kg, int grid) {
+  const int64_t cmin = nt * kg * (2 * T * topk + 3 * topk);
+  const int64_t span = kg * unit_cost((int)T) * grid;  // tile cost x grid
+  return (int)std::min<int64_t>(kg, (span + cmin - 1) / cmin + 1);
 }
 
 MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, int topk, int grid) {
@@ -550,9 +739,8 @@ MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, i
   // the prefill chain (more than kGMaxRows tokens) fuses the mid into the gate/up GEMM and
   // needs no fp32 gate/up rows; its down outputs are one part
   const bool decode = T <= kGMaxRows;
-  const int64_t max_groups = std::min<int64_t>(E, T * topk) + T;
-  L.p_gu = decode ? grouped_parts(max_groups, gu.nt, gu.kg, grid) : 1;
-  L.p_dn = decode ? grouped_parts(max_groups, dn.nt, dn.kg, grid) : 1;
+  L.p_gu = decode ? grouped_parts(T, topk, gu.nt, gu.kg, grid) : 1;
+  L.p_dn = decode ? grouped_parts(T, topk, dn.nt, dn.kg, grid) : 1;
   L.ld_gu = (gu.n + 7) / 8 * 8;
   L.pst_gu = R * L.ld_gu;
   L.gu = take(decode ? (size_t)L.p_gu * R * L.ld_gu * 4 : 0);
@@ -607,6 +795,10 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
                       void* out, int64_t ldo, void* ws, const DeviceInfo& dev, void* stream, int stage,
                       const float* logits, int32_t* topk_ids_out, float* topk_w_out) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the grouped GEMV splits work by cost in 32-bit arithmetic: (cost of every unit) x CTAs
+  const int64_t cu_max = 2 * T * topk + 3 * std::min<int64_t>(m->n_experts, T * topk) + unit_cost((int)T) + 1;
+  for (const Geometry* g : {&gu, &dn})
+    if (g->nt * g->kg * cu_max * dev.sms >= ((int64_t)1 << 32)) return QG_ERR_UNSUPPORTED;
   const RouteView rv = route_view(const_cast<void*>(route_ws), T, m->n_experts, topk);
   const MoeLayout L = moe_layout(gu, dn, T, m->n_experts, topk, dev.sms);
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -692,6 +884,8 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
     d.ldg = L.ld_gu;
     d.gu_parts = L.p_gu;
     d.gu_pstride = L.pst_gu;
+    d.gu_nt = (int)gu.nt;
+    d.gu_kg = (int)gu.kg;
   }
   d.out = reinterpret_cast<float*>(w + L.d);
   d.ldo = L.ld_d;

@@ -47,11 +47,15 @@ __device__ __forceinline__ void lane_best(const uint32_t (&key)[16], uint32_t& b
 }
 
 // Warp-level top-k of one token's logits (E <= 512): lane l holds the keys of logits l,
-// l+32, ... (16 registers; the expert of slot i is l + 32 i).  Each of k rounds takes the
-// warp maximum of the lanes' best keys and the warp minimum of the experts holding it (two
-// single-instruction warp reductions); the winner's lane clears that slot and finds its
-// next best.  Lane j keeps the j-th winner and the k lanes compute the softmax over the kept
-// logits in parallel.
+// l+32, ... (16 registers; the expert of slot i is l + 32 i).  Each lane first extracts its
+// three best keys in order (ties to the lower slot, i.e. the lower expert).  Each of k rounds
+// then takes the warp maximum of the lanes' current heads and the warp minimum of the experts
+// holding it (two single-instruction warp reductions), and the winner's lane steps to its
+// next key with three selects -- no search on the rounds' serial path.  A lane that has won
+// three times before the last round has no extracted key left: the rounds are then redone
+// from all 16 keys, the winner's lane searching its next best each time (the same result,
+// only slower; the fast rounds never pick a wrong key before that point).  Lane
+// j keeps the j-th winner and the k lanes compute the softmax over the kept logits in parallel.
 __device__ __forceinline__ void warp_topk(const float* lg, int E, int k, int32_t* ids, float* wts, int* ids_copy = nullptr) {
   const int lane = threadIdx.x & 31;
   uint32_t key[16];
@@ -60,23 +64,61 @@ __device__ __forceinline__ void warp_topk(const float* lg, int E, int k, int32_t
     const int e = lane + 32 * i;
     key[i] = e < E ? order_key(lg[e]) : 0u;
   }
-  uint32_t bk;
-  int bi;
-  lane_best(key, bk, bi);
+  uint32_t h0, h1, h2;  // the lane's three best keys, descending, and their experts
+  int e0, e1, e2;
+  {
+    uint32_t kk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) kk[i] = key[i];
+    int bi;
+    lane_best(kk, h0, bi);
+    e0 = lane + 32 * bi;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) kk[i] = (i == bi) ? 0u : kk[i];
+    lane_best(kk, h1, bi);
+    e1 = lane + 32 * bi;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) kk[i] = (i == bi) ? 0u : kk[i];
+    lane_best(kk, h2, bi);
+    e2 = lane + 32 * bi;
+  }
   uint32_t mine = 0u, top = 0u;
-  int mine_id = 0;
+  int mine_id = 0, taken = 0;
+  bool short_of_keys = false;
   for (int j = 0; j < k; ++j) {
-    const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, bk);
-    const int win = (int)__reduce_min_sync(0xFFFFFFFFu, bk == kmax ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
+    const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, h0);
+    const int win = (int)__reduce_min_sync(0xFFFFFFFFu, h0 == kmax ? (uint32_t)e0 : 0xFFFFFFFFu);
     if (j == 0) top = kmax;
     if (lane == j) {
       mine = kmax;
       mine_id = win;
     }
-    if ((win & 31) == lane) {  // the winner's lane takes the slot out and finds its next best
+    const bool w = (win & 31) == lane;
+    taken += w;
+    short_of_keys |= taken == 3 && j + 1 < k;  // its head is now empty though rounds remain
+    h0 = w ? h1 : h0;
+    e0 = w ? e1 : e0;
+    h1 = w ? h2 : h1;
+    e1 = w ? e2 : e1;
+    h2 = w ? 0u : h2;
+  }
+  if (__any_sync(0xFFFFFFFFu, short_of_keys)) {  // a lane may have needed a fourth key: redo from all 16
+    uint32_t bk;
+    int bi;
+    lane_best(key, bk, bi);
+    for (int j = 0; j < k; ++j) {
+      const uint32_t kmax = __reduce_max_sync(0xFFFFFFFFu, bk);
+      const int win = (int)__reduce_min_sync(0xFFFFFFFFu, bk == kmax ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
+      if (j == 0) top = kmax;
+      if (lane == j) {
+        mine = kmax;
+        mine_id = win;
+      }
+      if ((win & 31) == lane) {  // the winner's lane takes the slot out and finds its next best
 #pragma unroll
-      for (int i = 0; i < 16; ++i) key[i] = (i == (win >> 5)) ? 0u : key[i];
-      lane_best(key, bk, bi);
+        for (int i = 0; i < 16; ++i) key[i] = (i == (win >> 5)) ? 0u : key[i];
+        lane_best(key, bk, bi);
+      }
     }
   }
   // softmax over the k kept logits (descending order), shifted by the largest
@@ -91,48 +133,94 @@ __device__ __forceinline__ void warp_topk(const float* lg, int E, int k, int32_t
   }
 }
 
-// Shared-memory scratch of route_decode_block.
+// Shared-memory scratch of route_decode_block: each token's experts as a bit set over the
+// (at most kMaxExperts) experts, their union in row kRouteTokens, and per row and 32-bit
+// word the number of set bits in the words before it.
+constexpr int kRouteTokens = 4;
+constexpr int kRouteWords = kMaxExperts / 32;
 struct BlockRouteSmem {
   int ids[kBlockRoutePairs];
   float wts[kBlockRoutePairs];
-  int rank[kBlockRoutePairs];   // pairs of the same expert before this one
+  uint32_t mask[kRouteTokens + 1][kRouteWords];
+  int before[kRouteTokens + 1][kRouteWords];
   int groups[kBlockRoutePairs * kGroupInts];
   int n_active;
 };
 
-// Routing of T tokens (P = T*k <= kBlockRoutePairs pairs) by one CTA: warps 0..T-1 take one
-// token each (warp_topk), then threads 0..P-1 place the pairs -- experts ascending, pairs
-// ascending within an expert -- by counting (P is small), not sorting.  Every CTA that calls
-// it builds the same group table in shared memory (sm.groups, kGroupInts ints per active
-// expert; returns the number of active experts).  The CTA with `write` set also stores the
-// router's outputs, the same values qmoe_route stores for these tokens: ids, wts, counts,
-// offsets, active, zidx, groups, tiles (one per active expert: a decode expert has at most
-// T < tile pairs), pair_list, pair_pos and meta.  Every thread of the CTA must call it.
+// Routing of T <= kRouteTokens tokens (P = T*k <= kBlockRoutePairs pairs) by one CTA: warps
+// 0..T-1 take one token each (warp_topk); then every pair is placed -- experts ascending,
+// pairs ascending within an expert -- from the tokens' expert bit sets, in constant work a
+// pair: a token's experts are distinct, so the pairs of expert e before pair (t, j) are the
+// tokens before t that chose e; the pairs of smaller experts are the set bits below e of
+// every token; the active experts below e, the set bits below e of the union.  Every CTA
+// that calls it builds the same group table in shared memory (sm.groups, kGroupInts ints per
+// active expert; returns the number of active experts).  The CTA with `write` set also
+// stores the router's outputs, the same values qmoe_route stores for these tokens: ids,
+// wts, counts, offsets, active, zidx, groups, tiles (one per active expert: a decode expert
+// has at most T < tile pairs), pair_list, pair_pos and meta.  Every thread of the CTA must
+// call it; the threads of warps T and above run `idle()` (work that does not depend on the
+// routing) while warps 0..T-1 take the top-k.
+template <class Idle>
 __device__ __forceinline__ int route_decode_block(const float* logits, int T, int E, int k, BlockRouteSmem& sm,
-                                                  bool write, int32_t* ids, float* wts, const RouteView& r) {
+                                                  bool write, int32_t* ids, float* wts, const RouteView& r,
+                                                  Idle&& idle) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const int P = T * k;
-  if (warp < T) warp_topk(logits + (int64_t)warp * E, E, k, sm.ids + warp * k, sm.wts + warp * k);
-  __syncthreads();
-  int e = -1, rank = 0, first = 0, cnt = 0;
-  if (tid < P) {
-    e = sm.ids[tid];
-    for (int q = 0; q < P; ++q) {
-      const int eq = sm.ids[q];
-      first += eq < e;
-      cnt += eq == e;
-      rank += (eq == e) && (q < tid);
+  constexpr int kRows = kRouteTokens + 1, kU = kRouteTokens;  // row kU: the union
+  if (tid < kRouteTokens * kRouteWords && tid / kRouteWords >= T) (&sm.mask[0][0])[tid] = 0u;  // no token
+  if (warp < T) {  // the token's top-k, then its expert set, one word a lane (warp reductions)
+    const int lane = tid & 31;
+    warp_topk(logits + (int64_t)warp * E, E, k, sm.ids + warp * k, sm.wts + warp * k);
+    __syncwarp();
+    const int ex = lane < k ? sm.ids[warp * k + lane] : -1;
+    uint32_t word = 0u;
+#pragma unroll
+    for (int w = 0; w < kRouteWords; ++w) {
+      const uint32_t v = __reduce_or_sync(0xFFFFFFFFu, (ex >> 5) == w ? 1u << (ex & 31) : 0u);
+      if (lane == w) word = v;
     }
-    sm.rank[tid] = rank;
+    if (lane < kRouteWords) sm.mask[warp][lane] = word;
+  } else {
+    idle();
   }
   __syncthreads();
-  int z = 0, n_active = 0;
+  int e = -1, t = 0;
   if (tid < P) {
-    for (int q = 0; q < P; ++q) {
-      const bool lead = sm.rank[q] == 0;  // the first pair of its expert
-      n_active += lead;
-      z += lead && sm.ids[q] < e;
+    e = sm.ids[tid];
+    t = tid / k;
+  }
+  if (tid < 3 * 32) {  // rows in half-warps: word prefix counts by an inclusive scan of 16
+    const int row = tid >> 4, w = tid & 15;
+    uint32_t bits = 0u;
+    if (row < kRouteTokens) {
+      bits = sm.mask[row][w];
+    } else if (row == kU) {
+#pragma unroll
+      for (int tt = 0; tt < kRouteTokens; ++tt) bits |= sm.mask[tt][w];
+      sm.mask[kU][w] = bits;
     }
+    const int v = __popc(bits);
+    int sc = v;
+#pragma unroll
+    for (int d = 1; d < 16; d <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, sc, d, 16);
+      if (w >= d) sc += n;
+    }
+    if (row < kRows) sm.before[row][w] = sc - v;
+  }
+  __syncthreads();
+  int rank = 0, first = 0, cnt = 0, z = 0;
+  if (tid < P) {
+    const int w = e >> 5, b = e & 31;
+    const uint32_t low = (1u << b) - 1u;
+    for (int tt = 0; tt < T; ++tt) {
+      const uint32_t mw = sm.mask[tt][w];
+      const int bit = (int)((mw >> b) & 1u);
+      cnt += bit;
+      rank += tt < t ? bit : 0;
+      first += sm.before[tt][w] + __popc(mw & low);
+    }
+    z = sm.before[kU][w] + __popc(sm.mask[kU][w] & low);
     if (rank == 0) {
       int* g = sm.groups + z * kGroupInts;
       g[0] = e;
@@ -140,9 +228,9 @@ __device__ __forceinline__ int route_decode_block(const float* logits, int T, in
       g[2] = cnt;
       g[3] = 0;
     }
-    if (rank < kGroupRows) sm.groups[z * kGroupInts + 4 + rank] = tid / k;
-    if (tid == 0) sm.n_active = n_active;
+    if (rank < kGroupRows) sm.groups[z * kGroupInts + 4 + rank] = t;
   }
+  const int n_active = sm.before[kU][kRouteWords - 1] + __popc(sm.mask[kU][kRouteWords - 1]);
   __syncthreads();
   if (write) {
     if (tid < P) {
@@ -159,24 +247,27 @@ __device__ __forceinline__ int route_decode_block(const float* logits, int T, in
         r.tiles[3 * z + 2] = cnt;
         reinterpret_cast<int4*>(r.groups + (size_t)z * kGroupInts)[0] = make_int4(e, first, cnt, 0);
       }
-      if (rank < kGroupRows) r.groups[(size_t)z * kGroupInts + 4 + rank] = tid / k;
+      if (rank < kGroupRows) r.groups[(size_t)z * kGroupInts + 4 + rank] = t;
     }
-    for (int x = tid; x < E; x += blockDim.x) {
+    for (int x = tid; x < E; x += blockDim.x) {  // pairs of expert x, and of the experts below it
+      const int w = x >> 5, b = x & 31;
+      const uint32_t low = (1u << b) - 1u;
       int c = 0, f = 0;
-      for (int q = 0; q < P; ++q) {
-        c += sm.ids[q] == x;
-        f += sm.ids[q] < x;
+      for (int tt = 0; tt < T; ++tt) {
+        const uint32_t mw = sm.mask[tt][w];
+        c += (int)((mw >> b) & 1u);
+        f += sm.before[tt][w] + __popc(mw & low);
       }
       r.counts[x] = c;
       r.offsets[x] = f;
     }
     if (tid == 0) {
       r.offsets[E] = P;
-      r.meta[0] = sm.n_active;
-      r.meta[1] = sm.n_active;
+      r.meta[0] = n_active;
+      r.meta[1] = n_active;
     }
   }
-  return sm.n_active;
+  return n_active;
 }
 
 }  // namespace qg

@@ -11,6 +11,7 @@ namespace qg {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kStatusTimeout = 6;                           // QG_ERR_TIMEOUT
+constexpr int kStatusUnsupported = 2;                       // QG_ERR_UNSUPPORTED
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -71,6 +72,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
       return false;
     }
   }
+}
+
+// L2 policy for data read once per call (streamed weights): evict first, so the stream does
+// not push the hot lines -- activations, workspace, router tables, kernel code -- out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 1-D bulk copy global -> shared with an L2 cache policy, completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol) : "memory");
 }
 
 // 1-D bulk copy global -> shared (CTA-local destination), completion counted on `bar`.

@@ -59,6 +59,76 @@ def test_route_ties_go_to_lower_index(q):
     assert np.allclose(w.cpu().numpy(), rp, rtol=2e-6, atol=1e-7)
 
 
+def _clustered_logits(t, e, k, seed):
+    """Router logits whose winners crowd into few residues mod 32 (experts e, e+32, e+64, ...),
+    the ones a warp-wide top-k that gives each lane the experts of one residue finds hardest:
+    token 0 has all k winners on one residue, token 1 three on one residue and the rest on
+    another, token 2 exactly three on one residue (k = 3 case) and token 3 ties on one
+    residue."""
+    rng = np.random.default_rng(seed)
+    lg = rng.standard_normal((t, e)).astype(np.float32)
+    lane = 5
+    same = [lane + 32 * i for i in range(e // 32)]
+    for i, ex in enumerate(same[:k]):
+        lg[0, ex] = 10.0 - 0.5 * i
+    if t > 1:
+        for i, ex in enumerate(same[:3]):
+            lg[1, ex] = 9.0 - i
+        for i in range(k - 3):
+            lg[1, 17 + 32 * (i % (e // 32))] = 5.0 - 0.25 * i + (0.01 if i >= e // 32 else 0.0) * i
+    if t > 2:
+        lg[2, same[:3]] = [8.0, 7.5, 7.25]
+    if t > 3:
+        lg[3, same[: min(k + 2, len(same))]] = 3.0  # ties: lower experts first
+    return lg
+
+
+@pytest.mark.parametrize("t,e,k", [(4, 512, 10), (4, 512, 4), (3, 512, 3), (4, 128, 6), (2, 64, 4)])
+def test_route_winners_on_one_residue(q, t, e, k):
+    """Top-k whose winners share a residue mod 32: ids equal to the oracle's, weights within
+    rounding, for the router launch and for the router inside the decode chain's gate/up
+    launch (same ids and weights byte for byte)."""
+    lg = _clustered_logits(t, e, k, seed=700 + t + e + k)
+    lt = torch.from_numpy(np.ascontiguousarray(lg)).cuda()
+    ids, w, _ = q.route(lt, k)
+    torch.cuda.synchronize()
+    rid, rp = oracle.route(lg, k)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.allclose(w.cpu().numpy(), rp, rtol=2e-6, atol=1e-7)
+    H, F = 256, 128
+    layer = wl.moe_layer(wl.MXFP4, e, H, F, seed=701, shared=False)
+    pm = q.PackedMoE(layer)
+    xd = dev_bf16(wl.moe_tokens(t, H, seed=702))
+    _, ids_b, w_b, _ = q.moe_forward(pm, xd, lt, k)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids_b) and torch.equal(w, w_b)
+
+
+@pytest.mark.parametrize("fmt,e,h,f,k,shared", [(wl.MXFP4, 16, 256, 128, 4, True), (wl.NVFP4, 64, 1024, 512, 10, True),
+                                                 (wl.Q6K, 8, 512, 256, 1, False), (wl.MLX_AFFINE4_G64, 32, 256, 384, 2, True),
+                                                 (wl.MXFP4, 64, 2048, 512, 10, True)])
+def test_moe_decode_tokens_share_experts(q, fmt, e, h, f, k, shared):
+    """Four tokens that all chose the same experts (the fewest groups, so the longest row-tile
+    splits over CTAs and the most output parts): the decode chain against the oracle, and the
+    routed and pre-routed chains byte for byte."""
+    t = 4
+    layer = wl.moe_layer(fmt, e, h, f, seed=720 + k, shared=shared)
+    x = wl.moe_tokens(t, h, seed=721)
+    lg = np.repeat(wl.router_logits(1, e, seed=722), t, axis=0)
+    lg[2] *= 0.5  # the same ranking, other weights
+    pm = q.PackedMoE(layer)
+    xd, lt = dev_bf16(x), torch.from_numpy(np.ascontiguousarray(lg)).cuda()
+    ids, w, rws = q.route(lt, k)
+    out_a = q.moe_ffn(pm, xd, w, rws)
+    out_b, ids_b, w_b, _ = q.moe_forward(pm, xd, lt, k)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids_b) and torch.equal(w, w_b)
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    ref = oracle.moe_forward(layer, x, lg, k)
+    err = np.abs(to_f64(out_b) - ref)
+    assert np.all(err <= moe_tolerance(oracle, layer, x, lg, k, ref))
+
+
 @pytest.mark.parametrize("fmt", [wl.MXFP4, wl.NVFP4, wl.MLX_AFFINE4_G64, wl.Q6K])
 @pytest.mark.parametrize("t", [1, 2, 4])
 def test_moe_decode_small(q, fmt, t):
