@@ -327,6 +327,7 @@ __global__ void __launch_bounds__(gemv_warps(FMT, M) * 32 + 32, 1) gemv_kernel(c
   const int nch = (int)((len + C - 1) / C);
   if (warp == kCW) {  // producer: stream chunks of whole tiles into the ring
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first();  // each weight is read once per call
       int s = 0;
       uint32_t ph = 0;
       uint32_t ua = uu0;
@@ -347,10 +348,11 @@ __global__ void __launch_bounds__(gemv_warps(FMT, M) * 32 + 32, 1) gemv_kernel(c
           bytes += aux_n * SG::AUX;
         }
         mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s(dst, a.codes + (size_t)ua * SG::CODE, nu * SG::CODE, &full[s]);
-        bulk_g2s(dst + C * SG::CODE, a.scales + (size_t)ua * SG::SCALE, nu * SG::SCALE, &full[s]);
+        bulk_g2s_hint(dst, a.codes + (size_t)ua * SG::CODE, nu * SG::CODE, &full[s], pol);
+        bulk_g2s_hint(dst + C * SG::CODE, a.scales + (size_t)ua * SG::SCALE, nu * SG::SCALE, &full[s], pol);
         if (SG::AUX)
-          bulk_g2s(dst + C * (SG::CODE + SG::SCALE), a.aux + (size_t)aux_a * SG::AUX, aux_n * SG::AUX, &full[s]);
+          bulk_g2s_hint(dst + C * (SG::CODE + SG::SCALE), a.aux + (size_t)aux_a * SG::AUX, aux_n * SG::AUX, &full[s],
+                        pol);
         ua = ub;
         if (++s == S) {
           s = 0;
