@@ -319,9 +319,19 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
                                     if (warp < kGCW) stage_tokens(tid - 32 * a.T, kGCT - 32 * a.T);
                                   });
     groups = rs.groups;
-  } else {
-    n_active = a.meta[0];
-    groups = a.groups;
+  } else {  // the router's group table into shared memory, every entry it can hold at once
+    BlockRouteSmem& rs = *reinterpret_cast<BlockRouteSmem*>(smem + L.route);
+    const int nmax = min(a.E, a.T * a.topk);  // <= kBlockRoutePairs for 1..4 tokens
+    if (tid < nmax) {
+      const int4* src = reinterpret_cast<const int4*>(a.groups + (size_t)tid * kGroupInts);
+      int4* dst = reinterpret_cast<int4*>(rs.groups + tid * kGroupInts);
+      dst[0] = src[0];
+      dst[1] = src[1];
+    }
+    if (tid == 0) rs.n_active = a.meta[0];
+    __syncthreads();
+    n_active = rs.n_active;
+    groups = rs.groups;
   }
 
   // The unit range of this CTA: units (group, row tile, 64-input group) in that order, an
@@ -506,6 +516,63 @@ __global__ void __launch_bounds__(kGThreads, 1) grouped_gemv_kernel(const Groupe
   // kGInfoCache groups).
   if (a.mode == 0) {
     if (!routed) stage_tokens(tid, kGCT);
+  } else if (g_span <= kGInfoCache && a.gu != nullptr) {
+    // h = bf16( silu(g) * u ) of the groups' rows, four features a thread item (every thread
+    // busy however few rows), written as bf16 into the rows' staging slots; then each
+    // 16-input quarter is staged in place.
+    int nsr = 0;  // staged rows: the rows of the CTA's groups, in group order
+    for (int gs = 0; gs < g_span; ++gs) nsr += ginfo[gs].m;
+    auto row_of = [&](int r, int& gs) {
+      gs = 0;
+      while (r >= ginfo[gs].m) r -= ginfo[gs++].m;
+      return ginfo[gs].in_row[r];
+    };
+    const int F4 = KG * 16;  // float4 columns of a row padded to whole 64-input groups
+    const int64_t ps = a.gu_pstride / 4;
+    for (int it = tid; it < nsr * F4; it += kGCT) {
+      const int r = it / F4, c4 = it - r * F4, f = 4 * c4;
+      int gs;
+      const int row = row_of(r, gs);
+      uint2 hv = make_uint2(0u, 0u);
+      if (f < a.k) {
+        int npg = a.gu_parts, npu = a.gu_parts;
+        if (use_gpc) {
+          npg = gpc[gs * kGPcTiles + f / 128];
+          npu = gpc[gs * kGPcTiles + (int)((a.k + f) / 128)];
+        }
+        const float4* gp = reinterpret_cast<const float4*>(a.gu + (int64_t)row * a.ldg + f);
+        const float4* up = reinterpret_cast<const float4*>(a.gu + (int64_t)row * a.ldg + a.k + f);
+        float4 g4 = __ldcg(gp), u4 = __ldcg(up);
+        float4 g1 = make_float4(0.f, 0.f, 0.f, 0.f), u1 = g1;
+        if (npg > 1) g1 = __ldcg(gp + ps);
+        if (npu > 1) u1 = __ldcg(up + ps);
+        if (npg > 1) { g4.x += g1.x; g4.y += g1.y; g4.z += g1.z; g4.w += g1.w; }
+        if (npu > 1) { u4.x += u1.x; u4.y += u1.y; u4.z += u1.z; u4.w += u1.w; }
+        for (int pp = 2; pp < max(npg, npu); ++pp) {  // more parts (few tiles, or one token)
+          if (pp < npg) {
+            const float4 x = __ldcg(gp + pp * ps);
+            g4.x += x.x; g4.y += x.y; g4.z += x.z; g4.w += x.w;
+          }
+          if (pp < npu) {
+            const float4 x = __ldcg(up + pp * ps);
+            u4.x += x.x; u4.y += x.y; u4.z += x.z; u4.w += x.w;
+          }
+        }
+        hv = make_uint2(swiglu_bf16x2(g4.x, u4.x, g4.y, u4.y), swiglu_bf16x2(g4.z, u4.z, g4.w, u4.w));
+      }
+      *reinterpret_cast<uint2*>(xs + (size_t)(row * KG + (f >> 6)) * 32 + ((f & 63) >> 1)) = hv;
+    }
+    named_sync(1, kGCT);
+    for (int it = tid; it < nsr * KG * 4; it += kGCT) {
+      const int r = it / (KG * 4), rem = it - r * (KG * 4);
+      int gs;
+      const int row = row_of(r, gs), sl = rem >> 2, kq = rem & 3;
+      uint32_t* dst = xs + (size_t)(row * KG + sl) * 32 + kq * 8;
+      const uint4 v0 = reinterpret_cast<const uint4*>(dst)[0], v1 = reinterpret_cast<const uint4*>(dst)[1];
+      const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      const float4 z = stage_quarter<FMT>(u, dst);
+      reinterpret_cast<float4*>(sums)[(size_t)(row * KG + sl) * 4 + kq] = z;
+    }
   } else if (g_span <= kGInfoCache) {
     for (int it = tid; it < g_span * kGMaxRows * KG * 4; it += kGCT) {
       const int kq = it & 3, sl = (it >> 2) % KG, slot = (it >> 2) / KG;
@@ -823,6 +890,7 @@ int launch_moe_decode(const qg_moe_layer* m, const Geometry& gu, const Geometry&
   a.KG = (int)gu.kg;
   a.T = (int)T;
   a.topk = topk;
+  a.E = m->n_experts;
   a.mode = 0;
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.ldx = ldx;
