@@ -290,8 +290,9 @@ size_t qmoe_workspace_size(const qg_moe_layer* layer, int64_t t, int topk);
  *   F..2F-1 of the expert's 2F x H gate/up weight.
  * 1..4 tokens (decode / speculative verify; TurboEXL3 article §4.2): three launches --
  *   gate/up as one grouped GEMV over the active experts that reads each expert's weights
- *   once for all its tokens, with the shared expert as extra groups; down, whose blocks
- *   compute the mid (h = bf16(silu(gate) * up)) while staging their inputs; finish.
+ *   once for all its tokens, with the shared expert as one more group of all the tokens;
+ *   down, whose blocks compute the mid (h = bf16(silu(gate) * up)) while staging their
+ *   inputs; finish.
  * More tokens (prefill; §4.1): three launches -- one grouped tensor-core GEMM over the
  *   router's tile table for gate/up whose epilogue runs the mid, the same GEMM for down,
  *   and the finish; the shared expert runs as extra tiles of both GEMMs.  Needs

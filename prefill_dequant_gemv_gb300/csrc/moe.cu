@@ -1,6 +1,6 @@
 // Mixture-of-experts layer for 1..4 tokens (decode and speculative verify), in the five
 // dependent launches of the TurboEXL3 article §4.2: route (route.cu), gate/up, mid, down,
-// finish.  The shared expert runs as extra groups of the routed gate/up and down launches
+// finish.  The shared expert runs as one more group of the routed gate/up and down launches
 // (as §4.2 runs it inside the routed launches).
 //
 //   gate/up  grouped GEMV: every active expert's 2F x H weights are read from HBM and
@@ -14,9 +14,10 @@
 //
 // The grouped GEMV runs the dense GEMV's decode (qg_gemv_core.cuh) over the units (group,
 // 128-row tile, 64 inputs) of groups = active experts (ascending), then the shared expert as
-// one group of all the tokens.  Each CTA takes an equal contiguous share of the units
-// (stream-K, so the CTAs finish together whatever the routing); its 12 consumer warps hand
-// each row tile's partials to a reducer warp (two buffers, so they run on).  A row tile cut
+// one group of all the tokens.  Each CTA takes a contiguous share of the units of equal cost
+// (stream-K weighted by unit_cost, so the CTAs finish together whatever the routing); its 12
+// consumer warps hand each row tile's partials to two reducer warps (two buffers, so they
+// run on).  A row tile cut
 // by a share boundary is written as one output part per CTA (parts past the last piece are
 // zero), and the parts are summed by whoever reads the output next, in part order.
 #include <cuda_runtime.h>
@@ -107,8 +108,9 @@ struct GroupedSmem {
 constexpr int kGPcTiles = 64;  // gate/up row tiles a pieces table covers
 
 // Shared memory: mbarriers (full[S], empty[S], rfull[2], rempty[2]), the stage ring, the
-// staged activations, two reduction buffers (one per segment in flight), the E4M3 table
-// and the descriptors of the first groups the CTA touches.
+// staged activations, two reduction buffers (one per tile piece in flight), the E4M3 table,
+// the descriptors of the first groups the CTA touches, the down launch's table of gate/up
+// parts per tile, and the routing scratch (group table).
 __host__ __device__ inline GroupedSmem grouped_smem(int stage_bytes, int S, int nrows, int KG) {
   GroupedSmem L;
   size_t o = 0;
