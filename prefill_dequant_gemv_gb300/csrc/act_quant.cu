@@ -25,6 +25,8 @@
 // (exact ties and their neighbours among them) are divided exactly, as are an infinite or
 // NaN q' (a reciprocal that overflowed: low mantissa bits zero).  When den is a normal
 // power of two (or 0, where q' = x * 0 as q), q' is already the correctly rounded quotient.
+// The codes themselves come from the hardware's nearest-even E2M1 conversion, four
+// instructions for eight values; the bf16 expansion is computed only when it is asked for.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
@@ -77,11 +79,29 @@ __device__ __forceinline__ bool near_decision(float q) {
   return ((__float_as_uint(q) + 8u) & 0x1FFFFFu) <= 16u;
 }
 
+// E2M1 codes of eight values q[0..7] as one word (value i in bits 4i..4i+3), by the
+// hardware conversion: round to nearest even on the E2M1 grid, saturating at 6, the sign
+// kept -- the same decision e2m1_code takes for every number (NaN excepted: the caller
+// takes e2m1_code for a block with a NaN quotient).
+__device__ __forceinline__ uint32_t e2m1x8_cvt(const float* q) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n\t"
+      "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
+      : "=r"(w)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return w;
+}
+
 // fp32 bits of the E2M1 magnitude of code c (0..7): 0, 0.5, then (1 + m/2) * 2^(e-1).
 __device__ __forceinline__ uint32_t e2m1_mag_bits(uint32_t c) {
   return c < 2 ? (c ? 0x3F000000u : 0u) : (((126u + (c >> 1)) << 23) | ((c & 1u) << 22));
 }
 
+template <bool XE>  // XE: also write the bf16 expansion
 __global__ void __launch_bounds__(kQThreads) quant_act_nvfp4_kernel(QuantArgs a) {
   // A GEMV launched next (programmatic serialisation) may start streaming its weights now;
   // it waits for this grid to complete before it reads the expansion.
@@ -107,25 +127,37 @@ __global__ void __launch_bounds__(kQThreads) quant_act_nvfp4_kernel(QuantArgs a)
     const float rcp = den > 0.0f ? __frcp_rn(den) : 0.0f;  // den == 0: q' = x * 0, as q
     // a normal power of two has an exact reciprocal: then q' is x / den rounded once
     const bool exact = (__float_as_uint(den) & 0x7FFFFFu) == 0u;
-    uint32_t cw[2] = {0u, 0u};
-    uint32_t ew[8];
+    float q[16];
+    bool nan = false;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      float q = __fmul_rn(f[j], rcp);
-      if (!exact && near_decision(q)) q = __fdiv_rn(f[j], den);
-      const uint32_t c = e2m1_code(q);
-      cw[j >> 3] |= c << (4 * (j & 7));
-      // sf * magnitude has at most 6 significant bits: exact in fp32, and its low 16 bits
-      // are zero, so the top half is the bf16 value itself
-      const uint32_t e = __float_as_uint(__fmul_rn(sf, __uint_as_float(e2m1_mag_bits(c & 7u)))) | ((c >> 3) << 31);
-      if (j & 1)
-        ew[j >> 1] |= e & 0xFFFF0000u;
-      else
-        ew[j >> 1] = e >> 16;
+      q[j] = __fmul_rn(f[j], rcp);
+      if (!exact && near_decision(q[j])) q[j] = __fdiv_rn(f[j], den);
+      nan |= q[j] != q[j];
+    }
+    uint32_t cw[2] = {e2m1x8_cvt(q), e2m1x8_cvt(q + 8)};
+    if (nan) {  // a NaN input: the software encoder's saturating code
+      cw[0] = cw[1] = 0u;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) cw[j >> 3] |= e2m1_code(q[j]) << (4 * (j & 7));
+    }
+    uint32_t ew[8];
+    if (XE) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t c = (cw[j >> 3] >> (4 * (j & 7))) & 15u;
+        // sf * magnitude has at most 6 significant bits: exact in fp32, and its low 16 bits
+        // are zero, so the top half is the bf16 value itself
+        const uint32_t e = __float_as_uint(__fmul_rn(sf, __uint_as_float(e2m1_mag_bits(c & 7u)))) | ((c >> 3) << 31);
+        if (j & 1)
+          ew[j >> 1] |= e & 0xFFFF0000u;
+        else
+          ew[j >> 1] = e >> 16;
+      }
     }
     if (a.codes) *reinterpret_cast<uint2*>(a.codes + row * a.ldc + b * 8) = make_uint2(cw[0], cw[1]);
     if (a.scales) a.scales[row * a.lds + b] = (uint8_t)s;
-    if (a.xe) {
+    if (XE) {
       uint4* dst = reinterpret_cast<uint4*>(a.xe + row * a.lde + b * 16);
       dst[0] = make_uint4(ew[0], ew[1], ew[2], ew[3]);
       dst[1] = make_uint4(ew[4], ew[5], ew[6], ew[7]);
@@ -150,7 +182,10 @@ int launch_quant_act_nvfp4(const void* x, int64_t m, int64_t k, int64_t ldx, flo
   a.xe = static_cast<uint16_t*>(xe);
   a.lde = lde;
   const int64_t blocks = std::min<int64_t>((m * a.kb + kQThreads - 1) / kQThreads, (int64_t)1 << 20);
-  quant_act_nvfp4_kernel<<<(unsigned)blocks, kQThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  if (xe)
+    quant_act_nvfp4_kernel<true><<<(unsigned)blocks, kQThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  else
+    quant_act_nvfp4_kernel<false><<<(unsigned)blocks, kQThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }
 
