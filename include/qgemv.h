@@ -284,8 +284,10 @@ size_t qmoe_workspace_size(const qg_moe_layer* layer, int64_t t, int topk);
  *   shared expert's gate logits are given (TurboEXL3 article §4.2: the shared expert's
  *   sigmoid gate), else 1.  shared_gate: fp32 [t] on the device, or NULL; non-NULL
  *   without a shared expert is QG_ERR_INVALID_ARG.  Like the router's logits, the gate
- *   logit (the 1-output projection of x) is the caller's input.  The gate multiplies the
- *   shared expert's fp32 down output in the finish, before the single bf16 rounding.
+ *   logit (the 1-output projection of x) is the caller's input.  The finish forms the
+ *   weighted sum in fp32 and rounds it to bf16 once; its terms, the per-(token, expert) down
+ *   outputs, are fp32 at 1..4 tokens and rounded to bf16 (the GEMM's output type) in the
+ *   prefill chain.
  *   h = bf16(silu(gate) * up) per (token, expert), gate = rows 0..F-1 and up = rows
  *   F..2F-1 of the expert's 2F x H gate/up weight.
  * 1..4 tokens (decode / speculative verify; TurboEXL3 article §4.2): three launches --
@@ -294,8 +296,9 @@ size_t qmoe_workspace_size(const qg_moe_layer* layer, int64_t t, int topk);
  *   down, whose blocks compute the mid (h = bf16(silu(gate) * up)) while staging their
  *   inputs; finish.
  * More tokens (prefill; §4.1): three launches -- one grouped tensor-core GEMM over the
- *   router's tile table for gate/up whose epilogue runs the mid, the same GEMM for down,
- *   and the finish; the shared expert runs as extra tiles of both GEMMs.  Needs
+ *   router's tile table for gate/up whose epilogue runs the mid, the same GEMM for down
+ *   (bf16 outputs per pair), and the finish; the shared expert runs as extra tiles of both
+ *   GEMMs.  Needs
  *   ffn % 128 == 0 and hidden % 8 == 0, else QG_ERR_UNSUPPORTED.
  * x: bf16 [t][ldx] (H inputs); out: bf16 [t][ldo].  The workspace (qmoe_workspace_size
  * bytes for this t) must be zero-filled before first use and not be shared by

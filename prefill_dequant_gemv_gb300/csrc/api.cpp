@@ -298,7 +298,7 @@ extern "C" qg_status qmoe_ffn(const qg_moe_layer* layer, const void* x, int64_t 
   if (shared_gate && !layer->has_shared) return QG_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(shared_gate) % 4) return QG_ERR_MISALIGNED;
   // the prefill chain pairs gate rows f.. with up rows F+f.. inside one 128-row tile and
-  // finishes four features at a time
+  // finishes eight features at a time
   if (t > 4 && (layer->ffn % 128 != 0 || layer->hidden % 8 != 0)) return QG_ERR_UNSUPPORTED;
   if (t * (int64_t)(topk + 1) >= ((int64_t)1 << 31)) return QG_ERR_UNSUPPORTED;
   if (ldx < layer->hidden || ldo < layer->hidden) return QG_ERR_INVALID_ARG;

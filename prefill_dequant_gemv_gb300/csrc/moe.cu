@@ -806,7 +806,7 @@ MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, i
     return at;
   };
   // the prefill chain (more than kGMaxRows tokens) fuses the mid into the gate/up GEMM and
-  // needs no fp32 gate/up rows; its down outputs are one part
+  // needs no fp32 gate/up rows; its down outputs are one part, in bf16
   const bool decode = T <= kGMaxRows;
   L.p_gu = decode ? grouped_parts(T, topk, gu.nt, gu.kg, grid) : 1;
   L.p_dn = decode ? grouped_parts(T, topk, dn.nt, dn.kg, grid) : 1;
@@ -817,7 +817,7 @@ MoeLayout moe_layout(const Geometry& gu, const Geometry& dn, int64_t T, int E, i
   L.h = take(decode ? 0 : (size_t)R * L.ld_h * 2);  // decode: h never leaves the down GEMV
   L.ld_d = (dn.n + 7) / 8 * 8;
   L.pst_dn = R * L.ld_d;
-  L.d = take((size_t)L.p_dn * R * L.ld_d * 4);
+  L.d = take((size_t)L.p_dn * R * L.ld_d * (decode ? 4 : 2));
   L.total = o;
   return L;
 }

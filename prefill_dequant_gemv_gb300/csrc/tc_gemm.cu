@@ -10,7 +10,8 @@
 //                   h = bf16(silu(gate) * up) in fp32 (§4.1 "Mid"), so the gate/up outputs
 //                   never reach device memory
 //   MoE down        the same on h (rows already in grouped order), two row tiles per item,
-//                   fp32 outputs per (token, expert) pair for the finish
+//                   outputs per (token, expert) pair for the finish, rounded to bf16 (the
+//                   type a GEMM hands on; the finish sums them in fp32)
 // The MoE shared expert runs as extra token tiles of the gate/up and down GEMMs.  Tile widths are ragged: the MMA's N is the tile's token count
 // rounded up to 16.
 //
@@ -56,7 +57,7 @@ constexpr int kTcGatWarp0 = kTcEpiWarp0 + kTcEpiWarps;                  // 22
 constexpr int kTcTile = kRouteTile;  // tokens per tile = largest MMA N (192)
 constexpr int kTcSmemCap = 232448;   // opt-in shared memory per block on sm_100-family GPUs
 
-enum TcEpilogue { kEpiSwiglu = 0, kEpiPairF32 = 1 };
+enum TcEpilogue { kEpiSwiglu = 0, kEpiPairBf16 = 1 };
 
 // Tensor memory (512 columns x 128 lanes of 32 bits): accumulators of the two row tiles in
 // columns [0, 192) and [192, 384); A ring of 2 stages x 64 columns (first tile's 64 inputs in
@@ -105,7 +106,7 @@ struct TcArgs {
   int QN;     // items per token tile
   int T;      // tokens
   int topk;   // routed gate/up: input row = pair / topk
-  void* out;  // kEpiSwiglu: bf16 h [*][ldo]; kEpiPairF32: fp32 [*][ldo]
+  void* out;  // kEpiSwiglu: bf16 h [*][ldo]; kEpiPairBf16: bf16 [*][ldo]
   int64_t ldo;
   int64_t n_out;
   int64_t F;  // kEpiSwiglu: rows of the gate half (up rows start at F)
@@ -350,27 +351,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
         tmem_ld16(tmem + lane_base + kTcTile + (uint32_t)c, u);
         tmem_ld_wait();
         if (EPI == kEpiSwiglu) {
-          const int64_t n = it.feat0 + r;  // < F: F is a multiple of 128
-          __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(a.out) + (int64_t)(it.out_base + c) * a.ldo + n;
+          // h of features f, f+1 (f even) sits in lanes 2i, 2i+1: as in the down epilogue, the
+          // two lanes swap one value per pair of tokens and each stores one 4-byte h pair
+          const int odd = lane & 1;
+          const int64_t n = it.feat0 + (r & ~1);  // < F: F is a multiple of 128
+          uint32_t* hout = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) + n);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c + j < it.count) {
-              const float g = it.ts * __uint_as_float(v[j]);
-              const float up = it.ts * __uint_as_float(u[j]);
+          for (int j = 0; j < 16; j += 2) {
+            float h[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const float g = it.ts * __uint_as_float(v[j + i]);
+              const float up = it.ts * __uint_as_float(u[j + i]);
               // silu(g) = g / (1 + e^-g); e^-g capped at e^80 keeps the quotient finite
-              const float silu = __fdividef(g, 1.0f + __expf(-fmaxf(g, -80.0f)));
-              hout[(int64_t)j * a.ldo] = __float2bfloat16_rn(silu * up);
+              h[i] = __fdividef(g, 1.0f + __expf(-fmaxf(g, -80.0f))) * up;
+            }
+            const float hr = __shfl_xor_sync(0xffffffffu, odd ? h[0] : h[1], 1);
+            const int tok = c + j + odd;
+            if (tok < it.count) {
+              const __nv_bfloat162 ph = __floats2bfloat162_rn(odd ? hr : h[0], odd ? h[1] : hr);
+              hout[((int64_t)(it.out_base + tok) * a.ldo) >> 1] = *reinterpret_cast<const uint32_t*>(&ph);
             }
           }
         } else {
-          const int64_t n0 = (int64_t)it.rt0 * 128 + r, n1 = (int64_t)it.rt1 * 128 + r;
-          const bool w0 = n0 < a.n_out, w1 = it.second && n1 < a.n_out;
+          // lanes 2i and 2i+1 hold features f, f+1 (f even) of the same 16 tokens: each
+          // pair of tokens, they swap one value so that the even lane stores both features
+          // of token j and the odd lane both of token j+1, as one 4-byte bf16 pair
+          const int odd = lane & 1;
+          const int64_t n0 = (int64_t)it.rt0 * 128 + (r & ~1), n1 = (int64_t)it.rt1 * 128 + (r & ~1);
+          const bool w0 = n0 < a.n_out, w1 = it.second && n1 < a.n_out;  // n_out is even
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c + j < it.count) {
-              float* o = static_cast<float*>(a.out) + (int64_t)(it.out_base + c + j) * a.ldo;
-              if (w0) o[n0] = it.ts * __uint_as_float(v[j]);
-              if (w1) o[n1] = it.ts * __uint_as_float(u[j]);
+          for (int j = 0; j < 16; j += 2) {
+            const float v0 = __uint_as_float(v[j]), v1 = __uint_as_float(v[j + 1]);
+            const float u0 = __uint_as_float(u[j]), u1 = __uint_as_float(u[j + 1]);
+            const float vr = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+            const float ur = __shfl_xor_sync(0xffffffffu, odd ? u0 : u1, 1);
+            const int tok = c + j + odd;
+            if (tok < it.count) {
+              uint32_t* o = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.out) +
+                                                        (int64_t)(it.out_base + tok) * a.ldo);
+              const __nv_bfloat162 pv = __floats2bfloat162_rn(it.ts * (odd ? vr : v0), it.ts * (odd ? v1 : vr));
+              const __nv_bfloat162 pu = __floats2bfloat162_rn(it.ts * (odd ? ur : u0), it.ts * (odd ? u1 : ur));
+              if (w0) o[n0 >> 1] = *reinterpret_cast<const uint32_t*>(&pv);
+              if (w1) o[n1 >> 1] = *reinterpret_cast<const uint32_t*>(&pu);
             }
           }
         }
@@ -448,40 +471,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_con
   }
 }
 
-// out[t][n] = bf16( sum_j w[t][j] * d[pos(t, j)][n] + g_t * d[T*topk + t][n] ), fixed order,
-// four features per thread (TurboEXL3 article §4.1 "Finish"; g_t: the shared expert's
-// sigmoid gate, §4.2, or 1).
-__global__ void __launch_bounds__(256) moe_finish4_kernel(const float* d, int64_t ldd, const float* w,
+// out[t][n] = bf16( sum_j w[t][j] * d[pos(t, j)][n] + g_t * d[T*topk + t][n] ) with d the
+// bf16 per-pair down outputs, summed in fp32 in a fixed order, eight features per thread
+// (TurboEXL3 article §4.1 "Finish"; g_t: the shared expert's sigmoid gate, §4.2, or 1).
+__device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float p, uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] = fmaf(p, __uint_as_float(w[i] << 16), acc[2 * i]);
+    acc[2 * i + 1] = fmaf(p, __uint_as_float(w[i] & 0xffff0000u), acc[2 * i + 1]);
+  }
+}
+
+__global__ void __launch_bounds__(256) moe_finish8_kernel(const __nv_bfloat16* d, int64_t ldd, const float* w,
                                                           const int* pair_pos, int T, int topk, int has_shared,
                                                           const float* shared_gate, int64_t H, __nv_bfloat16* out,
                                                           int64_t ldo) {
-  const int64_t H4 = H / 4;
+  const int64_t H8 = H / 8;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (int64_t)T * H4) return;
-  const int t = (int)(idx / H4);
-  const int64_t n = (idx % H4) * 4;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (idx >= (int64_t)T * H8) return;
+  const int t = (int)(idx / H8);
+  const int64_t n = (idx % H8) * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int j = 0; j < topk; ++j) {
     const float p = w[(int64_t)t * topk + j];
-    const float4 v = __ldcs(reinterpret_cast<const float4*>(d + (int64_t)pair_pos[(int64_t)t * topk + j] * ldd + n));
-    acc.x = fmaf(p, v.x, acc.x);
-    acc.y = fmaf(p, v.y, acc.y);
-    acc.z = fmaf(p, v.z, acc.z);
-    acc.w = fmaf(p, v.w, acc.w);
+    fma_bf16x8(acc, p, __ldcs(reinterpret_cast<const uint4*>(d + (int64_t)pair_pos[(int64_t)t * topk + j] * ldd + n)));
   }
-  if (has_shared) {
-    const float4 v = __ldcs(reinterpret_cast<const float4*>(d + (int64_t)(T * topk + t) * ldd + n));
-    const float g = shared_gate_weight(shared_gate, t);
-    acc.x = fmaf(g, v.x, acc.x);
-    acc.y = fmaf(g, v.y, acc.y);
-    acc.z = fmaf(g, v.z, acc.z);
-    acc.w = fmaf(g, v.w, acc.w);
+  if (has_shared)
+    fma_bf16x8(acc, shared_gate_weight(shared_gate, t),
+               __ldcs(reinterpret_cast<const uint4*>(d + (int64_t)(T * topk + t) * ldd + n)));
+  uint32_t pk[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
   }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-  uint2 pk;
-  pk.x = *reinterpret_cast<uint32_t*>(&lo);
-  pk.y = *reinterpret_cast<uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(out + (int64_t)t * ldo + n) = pk;
+  *reinterpret_cast<uint4*>(out + (int64_t)t * ldo + n) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
 }
 
 // ---------------------------------------------------------------- host side
@@ -621,13 +646,13 @@ int launch_moe_prefill(const qg_moe_layer* m, const Geometry& gu, const Geometry
   d.out = w + L.d;
   d.ldo = L.ld_d;
   d.n_out = dn.n;
-  st = launch_tc_fmt<kEpiPairF32>(m->fmt, T * topk + (m->has_shared ? T : 0), d, dev.sms, dev, s);
+  st = launch_tc_fmt<kEpiPairBf16>(m->fmt, T * topk + (m->has_shared ? T : 0), d, dev.sms, dev, s);
   if (st != QG_OK) return st;
 
   const int64_t H = dn.n;
-  const int64_t n4 = T * (H / 4);
-  moe_finish4_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(
-      reinterpret_cast<const float*>(w + L.d), L.ld_d, topk_w, rv.pair_pos, (int)T, topk, m->has_shared, shared_gate, H,
+  const int64_t n8 = T * (H / 8);
+  moe_finish8_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(w + L.d), L.ld_d, topk_w, rv.pair_pos, (int)T, topk, m->has_shared, shared_gate, H,
       static_cast<__nv_bfloat16*>(out), ldo);
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ERR_CUDA;
 }

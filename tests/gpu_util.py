@@ -33,24 +33,32 @@ def to_f64(t) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def moe_tolerance(o, layer, x, lg, topk, out_ref, tokens=None):
+def moe_tolerance(o, layer, x, lg, topk, out_ref, tokens=None, pair_bf16=None):
     """Per-element bound for a mixture-of-experts output (rows = `tokens`, all by default):
     each expert's down output within the GEMV bound of its (bf16) input h plus one bf16 ulp
-    of h (rounding flips between the two sides), weighted by p; plus one output ulp."""
+    of h (rounding flips between the two sides), weighted by p; plus one output ulp.
+    pair_bf16 (default: more than 4 tokens, the prefill chain): each down output is also
+    rounded to bf16 before the weighted sum -- half an ulp, at most 2^-9 of the value; the
+    bound takes 2^-8 of the oracle's value so that it also covers the kernel's value lying
+    within the GEMV bound of it."""
+    if pair_bf16 is None:
+        pair_bf16 = x.shape[0] > 4
     _, _, ids, p, inter = o.moe_forward(layer, x, lg, topk, tokens=tokens, with_intermediates=True)
     toks = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens)
     tol = np.zeros((toks.size, layer.hidden))
     rn = {}
+    pr = 2.0 ** -8 if pair_bf16 else 0.0
     for i, t in enumerate(toks):
         for j in range(topk):
             e = int(ids[t, j])
             if e not in rn:
                 rn[e] = float(np.max(o.row_norms(layer.down[e])))
-            h = inter[(int(t), e)][2]
-            tol[i] += p[t, j] * (2e-3 + 2.0 ** -8) * np.linalg.norm(h) * rn[e]
+            _, _, h, d = inter[(int(t), e)]
+            tol[i] += p[t, j] * ((2e-3 + 2.0 ** -8) * np.linalg.norm(h) * rn[e] + pr * np.abs(d))
         if layer.shared_down is not None:
-            h = inter[(int(t), -1)][2]
-            tol[i] += (2e-3 + 2.0 ** -8) * np.linalg.norm(h) * float(np.max(o.row_norms(layer.shared_down)))
+            _, _, h, d = inter[(int(t), -1)]
+            tol[i] += (2e-3 + 2.0 ** -8) * np.linalg.norm(h) * float(np.max(o.row_norms(layer.shared_down))) \
+                + pr * np.abs(d)
     return tol + 2.0 ** -7 * np.abs(out_ref)
 
 
