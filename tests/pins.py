@@ -361,25 +361,45 @@ def check_moe_shared_gate(o, seed=30):
     assert np.array_equal(o.moe_forward(layer, x, lg, topk=2, shared_gate=np.full(4, 100.0, np.float32)), ungated)
 
 
+def _expert_by_gemv(o, gu, dn, x_row, f):
+    """One expert on one token through the dense GEMV oracle: gate/up GEMV (fp32 outputs),
+    h = bf16(silu(g)·u), down GEMV of h (fp64 value before rounding)."""
+    _, v = o.gemv(gu, x_row)
+    g, u = v[0, :f].astype(np.float32), v[0, f:].astype(np.float32)
+    h = o.round_to_bf16(o.silu(g) * u.astype(np.float64))
+    return o.gemv(dn, o.bf16_bits_of(h)[None, :])[1][0]
+
+
 def check_moe_composition(o, seed=29):
     """The MoE chain against the dense GEMV oracle: top-1 routing (p = 1) through one
-    expert equals gate/up GEMV -> SwiGLU -> down GEMV, and relabelling the experts
-    (with the logits) leaves the output unchanged."""
+    expert equals gate/up GEMV -> SwiGLU -> down GEMV; top-3 routing equals the sum of the
+    three experts' chains, each times its own slot's softmax weight, plus the shared
+    expert's; and relabelling the experts (with the logits) leaves the output unchanged."""
     layer = wl.moe_layer(wl.MXFP4, 6, 64, 32, seed=seed, shared=True)
     x = wl.moe_tokens(3, 64, seed=seed)
     lg = wl.router_logits(3, 6, seed=seed)
     out = o.moe_forward(layer, x, lg, topk=1)
     ids, p = o.route(lg, 1)
     assert np.all(p == 1.0)
-    x64 = o.bf16_value(x)
     for t in range(3):
         acc = np.zeros(64)
         for gu, dn in [(layer.gate_up[ids[t, 0]], layer.down[ids[t, 0]]), (layer.shared_gate_up, layer.shared_down)]:
-            _, v = o.gemv(gu, x[t:t + 1])
-            g, u = v[0, :32].astype(np.float32), v[0, 32:].astype(np.float32)
-            h = o.round_to_bf16(o.silu(g) * u.astype(np.float64))
-            acc += o.gemv(dn, o.bf16_bits_of(h)[None, :])[1][0]
+            acc += _expert_by_gemv(o, gu, dn, x[t:t + 1], 32)
         assert np.array_equal(out[t], o.round_to_bf16(acc)), t
+    # top-3 on logits with well-separated values (a different order per token): distinct
+    # weights per slot, so a weight on the wrong slot or no weight shows
+    rng = np.random.default_rng(seed)
+    lg3 = np.stack([rng.permutation(np.array([2.0, 1.0, 0.25, -0.5, -1.0, -2.0], np.float32)) for _ in range(3)])
+    _, acc3, ids3, _, _ = o.moe_forward(layer, x, lg3, topk=3, with_intermediates=True)
+    rids, rp = o.route(lg3, 3)
+    assert np.array_equal(ids3, rids)
+    assert np.all(np.abs(np.diff(rp, axis=1)) > 1e-3)
+    for t in range(3):
+        want = _expert_by_gemv(o, layer.shared_gate_up, layer.shared_down, x[t:t + 1], 32)
+        for j in range(3):
+            e = int(rids[t, j])
+            want = want + rp[t, j] * _expert_by_gemv(o, layer.gate_up[e], layer.down[e], x[t:t + 1], 32)
+        assert np.allclose(acc3[t], want, rtol=1e-12, atol=1e-12 * np.max(np.abs(want))), t
     perm = np.random.default_rng(seed).permutation(6)  # new index i holds old expert perm[i]
     layer2 = wl.MoELayer(layer.fmt, 6, 64, 32, [layer.gate_up[j] for j in perm], [layer.down[j] for j in perm],
                          layer.shared_gate_up, layer.shared_down)

@@ -157,6 +157,20 @@ def test_moe_shared_expert_dropped(monkeypatch):
     assert _fails(pins.check_moe_composition, oracle)
 
 
+def test_moe_routing_weights_dropped(monkeypatch):
+    # the finish sums the experts' outputs without their softmax weights
+    orig = MO.route
+    monkeypatch.setattr(MO, "route", lambda lg, k: (orig(lg, k)[0], np.ones_like(orig(lg, k)[1])))
+    assert _fails(pins.check_moe_composition, oracle)
+
+
+def test_moe_routing_weights_on_the_wrong_slots(monkeypatch):
+    # each expert's output weighed by another slot's weight (the slot order reversed)
+    orig = MO.route
+    monkeypatch.setattr(MO, "route", lambda lg, k: (orig(lg, k)[0], orig(lg, k)[1][:, ::-1]))
+    assert _fails(pins.check_moe_composition, oracle)
+
+
 def test_moe_swiglu_swapped(monkeypatch):
     orig = MO.swiglu_bf16
     monkeypatch.setattr(MO, "swiglu_bf16", lambda g, u: orig(u, g))
