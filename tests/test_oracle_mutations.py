@@ -171,6 +171,12 @@ def test_moe_routing_weights_on_the_wrong_slots(monkeypatch):
     assert _fails(pins.check_moe_composition, oracle)
 
 
+def test_moe_h_not_rounded_to_bf16(monkeypatch):
+    # the mid hands h to the down projection without its 16-bit rounding
+    monkeypatch.setattr(MO, "swiglu_bf16", lambda g, u: MO.silu(g) * np.asarray(u, dtype=np.float64))
+    assert _fails(pins.check_moe_composition, oracle)
+
+
 def test_moe_swiglu_swapped(monkeypatch):
     orig = MO.swiglu_bf16
     monkeypatch.setattr(MO, "swiglu_bf16", lambda g, u: orig(u, g))
