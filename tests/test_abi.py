@@ -172,6 +172,9 @@ def test_qgemm_grouped_host_validation(q):
     assert call(t=0) == 1
     assert call(gate=0xA000) == 1                               # gate logits without a shared expert
     assert call(layer=_moe_desc(q, fmt=wl.Q5_0)) == 2           # the 5-bit formats run on the dense paths only
+    # the prefill chain (more than 4 tokens) pairs gate and up rows in one 128-row tile
+    assert call(layer=_moe_desc(q, ffn=96), t=8, ldo=96) == 2
+    assert call(layer=_moe_desc(q, ffn=96), t=8, stage=q.QG_MOE_DOWN_COMBINE, ldi=96, ldo=256) == 2
     sh = _moe_desc(q, has_shared=1,
                    shared_gate_up=q.qg_weight(fmt=wl.MXFP4, n=256, k=256, codes=0x50000, scales=0x51000,
                                               tensor_scale=1.0),
